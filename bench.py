@@ -1,0 +1,346 @@
+"""MoE block forward benchmark: tokens/s and roofline fraction on one GB300.
+
+Headline: the decode workload (N=4 tokens, H=2048, 128 experts of inter 768, top-8, sigmoid-
+gated shared expert of inter 512), HBM-bound. The prefill workload (N=4096, Zipf-skewed
+routing) is measured in the same run and reported under "prefill" (tensor-bound).
+
+A step is one moe_forward over one batch with inputs resident in HBM; L2 is flushed (512 MiB
+write) before every timed step, outside the timed region. Times come from CUDA events on the
+launching stream. `--impl reference` times the CPU oracle instead (the only baseline there
+is). Multi-GPU runs are independent replicas (the block does not shard): value = all ranks'
+tokens / the slowest rank's time.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_experts_layer_08_gb300 import inputs as I  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (prefill N=4096, decode N=4) and % tensor/HBM roofline"
+FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"], "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "src": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev: int):
+        self.dev = dev
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def routing_stats(inp, idx):
+    s = inp.shape
+    flat = idx.reshape(-1)
+    real = flat[flat < s.num_experts]
+    counts = np.bincount(real, minlength=s.num_experts)
+    return {"Z": int(real.size), "distinct": int((counts > 0).sum()), "counts": counts}
+
+
+def algorithmic(inp, rs):
+    """Work the method must do (routed rows Z, not tile-padded; touched experts read once)."""
+    s = inp.shape
+    H, I_, S, R = s.hidden, s.inter, s.shared_inter, s.router_width
+    wb = 1 if s.weight_dtype == I.WDTYPE_FP8_E4M3_B128 else 2
+    expert_bytes = 3 * I_ * H * wb
+    bytes_ = (rs["distinct"] * expert_bytes + 3 * S * H * 2 + R * H * 2
+              + 2 * s.num_tokens * H * 2 + (H * 2 if s.shared_gated else 0))
+    flops_routed = 6.0 * rs["Z"] * H * I_
+    flops = flops_routed + 6.0 * s.num_tokens * H * S + 2.0 * s.num_tokens * H * R
+    gate_up_flops = 4.0 * rs["Z"] * H * I_
+    gate_up_bytes = rs["distinct"] * 2 * I_ * H * wb + (2 * S * H * 2)
+    return {"bytes": bytes_, "flops": flops, "gate_up_flops": gate_up_flops,
+            "gate_up_bytes": gate_up_bytes, "expert_bytes": expert_bytes}
+
+
+def kernels_per_step(B, cfg):
+    """Kernels of this library one forward launches (memsets are not kernels)."""
+    decode = cfg.path == B.PATH_DECODE or (cfg.path == B.PATH_AUTO and cfg.num_tokens <= 16
+                                            and cfg.weight_dtype == 0)
+    if decode:
+        return 4            # fused router + top-K + sort, gate/up, down, combine
+    return 8 + (2 if cfg.shared_inter else 0)   # router, top-K, 3 sort, [2 shared], 2 GEMM, combine
+
+
+def barrier():
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def time_ours(B, shape, steps, warmup, dev, peaks, with_e2e=True):
+    torch.cuda.set_device(dev)
+    inp = I.make_inputs(shape, device=f"cuda:{dev}")
+    blk = B.MoeBlock(inp)
+    N, K = shape.num_tokens, shape.top_k
+    idx = torch.empty(N, K, dtype=torch.int32, device=f"cuda:{dev}")
+    out = torch.empty_like(inp.x)
+    blk(inp.x, out=out, topk_idx_out=idx)
+    torch.cuda.synchronize()
+    rs = routing_stats(inp, idx.cpu().numpy())
+    alg = algorithmic(inp, rs)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=f"cuda:{dev}")
+    stream = torch.cuda.current_stream()
+    nst = len(B.STAGES)
+
+    def one(events):
+        B.moe_forward_profiled(blk.cfg, blk.weights, inp.x, out, blk.workspace, events, stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        one([None] * (2 * nst))
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nst)] for _ in range(steps)]
+    with ClockSampler(dev) as clk:
+        t_wall0 = time.time()
+        for i in range(steps):
+            flush.zero_()
+            one(ev[i])
+        torch.cuda.synchronize()
+        t_wall = time.time() - t_wall0
+    stage_ms = {n: [] for n in B.STAGES}
+    step_ms = []
+    for i in range(steps):
+        e = ev[i]
+        step_ms.append(e[0].elapsed_time(e[2 * nst - 1]))
+        for s, n in enumerate(B.STAGES):
+            stage_ms[n].append(e[2 * s].elapsed_time(e[2 * s + 1]))
+    ms = statistics.mean(step_ms)
+    res = {"inp": inp, "rs": rs, "alg": alg, "ms": ms, "stage_ms": {k: statistics.mean(v)
+                                                                     for k, v in stage_ms.items()},
+           "clocks": clk.summary(), "wall_s": t_wall,
+           "launches_per_step": kernels_per_step(B, blk.cfg)}
+    if with_e2e:
+        hx = torch.empty(inp.x.shape, dtype=inp.x.dtype, pin_memory=True)
+        hx.copy_(inp.x.cpu())
+        ho = torch.empty(inp.x.shape, dtype=inp.x.dtype, pin_memory=True)
+        dx = torch.empty_like(inp.x)
+        e2e = []
+        for i in range(warmup + steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            dx.copy_(hx, non_blocking=True)
+            B.moe_forward(blk.cfg, blk.weights, dx, out, blk.workspace, stream)
+            ho.copy_(out, non_blocking=True)
+            b.record()
+            torch.cuda.synchronize()
+            if i >= warmup:
+                e2e.append(a.elapsed_time(b))
+        res["e2e_ms"] = statistics.mean(e2e)
+        res["io_bytes"] = hx.numel() * hx.element_size()
+    return res
+
+
+def cpu_oracle_tokens_per_s(inp, budget_s=12.0, max_tokens=None):
+    """Times the oracle (as it stands) on the host cores on a bounded sample of tokens."""
+    from oracle import oracle as O
+    n = inp.shape.num_tokens
+    tokens = np.arange(n if max_tokens is None else min(n, max_tokens))
+    host = inp.to("cpu")
+    O.moe_forward(host, tokens=tokens[:1])   # build + warm-up, untimed
+    done, t0 = 0, time.time()
+    reps = 0
+    while True:
+        O.moe_forward(host, tokens=tokens)
+        done += len(tokens)
+        reps += 1
+        if time.time() - t0 > budget_s or reps >= 50:
+            break
+    dt = time.time() - t0
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": done / dt, "unit": "tokens/s", "cores": min(threads, len(tokens)),
+            "kind": "oracle",
+            "sample": f"{reps} x {len(tokens)} tokens of the {inp.shape.name} workload "
+                      f"(fp64 C oracle, OpenMP over tokens), {dt:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    shape = I.DECODE
+    peaks = load_peaks()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        inp = I.make_inputs(shape)
+        times = []
+        from oracle import oracle as O
+        O.moe_forward(inp, tokens=[0])
+        for _ in range(warmup):
+            O.moe_forward(inp)
+        for _ in range(args.steps):
+            t0 = time.time()
+            O.moe_forward(inp)
+            times.append(time.time() - t0)
+        ms = 1000 * statistics.mean(times)
+        v = shape.num_tokens / (ms / 1000)
+        threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic",
+                "config": {"workload": shape.name, "N": shape.num_tokens, "H": shape.hidden,
+                           "E": shape.num_experts, "K": shape.top_k, "I": shape.inter,
+                           "S": shape.shared_inter},
+                "cpu_baseline": {"value": v, "unit": "tokens/s",
+                                 "cores": min(threads, shape.num_tokens), "kind": "oracle",
+                                 "sample": f"each step: the whole {shape.num_tokens}-token batch"},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    dev = local
+    torch.cuda.set_device(dev)
+    try:
+        from mixture_experts_layer_08_gb300 import binding as B
+    except ImportError:
+        from mixture_experts_layer_08_gb300 import build as _b
+        _b.build()
+        from mixture_experts_layer_08_gb300 import binding as B
+
+    r = time_ours(B, shape, args.steps, warmup, dev, peaks)
+    ms = r["ms"]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=f"cuda:{dev}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * shape.num_tokens / (ms / 1000.0)
+    alg = r["alg"]
+    # dominant kernel of the decode chain: the gate/up GEMV (2/3 of the streamed bytes)
+    gu_ms = r["stage_ms"]["gate_up"]
+    gu_ach = alg["gate_up_bytes"] / (gu_ms / 1000.0) / 1e9
+    step_ach = alg["bytes"] / (ms / 1000.0) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": shape.name, "N": shape.num_tokens, "H": shape.hidden,
+                   "E": shape.num_experts, "R": shape.router_width, "K": shape.top_k,
+                   "I": shape.inter, "S": shape.shared_inter, "parallelism": "replicas",
+                   "l2": "flushed before every timed step (512 MiB write, untimed)",
+                   "distinct_experts": r["rs"]["distinct"]},
+        "roofline": {"bound": "hbm", "kernel": "decode_gateup_kernel",
+                     "achieved": gu_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gu_ach / peaks["hbm_gbs"], "traffic": None,
+                     "peak_src": peaks["src"],
+                     "step_achieved_gbs": step_ach, "step_frac": step_ach / peaks["hbm_gbs"],
+                     "algorithmic_bytes_per_launch": alg["gate_up_bytes"],
+                     "algorithmic_bytes_per_step": alg["bytes"]},
+        "stage_us": {k: 1000 * v for k, v in r["stage_ms"].items()},
+        "gpu_launches": r["launches_per_step"] * args.steps,
+        "clocks": r["clocks"],
+        "e2e": {"value": world * shape.num_tokens / (r["e2e_ms"] / 1000.0), "unit": "tokens/s",
+                "h2d_bytes_per_step": r["io_bytes"], "d2h_bytes_per_step": r["io_bytes"]},
+    }
+    if not args.no_prefill:
+        p = time_ours(B, I.PREFILL, max(3, args.steps // 2), warmup, dev, peaks, with_e2e=False)
+        pa = p["alg"]
+        gu = p["stage_ms"]["gate_up"]
+        gu_tf = pa["gate_up_flops"] / (gu / 1000.0) / 1e12
+        line["prefill"] = {
+            "workload": I.PREFILL.name, "value": I.PREFILL.num_tokens / (p["ms"] / 1000.0),
+            "unit": "tokens/s", "ms_per_step": p["ms"],
+            "stage_us": {k: 1000 * v for k, v in p["stage_ms"].items()},
+            "roofline": {"bound": "tensor", "kernel": "gemm_bf16_kernel<256,SwiGLU>",
+                         "achieved": gu_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": gu_tf / peaks["bf16_tflops"], "traffic": None,
+                         "step_tflops": pa["flops"] / (p["ms"] / 1000.0) / 1e12,
+                         "step_frac": pa["flops"] / (p["ms"] / 1000.0) / 1e12 / peaks["bf16_tflops"]},
+            "Z": p["rs"]["Z"], "max_expert_rows": int(p["rs"]["counts"].max()),
+            "min_expert_rows": int(p["rs"]["counts"].min()),
+            "clocks": p["clocks"]}
+        line["gpu_launches"] += p["launches_per_step"] * max(3, args.steps // 2)
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_oracle_tokens_per_s(r["inp"])
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,178 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) Mixture-of-Experts block forward.
+ *
+ * The operation is the MoE block forward of LLM serving, as dispatched by the pages
+ * "metrale_model_layers/layers/moe/forward_prefill.rs" (`MoeLayer::forward_prefill`: shared
+ * expert, router gate GEMM, top-K, sort by expert, grouped gate/up GEMM + activation, grouped
+ * down GEMM, unpermute + weighted reduce, shared blend), "spark_model/layers/moe/forward.rs"
+ * (`forward` single-token decode, softmax + correction-bias routing, `apply_zero_expert`) and
+ * "metrale_model_layers/layers/moe/forward_atomic_c4.rs" (4-row decode with FP32 atomic
+ * accumulation of the routed down projections, then a finalize that casts to BF16 and blends
+ * the shared expert):
+ *
+ *   L[t,:]   = x[t,:] . Wr^T (+ router_logit_bias)                       fp32 accumulate
+ *   p[t,:]   = softmax(L[t,:]) over all R router columns                  fp32
+ *   idx[t,:] = top-K of p (or of p + correction_bias), ties to the lower id
+ *   w[t,k]   = p[t,idx] (/ sum_k if norm_topk_prob) * routed_scaling_factor
+ *   out[t,:] = sum_{k: idx<E} w[t,k] * (SiLU(x Wg_e^T) * (x Wu_e^T)) Wd_e^T
+ *            + (sum_{k: idx>=E} w[t,k]) * x[t,:]            identity ("zero-computation") experts
+ *            + gamma_t * (SiLU(x Sg^T) * (x Su^T)) Sd^T      shared expert, gamma_t = sigmoid(x.g)
+ *                                                             or 1 when g is NULL
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers, row-major, with the contraction dim contiguous
+ *    ([out_features, in_features], like an nn.Linear weight). bf16 is IEEE bfloat16; FP8 is
+ *    OCP E4M3 ("e4m3fn").
+ *  - The caller owns every buffer. The library allocates nothing, keeps no state between
+ *    calls (apart from a per-process cache of CUDA device attributes), and never
+ *    synchronises the host: all work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream), so a call can be captured into a CUDA graph.
+ *  - Errors are returned as moe_status_t, never thrown; on a non-OK return nothing has been
+ *    enqueued unless the status is MOE_ERR_CUDA (a launch failed part-way).
+ *  - Device-side waits are bounded: a kernel that gives up writes MOE_ERR_DEVICE_TIMEOUT into
+ *    the workspace status word (read it with moe_read_device_status) and returns.
+ *  - Sizes: hidden, inter and shared_inter must be multiples of 128; 1 <= top_k <= 32,
+ *    top_k <= router_width <= 1024, num_experts <= router_width, num_experts <= 1024.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_SCORING_SOFTMAX = 0,      /* p = softmax(L); select by p */
+  MOE_SCORING_SOFTMAX_BIAS = 1  /* p = softmax(L); select by p + correction_bias; weights from p */
+} moe_scoring_t;
+
+typedef enum {
+  MOE_W_BF16 = 0,               /* routed expert weights bf16 */
+  MOE_W_FP8_E4M3_B128 = 1       /* routed expert weights E4M3 + one fp32 scale per 128x128 block;
+                                   expert inputs and the SwiGLU intermediate are quantised per
+                                   1x128 (along the contraction) to E4M3, scale = amax/448 */
+} moe_wdtype_t;
+
+typedef enum {
+  MOE_PATH_AUTO = 0,            /* decode chain for bf16 experts and num_tokens <= 16, else grouped */
+  MOE_PATH_DECODE = 1,          /* weight-streaming GEMV chain (bf16 experts, num_tokens <= 16) */
+  MOE_PATH_GROUPED = 2          /* sort + tcgen05 grouped GEMM chain (any num_tokens) */
+} moe_path_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,          /* NULL where a pointer is required, negative size, ... */
+  MOE_ERR_UNSUPPORTED = 2,          /* valid but not implemented (e.g. hidden % 128 != 0) */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes < moe_workspace_size() */
+  MOE_ERR_CUDA = 4,                 /* a CUDA runtime call failed */
+  MOE_ERR_DEVICE_TIMEOUT = 5        /* a bounded device wait gave up (reported on device) */
+} moe_status_t;
+
+typedef struct {
+  int32_t num_tokens;    /* N >= 0 */
+  int32_t hidden;        /* H */
+  int32_t num_experts;   /* E: SwiGLU experts, ids 0..E-1 */
+  int32_t router_width;  /* R >= E: router columns; ids E..R-1 are identity experts.
+                            R > E requires MOE_SCORING_SOFTMAX_BIAS (the pages wire identity
+                            experts only on that arm) */
+  int32_t top_k;         /* K */
+  int32_t inter;         /* I: routed expert intermediate size */
+  int32_t shared_inter;  /* S: shared expert intermediate size, 0 = no shared expert */
+  int32_t scoring;       /* moe_scoring_t */
+  int32_t norm_topk_prob;          /* nonzero: renormalise the K weights to sum 1 */
+  float routed_scaling_factor;     /* multiplies every routing weight */
+  int32_t weight_dtype;  /* moe_wdtype_t */
+  int32_t deterministic; /* nonzero: bitwise run-to-run reproducible (slot-ordered reduction);
+                            0: the decode chain accumulates the routed down projections with
+                            FP32 atomics */
+  int32_t path;          /* moe_path_t */
+} moe_config_t;
+
+typedef struct {
+  const void *router_w;            /* bf16 [R,H] */
+  const float *router_logit_bias;  /* nullable fp32 [R], added to the logits before softmax */
+  const float *correction_bias;    /* fp32 [R], MOE_SCORING_SOFTMAX_BIAS only (selection only) */
+  const void *w_gate;              /* [E,I,H] bf16 or E4M3 */
+  const void *w_up;                /* [E,I,H] bf16 or E4M3 */
+  const void *w_down;              /* [E,H,I] bf16 or E4M3 */
+  const float *s_gate;             /* FP8 only: fp32 [E,I/128,H/128] */
+  const float *s_up;               /* FP8 only: fp32 [E,I/128,H/128] */
+  const float *s_down;             /* FP8 only: fp32 [E,H/128,I/128] */
+  const void *sh_gate;             /* bf16 [S,H]; NULL iff S == 0 */
+  const void *sh_up;               /* bf16 [S,H] */
+  const void *sh_down;             /* bf16 [H,S] */
+  const void *sh_gate_vec;         /* nullable bf16 [H]: shared blend weight sigmoid(x . g);
+                                      NULL = weight 1 */
+} moe_weights_t;
+
+/* Bytes of device workspace moe_forward / moe_route need for `cfg` (path resolved as in
+ * moe_forward). Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for a config they reject. */
+MOE_API moe_status_t moe_workspace_size(const moe_config_t *cfg, size_t *bytes);
+
+/* The whole block forward (all steps above) on `stream`.
+ *  x          bf16 [N,H] device, read only; must not overlap `out`.
+ *  out        bf16 [N,H] device, fully overwritten (FP32 accumulation, one rounding to bf16).
+ *  workspace  device scratch of >= moe_workspace_size() bytes, 256-byte aligned; its contents
+ *             on entry do not matter; it must not be used by another call still in flight.
+ *  topk_idx_out / topk_w_out  nullable uint32 / fp32 [N,K]: the routing actually used.
+ *  forced_idx nullable uint32 [N,K] expert ids that replace the top-K selection (test hook;
+ *             the weights are then the probabilities of those ids, renormalised as configured).
+ * Pages: forward_prefill.rs `forward_prefill` (prefill chain), forward.rs `forward`
+ * (decode), forward_atomic_c4.rs (atomic decode accumulation), forward.rs `apply_zero_expert`. */
+MOE_API moe_status_t moe_forward(const moe_config_t *cfg, const moe_weights_t *weights, const void *x,
+                         void *out, void *workspace, size_t workspace_bytes, void *stream,
+                         uint32_t *topk_idx_out, float *topk_w_out, const uint32_t *forced_idx);
+
+/* Routing steps only (router GEMM, scoring + top-K + weights, identity-expert sum, and the
+ * stable sort of the (token, slot) pairs by expert), for inspection and tests. Each output
+ * pointer is a nullable device buffer:
+ *  idx_out uint32 [N,K], w_out fp32 [N,K], zsum_out fp32 [N] (summed identity-expert weight),
+ *  offsets_out uint32 [E+1] (row offset of each expert in the sorted order),
+ *  sorted_pairs_out uint32 [N*K] (flat pair index t*K+k of each sorted row; entries past
+ *  offsets[E] are unspecified), pair_to_row_out uint32 [N*K] (sorted row of each pair,
+ *  0xFFFFFFFF for identity-expert pairs). Within an expert, rows keep the pair order.
+ * Pages: forward_prefill.rs gate GEMM / top-K / `moe_sort_by_expert`. */
+MOE_API moe_status_t moe_route(const moe_config_t *cfg, const moe_weights_t *weights, const void *x,
+                       void *workspace, size_t workspace_bytes, void *stream,
+                       uint32_t *idx_out, float *w_out, float *zsum_out, uint32_t *offsets_out,
+                       uint32_t *sorted_pairs_out, uint32_t *pair_to_row_out);
+
+/* Stages of one forward, in launch order, for moe_forward_profiled. The decode chain runs the
+ * shared expert inside its gate/up and down launches, so its SHARED stage is empty. */
+typedef enum {
+  MOE_STAGE_ROUTE = 0,     /* router GEMM, scoring + top-K, sort (+ gather of expert rows) */
+  MOE_STAGE_SHARED = 1,    /* shared expert gate/up + down (grouped chain) */
+  MOE_STAGE_GATE_UP = 2,   /* routed gate/up projection with fused SiLU(gate) * up */
+  MOE_STAGE_DOWN = 3,      /* routed down projection */
+  MOE_STAGE_COMBINE = 4,   /* unpermute + weighted reduce + identity add + shared blend */
+  MOE_NUM_STAGES = 5
+} moe_stage_t;
+
+/* moe_forward that also records `events[2*s]` before and `events[2*s+1]` after stage s on
+ * `stream` (events: MOE_NUM_STAGES*2 cudaEvent_t handles created by the caller; NULL entries
+ * are skipped). For measuring per-kernel durations; results are identical to moe_forward. */
+MOE_API moe_status_t moe_forward_profiled(const moe_config_t *cfg, const moe_weights_t *weights,
+                                          const void *x, void *out, void *workspace,
+                                          size_t workspace_bytes, void *stream, void **events);
+
+/* Synchronises `stream` and reads the device status word of `workspace` into *status
+ * (MOE_OK or MOE_ERR_DEVICE_TIMEOUT). For tests and debugging; it blocks the host. */
+MOE_API moe_status_t moe_read_device_status(const void *workspace, void *stream, int32_t *status);
+
+/* Static description of a status code. */
+MOE_API const char *moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

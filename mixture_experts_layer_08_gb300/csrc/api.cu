@@ -1,0 +1,531 @@
+// C ABI of the MoE block forward: validation, workspace carving, dispatch of the kernel
+// chains on the caller's stream. Allocates nothing and never synchronises the host (except
+// moe_read_device_status, which exists to do exactly that).
+//
+// Pages: "metrale_model_layers/layers/moe/forward_prefill.rs" (`forward_prefill` picks the
+// grouped GEMM body above a row threshold and the per-token path below it; named refusals
+// instead of silent wrong results), "spark_model/layers/moe/forward_batched.rs" (refuses
+// identity-expert routing except on the softmax + correction-bias arm),
+// "metrale_model_layers/layers/moe/forward_atomic_c4.rs" (scratch-size check reporting the
+// bytes needed and available; the FP32 accumulator sits at a 256-byte aligned offset).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr int kDecodeMaxTokens = 16;
+constexpr int kSmallRouterMaxTokens = 64;
+
+enum Region {
+  R_HDR, R_LOGITS, R_IDX, R_W, R_ZSUM, R_BLK, R_LRANK, R_OFFS, R_P2R, R_SPAIRS, R_ACTIVE,
+  R_TILES, R_XP, R_XS, R_HH, R_HS, R_Y, R_SHH, R_SHY, R_HD, R_YD, R_ACC, R_NUM
+};
+
+struct Layout {
+  size_t off[R_NUM];
+  size_t size[R_NUM];
+  size_t total;
+  int path;
+  int te, max_mtiles, nblk;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+int resolve_path(const moe_config_t* c) {
+  if (c->path != MOE_PATH_AUTO) return c->path;
+  const bool decode_ok = c->weight_dtype == MOE_W_BF16 && c->num_tokens <= kDecodeMaxTokens &&
+                         c->inter <= 1024 && c->shared_inter <= 1024;
+  return decode_ok ? MOE_PATH_DECODE : MOE_PATH_GROUPED;
+}
+
+moe_status_t validate_config(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->num_tokens < 0 || c->hidden <= 0 || c->num_experts <= 0 || c->router_width <= 0 ||
+      c->top_k <= 0 || c->inter <= 0 || c->shared_inter < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->router_width < c->num_experts || c->top_k > c->router_width) return MOE_ERR_INVALID_ARG;
+  if (c->scoring != MOE_SCORING_SOFTMAX && c->scoring != MOE_SCORING_SOFTMAX_BIAS)
+    return MOE_ERR_INVALID_ARG;
+  if (c->weight_dtype != MOE_W_BF16 && c->weight_dtype != MOE_W_FP8_E4M3_B128)
+    return MOE_ERR_INVALID_ARG;
+  if (c->path < MOE_PATH_AUTO || c->path > MOE_PATH_GROUPED) return MOE_ERR_INVALID_ARG;
+  // identity experts are wired only on the softmax + correction-bias arm
+  if (c->router_width != c->num_experts && c->scoring != MOE_SCORING_SOFTMAX_BIAS)
+    return MOE_ERR_UNSUPPORTED;
+  if (c->hidden % 128 || c->inter % 128 || c->shared_inter % 128) return MOE_ERR_UNSUPPORTED;
+  if (c->top_k > 32 || c->router_width > 1024 || c->num_experts > 1024) return MOE_ERR_UNSUPPORTED;
+  if (c->weight_dtype == MOE_W_FP8_E4M3_B128) return MOE_ERR_UNSUPPORTED;
+  const int path = resolve_path(c);
+  if (path == MOE_PATH_DECODE &&
+      (c->weight_dtype != MOE_W_BF16 || c->num_tokens > kDecodeMaxTokens || c->inter > 1024 ||
+       c->shared_inter > 1024))
+    return MOE_ERR_UNSUPPORTED;
+  const long long te = (long long)c->num_tokens * c->top_k;
+  if (te > (1ll << 30) || (long long)c->num_tokens * c->hidden > (1ll << 40))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+Layout make_layout(const moe_config_t* c) {
+  Layout L{};
+  const size_t N = c->num_tokens, H = c->hidden, E = c->num_experts, R = c->router_width;
+  const size_t K = c->top_k, I = c->inter, S = c->shared_inter;
+  const size_t te = N * K;
+  L.path = resolve_path(c);
+  L.te = (int)te;
+  L.nblk = (int)((te + 1023) / 1024);
+  L.max_mtiles = (int)((te < E ? te : E) + te / 128);
+  size_t sz[R_NUM] = {};
+  sz[R_HDR] = sizeof(WsHeader);
+  sz[R_LOGITS] = N * R * 4;
+  sz[R_IDX] = te * 4;
+  sz[R_W] = te * 4;
+  sz[R_ZSUM] = N * 4;
+  sz[R_OFFS] = (E + 1) * 4;
+  sz[R_P2R] = te * 4;
+  sz[R_SPAIRS] = te * 4;
+  sz[R_ACTIVE] = E * 4;
+  if (L.path == MOE_PATH_GROUPED) {
+    sz[R_BLK] = (size_t)L.nblk * E * 4;
+    sz[R_LRANK] = te * 4;
+    sz[R_TILES] = (size_t)L.max_mtiles * 16;
+    sz[R_XP] = te * H * 2;
+    sz[R_HH] = te * I * 2;
+    sz[R_Y] = te * H * 2;
+    sz[R_SHH] = N * S * 2;
+    sz[R_SHY] = S ? N * H * 2 : 0;
+  } else {
+    const size_t L2 = I > S ? I : S;
+    sz[R_HD] = (te + N) * L2 * 4;
+    if (c->deterministic) sz[R_YD] = te * H * 4;
+    else sz[R_ACC] = N * H * 4;
+    sz[R_SHY] = S ? N * H * 4 : 0;
+  }
+  size_t off = 0;
+  for (int r = 0; r < R_NUM; ++r) {
+    L.off[r] = off;
+    L.size[r] = sz[r];
+    off += align256(sz[r]);
+  }
+  L.total = off;
+  return L;
+}
+
+// ------------------------------------------------------------------ device attributes
+
+int g_num_sms[64];
+std::mutex g_mu;
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_num_sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    g_num_sms[dev] = n;
+  }
+  return g_num_sms[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool encode_fn() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return true;
+}
+
+// 2D bf16 map over a [rows, inner] row-major matrix; box {64, box_rows}, 128-byte swizzle,
+// zero fill outside the matrix.
+bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows,
+                   uint32_t box_rows) {
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+moe_status_t validate_weights(const moe_config_t* c, const moe_weights_t* w) {
+  if (!w || !w->router_w || !w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
+  if (c->scoring == MOE_SCORING_SOFTMAX_BIAS && !w->correction_bias) return MOE_ERR_INVALID_ARG;
+  if (c->weight_dtype == MOE_W_FP8_E4M3_B128 && (!w->s_gate || !w->s_up || !w->s_down))
+    return MOE_ERR_INVALID_ARG;
+  if (c->shared_inter > 0 && (!w->sh_gate || !w->sh_up || !w->sh_down)) return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {w->router_w, w->w_gate, w->w_up, w->w_down, w->sh_gate, w->sh_up,
+                      w->sh_down, w->sh_gate_vec};
+  for (const void* p : ps)
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+struct Marks {
+  void** ev;
+  cudaStream_t st;
+  void mark(int stage, int end) const {
+    if (ev && ev[2 * stage + end])
+      cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * stage + end]), st);
+  }
+};
+
+#define CK(expr)                                   \
+  do {                                             \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+struct Ptrs {
+  uint8_t* base;
+  const Layout* L;
+  template <typename T>
+  T* at(Region r) const {
+    return L->size[r] ? reinterpret_cast<T*>(base + L->off[r]) : nullptr;
+  }
+};
+
+// Router + top-K + sort (+ gather of x rows for the grouped chain).
+moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const void* x,
+                         const Ptrs& P, const uint32_t* forced, bool gather, cudaStream_t st) {
+  const Layout& L = *P.L;
+  WsHeader* hdr = P.at<WsHeader>(R_HDR);
+  RouteArgs ra{};
+  ra.x = static_cast<const __nv_bfloat16*>(x);
+  ra.router_w = static_cast<const __nv_bfloat16*>(w->router_w);
+  ra.logit_bias = w->router_logit_bias;
+  ra.corr_bias = c->scoring == MOE_SCORING_SOFTMAX_BIAS ? w->correction_bias : nullptr;
+  ra.forced = forced;
+  ra.N = c->num_tokens;
+  ra.H = c->hidden;
+  ra.E = c->num_experts;
+  ra.R = c->router_width;
+  ra.K = c->top_k;
+  ra.scoring = c->scoring;
+  ra.norm = c->norm_topk_prob;
+  ra.scale = c->routed_scaling_factor;
+  ra.logits = P.at<float>(R_LOGITS);
+  ra.idx = P.at<uint32_t>(R_IDX);
+  ra.w = P.at<float>(R_W);
+  ra.zsum = P.at<float>(R_ZSUM);
+  ra.hdr = hdr;
+  SortArgs sa{};
+  sa.idx = ra.idx;
+  sa.te = L.te;
+  sa.E = c->num_experts;
+  sa.K = c->top_k;
+  sa.blk_counts = P.at<uint32_t>(R_BLK);
+  sa.local_rank = P.at<uint32_t>(R_LRANK);
+  sa.offsets = P.at<uint32_t>(R_OFFS);
+  sa.pair_to_row = P.at<uint32_t>(R_P2R);
+  sa.sorted_pairs = P.at<uint32_t>(R_SPAIRS);
+  sa.active = P.at<uint32_t>(R_ACTIVE);
+  sa.tiles = P.at<int4>(R_TILES);
+  sa.hdr = hdr;
+
+  CK(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
+  if (L.path == MOE_PATH_DECODE) {
+    CK(launch_router_small(ra, sa, true, st));
+    return MOE_OK;
+  }
+  if (c->num_tokens <= kSmallRouterMaxTokens) {
+    CK(launch_router_small(ra, sa, false, st));
+  } else {
+    // router logits on the tensor cores: [N,H] x [R,H]^T -> fp32 [N,R]
+    CUtensorMap ma, mb;
+    if (!make_map_bf16(&ma, x, c->hidden, c->num_tokens, 128) ||
+        !make_map_bf16(&mb, w->router_w, c->hidden, c->router_width, 128))
+      return MOE_ERR_CUDA;
+    GemmArgs g{};
+    g.dense_m = c->num_tokens;
+    g.max_mtiles = (c->num_tokens + 127) / 128;
+    g.n_tiles = (c->router_width + 127) / 128;
+    g.num_kb = c->hidden / 64;
+    g.b_rows_per_expert = 0;
+    g.out = ra.logits;
+    g.ldo = c->router_width;
+    g.n_valid = c->router_width;
+    g.status = hdr;
+    CK(launch_gemm_bf16(kGemmStoreF32, 128, ma, mb, mb, g, num_sms(), st));
+  }
+  CK(launch_topk(ra, st));
+  CK(launch_sort(sa, ra.x, c->hidden, gather ? P.at<__nv_bfloat16>(R_XP) : nullptr, nullptr,
+                 nullptr, st));
+  return MOE_OK;
+}
+
+moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const void* x, void* out,
+                         const Ptrs& P, cudaStream_t st, const Marks& M) {
+  const Layout& L = *P.L;
+  const int N = c->num_tokens, H = c->hidden, E = c->num_experts, I = c->inter,
+            S = c->shared_inter;
+  WsHeader* hdr = P.at<WsHeader>(R_HDR);
+  const int sms = num_sms();
+  const int bn_h = (H % 256 == 0) ? 256 : 128;   // N-tile of the projections back to H
+  // shared expert: dense SwiGLU FFN on all N rows
+  M.mark(MOE_STAGE_SHARED, 0);
+  if (S > 0) {
+    CUtensorMap ma, mg, mu, mh, md;
+    if (!make_map_bf16(&ma, x, H, N, 128) || !make_map_bf16(&mg, w->sh_gate, H, S, 128) ||
+        !make_map_bf16(&mu, w->sh_up, H, S, 128) ||
+        !make_map_bf16(&mh, P.at<void>(R_SHH), S, N, 128) ||
+        !make_map_bf16(&md, w->sh_down, S, H, bn_h))
+      return MOE_ERR_CUDA;
+    GemmArgs g{};
+    g.dense_m = N;
+    g.max_mtiles = (N + 127) / 128;
+    g.n_tiles = S / 128;
+    g.num_kb = H / 64;
+    g.out = P.at<void>(R_SHH);
+    g.ldo = S;
+    g.status = hdr;
+    CK(launch_gemm_bf16(kGemmSwiGLU, 256, ma, mg, mu, g, sms, st));
+    g.n_tiles = H / bn_h;
+    g.num_kb = S / 64;
+    g.out = P.at<void>(R_SHY);
+    g.ldo = H;
+    CK(launch_gemm_bf16(kGemmStoreBF16, bn_h, mh, md, md, g, sms, st));
+  }
+  M.mark(MOE_STAGE_SHARED, 1);
+  // routed experts: grouped gate/up + SiLU*up, then grouped down, over the sorted rows
+  {
+    CUtensorMap ma, mg, mu, mh, md;
+    const uint64_t rows = (uint64_t)L.te;
+    if (!make_map_bf16(&ma, P.at<void>(R_XP), H, rows, 128) ||
+        !make_map_bf16(&mg, w->w_gate, H, (uint64_t)E * I, 128) ||
+        !make_map_bf16(&mu, w->w_up, H, (uint64_t)E * I, 128) ||
+        !make_map_bf16(&mh, P.at<void>(R_HH), I, rows, 128) ||
+        !make_map_bf16(&md, w->w_down, I, (uint64_t)E * H, bn_h))
+      return MOE_ERR_CUDA;
+    GemmArgs g{};
+    g.tiles = P.at<int4>(R_TILES);
+    g.hdr = hdr;
+    g.max_mtiles = L.max_mtiles;
+    g.n_tiles = I / 128;
+    g.num_kb = H / 64;
+    g.b_rows_per_expert = I;
+    g.out = P.at<void>(R_HH);
+    g.ldo = I;
+    g.status = hdr;
+    M.mark(MOE_STAGE_GATE_UP, 0);
+    CK(launch_gemm_bf16(kGemmSwiGLU, 256, ma, mg, mu, g, sms, st));
+    M.mark(MOE_STAGE_GATE_UP, 1);
+    g.n_tiles = H / bn_h;
+    g.num_kb = I / 64;
+    g.b_rows_per_expert = H;
+    g.out = P.at<void>(R_Y);
+    g.ldo = H;
+    M.mark(MOE_STAGE_DOWN, 0);
+    CK(launch_gemm_bf16(kGemmStoreBF16, bn_h, mh, md, md, g, sms, st));
+    M.mark(MOE_STAGE_DOWN, 1);
+  }
+  CombineArgs ca{};
+  ca.x = static_cast<const __nv_bfloat16*>(x);
+  ca.pair_to_row = P.at<uint32_t>(R_P2R);
+  ca.w = P.at<float>(R_W);
+  ca.zsum = P.at<float>(R_ZSUM);
+  ca.y = P.at<void>(R_Y);
+  ca.y_is_f32 = 0;
+  ca.shy = S > 0 ? P.at<void>(R_SHY) : nullptr;
+  ca.shy_is_f32 = 0;
+  ca.sh_gate_vec = static_cast<const __nv_bfloat16*>(w->sh_gate_vec);
+  ca.N = N;
+  ca.H = H;
+  ca.K = c->top_k;
+  ca.out = static_cast<__nv_bfloat16*>(out);
+  M.mark(MOE_STAGE_COMBINE, 0);
+  CK(launch_combine(ca, st));
+  M.mark(MOE_STAGE_COMBINE, 1);
+  return MOE_OK;
+}
+
+moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const void* x, void* out,
+                        const Ptrs& P, cudaStream_t st, const Marks& M) {
+  const Layout& L = *P.L;
+  const int N = c->num_tokens, H = c->hidden, S = c->shared_inter;
+  DecodeArgs d{};
+  d.x = static_cast<const __nv_bfloat16*>(x);
+  d.wg = static_cast<const __nv_bfloat16*>(w->w_gate);
+  d.wu = static_cast<const __nv_bfloat16*>(w->w_up);
+  d.wd = static_cast<const __nv_bfloat16*>(w->w_down);
+  d.sg = static_cast<const __nv_bfloat16*>(w->sh_gate);
+  d.su = static_cast<const __nv_bfloat16*>(w->sh_up);
+  d.sd = static_cast<const __nv_bfloat16*>(w->sh_down);
+  d.offsets = P.at<uint32_t>(R_OFFS);
+  d.sorted_pairs = P.at<uint32_t>(R_SPAIRS);
+  d.active = P.at<uint32_t>(R_ACTIVE);
+  d.w = P.at<float>(R_W);
+  d.N = N;
+  d.H = H;
+  d.E = c->num_experts;
+  d.K = c->top_k;
+  d.I = c->inter;
+  d.S = S;
+  d.te = L.te;
+  d.hd = P.at<float>(R_HD);
+  d.ldh = c->inter > S ? c->inter : S;
+  d.yd = P.at<float>(R_YD);
+  d.acc = P.at<float>(R_ACC);
+  d.shy = P.at<float>(R_SHY);
+  d.hdr = P.at<WsHeader>(R_HDR);
+  M.mark(MOE_STAGE_SHARED, 0);
+  M.mark(MOE_STAGE_SHARED, 1);
+  M.mark(MOE_STAGE_GATE_UP, 0);
+  if (d.acc) CK(cudaMemsetAsync(d.acc, 0, (size_t)N * H * 4, st));
+  CK(launch_decode_gateup(d, st));
+  M.mark(MOE_STAGE_GATE_UP, 1);
+  M.mark(MOE_STAGE_DOWN, 0);
+  CK(launch_decode_down(d, st));
+  M.mark(MOE_STAGE_DOWN, 1);
+  CombineArgs ca{};
+  ca.x = d.x;
+  ca.pair_to_row = P.at<uint32_t>(R_P2R);
+  ca.w = d.w;
+  ca.zsum = P.at<float>(R_ZSUM);
+  ca.y = d.yd;
+  ca.y_is_f32 = 1;
+  ca.acc = d.acc;
+  ca.shy = S > 0 ? d.shy : nullptr;
+  ca.shy_is_f32 = 1;
+  ca.sh_gate_vec = static_cast<const __nv_bfloat16*>(w->sh_gate_vec);
+  ca.N = N;
+  ca.H = H;
+  ca.K = c->top_k;
+  ca.out = static_cast<__nv_bfloat16*>(out);
+  M.mark(MOE_STAGE_COMBINE, 0);
+  CK(launch_combine(ca, st));
+  M.mark(MOE_STAGE_COMBINE, 1);
+  return MOE_OK;
+}
+
+moe_status_t check_call(const moe_config_t* cfg, const moe_weights_t* w, const void* x,
+                        void* workspace, size_t workspace_bytes, Layout* L) {
+  moe_status_t s = validate_config(cfg);
+  if (s != MOE_OK) return s;
+  s = validate_weights(cfg, w);
+  if (s != MOE_OK) return s;
+  *L = make_layout(cfg);
+  if (cfg->num_tokens == 0) return MOE_OK;
+  if (!x || !workspace || !aligned16(x)) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < L->total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!encode_fn()) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t forward_impl(const moe_config_t* cfg, const moe_weights_t* weights, const void* x,
+                          void* out, void* workspace, size_t workspace_bytes, void* stream,
+                          uint32_t* topk_idx_out, float* topk_w_out, const uint32_t* forced_idx,
+                          void** events) {
+  Layout L;
+  moe_status_t s = check_call(cfg, weights, x, workspace, workspace_bytes, &L);
+  if (s != MOE_OK) return s;
+  if (cfg->num_tokens == 0) return MOE_OK;
+  if (!out || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Ptrs P{static_cast<uint8_t*>(workspace), &L};
+  Marks M{events, st};
+  M.mark(MOE_STAGE_ROUTE, 0);
+  s = run_routing(cfg, weights, x, P, forced_idx, L.path == MOE_PATH_GROUPED, st);
+  if (s != MOE_OK) return s;
+  M.mark(MOE_STAGE_ROUTE, 1);
+  s = L.path == MOE_PATH_GROUPED ? run_grouped(cfg, weights, x, out, P, st, M)
+                                 : run_decode(cfg, weights, x, out, P, st, M);
+  if (s != MOE_OK) return s;
+  const size_t te = (size_t)L.te;
+  if (topk_idx_out)
+    CK(cudaMemcpyAsync(topk_idx_out, P.at<void>(R_IDX), te * 4, cudaMemcpyDeviceToDevice, st));
+  if (topk_w_out)
+    CK(cudaMemcpyAsync(topk_w_out, P.at<void>(R_W), te * 4, cudaMemcpyDeviceToDevice, st));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* weights, const void* x,
+                         void* out, void* workspace, size_t workspace_bytes, void* stream,
+                         uint32_t* topk_idx_out, float* topk_w_out, const uint32_t* forced_idx) {
+  return forward_impl(cfg, weights, x, out, workspace, workspace_bytes, stream, topk_idx_out,
+                      topk_w_out, forced_idx, nullptr);
+}
+
+moe_status_t moe_forward_profiled(const moe_config_t* cfg, const moe_weights_t* weights,
+                                  const void* x, void* out, void* workspace,
+                                  size_t workspace_bytes, void* stream, void** events) {
+  return forward_impl(cfg, weights, x, out, workspace, workspace_bytes, stream, nullptr, nullptr,
+                      nullptr, events);
+}
+
+
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  moe_status_t s = validate_config(cfg);
+  if (s != MOE_OK) return s;
+  *bytes = make_layout(cfg).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const moe_weights_t* weights, const void* x,
+                       void* workspace, size_t workspace_bytes, void* stream, uint32_t* idx_out,
+                       float* w_out, float* zsum_out, uint32_t* offsets_out,
+                       uint32_t* sorted_pairs_out, uint32_t* pair_to_row_out) {
+  Layout L;
+  moe_status_t s = check_call(cfg, weights, x, workspace, workspace_bytes, &L);
+  if (s != MOE_OK) return s;
+  if (cfg->num_tokens == 0) return MOE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Ptrs P{static_cast<uint8_t*>(workspace), &L};
+  s = run_routing(cfg, weights, x, P, nullptr, false, st);
+  if (s != MOE_OK) return s;
+  const size_t te = (size_t)L.te, N = cfg->num_tokens, E = cfg->num_experts;
+  struct Copy { void* dst; Region r; size_t bytes; } copies[] = {
+      {idx_out, R_IDX, te * 4},        {w_out, R_W, te * 4},
+      {zsum_out, R_ZSUM, N * 4},       {offsets_out, R_OFFS, (E + 1) * 4},
+      {sorted_pairs_out, R_SPAIRS, te * 4}, {pair_to_row_out, R_P2R, te * 4}};
+  for (const Copy& cp : copies)
+    if (cp.dst)
+      CK(cudaMemcpyAsync(cp.dst, P.at<void>(cp.r), cp.bytes, cudaMemcpyDeviceToDevice, st));
+  return MOE_OK;
+}
+
+moe_status_t moe_read_device_status(const void* workspace, void* stream, int32_t* status) {
+  if (!workspace || !status) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CK(cudaStreamSynchronize(st));
+  CK(cudaMemcpy(status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

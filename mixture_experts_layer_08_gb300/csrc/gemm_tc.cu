@@ -1,0 +1,275 @@
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05) for sm_103a.
+//
+// D[rows of expert e, n-tile] = A[rows, K] . B_e[n-tile rows, K]^T over the expert-sorted
+// rows, with the epilogue fused: SiLU(gate) * up -> bf16 (gate/up projection), plain bf16
+// store (down projection, shared expert), or fp32 store (router logits).
+//
+// Pages: "metrale_model_layers/layers/moe/forward_prefill.rs" (`run_routed_grouped_gemm`:
+// grouped gate/up GEMM, activation and grouped down GEMM over the rows sorted by expert,
+// the sorted result left for the unpermute; the shared expert as a dense FFN on all rows).
+//
+// Design (one persistent CTA per SM, 192 threads):
+//   warp 0      TMA producer: A tile 128 x 64 and B tile BN x 64 (bf16, 128-byte swizzle)
+//               per stage into a ring of kStages stages.
+//   warp 1      allocates TMEM (2 x BN fp32 columns: two accumulators), one lane issues
+//               tcgen05.mma (M=128, N=BN, K=16) x 4 per stage and commits stage releases.
+//   warps 2-5   epilogue: tcgen05.ld of the finished accumulator (warp w reads TMEM lanes
+//               32*(w%4)...), fused activation, masked stores; releases the accumulator so the
+//               MMA of the next tile overlaps this epilogue.
+// Tiles are (m-tile, n-tile) pairs, m-tiles taken from the device-built list of 128-row
+// windows of each expert; n is the fastest index so the CTAs working at the same time share
+// A rows and the same expert's weights in L2.
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;
+constexpr int kBK = 64;                 // bf16 elements per 128-byte swizzle row
+constexpr int kATileBytes = kBM * 128;  // 16 KB
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kBTileBytes = BN * 128;
+  static constexpr int kStageBytes = kATileBytes + kBTileBytes;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024 + 256;
+};
+
+__device__ __forceinline__ void tile_coords(const GemmArgs& g, int tile, int& e, int& row0,
+                                            int& row1, int& n) {
+  const int m = tile / g.n_tiles;
+  n = tile % g.n_tiles;
+  if (g.tiles) {
+    const int4 t = g.tiles[m];
+    e = t.x;
+    row0 = t.y;
+    row1 = t.z;
+  } else {
+    e = 0;
+    row0 = m * kBM;
+    row1 = min(g.dense_m, row0 + kBM);
+  }
+}
+
+template <int BN, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tm_a,
+                     const __grid_constant__ CUtensorMap tm_b0,
+                     const __grid_constant__ CUtensorMap tm_b1, const GemmArgs g) {
+  using C = Cfg<BN>;
+  constexpr int S = C::kStages;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte swizzle atoms
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + S * kATileBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  WsHeader* hdr = g.status;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
+    }
+    mbar_init(drain, 1);
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_b0);
+    if (MODE == kGemmSwiGLU) tma_prefetch_desc(&tm_b1);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_m = g.tiles ? (int)g.hdr->num_mtiles : (g.dense_m + kBM - 1) / kBM;
+  const int total = num_m * g.n_tiles;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------ TMA producer
+    int s = 0;
+    uint32_t ph = 0;
+    long long issued = 0;
+    bool ok = true;
+    constexpr int b_rows = MODE == kGemmSwiGLU ? BN / 2 : BN;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int e, row0, row1, n;
+      tile_coords(g, tile, e, row0, row1, n);
+      const int brow = e * g.b_rows_per_expert + n * b_rows;
+      for (int kb = 0; kb < g.num_kb; ++kb) {
+        if (!mbar_wait(&empty[s], ph ^ 1, hdr)) { ok = false; break; }
+        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+        tma_load_2d(sA + s * kATileBytes, &tm_a, kb * kBK, row0, &full[s]);
+        tma_load_2d(sB + s * C::kBTileBytes, &tm_b0, kb * kBK, brow, &full[s]);
+        if (MODE == kGemmSwiGLU)
+          tma_load_2d(sB + s * C::kBTileBytes + (BN / 2) * 128, &tm_b1, kb * kBK, brow, &full[s]);
+        ++issued;
+        if (++s == S) { s = 0; ph ^= 1; }
+      }
+    }
+    if (!ok) {
+      // let the copies already issued land before the CTA can exit
+      for (long long i = issued > S ? issued - S : 0; i < issued; ++i)
+        mbar_wait(&full[i % S], (uint32_t)((i / S) & 1), nullptr);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_make(kBM, BN, 1, 1);
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      if (!mbar_wait(&tempty[acc], ((it >> 1) & 1) ^ 1, hdr)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d = tmem_base + acc * BN;
+      for (int kb = 0; kb < g.num_kb; ++kb) {
+        if (!mbar_wait(&full[s], ph, hdr)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sA + s * kATileBytes);
+        const uint32_t b0 = smem_u32(sB + s * C::kBTileBytes);
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k) {
+          tc_mma_bf16(d, sdesc_k_sw128(a0 + k * 32), sdesc_k_sw128(b0 + k * 32), idesc,
+                      (kb | k) != 0 ? 1u : 0u);
+        }
+        tc_commit(&empty[s]);
+        if (++s == S) { s = 0; ph ^= 1; }
+      }
+      if (ok) tc_commit(&tfull[acc]);
+    }
+    // all MMAs of this thread complete before TMEM can be released
+    tc_commit(drain);
+    mbar_wait(drain, 0, hdr);
+  } else if (warp >= 2) {
+    // ------------------------------------------------ epilogue
+    const int q = warp & 3;                  // TMEM lane quadrant of this warp
+    const int r_local = q * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+      int e, row0, row1, n;
+      tile_coords(g, tile, e, row0, row1, n);
+      const int acc = it & 1;
+      if (!mbar_wait(&tfull[acc], (it >> 1) & 1, hdr)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      const int row = row0 + r_local;
+      const bool valid = row < row1;
+      if (MODE == kGemmSwiGLU) {
+        __nv_bfloat16* orow =
+            static_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + n * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          float gv[32], uv[32];
+          tmem_ld32(taddr + c, gv);
+          tmem_ld32(taddr + BN / 2 + c, uv);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 o;
+              o.x = pack_bf16x2(silu(gv[8 * v + 0]) * uv[8 * v + 0], silu(gv[8 * v + 1]) * uv[8 * v + 1]);
+              o.y = pack_bf16x2(silu(gv[8 * v + 2]) * uv[8 * v + 2], silu(gv[8 * v + 3]) * uv[8 * v + 3]);
+              o.z = pack_bf16x2(silu(gv[8 * v + 4]) * uv[8 * v + 4], silu(gv[8 * v + 5]) * uv[8 * v + 5]);
+              o.w = pack_bf16x2(silu(gv[8 * v + 6]) * uv[8 * v + 6], silu(gv[8 * v + 7]) * uv[8 * v + 7]);
+              dst[v] = o;
+            }
+          }
+        }
+      } else if (MODE == kGemmStoreBF16) {
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + n * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(taddr + c, v);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint4 o;
+              o.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+              o.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+              o.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+              o.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+              dst[j] = o;
+            }
+          }
+        }
+      } else {
+        float* orow = static_cast<float*>(g.out) + (size_t)row * g.ldo;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(taddr + c, v);
+          if (valid) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int col = n * BN + c + j;
+              if (col < g.n_valid) orow[col] = v[j];
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+template <int BN, int MODE>
+cudaError_t launch_t(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                     const GemmArgs& g, int num_sms, cudaStream_t st) {
+  using C = Cfg<BN>;
+  auto kern = gemm_bf16_kernel<BN, MODE>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int max_tiles = g.max_mtiles * g.n_tiles;
+  int grid = max_tiles < num_sms ? max_tiles : num_sms;
+  if (grid < 1) grid = 1;
+  kern<<<grid, kThreads, C::kSmemBytes, st>>>(a, b0, b1, g);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_bf16(int mode, int bn, const CUtensorMap& a, const CUtensorMap& b0,
+                             const CUtensorMap& b1, const GemmArgs& g, int num_sms,
+                             cudaStream_t st) {
+  if (bn == 256) {
+    if (mode == kGemmSwiGLU) return launch_t<256, kGemmSwiGLU>(a, b0, b1, g, num_sms, st);
+    if (mode == kGemmStoreBF16) return launch_t<256, kGemmStoreBF16>(a, b0, b1, g, num_sms, st);
+  } else if (bn == 128) {
+    if (mode == kGemmSwiGLU) return launch_t<128, kGemmSwiGLU>(a, b0, b1, g, num_sms, st);
+    if (mode == kGemmStoreBF16) return launch_t<128, kGemmStoreBF16>(a, b0, b1, g, num_sms, st);
+    if (mode == kGemmStoreF32) return launch_t<128, kGemmStoreF32>(a, b0, b1, g, num_sms, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -1,0 +1,113 @@
+// Host-side launchers of the MoE kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+struct RouteArgs {
+  const __nv_bfloat16* x;          // [N,H]
+  const __nv_bfloat16* router_w;   // [R,H]
+  const float* logit_bias;         // [R] or null
+  const float* corr_bias;          // [R] or null (selection only)
+  const uint32_t* forced;          // [N,K] or null
+  int N, H, E, R, K, scoring, norm;
+  float scale;
+  float* logits;                   // [N,R]
+  uint32_t* idx;                   // [N,K]
+  float* w;                        // [N,K]
+  float* zsum;                     // [N]
+  WsHeader* hdr;
+};
+
+struct SortArgs {
+  const uint32_t* idx;             // [te]
+  int te, E, K;
+  uint32_t* blk_counts;            // [ceil(te/1024), E]
+  uint32_t* local_rank;            // [te]
+  uint32_t* offsets;               // [E+1]
+  uint32_t* pair_to_row;           // [te]
+  uint32_t* sorted_pairs;          // [te]
+  uint32_t* active;                // [E] experts with rows, ascending
+  int4* tiles;                     // [max m-tiles] (expert, row0, row1, 0)
+  WsHeader* hdr;
+};
+
+// Router logits (warp per router column, up to 16 tokens per block) followed, when
+// `fuse_tail` is set (N <= 16), by top-K of every token and the stable sort in the last
+// block to finish. Otherwise only the logits are written.
+cudaError_t launch_router_small(const RouteArgs& a, const SortArgs& s, bool fuse_tail,
+                                cudaStream_t st);
+// Scoring + top-K + weights, one warp per token.
+cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st);
+// Stable counting sort of the (token, slot) pairs by expert (count / scan / scatter) and the
+// m-tile list of the grouped GEMM. Scatter also gathers x rows (bf16) into `xp` when given,
+// or quantises them per 1x128 to E4M3 into `xq` + `xs` (kb-major scales [H/128, te]).
+cudaError_t launch_sort(const SortArgs& s, const __nv_bfloat16* x, int H, __nv_bfloat16* xp,
+                        uint8_t* xq, float* xs, cudaStream_t st);
+
+// Decode chain: gate/up GEMV (+ SiLU*up) over the active experts and the shared expert.
+struct DecodeArgs {
+  const __nv_bfloat16* x;          // [N,H]
+  const __nv_bfloat16 *wg, *wu, *wd;   // [E,I,H], [E,I,H], [E,H,I]
+  const __nv_bfloat16 *sg, *su, *sd;   // [S,H], [S,H], [H,S] or null
+  const uint32_t* offsets;
+  const uint32_t* sorted_pairs;
+  const uint32_t* active;
+  const float* w;                  // routing weights [N,K]
+  int N, H, E, K, I, S, te;
+  float* hd;                       // [te + N, max(I,S)] fp32 SwiGLU outputs (row = sorted row,
+                                   // shared rows te + t)
+  int ldh;
+  float* yd;                       // [te, H] fp32 (deterministic) or null
+  float* acc;                      // [N, H] fp32 atomic accumulator or null
+  float* shy;                      // [N, H] fp32 shared expert output
+  WsHeader* hdr;
+};
+cudaError_t launch_decode_gateup(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_decode_down(const DecodeArgs& a, cudaStream_t st);
+
+// out[t] = sum_k w[t,k] * Y[pair_to_row[t,k]] (+ acc[t]) + zsum[t] * x[t] + gamma_t * shy[t]
+struct CombineArgs {
+  const __nv_bfloat16* x;
+  const uint32_t* pair_to_row;
+  const float* w;
+  const float* zsum;
+  const void* y;                   // [rows, H] bf16 (y_is_f32 = 0) or fp32; may be null
+  int y_is_f32;
+  const float* acc;                // [N,H] or null
+  const void* shy;                 // [N,H] bf16 or fp32 (shy_is_f32) or null
+  int shy_is_f32;
+  const __nv_bfloat16* sh_gate_vec;    // [H] or null
+  int N, H, K;
+  __nv_bfloat16* out;
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
+
+// tcgen05 grouped GEMM. Epilogue modes.
+enum GemmMode { kGemmSwiGLU = 0, kGemmStoreBF16 = 1, kGemmStoreF32 = 2 };
+
+struct GemmArgs {
+  const int4* tiles;               // m-tile list, or null for a dense problem
+  const WsHeader* hdr;             // number of m-tiles when `tiles` is given
+  int dense_m;                     // rows of the dense problem
+  int max_mtiles;                  // upper bound on m-tiles (grid sizing)
+  int n_tiles;                     // output tiles along N per m-tile
+  int num_kb;                      // contraction blocks of 64 (bf16)
+  int b_rows_per_expert;           // rows of one expert in the B tensor map
+  void* out;
+  int ldo;                         // elements
+  int n_valid;                     // valid output columns (fp32 store mode)
+  WsHeader* status;
+};
+// A: [rows, K] bf16 map, box {64, 128}; B0 (and B1 for SwiGLU): [rows, K] bf16, box {64,
+// BN/2 (SwiGLU) or BN}.
+cudaError_t launch_gemm_bf16(int mode, int bn, const CUtensorMap& a, const CUtensorMap& b0,
+                             const CUtensorMap& b1, const GemmArgs& g, int num_sms,
+                             cudaStream_t st);
+
+}  // namespace moe

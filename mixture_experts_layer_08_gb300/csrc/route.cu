@@ -1,0 +1,442 @@
+// Routing: router logits, softmax (+ selection-only correction bias) top-K with
+// renormalisation and identity-expert fold, and the stable sort of (token, slot) pairs by
+// expert.
+//
+// Pages: "metrale_model_layers/layers/moe/forward_prefill.rs" (`forward_prefill`: the gate
+// GEMM keeps a fixed accumulation order; `moe_topk_softmax_batched` with `norm_topk_prob`;
+// `moe_sort_by_expert` writes sorted ids, expert offsets [E+1] and token_to_perm [te]),
+// "spark_model/layers/moe/forward.rs" (`forward`: softmax scores + correction bias for
+// selection, unbiased softmax x scaling for the weights, selected identity experts folded
+// into zero_accum; the single-CTA fused gate+top-K was too slow for 256 experts, so here
+// routing is one warp per token and the router spreads its columns over many blocks).
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+// Does candidate (va, ia) rank before (vb, ib)? Higher score first, lower id on a tie.
+__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// One warp routes one token. `L` is the token's fp32 logit row; `p` and `sel` are per-warp
+// shared scratch of R floats. Lane k < K writes slot k of idx/w; lane 0 writes zsum.
+__device__ void route_token_warp(const float* L, const float* logit_bias, const float* corr_bias,
+                                 int R, int E, int K, int scoring, int norm, float scale,
+                                 const uint32_t* forced, float* p, float* sel, uint32_t* idx_out,
+                                 float* w_out, float* zsum_out, uint32_t* idx_smem) {
+  const int lane = threadIdx.x & 31;
+  float mx = -INFINITY;
+  for (int r = lane; r < R; r += 32) {
+    float v = __ldcg(L + r) + (logit_bias ? logit_bias[r] : 0.0f);
+    p[r] = v;
+    mx = fmaxf(mx, v);
+  }
+  mx = warp_max(mx);
+  float den = 0.0f;
+  for (int r = lane; r < R; r += 32) {
+    float e = expf(p[r] - mx);
+    p[r] = e;
+    den += e;
+  }
+  den = warp_sum(den);
+  for (int r = lane; r < R; r += 32) {
+    float pr = p[r] / den;
+    p[r] = pr;
+    sel[r] = pr + ((scoring == MOE_SCORING_SOFTMAX_BIAS && corr_bias) ? corr_bias[r] : 0.0f);
+  }
+  __syncwarp();
+  uint32_t my_idx = 0;
+  for (int k = 0; k < K; ++k) {
+    int best;
+    if (forced) {
+      best = (int)forced[k];
+    } else {
+      float bv = -INFINITY;
+      best = 0x7fffffff;
+      for (int r = lane; r < R; r += 32) {
+        float v = sel[r];
+        if (ranks_before(v, r, bv, best)) { bv = v; best = r; }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        int oi = __shfl_xor_sync(0xffffffffu, best, o);
+        if (ranks_before(ov, oi, bv, best)) { bv = ov; best = oi; }
+      }
+      __syncwarp();
+      if (lane == 0) sel[best] = -INFINITY;   // taken
+      __syncwarp();
+    }
+    if (lane == k) my_idx = (uint32_t)best;
+  }
+  // weights: unbiased probabilities of the chosen ids, renormalised over all K slots
+  float wk = (lane < K) ? p[my_idx] : 0.0f;
+  float sum = warp_sum(wk);
+  if (norm) wk = wk / sum;
+  wk *= scale;
+  float z = (lane < K && (int)my_idx >= E) ? wk : 0.0f;
+  z = warp_sum(z);
+  if (lane < K) {
+    idx_out[lane] = my_idx;
+    w_out[lane] = wk;
+    if (idx_smem) idx_smem[lane] = my_idx;
+  }
+  if (lane == 0) *zsum_out = z;
+}
+
+// ------------------------------------------------------------------ small-N router
+
+constexpr int kRouterWarps = 8;      // router columns per block
+constexpr int kRouterTok = 16;       // tokens per block
+
+// Block-wide exclusive scan of one value per thread (blockDim.x <= 1024, multiple of 32).
+__device__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_tot, uint32_t* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  uint32_t inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) warp_tot[wid] = inc;
+  __syncthreads();
+  if (wid == 0) {
+    uint32_t t = lane < nw ? warp_tot[lane] : 0;
+    uint32_t ti = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t n = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) ti += n;
+    }
+    if (lane < nw) warp_tot[lane] = ti - t;
+    if (lane == 31 && total) *total = ti;
+  }
+  __syncthreads();
+  uint32_t r = warp_tot[wid] + inc - v;
+  __syncthreads();
+  return r;
+}
+
+// Stable sort of te <= 1024 * k pairs inside one block (used by the fused decode tail).
+// idx_s: the pair expert ids in shared memory.
+__device__ void sort_in_block(const uint32_t* idx_s, int te, int E, int K, uint32_t* cnt_s,
+                              uint32_t* scan_s, const SortArgs& s) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = 0;
+  __syncthreads();
+  for (int j = threadIdx.x; j < te; j += blockDim.x) {
+    uint32_t e = idx_s[j];
+    if ((int)e < E) atomicAdd(&cnt_s[e], 1u);
+  }
+  __syncthreads();
+  // exclusive scans of counts (row offsets) and of the "has rows" flags (active list),
+  // E <= 1024 handled in chunks of blockDim
+  uint32_t run_off = 0, run_act = 0;
+  for (int base = 0; base < E; base += blockDim.x) {
+    int e = base + threadIdx.x;
+    uint32_t c = e < E ? cnt_s[e] : 0;
+    uint32_t tot_c, tot_a;
+    uint32_t off = block_excl_scan(c, scan_s, &scan_s[32]);
+    tot_c = scan_s[32];
+    __syncthreads();
+    uint32_t act = block_excl_scan(c > 0 ? 1u : 0u, scan_s, &scan_s[32]);
+    tot_a = scan_s[32];
+    __syncthreads();
+    if (e < E) {
+      s.offsets[e] = run_off + off;
+      if (c > 0) s.active[run_act + act] = (uint32_t)e;
+      cnt_s[e] = run_off + off;     // becomes the row base of expert e
+    }
+    run_off += tot_c;
+    run_act += tot_a;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    s.offsets[E] = run_off;
+    s.hdr->num_active = run_act;
+  }
+  __syncthreads();
+  // rank of each pair among the earlier pairs of its expert (stable in the pair index)
+  for (int j = threadIdx.x; j < te; j += blockDim.x) {
+    uint32_t e = idx_s[j];
+    if ((int)e >= E) {
+      s.pair_to_row[j] = kNoRow;
+      continue;
+    }
+    uint32_t rank = 0;
+    for (int i = 0; i < j; ++i) rank += (idx_s[i] == e) ? 1u : 0u;
+    uint32_t row = cnt_s[e] + rank;
+    s.pair_to_row[j] = row;
+    s.sorted_pairs[row] = (uint32_t)j;
+  }
+}
+
+__global__ void __launch_bounds__(256) router_small_kernel(RouteArgs a, SortArgs s,
+                                                           int fuse_tail) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);     // [tok, H]
+  const int H = a.H, R = a.R;
+  const int tok0 = blockIdx.y * kRouterTok;
+  const int ntok = min(kRouterTok, a.N - tok0);
+  // stage the block's tokens in shared memory (16-byte chunks)
+  const int chunks = H / 8;
+  for (int i = threadIdx.x; i < ntok * chunks; i += blockDim.x) {
+    int t = i / chunks, c = i % chunks;
+    reinterpret_cast<uint4*>(xs)[t * chunks + c] =
+        reinterpret_cast<const uint4*>(a.x + (size_t)(tok0 + t) * H)[c];
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int r = blockIdx.x * kRouterWarps + wid;
+  if (r < R) {
+    float acc[kRouterTok];
+#pragma unroll
+    for (int t = 0; t < kRouterTok; ++t) acc[t] = 0.0f;
+    const uint4* wrow = reinterpret_cast<const uint4*>(a.router_w + (size_t)r * H);
+    for (int c = lane; c < chunks; c += 32) {
+      float wf[8];
+      bf16x8_to_f32(wrow[c], wf);
+#pragma unroll
+      for (int t = 0; t < kRouterTok; ++t) {
+        if (t < ntok) {
+          float xf[8];
+          bf16x8_to_f32(reinterpret_cast<const uint4*>(xs)[t * chunks + c], xf);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[t] = fmaf(wf[i], xf[i], acc[t]);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kRouterTok; ++t) {
+      if (t < ntok) {
+        float v = warp_sum(acc[t]);
+        if (lane == 0) a.logits[(size_t)(tok0 + t) * R + r] = v;
+      }
+    }
+  }
+  if (!fuse_tail) return;
+  // ---- last block to finish: top-K of every token and the stable sort (N <= 16)
+  __shared__ uint32_t is_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t prev = atomicAdd(&a.hdr->done_blocks, 1u);
+    is_last = (prev == gridDim.x * gridDim.y - 1) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  float* pbuf = reinterpret_cast<float*>(smem);                   // [8 warps][R] probs
+  float* sbuf = pbuf + kRouterWarps * R;                          // [8 warps][R] scores
+  uint32_t* idx_s = reinterpret_cast<uint32_t*>(sbuf + kRouterWarps * R);   // [te]
+  uint32_t* cnt_s = idx_s + a.N * a.K;                            // [E]
+  uint32_t* scan_s = cnt_s + a.E;                                 // [33]
+  for (int t = wid; t < a.N; t += kRouterWarps) {
+    route_token_warp(a.logits + (size_t)t * R, a.logit_bias, a.corr_bias, R, a.E, a.K,
+                     a.scoring, a.norm, a.scale, a.forced ? a.forced + (size_t)t * a.K : nullptr,
+                     pbuf + wid * R, sbuf + wid * R, a.idx + (size_t)t * a.K,
+                     a.w + (size_t)t * a.K, a.zsum + t, idx_s + t * a.K);
+  }
+  __syncthreads();
+  sort_in_block(idx_s, a.N * a.K, a.E, a.K, cnt_s, scan_s, s);
+  if (threadIdx.x == 0) a.hdr->done_blocks = 0;
+}
+
+__global__ void __launch_bounds__(256) topk_kernel(RouteArgs a) {
+  extern __shared__ __align__(16) float sm[];
+  const int wid = threadIdx.x >> 5;
+  const int t = blockIdx.x * 8 + wid;
+  if (t >= a.N) return;
+  float* p = sm + wid * 2 * a.R;
+  route_token_warp(a.logits + (size_t)t * a.R, a.logit_bias, a.corr_bias, a.R, a.E, a.K,
+                   a.scoring, a.norm, a.scale, a.forced ? a.forced + (size_t)t * a.K : nullptr,
+                   p, p + a.R, a.idx + (size_t)t * a.K, a.w + (size_t)t * a.K, a.zsum + t,
+                   nullptr);
+}
+
+// ------------------------------------------------------------------ large-N sort
+
+constexpr int kSortBlock = 1024;
+
+// Per block of 1024 pairs: per-expert counts and each pair's rank among the block's earlier
+// pairs of the same expert.
+__global__ void __launch_bounds__(kSortBlock) sort_count_kernel(SortArgs s) {
+  extern __shared__ uint32_t wcnt[];                 // [32 warps][E]
+  const int E = s.E;
+  const int j = blockIdx.x * kSortBlock + threadIdx.x;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < 32 * E; i += kSortBlock) wcnt[i] = 0;
+  __syncthreads();
+  uint32_t e = j < s.te ? s.idx[j] : kNoRow;
+  bool real = e != kNoRow && e < (uint32_t)E;
+  uint32_t key = real ? e : kNoRow;
+  uint32_t peers = __match_any_sync(0xffffffffu, key);
+  uint32_t lt = (1u << lane) - 1u;
+  uint32_t rank_w = __popc(peers & lt);
+  if (real && rank_w == 0) wcnt[wid * E + e] = __popc(peers);
+  __syncthreads();
+  for (int ex = threadIdx.x; ex < E; ex += kSortBlock) {
+    uint32_t run = 0;
+    for (int w = 0; w < 32; ++w) {
+      uint32_t c = wcnt[w * E + ex];
+      wcnt[w * E + ex] = run;
+      run += c;
+    }
+    s.blk_counts[(size_t)blockIdx.x * E + ex] = run;
+  }
+  __syncthreads();
+  if (j < s.te) s.local_rank[j] = real ? wcnt[wid * E + e] + rank_w : kNoRow;
+}
+
+// One block: expert totals, row offsets, per-block bases (in place), m-tile list, active list.
+__global__ void __launch_bounds__(1024) sort_scan_kernel(SortArgs s, int nblk) {
+  __shared__ uint32_t scan_s[40];
+  const int E = s.E;
+  uint32_t run_off = 0, run_act = 0, run_tiles = 0;
+  for (int base = 0; base < E; base += blockDim.x) {
+    int e = base + threadIdx.x;
+    uint32_t c = 0;
+    if (e < E)
+      for (int b = 0; b < nblk; ++b) c += s.blk_counts[(size_t)b * E + e];
+    uint32_t off = block_excl_scan(c, scan_s, &scan_s[32]);
+    uint32_t tot_c = scan_s[32];
+    __syncthreads();
+    uint32_t act = block_excl_scan(c > 0 ? 1u : 0u, scan_s, &scan_s[32]);
+    uint32_t tot_a = scan_s[32];
+    __syncthreads();
+    uint32_t nt = (c + 127) / 128;
+    uint32_t tstart = block_excl_scan(nt, scan_s, &scan_s[32]);
+    uint32_t tot_t = scan_s[32];
+    __syncthreads();
+    if (e < E) {
+      uint32_t o = run_off + off;
+      s.offsets[e] = o;
+      if (c > 0) s.active[run_act + act] = (uint32_t)e;
+      uint32_t r = o;
+      for (int b = 0; b < nblk; ++b) {
+        uint32_t cb = s.blk_counts[(size_t)b * E + e];
+        s.blk_counts[(size_t)b * E + e] = r;
+        r += cb;
+      }
+      for (uint32_t i = 0; i < nt; ++i) {
+        uint32_t r0 = o + 128 * i;
+        uint32_t r1 = min(o + c, r0 + 128);
+        s.tiles[run_tiles + tstart + i] = make_int4(e, (int)r0, (int)r1, 0);
+      }
+    }
+    run_off += tot_c;
+    run_act += tot_a;
+    run_tiles += tot_t;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    s.offsets[E] = run_off;
+    s.hdr->num_active = run_act;
+    s.hdr->num_mtiles = run_tiles;
+  }
+}
+
+// One warp per pair: final row, inverse map, and the gathered (or quantised) x row.
+__global__ void __launch_bounds__(256) sort_scatter_kernel(SortArgs s, const __nv_bfloat16* x,
+                                                           int H, __nv_bfloat16* xp,
+                                                           uint8_t* xq, float* xsc) {
+  const int lane = threadIdx.x & 31;
+  const int j = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (j >= s.te) return;
+  uint32_t e = s.idx[j];
+  if ((int)e >= s.E) {
+    if (lane == 0) s.pair_to_row[j] = kNoRow;
+    return;
+  }
+  uint32_t row = s.blk_counts[(size_t)(j / kSortBlock) * s.E + e] + s.local_rank[j];
+  if (lane == 0) {
+    s.pair_to_row[j] = row;
+    s.sorted_pairs[row] = (uint32_t)j;
+  }
+  const int t = j / s.K;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  if (xp) {
+    uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)row * H);
+    for (int c = lane; c < H / 8; c += 32) dst[c] = src[c];
+  }
+  if (xq) {
+    // 1x128 groups: 16 lanes x 8 values; amax, scale = amax/448 (1 if 0), code = e4m3(v/scale)
+    const int te_stride = s.te;
+    for (int c0 = 0; c0 < H / 8; c0 += 32) {
+      const int c = c0 + lane;
+      const bool on = c < H / 8;
+      float f[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = 0.0f;
+      if (on) bf16x8_to_f32(src[c], f);
+      float am = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      const float sc = am > 0.0f ? __fdiv_rn(am, 448.0f) : 1.0f;
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int i = 0; i < 4; i += 2) {
+        lo |= (uint32_t)__nv_cvt_float2_to_fp8x2(
+                  make_float2(__fdiv_rn(f[i], sc), __fdiv_rn(f[i + 1], sc)), __NV_SATFINITE,
+                  __NV_E4M3) << (8 * i);
+        hi |= (uint32_t)__nv_cvt_float2_to_fp8x2(
+                  make_float2(__fdiv_rn(f[4 + i], sc), __fdiv_rn(f[5 + i], sc)), __NV_SATFINITE,
+                  __NV_E4M3) << (8 * i);
+      }
+      if (on) {
+        reinterpret_cast<uint2*>(xq + (size_t)row * H)[c] = make_uint2(lo, hi);
+        if ((lane & 15) == 0) xsc[(size_t)(c / 16) * te_stride + row] = sc;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_router_small(const RouteArgs& a, const SortArgs& s, bool fuse_tail,
+                                cudaStream_t st) {
+  dim3 grid((a.R + kRouterWarps - 1) / kRouterWarps, (a.N + kRouterTok - 1) / kRouterTok);
+  size_t sm_x = (size_t)kRouterTok * a.H * 2;
+  size_t sm_tail = fuse_tail ? (size_t)2 * kRouterWarps * a.R * 4 + (size_t)a.N * a.K * 4 +
+                                   (size_t)a.E * 4 + 40 * 4
+                             : 0;
+  size_t sm = sm_x > sm_tail ? sm_x : sm_tail;
+  if (sm > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(router_small_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+  }
+  router_small_kernel<<<grid, 256, sm, st>>>(a, s, fuse_tail ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st) {
+  size_t sm = (size_t)8 * 2 * a.R * 4;
+  if (sm > 48 * 1024) {
+    cudaError_t e =
+        cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+  }
+  topk_kernel<<<(a.N + 7) / 8, 256, sm, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sort(const SortArgs& s, const __nv_bfloat16* x, int H, __nv_bfloat16* xp,
+                        uint8_t* xq, float* xs, cudaStream_t st) {
+  const int nblk = (s.te + kSortBlock - 1) / kSortBlock;
+  size_t sm = (size_t)32 * s.E * 4;
+  if (sm > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(sort_count_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+  }
+  sort_count_kernel<<<nblk, kSortBlock, sm, st>>>(s);
+  sort_scan_kernel<<<1, 1024, 0, st>>>(s, nblk);
+  sort_scatter_kernel<<<(s.te + 7) / 8, 256, 0, st>>>(s, x, H, xp, xq, xs);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,208 @@
+"""CUDA path vs the CPU oracle, through the C ABI (GPU only).
+
+Bars (element by element):
+  * routing: top-K index sets exact on every token whose K-th and (K+1)-th selection scores
+    differ by more than 1e-3; weights within 1e-5 relative; sort outputs bit-exact;
+  * bf16 experts: |out - ref| <= 2e-2 + 2e-2 |ref| per element, and -- because expert outputs
+    here are ~0.1 in magnitude, where that absolute term alone would hide real errors -- a
+    relative L2 error <= 1e-2 over the whole output.
+The output reference is the oracle run with the GPU's own index set (`forced_idx`), so
+near-tie tokens whose selection legitimately differs are still checked.
+"""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_08_gb300 import inputs as I
+from oracle import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+TIE_GAP = 1e-3
+ATOL, RTOL, REL_L2 = 2e-2, 2e-2, 1e-2
+
+
+@pytest.fixture(scope="module")
+def B():
+    from mixture_experts_layer_08_gb300 import build as _b
+    _b.build()
+    from mixture_experts_layer_08_gb300 import binding
+    assert torch.cuda.is_available()
+    return binding
+
+
+# ------------------------------------------------------------------ workloads
+
+# Reduced copies of the five workloads: several tiles and ragged per-expert tails, small
+# enough for the full oracle.
+SMALL = {
+    "tiny": I.TINY,
+    "decode": I.DECODE,
+    "prefill_zipf_small": I.PREFILL.with_(name="prefill_zipf_small", num_tokens=300, hidden=512,
+                                          num_experts=16, router_width=16, top_k=4, inter=256,
+                                          shared_inter=256),
+    "zero_expert_small": I.ZERO_EXPERT.with_(name="zero_expert_small", num_tokens=200,
+                                             hidden=512, num_experts=32, router_width=48,
+                                             top_k=8, inter=256),
+    "wide_small": I.PREFILL.with_(name="wide_small", num_tokens=1000, hidden=1024,
+                                  num_experts=8, router_width=8, top_k=2, inter=384,
+                                  shared_inter=128, zipf_s=0.0, shared_gated=True),
+}
+
+
+def run_gpu(B, inp, path=0, deterministic=True, forced=None):
+    dev = inp.to("cuda")
+    cfg = B.make_config(inp.shape, deterministic, path)
+    w = B.make_weights(dev)
+    ws = B.alloc_workspace(cfg)
+    N, K = inp.shape.num_tokens, inp.shape.top_k
+    out = torch.empty_like(dev.x)
+    idx = torch.empty(N, K, dtype=torch.int32, device="cuda")
+    wt = torch.empty(N, K, dtype=torch.float32, device="cuda")
+    f = None if forced is None else torch.as_tensor(forced, dtype=torch.int32, device="cuda")
+    B.moe_forward(cfg, w, dev.x, out, ws, None, idx, wt, f)
+    torch.cuda.synchronize()
+    assert B.moe_read_device_status(ws) == B.MOE_OK
+    return out.float().cpu().numpy(), idx.cpu().numpy(), wt.cpu().numpy()
+
+
+def check_routing(gpu_idx, ref):
+    far = ref["gap"] > TIE_GAP
+    assert far.mean() > 0.5, "too many near-ties for the routing check to mean anything"
+    np.testing.assert_array_equal(gpu_idx[far], ref["idx"][far])
+    return int((~far).sum())
+
+
+def check_out(got, ref, atol=ATOL, rtol=RTOL, rel_l2=REL_L2):
+    err = np.abs(got - ref)
+    bad = err > atol + rtol * np.abs(ref)
+    assert not bad.any(), f"{bad.sum()} elements out of tolerance, max err {err.max():.3e}"
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    assert rel <= rel_l2, f"relative L2 error {rel:.3e}"
+    return rel
+
+
+# ------------------------------------------------------------------ routing
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("path", [1, 2], ids=["decode", "grouped"])
+def test_route_matches_oracle(B, name, path):
+    shape = SMALL[name]
+    if path == 1 and shape.num_tokens > 16:
+        pytest.skip("decode chain is for <= 16 tokens")
+    inp = I.make_inputs(shape)
+    dev = inp.to("cuda")
+    cfg = B.make_config(shape, True, path)
+    ws = B.alloc_workspace(cfg)
+    N, K, E = shape.num_tokens, shape.top_k, shape.num_experts
+    idx = torch.empty(N, K, dtype=torch.int32, device="cuda")
+    wt = torch.empty(N, K, dtype=torch.float32, device="cuda")
+    zs = torch.empty(N, dtype=torch.float32, device="cuda")
+    offs = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    spairs = torch.empty(N * K, dtype=torch.int32, device="cuda")
+    p2r = torch.empty(N * K, dtype=torch.int32, device="cuda")
+    B.moe_route(cfg, B.make_weights(dev), dev.x, ws, None, idx, wt, zs, offs, spairs, p2r)
+    torch.cuda.synchronize()
+    ref = O.moe_forward(inp, routing_only=True)
+    gi = idx.cpu().numpy()
+    check_routing(gi, ref)
+    far = ref["gap"] > TIE_GAP
+    np.testing.assert_allclose(wt.cpu().numpy()[far], ref["w"][far], rtol=1e-5, atol=1e-7)
+    np.testing.assert_allclose(zs.cpu().numpy()[far], ref["zsum"][far], rtol=1e-5, atol=1e-7)
+    # the sort is integer work: bit-exact against the oracle's stable sort of the GPU's ids
+    o_off, o_pairs, o_p2r = O.sort_by_expert(gi, E)
+    np.testing.assert_array_equal(offs.cpu().numpy().view(np.uint32), o_off)
+    Z = int(o_off[-1])
+    np.testing.assert_array_equal(spairs.cpu().numpy().view(np.uint32)[:Z], o_pairs)
+    np.testing.assert_array_equal(p2r.cpu().numpy().view(np.uint32), o_p2r)
+
+
+# ------------------------------------------------------------------ whole forward
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("path", [0, 1, 2], ids=["auto", "decode", "grouped"])
+def test_forward_matches_oracle(B, name, path):
+    shape = SMALL[name]
+    if path == 1 and shape.num_tokens > 16:
+        pytest.skip("decode chain is for <= 16 tokens")
+    inp = I.make_inputs(shape)
+    got, gidx, gw = run_gpu(B, inp, path)
+    ref_sel = O.moe_forward(inp, routing_only=True)
+    check_routing(gidx, ref_sel)
+    ref = O.moe_forward(inp, forced_idx=gidx)
+    np.testing.assert_allclose(gw, ref["w"], rtol=1e-5, atol=1e-7)
+    check_out(got, ref["out"])
+
+
+def test_forced_identity_experts_are_exact(B):
+    """Every slot on an identity expert, no shared expert: out == bf16(zsum * x) bitwise."""
+    shape = SMALL["zero_expert_small"]
+    inp = I.make_inputs(shape)
+    N, K, E, R = shape.num_tokens, shape.top_k, shape.num_experts, shape.router_width
+    rng = np.random.default_rng(3)
+    forced = np.stack([rng.choice(np.arange(E, R), K, replace=False) for _ in range(N)])
+    for path in (2,):
+        got, gidx, gw = run_gpu(B, inp, path, forced=forced)
+        assert (gidx == forced).all()
+        z = torch.tensor(gw.sum(axis=1), dtype=torch.float32)
+        want = (z[:, None] * inp.x.float()).to(torch.bfloat16).float().numpy()
+        assert np.array_equal(got, want)
+
+
+def test_decode_and_grouped_chains_agree(B):
+    for n in (4, 16):
+        inp = I.make_inputs(I.DECODE.with_(num_tokens=n))
+        a, ia, _ = run_gpu(B, inp, 1)
+        b, ib, _ = run_gpu(B, inp, 2)
+        np.testing.assert_array_equal(ia, ib)
+        check_out(a, b.astype(np.float64), rel_l2=1e-2)
+
+
+@pytest.mark.parametrize("path", [1, 2], ids=["decode", "grouped"])
+def test_deterministic_mode_is_bitwise_stable(B, path):
+    inp = I.make_inputs(I.DECODE.with_(num_tokens=12) if path == 1 else SMALL["prefill_zipf_small"])
+    first = run_gpu(B, inp, path)[0]
+    for _ in range(4):
+        assert np.array_equal(run_gpu(B, inp, path)[0], first)
+
+
+def test_atomic_decode_accumulation_matches_oracle(B):
+    inp = I.make_inputs(I.DECODE)
+    got, gidx, _ = run_gpu(B, inp, 1, deterministic=False)
+    ref = O.moe_forward(inp, forced_idx=gidx)
+    check_out(got, ref["out"])
+
+
+def test_output_guard_bands_untouched(B):
+    inp = I.make_inputs(SMALL["prefill_zipf_small"])
+    dev = inp.to("cuda")
+    cfg = B.make_config(inp.shape, True, 2)
+    ws = B.alloc_workspace(cfg)
+    N, H = inp.shape.num_tokens, inp.shape.hidden
+    buf = torch.full((N * H + 2 * 4096,), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[4096:4096 + N * H].view(N, H)
+    B.moe_forward(cfg, B.make_weights(dev), dev.x, out, ws)
+    torch.cuda.synchronize()
+    assert (buf[:4096] == 7.0).all() and (buf[-4096:] == 7.0).all()
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+def _sample_tokens(n, k=12, seed=0):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, n - 1], rng.choice(n, k, replace=False)]))
+
+
+@pytest.mark.parametrize("shape", [I.DECODE, I.PREFILL, I.ZERO_EXPERT], ids=lambda s: s.name)
+def test_full_size_sampled_tokens(B, shape):
+    """The bench's launch configuration at full size; the oracle recomputes sampled tokens
+    one by one, and the routing of every token is checked."""
+    inp = I.make_inputs(shape, device="cuda")
+    got, gidx, gw = run_gpu(B, inp, 0)
+    ref_sel = O.moe_forward(inp, routing_only=True)
+    excluded = check_routing(gidx, ref_sel)
+    assert excluded < 0.2 * shape.num_tokens
+    toks = _sample_tokens(shape.num_tokens)
+    ref = O.moe_forward(inp, tokens=toks, forced_idx=gidx)
+    np.testing.assert_allclose(gw[toks], ref["w"], rtol=1e-5, atol=1e-7)
+    check_out(got[toks], ref["out"])
