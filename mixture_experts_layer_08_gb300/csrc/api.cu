@@ -59,7 +59,8 @@ moe_status_t validate_config(const moe_config_t* c) {
     return MOE_ERR_UNSUPPORTED;
   if (c->hidden % 128 || c->inter % 128 || c->shared_inter % 128) return MOE_ERR_UNSUPPORTED;
   if (c->top_k > 32 || c->router_width > 1024 || c->num_experts > 1024) return MOE_ERR_UNSUPPORTED;
-  if (c->weight_dtype == MOE_W_FP8_E4M3_B128) return MOE_ERR_UNSUPPORTED;
+  // FP8 experts: the down projection's N-tile is 256 wide
+  if (c->weight_dtype == MOE_W_FP8_E4M3_B128 && c->hidden % 256) return MOE_ERR_UNSUPPORTED;
   const int path = resolve_path(c);
   if (path == MOE_PATH_DECODE &&
       (c->weight_dtype != MOE_W_BF16 || c->num_tokens > kDecodeMaxTokens || c->inter > 1024 ||
@@ -94,8 +95,15 @@ Layout make_layout(const moe_config_t* c) {
     sz[R_BLK] = (size_t)L.nblk * E * 4;
     sz[R_LRANK] = te * 4;
     sz[R_TILES] = (size_t)L.max_mtiles * 16;
-    sz[R_XP] = te * H * 2;
-    sz[R_HH] = te * I * 2;
+    if (c->weight_dtype == MOE_W_FP8_E4M3_B128) {
+      sz[R_XP] = te * H;                 // E4M3 codes of the gathered rows
+      sz[R_XS] = (H / 128) * te * 4;     // their 1x128 scales, [H/128, te]
+      sz[R_HH] = te * I;                 // E4M3 codes of the SwiGLU intermediate
+      sz[R_HS] = (I / 128) * te * 4;
+    } else {
+      sz[R_XP] = te * H * 2;
+      sz[R_HH] = te * I * 2;
+    }
     sz[R_Y] = te * H * 2;
     sz[R_SHH] = N * S * 2;
     sz[R_SHY] = S ? N * H * 2 : 0;
@@ -159,6 +167,20 @@ bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t row
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 2D E4M3 (byte) map over a [rows, inner] row-major matrix; box {128, box_rows}.
+bool make_map_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows,
+                 uint32_t box_rows) {
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -267,8 +289,11 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
     CK(launch_gemm_bf16(kGemmStoreF32, 128, ma, mb, mb, g, num_sms(), st));
   }
   CK(launch_topk(ra, st));
-  CK(launch_sort(sa, ra.x, c->hidden, gather ? P.at<__nv_bfloat16>(R_XP) : nullptr, nullptr,
-                 nullptr, st));
+  const bool fp8 = c->weight_dtype == MOE_W_FP8_E4M3_B128;
+  CK(launch_sort(sa, ra.x, c->hidden,
+                 gather && !fp8 ? P.at<__nv_bfloat16>(R_XP) : nullptr,
+                 gather && fp8 ? P.at<uint8_t>(R_XP) : nullptr,
+                 gather && fp8 ? P.at<float>(R_XS) : nullptr, st));
   return MOE_OK;
 }
 
@@ -306,7 +331,49 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
   }
   M.mark(MOE_STAGE_SHARED, 1);
   // routed experts: grouped gate/up + SiLU*up, then grouped down, over the sorted rows
-  {
+  if (c->weight_dtype == MOE_W_FP8_E4M3_B128) {
+    CUtensorMap ma, mg, mu, mh, md;
+    const uint64_t rows = (uint64_t)L.te;
+    if (!make_map_u8(&ma, P.at<void>(R_XP), H, rows, 128) ||
+        !make_map_u8(&mg, w->w_gate, H, (uint64_t)E * I, 128) ||
+        !make_map_u8(&mu, w->w_up, H, (uint64_t)E * I, 128) ||
+        !make_map_u8(&mh, P.at<void>(R_HH), I, rows, 128) ||
+        !make_map_u8(&md, w->w_down, I, (uint64_t)E * H, 256))
+      return MOE_ERR_CUDA;
+    Fp8GemmArgs g{};
+    g.tiles = P.at<int4>(R_TILES);
+    g.hdr = hdr;
+    g.max_mtiles = L.max_mtiles;
+    g.n_tiles = I / 128;
+    g.num_kb = H / 128;
+    g.b_rows_per_expert = I;
+    g.b_blocks_per_expert = I / 128;
+    g.sa = P.at<float>(R_XS);
+    g.sa_stride = L.te;
+    g.sb0 = w->s_gate;
+    g.sb1 = w->s_up;
+    g.out = P.at<void>(R_HH);
+    g.ldo = I;
+    g.out_scales = P.at<float>(R_HS);
+    g.out_scale_stride = L.te;
+    g.status = hdr;
+    M.mark(MOE_STAGE_GATE_UP, 0);
+    CK(launch_gemm_fp8(0, ma, mg, mu, g, sms, st));
+    M.mark(MOE_STAGE_GATE_UP, 1);
+    g.n_tiles = H / 256;
+    g.num_kb = I / 128;
+    g.b_rows_per_expert = H;
+    g.b_blocks_per_expert = H / 128;
+    g.sa = P.at<float>(R_HS);
+    g.sb0 = w->s_down;
+    g.sb1 = nullptr;
+    g.out = P.at<void>(R_Y);
+    g.ldo = H;
+    g.out_scales = nullptr;
+    M.mark(MOE_STAGE_DOWN, 0);
+    CK(launch_gemm_fp8(1, mh, md, md, g, sms, st));
+    M.mark(MOE_STAGE_DOWN, 1);
+  } else {
     CUtensorMap ma, mg, mu, mh, md;
     const uint64_t rows = (uint64_t)L.te;
     if (!make_map_bf16(&ma, P.at<void>(R_XP), H, rows, 128) ||

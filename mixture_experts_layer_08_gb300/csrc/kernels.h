@@ -110,4 +110,30 @@ cudaError_t launch_gemm_bf16(int mode, int bn, const CUtensorMap& a, const CUten
                              const CUtensorMap& b1, const GemmArgs& g, int num_sms,
                              cudaStream_t st);
 
+// FP8 (E4M3, block-scaled) grouped GEMM over the expert-sorted rows. mode 0: gate/up with
+// SwiGLU and 1x128 E4M3 quantisation of the intermediate; mode 1: down projection to bf16.
+struct Fp8GemmArgs {
+  const int4* tiles;               // m-tile list (expert, row0, row1, 0)
+  const WsHeader* hdr;             // number of m-tiles
+  int max_mtiles;
+  int n_tiles;                     // mode 0: I/128 (gate/up pairs); mode 1: H/256
+  int num_kb;                      // contraction / 128
+  int b_rows_per_expert;           // rows of one expert in the B maps
+  int b_blocks_per_expert;         // b_rows_per_expert / 128 (scale rows per expert)
+  const float* sa;                 // A scales [num_kb, sa_stride]
+  int sa_stride;
+  const float* sb0;                // B scales [E, b_blocks, num_kb] (gate, or down)
+  const float* sb1;                // up scales (mode 0)
+  void* out;                       // mode 0: E4M3 codes [rows, ldo]; mode 1: bf16 [rows, ldo]
+  int ldo;
+  float* out_scales;               // mode 0: [ldo/128, out_scale_stride]
+  int out_scale_stride;
+  WsHeader* status;
+};
+// A: uint8 map [rows, K], box {128, 128}; B: uint8 map [rows, K], box {128, 128 (mode 0) or
+// 256 (mode 1)}.
+cudaError_t launch_gemm_fp8(int mode, const CUtensorMap& a, const CUtensorMap& b0,
+                            const CUtensorMap& b1, const Fp8GemmArgs& g, int num_sms,
+                            cudaStream_t st);
+
 }  // namespace moe

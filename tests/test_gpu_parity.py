@@ -206,3 +206,35 @@ def test_full_size_sampled_tokens(B, shape):
     ref = O.moe_forward(inp, tokens=toks, forced_idx=gidx)
     np.testing.assert_allclose(gw[toks], ref["w"], rtol=1e-5, atol=1e-7)
     check_out(got[toks], ref["out"])
+
+
+# ------------------------------------------------------------------ FP8 experts
+
+FP8_ATOL, FP8_RTOL, FP8_REL_L2 = 5e-2, 5e-2, 2e-2
+
+FP8_SMALL = I.FP8_PREFILL.with_(name="fp8_small", num_tokens=300, hidden=512, num_experts=8,
+                                router_width=8, top_k=2, inter=256)
+
+
+@pytest.mark.parametrize("shape", [FP8_SMALL,
+                                   FP8_SMALL.with_(name="fp8_small_k4", num_tokens=77,
+                                                   num_experts=16, router_width=16, top_k=4,
+                                                   inter=384, hidden=768)],
+                         ids=lambda s: s.name)
+def test_fp8_forward_matches_oracle(B, shape):
+    inp = I.make_inputs(shape)
+    got, gidx, gw = run_gpu(B, inp, 0)
+    check_routing(gidx, O.moe_forward(inp, routing_only=True))
+    ref = O.moe_forward(inp, forced_idx=gidx)
+    check_out(got, ref["out"], FP8_ATOL, FP8_RTOL, FP8_REL_L2)
+
+
+def test_fp8_full_size_sampled_tokens(B):
+    shape = I.FP8_PREFILL
+    inp = I.make_inputs(shape, device="cuda")
+    got, gidx, gw = run_gpu(B, inp, 0)
+    excluded = check_routing(gidx, O.moe_forward(inp, routing_only=True))
+    assert excluded < 0.2 * shape.num_tokens
+    toks = _sample_tokens(shape.num_tokens, k=10)
+    ref = O.moe_forward(inp, tokens=toks, forced_idx=gidx)
+    check_out(got[toks], ref["out"], FP8_ATOL, FP8_RTOL, FP8_REL_L2)
