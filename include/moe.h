@@ -168,6 +168,14 @@ MOE_API moe_status_t moe_forward_profiled(const moe_config_t *cfg, const moe_wei
  * (MOE_OK or MOE_ERR_DEVICE_TIMEOUT). For tests and debugging; it blocks the host. */
 MOE_API moe_status_t moe_read_device_status(const void *workspace, void *stream, int32_t *status);
 
+/* Failure-detection self test: clears the workspace status word, then one device thread waits
+ * (with the same bounded wait every kernel here uses) on a barrier that nothing completes,
+ * giving up after `limit_cycles` SM clock cycles (1 <= limit_cycles <= 2e9). Afterwards
+ * moe_read_device_status() reports MOE_ERR_DEVICE_TIMEOUT and the CUDA context stays usable.
+ * workspace: >= 256 bytes, 256-byte aligned. */
+MOE_API moe_status_t moe_selftest_bounded_wait(void *workspace, long long limit_cycles,
+                                               void *stream);
+
 /* Static description of a status code. */
 MOE_API const char *moe_status_string(moe_status_t status);
 

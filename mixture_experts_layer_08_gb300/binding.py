@@ -68,6 +68,8 @@ _lib.moe_route.argtypes = [ctypes.POINTER(moe_config_t), ctypes.POINTER(moe_weig
                            ctypes.c_size_t, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.moe_read_device_status.restype = ctypes.c_int
 _lib.moe_read_device_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]
+_lib.moe_selftest_bounded_wait.restype = ctypes.c_int
+_lib.moe_selftest_bounded_wait.argtypes = [_vp, ctypes.c_longlong, _vp]
 _lib.moe_status_string.restype = ctypes.c_char_p
 _lib.moe_status_string.argtypes = [ctypes.c_int]
 
@@ -163,6 +165,13 @@ def moe_read_device_status(workspace: torch.Tensor, stream=None) -> int:
     if st != MOE_OK:
         raise MoeError(st, "moe_read_device_status")
     return v.value
+
+
+def moe_selftest_bounded_wait(workspace: torch.Tensor, limit_cycles: int, stream=None) -> int:
+    st = _lib.moe_selftest_bounded_wait(_ptr(workspace), int(limit_cycles), _stream(stream))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_selftest_bounded_wait")
+    return st
 
 
 class MoeBlock:

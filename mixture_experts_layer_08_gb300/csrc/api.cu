@@ -583,6 +583,17 @@ moe_status_t moe_read_device_status(const void* workspace, void* stream, int32_t
   return MOE_OK;
 }
 
+moe_status_t moe_selftest_bounded_wait(void* workspace, long long limit_cycles, void* stream) {
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) || limit_cycles < 1 ||
+      limit_cycles > kSpinLimitCycles)
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WsHeader* hdr = static_cast<WsHeader*>(workspace);
+  CK(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
+  CK(launch_bounded_wait_selftest(hdr, limit_cycles, st));
+  return MOE_OK;
+}
+
 const char* moe_status_string(moe_status_t s) {
   switch (s) {
     case MOE_OK: return "ok";

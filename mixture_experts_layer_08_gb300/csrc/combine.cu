@@ -93,7 +93,21 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(CombineArgs a) {
   reinterpret_cast<uint4*>(a.out + (size_t)t * H)[c] = o;
 }
 
+// One thread waits, with the library's bounded wait, on an mbarrier nothing arrives on.
+__global__ void bounded_wait_selftest_kernel(WsHeader* hdr, long long limit_cycles) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbarrier_init();
+  mbar_wait(&bar, 0, hdr, limit_cycles);
+}
+
 }  // namespace
+
+cudaError_t launch_bounded_wait_selftest(WsHeader* hdr, long long limit_cycles, cudaStream_t st) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, st>>>(hdr, limit_cycles);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
   dim3 grid(a.N, (a.H / 8 + kCombThreads - 1) / kCombThreads);

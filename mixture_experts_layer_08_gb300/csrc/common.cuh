@@ -104,13 +104,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete. Gives up after kSpinLimitCycles,
+// Waits for the phase with the given parity to complete. Gives up after `limit` cycles,
 // reports MOE_ERR_DEVICE_TIMEOUT and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WsHeader* hdr) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WsHeader* hdr,
+                                          long long limit = kSpinLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kSpinLimitCycles) {
+    if (clock64() - t0 > limit) {
       report_timeout(hdr);
       return false;
     }

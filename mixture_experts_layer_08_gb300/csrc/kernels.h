@@ -88,6 +88,10 @@ struct CombineArgs {
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 
+// Exercises the bounded device wait: waits `limit_cycles` on a barrier that never completes,
+// then records MOE_ERR_DEVICE_TIMEOUT in the header.
+cudaError_t launch_bounded_wait_selftest(WsHeader* hdr, long long limit_cycles, cudaStream_t st);
+
 // tcgen05 grouped GEMM. Epilogue modes.
 enum GemmMode { kGemmSwiGLU = 0, kGemmStoreBF16 = 1, kGemmStoreF32 = 2 };
 

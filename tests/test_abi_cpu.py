@@ -120,3 +120,10 @@ def test_zero_tokens_is_a_no_op(B):
     w.sh_gate_vec = None
     assert B.lib.moe_forward(ctypes.byref(cfg), ctypes.byref(w), None, None, None, 0, None, None,
                              None, None) == B.MOE_OK
+
+
+def test_selftest_refuses_bad_arguments(B):
+    assert B.lib.moe_selftest_bounded_wait(None, 1000, None) == B.MOE_ERR_INVALID_ARG
+    assert B.lib.moe_selftest_bounded_wait(1 << 20, 0, None) == B.MOE_ERR_INVALID_ARG
+    assert B.lib.moe_selftest_bounded_wait((1 << 20) + 8, 1000, None) == B.MOE_ERR_INVALID_ARG
+    assert B.lib.moe_selftest_bounded_wait(1 << 20, 10 ** 12, None) == B.MOE_ERR_INVALID_ARG

@@ -238,3 +238,16 @@ def test_fp8_full_size_sampled_tokens(B):
     toks = _sample_tokens(shape.num_tokens, k=10)
     ref = O.moe_forward(inp, tokens=toks, forced_idx=gidx)
     check_out(got[toks], ref["out"], FP8_ATOL, FP8_RTOL, FP8_REL_L2)
+
+
+# ------------------------------------------------------------------ failure detection
+
+def test_bounded_wait_reports_timeout_and_context_survives(B):
+    """A device wait on a barrier nothing completes gives up after its limit and reports
+    MOE_ERR_DEVICE_TIMEOUT; the next forward on the same context still matches the oracle."""
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    B.moe_selftest_bounded_wait(ws, 20_000_000)       # ~10 ms
+    assert B.moe_read_device_status(ws) == B.MOE_ERR_DEVICE_TIMEOUT
+    inp = I.make_inputs(I.TINY)
+    got, gidx, _ = run_gpu(B, inp, 2)
+    check_out(got, O.moe_forward(inp, forced_idx=gidx)["out"])
