@@ -156,6 +156,10 @@ def time_ours(B, shape, steps, warmup, dev, peaks, with_e2e=True):
     barrier()
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nst)] for _ in range(steps)]
+    for row in ev:          # torch creates the CUDA event on first record
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
     with ClockSampler(dev) as clk:
         t_wall0 = time.time()
         for i in range(steps):

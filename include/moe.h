@@ -176,6 +176,10 @@ MOE_API moe_status_t moe_read_device_status(const void *workspace, void *stream,
 MOE_API moe_status_t moe_selftest_bounded_wait(void *workspace, long long limit_cycles,
                                                void *stream);
 
+/* After MOE_ERR_CUDA: the failing CUDA call and its error text, for the calling thread
+ * (empty string if none failed). The pointer stays valid until the thread's next call. */
+MOE_API const char *moe_last_error_detail(void);
+
 /* Static description of a status code. */
 MOE_API const char *moe_status_string(moe_status_t status);
 

@@ -27,7 +27,10 @@ PATH_AUTO, PATH_DECODE, PATH_GROUPED = 0, 1, 2
 
 class MoeError(RuntimeError):
     def __init__(self, status: int, what: str):
-        super().__init__(f"{what}: {moe_status_string(status)} (status {status})")
+        detail = ""
+        if status == MOE_ERR_CUDA:
+            detail = " -- " + _lib.moe_last_error_detail().decode()
+        super().__init__(f"{what}: {moe_status_string(status)} (status {status}){detail}")
         self.status = status
 
 
@@ -70,6 +73,8 @@ _lib.moe_read_device_status.restype = ctypes.c_int
 _lib.moe_read_device_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]
 _lib.moe_selftest_bounded_wait.restype = ctypes.c_int
 _lib.moe_selftest_bounded_wait.argtypes = [_vp, ctypes.c_longlong, _vp]
+_lib.moe_last_error_detail.restype = ctypes.c_char_p
+_lib.moe_last_error_detail.argtypes = []
 _lib.moe_status_string.restype = ctypes.c_char_p
 _lib.moe_status_string.argtypes = [ctypes.c_int]
 

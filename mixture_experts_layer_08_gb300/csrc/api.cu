@@ -10,6 +10,7 @@
 // bytes needed and available; the FP32 accumulator sits at a 256-byte aligned offset).
 #include <cudaTypedefs.h>
 
+#include <cstdio>
 #include <mutex>
 
 #include "kernels.h"
@@ -202,18 +203,36 @@ moe_status_t validate_weights(const moe_config_t* c, const moe_weights_t* w) {
   return MOE_OK;
 }
 
+// Text of the last failing CUDA call of this thread (moe_last_error_detail).
+thread_local char g_detail[256];
+
+moe_status_t cuda_fail(cudaError_t e, const char* what, int line) {
+  snprintf(g_detail, sizeof g_detail, "%s failed at api.cu:%d: %s (%d)", what, line,
+           cudaGetErrorString(e), (int)e);
+  return MOE_ERR_CUDA;
+}
+
+#define CK(expr)                                                     \
+  do {                                                               \
+    cudaError_t ck_e = (expr);                                       \
+    if (ck_e != cudaSuccess) return cuda_fail(ck_e, #expr, __LINE__); \
+  } while (0)
+
 struct Marks {
   void** ev;
   cudaStream_t st;
-  void mark(int stage, int end) const {
+  // Records the caller's event for the start (end = 0) or end (end = 1) of a stage.
+  moe_status_t mark(int stage, int end) const {
     if (ev && ev[2 * stage + end])
-      cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * stage + end]), st);
+      CK(cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * stage + end]), st));
+    return MOE_OK;
   }
 };
 
-#define CK(expr)                                   \
-  do {                                             \
-    if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
+#define MARK(stage, end)                          \
+  do {                                            \
+    moe_status_t mk_s = M.mark((stage), (end));   \
+    if (mk_s != MOE_OK) return mk_s;              \
   } while (0)
 
 struct Ptrs {
@@ -306,7 +325,7 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
   const int sms = num_sms();
   const int bn_h = (H % 256 == 0) ? 256 : 128;   // N-tile of the projections back to H
   // shared expert: dense SwiGLU FFN on all N rows
-  M.mark(MOE_STAGE_SHARED, 0);
+  MARK(MOE_STAGE_SHARED, 0);
   if (S > 0) {
     CUtensorMap ma, mg, mu, mh, md;
     if (!make_map_bf16(&ma, x, H, N, 128) || !make_map_bf16(&mg, w->sh_gate, H, S, 128) ||
@@ -329,7 +348,7 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
     g.ldo = H;
     CK(launch_gemm_bf16(kGemmStoreBF16, bn_h, mh, md, md, g, sms, st));
   }
-  M.mark(MOE_STAGE_SHARED, 1);
+  MARK(MOE_STAGE_SHARED, 1);
   // routed experts: grouped gate/up + SiLU*up, then grouped down, over the sorted rows
   if (c->weight_dtype == MOE_W_FP8_E4M3_B128) {
     CUtensorMap ma, mg, mu, mh, md;
@@ -357,9 +376,9 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
     g.out_scales = P.at<float>(R_HS);
     g.out_scale_stride = L.te;
     g.status = hdr;
-    M.mark(MOE_STAGE_GATE_UP, 0);
+    MARK(MOE_STAGE_GATE_UP, 0);
     CK(launch_gemm_fp8(0, ma, mg, mu, g, sms, st));
-    M.mark(MOE_STAGE_GATE_UP, 1);
+    MARK(MOE_STAGE_GATE_UP, 1);
     g.n_tiles = H / 256;
     g.num_kb = I / 128;
     g.b_rows_per_expert = H;
@@ -370,9 +389,9 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
     g.out = P.at<void>(R_Y);
     g.ldo = H;
     g.out_scales = nullptr;
-    M.mark(MOE_STAGE_DOWN, 0);
+    MARK(MOE_STAGE_DOWN, 0);
     CK(launch_gemm_fp8(1, mh, md, md, g, sms, st));
-    M.mark(MOE_STAGE_DOWN, 1);
+    MARK(MOE_STAGE_DOWN, 1);
   } else {
     CUtensorMap ma, mg, mu, mh, md;
     const uint64_t rows = (uint64_t)L.te;
@@ -392,17 +411,17 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
     g.out = P.at<void>(R_HH);
     g.ldo = I;
     g.status = hdr;
-    M.mark(MOE_STAGE_GATE_UP, 0);
+    MARK(MOE_STAGE_GATE_UP, 0);
     CK(launch_gemm_bf16(kGemmSwiGLU, 256, ma, mg, mu, g, sms, st));
-    M.mark(MOE_STAGE_GATE_UP, 1);
+    MARK(MOE_STAGE_GATE_UP, 1);
     g.n_tiles = H / bn_h;
     g.num_kb = I / 64;
     g.b_rows_per_expert = H;
     g.out = P.at<void>(R_Y);
     g.ldo = H;
-    M.mark(MOE_STAGE_DOWN, 0);
+    MARK(MOE_STAGE_DOWN, 0);
     CK(launch_gemm_bf16(kGemmStoreBF16, bn_h, mh, md, md, g, sms, st));
-    M.mark(MOE_STAGE_DOWN, 1);
+    MARK(MOE_STAGE_DOWN, 1);
   }
   CombineArgs ca{};
   ca.x = static_cast<const __nv_bfloat16*>(x);
@@ -418,9 +437,9 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
   ca.H = H;
   ca.K = c->top_k;
   ca.out = static_cast<__nv_bfloat16*>(out);
-  M.mark(MOE_STAGE_COMBINE, 0);
+  MARK(MOE_STAGE_COMBINE, 0);
   CK(launch_combine(ca, st));
-  M.mark(MOE_STAGE_COMBINE, 1);
+  MARK(MOE_STAGE_COMBINE, 1);
   return MOE_OK;
 }
 
@@ -453,15 +472,15 @@ moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const voi
   d.acc = P.at<float>(R_ACC);
   d.shy = P.at<float>(R_SHY);
   d.hdr = P.at<WsHeader>(R_HDR);
-  M.mark(MOE_STAGE_SHARED, 0);
-  M.mark(MOE_STAGE_SHARED, 1);
-  M.mark(MOE_STAGE_GATE_UP, 0);
+  MARK(MOE_STAGE_SHARED, 0);
+  MARK(MOE_STAGE_SHARED, 1);
+  MARK(MOE_STAGE_GATE_UP, 0);
   if (d.acc) CK(cudaMemsetAsync(d.acc, 0, (size_t)N * H * 4, st));
   CK(launch_decode_gateup(d, st));
-  M.mark(MOE_STAGE_GATE_UP, 1);
-  M.mark(MOE_STAGE_DOWN, 0);
+  MARK(MOE_STAGE_GATE_UP, 1);
+  MARK(MOE_STAGE_DOWN, 0);
   CK(launch_decode_down(d, st));
-  M.mark(MOE_STAGE_DOWN, 1);
+  MARK(MOE_STAGE_DOWN, 1);
   CombineArgs ca{};
   ca.x = d.x;
   ca.pair_to_row = P.at<uint32_t>(R_P2R);
@@ -477,9 +496,9 @@ moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const voi
   ca.H = H;
   ca.K = c->top_k;
   ca.out = static_cast<__nv_bfloat16*>(out);
-  M.mark(MOE_STAGE_COMBINE, 0);
+  MARK(MOE_STAGE_COMBINE, 0);
   CK(launch_combine(ca, st));
-  M.mark(MOE_STAGE_COMBINE, 1);
+  MARK(MOE_STAGE_COMBINE, 1);
   return MOE_OK;
 }
 
@@ -507,13 +526,14 @@ moe_status_t forward_impl(const moe_config_t* cfg, const moe_weights_t* weights,
   if (s != MOE_OK) return s;
   if (cfg->num_tokens == 0) return MOE_OK;
   if (!out || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  (void)cudaGetLastError();   // a stale error of an earlier call must not fail this one
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Ptrs P{static_cast<uint8_t*>(workspace), &L};
   Marks M{events, st};
-  M.mark(MOE_STAGE_ROUTE, 0);
+  MARK(MOE_STAGE_ROUTE, 0);
   s = run_routing(cfg, weights, x, P, forced_idx, L.path == MOE_PATH_GROUPED, st);
   if (s != MOE_OK) return s;
-  M.mark(MOE_STAGE_ROUTE, 1);
+  MARK(MOE_STAGE_ROUTE, 1);
   s = L.path == MOE_PATH_GROUPED ? run_grouped(cfg, weights, x, out, P, st, M)
                                  : run_decode(cfg, weights, x, out, P, st, M);
   if (s != MOE_OK) return s;
@@ -560,6 +580,7 @@ moe_status_t moe_route(const moe_config_t* cfg, const moe_weights_t* weights, co
   moe_status_t s = check_call(cfg, weights, x, workspace, workspace_bytes, &L);
   if (s != MOE_OK) return s;
   if (cfg->num_tokens == 0) return MOE_OK;
+  (void)cudaGetLastError();
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Ptrs P{static_cast<uint8_t*>(workspace), &L};
   s = run_routing(cfg, weights, x, P, nullptr, false, st);
@@ -593,6 +614,8 @@ moe_status_t moe_selftest_bounded_wait(void* workspace, long long limit_cycles, 
   CK(launch_bounded_wait_selftest(hdr, limit_cycles, st));
   return MOE_OK;
 }
+
+const char* moe_last_error_detail(void) { return g_detail; }
 
 const char* moe_status_string(moe_status_t s) {
   switch (s) {

@@ -249,12 +249,13 @@ static void shared_ffn(const orc_config_t *c, const orc_weights_t *w, const doub
 /* Forward of the tokens listed in `tokens` (n_sel of them; NULL = all N in order).
  * x: bf16 [N,H]. forced_idx: NULL, or [N,K] expert ids that replace the selection (the
  * weights are then the (renormalised) probabilities of those ids).
- * Outputs, per listed token j: out[j,H] fp64, idx[j,K], w[j,K], zsum[j], gap[j], gamma[j].
+ * Outputs, per listed token j: out[j,H] fp64, idx[j,K], w[j,K], zsum[j], gap[j], gamma[j],
+ * sel[j,R] (the selection score of every router column).
  * Any output pointer may be NULL. Returns 0, or -1 on a bad argument. */
 int orc_moe_forward(const orc_config_t *c, const orc_weights_t *w, const uint16_t *x,
                     int n_sel, const int32_t *tokens, const int32_t *forced_idx,
                     double *out, int32_t *idx_out, double *w_out, double *zsum_out,
-                    double *gap_out, double *gamma_out, int routing_only) {
+                    double *gap_out, double *gamma_out, double *sel_out, int routing_only) {
     int N = c->num_tokens, H = c->hidden, R = c->router_width, K = c->top_k;
     int E = c->num_experts, I = c->inter, S = c->shared_inter;
     if (N < 0 || H <= 0 || E <= 0 || R < E || K <= 0 || K > R || K > 64 || I <= 0 || S < 0)
@@ -314,6 +315,10 @@ int orc_moe_forward(const orc_config_t *c, const orc_weights_t *w, const uint16_
         if (zsum_out) zsum_out[j] = zsum;
         if (gap_out) gap_out[j] = gap;
         if (gamma_out) gamma_out[j] = gamma;
+        if (sel_out) {
+            /* route_token marks taken columns only in `taken`; sel itself is intact */
+            memcpy(sel_out + (size_t)j * R, sel, sizeof(double) * R);
+        }
         free(xt); free(xe); free(x32); free(L); free(p); free(sel); free(taken);
         free(hbuf); free(y); free(acc);
     }

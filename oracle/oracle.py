@@ -72,7 +72,7 @@ def _load():
             lib = ctypes.CDLL(build())
             lib.orc_moe_forward.restype = ctypes.c_int
             lib.orc_moe_forward.argtypes = [ctypes.POINTER(_Config), ctypes.POINTER(_Weights)] \
-                + [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 8 + [ctypes.c_int]
+                + [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 9 + [ctypes.c_int]
             lib.orc_e4m3_decode.restype = ctypes.c_double
             lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
             lib.orc_e4m3_encode.restype = ctypes.c_uint8
@@ -108,7 +108,8 @@ def moe_forward(inp, tokens=None, forced_idx=None, routing_only: bool = False):
 
     Returns a dict of numpy arrays: ``out`` [n, H] fp64, ``idx`` [n, K] int32, ``w`` [n, K]
     fp64, ``zsum`` [n], ``gap`` [n] (selection-score gap between the K-th and (K+1)-th
-    choice), ``gamma`` [n] (shared-expert blend weight)."""
+    choice), ``gamma`` [n] (shared-expert blend weight), ``sel`` [n, R] (selection score of
+    every router column)."""
     lib = _load()
     s = inp.shape
     keep: list = []
@@ -131,6 +132,7 @@ def moe_forward(inp, tokens=None, forced_idx=None, routing_only: bool = False):
     zsum = np.zeros(n, dtype=np.float64)
     gap = np.zeros(n, dtype=np.float64)
     gamma = np.zeros(n, dtype=np.float64)
+    sel = np.zeros((n, s.router_width), dtype=np.float64)
 
     def ptr(a):
         return None if a is None else a.ctypes.data
@@ -138,10 +140,11 @@ def moe_forward(inp, tokens=None, forced_idx=None, routing_only: bool = False):
     cfg = _cfg(s)
     rc = lib.orc_moe_forward(ctypes.byref(cfg), ctypes.byref(wts), x, n, ptr(tok), ptr(fi),
                              ptr(out), ptr(idx), ptr(w), ptr(zsum), ptr(gap), ptr(gamma),
-                             int(routing_only))
+                             ptr(sel), int(routing_only))
     if rc != 0:
         raise ValueError("oracle rejected the configuration or token list")
-    return {"out": out, "idx": idx, "w": w, "zsum": zsum, "gap": gap, "gamma": gamma}
+    return {"out": out, "idx": idx, "w": w, "zsum": zsum, "gap": gap, "gamma": gamma,
+            "sel": sel}
 
 
 def e4m3_decode(code: int) -> float:

@@ -66,10 +66,22 @@ def run_gpu(B, inp, path=0, deterministic=True, forced=None):
     return out.float().cpu().numpy(), idx.cpu().numpy(), wt.cpu().numpy()
 
 
-def check_routing(gpu_idx, ref):
+def check_routing(gpu_idx, ref, eps=1e-5):
+    """Index sets equal the oracle's on every token whose K-th/(K+1)-th selection-score gap
+    exceeds 1e-3; on every token, the GPU's set is a valid top-K of the oracle's fp64 scores
+    (each chosen score >= each unchosen score - eps, eps >> the fp32-vs-fp64 score error).
+    Returns the number of near-tie tokens."""
     far = ref["gap"] > TIE_GAP
-    assert far.mean() > 0.5, "too many near-ties for the routing check to mean anything"
     np.testing.assert_array_equal(gpu_idx[far], ref["idx"][far])
+    sel = ref["sel"]
+    n, R = sel.shape
+    chosen = np.zeros((n, R), dtype=bool)
+    np.put_along_axis(chosen, gpu_idx.astype(np.int64), True, axis=1)
+    assert (chosen.sum(axis=1) == gpu_idx.shape[1]).all(), "repeated expert id in a token"
+    lo = np.where(chosen, sel, np.inf).min(axis=1)
+    hi = np.where(chosen, -np.inf, sel).max(axis=1)
+    bad = lo < hi - eps
+    assert not bad.any(), f"{bad.sum()} tokens with an invalid top-K selection"
     return int((~far).sum())
 
 
@@ -200,8 +212,7 @@ def test_full_size_sampled_tokens(B, shape):
     inp = I.make_inputs(shape, device="cuda")
     got, gidx, gw = run_gpu(B, inp, 0)
     ref_sel = O.moe_forward(inp, routing_only=True)
-    excluded = check_routing(gidx, ref_sel)
-    assert excluded < 0.2 * shape.num_tokens
+    check_routing(gidx, ref_sel)
     toks = _sample_tokens(shape.num_tokens)
     ref = O.moe_forward(inp, tokens=toks, forced_idx=gidx)
     np.testing.assert_allclose(gw[toks], ref["w"], rtol=1e-5, atol=1e-7)
@@ -233,8 +244,7 @@ def test_fp8_full_size_sampled_tokens(B):
     shape = I.FP8_PREFILL
     inp = I.make_inputs(shape, device="cuda")
     got, gidx, gw = run_gpu(B, inp, 0)
-    excluded = check_routing(gidx, O.moe_forward(inp, routing_only=True))
-    assert excluded < 0.2 * shape.num_tokens
+    check_routing(gidx, O.moe_forward(inp, routing_only=True))
     toks = _sample_tokens(shape.num_tokens, k=10)
     ref = O.moe_forward(inp, tokens=toks, forced_idx=gidx)
     check_out(got[toks], ref["out"], FP8_ATOL, FP8_RTOL, FP8_REL_L2)

@@ -179,6 +179,15 @@ def test_correction_bias_selects_but_does_not_weight():
             assert list(r["idx"][t]) == sorted([5, 9, 2], key=lambda e: (-p[t, e], e))
 
 
+def test_selection_scores_are_probabilities_plus_bias():
+    shape = small(I.ZERO_EXPERT, num_tokens=16, hidden=256, num_experts=16, router_width=24,
+                  inter=128)
+    inp = I.make_inputs(shape)
+    r = O.moe_forward(inp, routing_only=True)
+    want = torch_probs(inp) + inp.correction_bias.double().numpy()[None, :]
+    np.testing.assert_allclose(r["sel"], want, rtol=1e-12, atol=1e-15)
+
+
 def test_gap_matches_sorted_scores_with_bias():
     shape = small(I.ZERO_EXPERT, num_tokens=32, hidden=256, num_experts=16, router_width=24,
                   inter=128)
