@@ -232,6 +232,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile-only", choices=["decode", "prefill", "fp8", "zero_expert"],
+                    help="run one workload's timing loop only (for ncu captures); prints a "
+                         "reduced line")
     args = ap.parse_args()
     warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -282,6 +285,16 @@ def main():
         from mixture_experts_layer_08_gb300 import build as _b
         _b.build()
         from mixture_experts_layer_08_gb300 import binding as B
+
+    if args.profile_only:
+        shp = {"decode": I.DECODE, "prefill": I.PREFILL, "fp8": I.FP8_PREFILL,
+               "zero_expert": I.ZERO_EXPERT}[args.profile_only]
+        r = time_ours(B, shp, args.steps, warmup, dev, peaks, with_e2e=False)
+        print(json.dumps({"profile_only": shp.name, "ms_per_step": r["ms"],
+                          "tokens_per_s": shp.num_tokens / (r["ms"] / 1000.0),
+                          "stage_us": {k: 1000 * v for k, v in r["stage_ms"].items()},
+                          "Z": r["rs"]["Z"], "distinct_experts": r["rs"]["distinct"]}))
+        return
 
     r = time_ours(B, shape, args.steps, warmup, dev, peaks)
     ms = r["ms"]

@@ -61,6 +61,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+
+// Blocks until the preceding kernel of the stream has completed and its writes are visible
+// (a no-op when this kernel was not launched as a programmatic dependent).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel of the stream start launching once every block of this one got here.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ shared-memory addresses
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -42,9 +42,9 @@ struct Slot {
 __device__ bool resolve_slot(const DecodeArgs& a, int slot, int n_slots, bool down, Slot& sl,
                              int* tok_s, int* row_s) {
   if (slot < n_slots) {
-    if ((uint32_t)slot >= a.hdr->num_active) return false;
-    const int e = (int)a.active[slot];
-    const int r0 = (int)a.offsets[e], r1 = (int)a.offsets[e + 1];
+    if ((uint32_t)slot >= __ldcg(&a.hdr->num_active)) return false;
+    const int e = (int)__ldcg(a.active + slot);
+    const int r0 = (int)__ldcg(a.offsets + e), r1 = (int)__ldcg(a.offsets + e + 1);
     sl.ntok = r1 - r0;
     if (down) {
       sl.w0 = a.wd + (size_t)e * a.H * a.I;
@@ -55,7 +55,7 @@ __device__ bool resolve_slot(const DecodeArgs& a, int slot, int n_slots, bool do
       sl.nrows = a.I;
     }
     for (int j = threadIdx.x; j < sl.ntok; j += blockDim.x) {
-      tok_s[j] = (int)(a.sorted_pairs[r0 + j] / (uint32_t)a.K);
+      tok_s[j] = (int)(__ldcg(a.sorted_pairs + r0 + j) / (uint32_t)a.K);
       row_s[j] = r0 + j;
     }
   } else {
@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(DecodeArgs a, int n_
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int tok_s[kMaxTok], row_s[kMaxTok];
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);   // [ntok, H]
+  pdl_wait();       // routing of the router kernel
+  pdl_trigger();    // the down projection may start issuing its weight loads
   Slot sl;
   if (!resolve_slot(a, blockIdx.y, n_slots, false, sl, tok_s, row_s)) return;
   const int row_base = blockIdx.x * kGuRows;
@@ -155,25 +157,18 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a, int n_sl
   __shared__ float wt_s[kMaxTok];
   Slot sl;
   const bool shared_slot = (int)blockIdx.y >= n_slots;
-  if (!resolve_slot(a, blockIdx.y, n_slots, true, sl, tok_s, row_s)) return;
+  // Routing metadata comes from the router kernel, which finished before the gate/up kernel
+  // passed its own wait; only the SwiGLU outputs need this kernel's wait below.
+  const bool active = resolve_slot(a, blockIdx.y, n_slots, true, sl, tok_s, row_s);
   const int row_base = blockIdx.x * kDnRows;
-  if (row_base >= sl.nrows) return;
+  if (!active || row_base >= sl.nrows) return;
   __syncthreads();
   const int L = shared_slot ? a.S : a.I;        // contraction length
-  for (int i = threadIdx.x; i < sl.ntok * (L / 4); i += blockDim.x) {
-    int j = i / (L / 4), c = i % (L / 4);
-    reinterpret_cast<float4*>(hs)[j * (L / 4) + c] =
-        reinterpret_cast<const float4*>(a.hd + (size_t)row_s[j] * a.ldh)[c];
-  }
-  if (!shared_slot && a.acc) {
-    for (int j = threadIdx.x; j < sl.ntok; j += blockDim.x)
-      wt_s[j] = a.w[a.sorted_pairs[row_s[j]]];
-  }
-  __syncthreads();
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int ntok = sl.ntok, chunks = L / 8;
   const int r0 = row_base + wid * kDnRowsPerWarp;
-  // contraction <= 1024 elements: each lane holds at most 4 chunks of each of its rows
+  // stream this warp's weight rows first: they do not depend on the gate/up results
+  // (contraction <= 1024 elements: each lane holds at most 4 chunks of each of its rows)
   uint4 wv[kDnRowsPerWarp][4];
 #pragma unroll
   for (int rr = 0; rr < kDnRowsPerWarp; ++rr) {
@@ -184,6 +179,18 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a, int n_sl
         wv[rr][q] = ld_stream(reinterpret_cast<const uint4*>(sl.w0 + (size_t)(r0 + rr) * L) + c);
     }
   }
+  pdl_wait();       // SwiGLU outputs of the gate/up kernel
+  pdl_trigger();
+  for (int i = threadIdx.x; i < sl.ntok * (L / 4); i += blockDim.x) {
+    int j = i / (L / 4), c = i % (L / 4);
+    reinterpret_cast<float4*>(hs)[j * (L / 4) + c] =
+        __ldcg(reinterpret_cast<const float4*>(a.hd + (size_t)row_s[j] * a.ldh) + c);
+  }
+  if (!shared_slot && a.acc) {
+    for (int j = threadIdx.x; j < sl.ntok; j += blockDim.x)
+      wt_s[j] = a.w[a.sorted_pairs[row_s[j]]];
+  }
+  __syncthreads();
 #pragma unroll
   for (int rr = 0; rr < kDnRowsPerWarp; ++rr) {
     const int r = r0 + rr;
@@ -240,13 +247,12 @@ cudaError_t launch_decode_gateup(const DecodeArgs& a, cudaStream_t st) {
   dim3 grid((maxrows + kGuRows - 1) / kGuRows, n_slots + 1);
   const int maxtok = a.N < kMaxTok ? a.N : kMaxTok;
   size_t sm = (size_t)maxtok * a.H * 2;
-  if (sm > 48 * 1024) {
+  if (sm > 32 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(decode_gateup_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
   }
-  decode_gateup_kernel<<<grid, 256, sm, st>>>(a, n_slots);
-  return cudaGetLastError();
+  return launch_dependent(decode_gateup_kernel, grid, dim3(256), sm, st, a, n_slots);
 }
 
 cudaError_t launch_decode_down(const DecodeArgs& a, cudaStream_t st) {
@@ -255,13 +261,12 @@ cudaError_t launch_decode_down(const DecodeArgs& a, cudaStream_t st) {
   const int maxtok = a.N < kMaxTok ? a.N : kMaxTok;
   const int maxl = a.I > a.S ? a.I : a.S;
   size_t sm = (size_t)maxtok * maxl * 4;
-  if (sm > 48 * 1024) {
+  if (sm > 32 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(decode_down_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
   }
-  decode_down_kernel<<<grid, 256, sm, st>>>(a, n_slots);
-  return cudaGetLastError();
+  return launch_dependent(decode_down_kernel, grid, dim3(256), sm, st, a, n_slots);
 }
 
 }  // namespace moe

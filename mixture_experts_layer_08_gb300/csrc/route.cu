@@ -176,6 +176,7 @@ __global__ void __launch_bounds__(256) router_small_kernel(RouteArgs a, SortArgs
                                                            int fuse_tail) {
   extern __shared__ __align__(16) uint8_t smem[];
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);     // [tok, H]
+  pdl_trigger();    // the next kernel may launch now and wait for this one's results
   const int H = a.H, R = a.R;
   const int tok0 = blockIdx.y * kRouterTok;
   const int ntok = min(kRouterTok, a.N - tok0);
@@ -404,7 +405,7 @@ cudaError_t launch_router_small(const RouteArgs& a, const SortArgs& s, bool fuse
                                    (size_t)a.E * 4 + 40 * 4
                              : 0;
   size_t sm = sm_x > sm_tail ? sm_x : sm_tail;
-  if (sm > 48 * 1024) {
+  if (sm > 32 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(router_small_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
@@ -415,7 +416,7 @@ cudaError_t launch_router_small(const RouteArgs& a, const SortArgs& s, bool fuse
 
 cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st) {
   size_t sm = (size_t)8 * 2 * a.R * 4;
-  if (sm > 48 * 1024) {
+  if (sm > 32 * 1024) {
     cudaError_t e =
         cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
@@ -428,7 +429,7 @@ cudaError_t launch_sort(const SortArgs& s, const __nv_bfloat16* x, int H, __nv_b
                         uint8_t* xq, float* xs, cudaStream_t st) {
   const int nblk = (s.te + kSortBlock - 1) / kSortBlock;
   size_t sm = (size_t)32 * s.E * 4;
-  if (sm > 48 * 1024) {
+  if (sm > 32 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(sort_count_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;

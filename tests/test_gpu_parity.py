@@ -202,7 +202,7 @@ def test_output_guard_bands_untouched(B):
 
 def _sample_tokens(n, k=12, seed=0):
     rng = np.random.default_rng(seed)
-    return np.unique(np.concatenate([[0, n - 1], rng.choice(n, k, replace=False)]))
+    return np.unique(np.concatenate([[0, n - 1], rng.choice(n, min(k, n), replace=False)]))
 
 
 @pytest.mark.parametrize("shape", [I.DECODE, I.PREFILL, I.ZERO_EXPERT], ids=lambda s: s.name)
