@@ -164,6 +164,28 @@ MOE_API moe_status_t moe_forward_profiled(const moe_config_t *cfg, const moe_wei
                                           const void *x, void *out, void *workspace,
                                           size_t workspace_bytes, void *stream, void **events);
 
+/* The decode chain of moe_forward (bf16 experts, num_tokens <= 16) for callers that cannot
+ * allocate device memory: a plugin hosted by another runtime that owns every allocation and
+ * offers no allocator, or a latency-critical loop that may not call cudaMalloc because it can
+ * synchronise the whole device. The pages have no counterpart; it exists for such callers.
+ * Instead of a caller workspace it uses one 4 MiB scratch array that the CUDA driver places in
+ * device memory when it loads this library's device code (every GPU that loads it holds the
+ * array until the process exits). It allocates nothing and calls no allocating routine.
+ *  - cfg->path must be MOE_PATH_AUTO or MOE_PATH_DECODE; the decode chain is always used.
+ *  - Configurations whose scratch would exceed 4 MiB return MOE_ERR_WORKSPACE_TOO_SMALL
+ *    (moe_workspace_size() with path = MOE_PATH_DECODE gives the bytes needed); grouped-only
+ *    configurations return MOE_ERR_UNSUPPORTED.
+ *  - The first call on each device looks up the array's device address (with that device
+ *    current); make that first call before any stream capture.
+ *  - Every call shares the array and clears what must start at zero itself; calls that
+ *    overlap on the GPU (unordered streams or host threads) race on it.
+ *  - There is no caller workspace, so moe_read_device_status() cannot read this call's
+ *    device status word; a device wait that times out still ends its kernel.
+ * x, out, stream and the weights are as for moe_forward. */
+MOE_API moe_status_t moe_forward_decode_noalloc(const moe_config_t *cfg,
+                                                const moe_weights_t *weights, const void *x,
+                                                void *out, void *stream);
+
 /* Synchronises `stream` and reads the device status word of `workspace` into *status
  * (MOE_OK or MOE_ERR_DEVICE_TIMEOUT). For tests and debugging; it blocks the host. */
 MOE_API moe_status_t moe_read_device_status(const void *workspace, void *stream, int32_t *status);
