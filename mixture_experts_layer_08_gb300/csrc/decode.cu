@@ -8,265 +8,342 @@
 // "metrale_model_layers/layers/moe/forward_atomic_c4.rs" (token-major gate/up for a few rows,
 // routed down projections weighted and FP32-atomic-added into a [N,H] accumulator zeroed
 // first, then a finalize that casts to BF16 and blends the shared expert).
+//
+// Both kernels are persistent (one block per SM) and split the work into items: a few
+// consecutive weight rows of one slot, contiguous in memory. Warp 0 streams items into a
+// shared-memory ring with 1D bulk copies (150-200 KB in flight per SM, enough to keep HBM
+// busy); 8 consumer warps take the dot products against the slot's token vectors. Each block
+// owns a contiguous range of items, so a slot's token list changes rarely within a block.
 #include "kernels.h"
 
 namespace moe {
 
 namespace {
 
-constexpr int kMaxTok = 16;        // tokens per expert the decode chain handles
-constexpr int kGuRowsPerWarp = 2;  // gate/up row pairs per warp
-constexpr int kGuRows = 8 * kGuRowsPerWarp;
-constexpr int kDnRowsPerWarp = 4;  // down rows per warp
-constexpr int kDnRows = 8 * kDnRowsPerWarp;
+constexpr int kMaxTok = 16;          // tokens per expert the decode chain handles
+constexpr int kConsumers = 8;        // consumer warps
+constexpr int kThreads = 32 * (1 + kConsumers);
+constexpr int kSmemBudget = 224 * 1024;   // of the 227 KB a block may opt into
+constexpr int kMaxStages = 4;
+constexpr int kDownRows = 32;        // down-projection rows per item (4 per consumer warp)
 
-// Streaming 16-byte load that does not allocate in L1 (weights are read exactly once).
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+// Contiguous, balanced share [i0, i1) of `total` items for this block.
+__device__ __forceinline__ void item_range(int total, int& i0, int& i1) {
+  const long long G = gridDim.x, b = blockIdx.x;
+  i0 = (int)((total * b) / G);
+  i1 = (int)((total * (b + 1)) / G);
 }
 
-struct Slot {
-  int ntok;
-  const __nv_bfloat16* w0;
-  const __nv_bfloat16* w1;
-  int nrows;
-};
-
-// Resolves block slot `slot`: an active routed expert (slot < n_slots) or the shared expert.
-// Fills the token ids and output rows of the slot in shared memory. Returns false if the
-// slot has no work.
-__device__ bool resolve_slot(const DecodeArgs& a, int slot, int n_slots, bool down, Slot& sl,
-                             int* tok_s, int* row_s) {
-  if (slot < n_slots) {
-    if ((uint32_t)slot >= __ldcg(&a.hdr->num_active)) return false;
-    const int e = (int)__ldcg(a.active + slot);
-    const int r0 = (int)__ldcg(a.offsets + e), r1 = (int)__ldcg(a.offsets + e + 1);
-    sl.ntok = r1 - r0;
-    if (down) {
-      sl.w0 = a.wd + (size_t)e * a.H * a.I;
-      sl.nrows = a.H;
-    } else {
-      sl.w0 = a.wg + (size_t)e * a.I * a.H;
-      sl.w1 = a.wu + (size_t)e * a.I * a.H;
-      sl.nrows = a.I;
-    }
-    for (int j = threadIdx.x; j < sl.ntok; j += blockDim.x) {
-      tok_s[j] = (int)(__ldcg(a.sorted_pairs + r0 + j) / (uint32_t)a.K);
-      row_s[j] = r0 + j;
-    }
-  } else {
-    if (a.S == 0) return false;
-    sl.ntok = a.N;
-    if (down) {
-      sl.w0 = a.sd;
-      sl.nrows = a.H;
-    } else {
-      sl.w0 = a.sg;
-      sl.w1 = a.su;
-      sl.nrows = a.S;
-    }
-    for (int j = threadIdx.x; j < a.N; j += blockDim.x) {
-      tok_s[j] = j;
-      row_s[j] = a.te + j;
-    }
-  }
-  return sl.ntok > 0;
+// Token list of a routed expert: lane j < ntok gets the token id and sorted row of the j-th
+// pair routed to it. Routing metadata is read through L2 (written by an earlier kernel).
+__device__ __forceinline__ int expert_tokens(const DecodeArgs& a, int e, int lane, int& tok,
+                                             int& row) {
+  const int r0 = (int)__ldcg(a.offsets + e), r1 = (int)__ldcg(a.offsets + e + 1);
+  const int ntok = r1 - r0;
+  tok = 0;
+  row = r0 + lane;
+  if (lane < ntok) tok = (int)(__ldcg(a.sorted_pairs + r0 + lane) / (uint32_t)a.K);
+  return ntok;
 }
+
+// ------------------------------------------------------------------ gate/up
 
 // hd[row_j, i] = SiLU(x_j . Wg[i]) * (x_j . Wu[i]) for every token j of the slot.
-__global__ void __launch_bounds__(256) decode_gateup_kernel(DecodeArgs a, int n_slots) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ int tok_s[kMaxTok], row_s[kMaxTok];
-  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);   // [ntok, H]
-  pdl_wait();       // routing of the router kernel
-  pdl_trigger();    // the down projection may start issuing its weight loads
-  Slot sl;
-  if (!resolve_slot(a, blockIdx.y, n_slots, false, sl, tok_s, row_s)) return;
-  const int row_base = blockIdx.x * kGuRows;
-  if (row_base >= sl.nrows) return;
-  __syncthreads();
-  const int H = a.H, chunks = H / 8;
-  for (int i = threadIdx.x; i < sl.ntok * chunks; i += blockDim.x) {
-    int j = i / chunks, c = i % chunks;
-    reinterpret_cast<uint4*>(xs)[j * chunks + c] =
-        reinterpret_cast<const uint4*>(a.x + (size_t)tok_s[j] * H)[c];
+// Item = `rp` consecutive row pairs of one slot: rp gate rows then rp up rows in the stage.
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_gateup_kernel(DecodeArgs a, int rp, int stages, int item_bytes, int xbytes) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int H = a.H, N = a.N;
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);             // [N, H]
+  uint8_t* ring = smem + xbytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)stages * item_bytes);
+  uint64_t* empty = full + kMaxStages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers);
+    }
+    fence_mbarrier_init();
   }
+  // the block input is not produced by the router: stage it before waiting on the router
+  for (int i = threadIdx.x; i < N * H / 8; i += blockDim.x)
+    reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(a.x)[i];
   __syncthreads();
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int ntok = sl.ntok;
-  for (int rr = 0; rr < kGuRowsPerWarp; ++rr) {
-    const int i = row_base + wid * kGuRowsPerWarp + rr;
-    if (i >= sl.nrows) break;
-    float ag[kMaxTok], au[kMaxTok];
-#pragma unroll
-    for (int j = 0; j < kMaxTok; ++j) ag[j] = au[j] = 0.0f;
-    const uint4* g = reinterpret_cast<const uint4*>(sl.w0 + (size_t)i * H);
-    const uint4* u = reinterpret_cast<const uint4*>(sl.w1 + (size_t)i * H);
-    for (int c0 = 0; c0 < chunks; c0 += 256) {
-      uint4 gv[8], uv[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int c = c0 + q * 32 + lane;
-        if (c < chunks) {
-          gv[q] = ld_stream(g + c);
-          uv[q] = ld_stream(u + c);
+  pdl_wait();       // routing of the router kernel
+  pdl_trigger();    // the down projection may start streaming its weights
+
+  const int per_slot = a.I / rp;
+  const int routed = (int)__ldcg(&a.hdr->num_active) * per_slot;
+  const int total = routed + (a.S > 0 ? a.S / rp : 0);
+  int i0, i1;
+  item_range(total, i0, i1);
+  const uint32_t half_bytes = (uint32_t)(rp * H * 2);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      int issued = 0;
+      for (int it = i0; it < i1; ++it, ++issued) {
+        const int k = it - i0, s = k % stages;
+        if (!mbar_wait(&empty[s], ((k / stages) & 1) ^ 1, a.hdr)) { ok = false; break; }
+        const __nv_bfloat16 *g, *u;
+        if (it < routed) {
+          const int e = (int)__ldcg(a.active + it / per_slot);
+          const size_t r = (size_t)e * a.I + (size_t)(it % per_slot) * rp;
+          g = a.wg + r * H;
+          u = a.wu + r * H;
+        } else {
+          const size_t r = (size_t)(it - routed) * rp;
+          g = a.sg + r * H;
+          u = a.su + r * H;
+        }
+        uint8_t* dst = ring + (size_t)s * item_bytes;
+        mbar_arrive_expect_tx(&full[s], 2 * half_bytes);
+        bulk_load(dst, g, half_bytes, &full[s]);
+        bulk_load(dst + half_bytes, u, half_bytes, &full[s]);
+      }
+      if (!ok)   // let the copies already issued land before the block can exit
+        for (int k = issued > stages ? issued - stages : 0; k < issued; ++k)
+          mbar_wait(&full[k % stages], (k / stages) & 1, nullptr);
+    }
+  } else {
+    const int cw = warp - 1;
+    int cur_slot = -2, ntok = 0, tok = 0, orow = 0;
+    for (int it = i0; it < i1; ++it) {
+      const int k = it - i0, s = k % stages;
+      const int slot = it < routed ? it / per_slot : -1;
+      const int i = (it < routed ? (it % per_slot) : (it - routed)) * rp + cw;
+      if (slot != cur_slot) {
+        cur_slot = slot;
+        if (slot >= 0) {
+          ntok = expert_tokens(a, (int)__ldcg(a.active + slot), lane, tok, orow);
+        } else {
+          ntok = N;
+          tok = lane;
+          orow = a.te + lane;
         }
       }
+      if (!mbar_wait(&full[s], (k / stages) & 1, a.hdr)) break;
+      if (cw < rp) {
+        const uint8_t* st = ring + (size_t)s * item_bytes + (size_t)cw * H * 2;
+        const uint4* gr = reinterpret_cast<const uint4*>(st);
+        const uint4* ur = reinterpret_cast<const uint4*>(st + half_bytes);
+        float ag[kMaxTok], au[kMaxTok];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int c = c0 + q * 32 + lane;
-        if (c < chunks) {
+        for (int j = 0; j < kMaxTok; ++j) ag[j] = au[j] = 0.0f;
+        for (int c = lane; c < H / 8; c += 32) {
           float gf[8], uf[8];
-          bf16x8_to_f32(gv[q], gf);
-          bf16x8_to_f32(uv[q], uf);
+          bf16x8_to_f32(gr[c], gf);
+          bf16x8_to_f32(ur[c], uf);
 #pragma unroll
           for (int j = 0; j < kMaxTok; ++j) {
             if (j < ntok) {
+              const int tj = __shfl_sync(0xffffffffu, tok, j);
               float xf[8];
-              bf16x8_to_f32(reinterpret_cast<const uint4*>(xs)[j * chunks + c], xf);
+              bf16x8_to_f32(reinterpret_cast<const uint4*>(xs + (size_t)tj * H)[c], xf);
 #pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                ag[j] = fmaf(gf[k], xf[k], ag[j]);
-                au[j] = fmaf(uf[k], xf[k], au[j]);
+              for (int q = 0; q < 8; ++q) {
+                ag[j] = fmaf(gf[q], xf[q], ag[j]);
+                au[j] = fmaf(uf[q], xf[q], au[j]);
               }
             }
           }
         }
-      }
-    }
 #pragma unroll
-    for (int j = 0; j < kMaxTok; ++j) {
-      if (j < ntok) {
-        const float gs = warp_sum(ag[j]);
-        const float us = warp_sum(au[j]);
-        if (lane == 0) a.hd[(size_t)row_s[j] * a.ldh + i] = silu(gs) * us;
+        for (int j = 0; j < kMaxTok; ++j) {
+          if (j < ntok) {
+            const float gs = warp_sum(ag[j]);
+            const float us = warp_sum(au[j]);
+            const int rj = __shfl_sync(0xffffffffu, orow, j);
+            if (lane == 0) a.hd[(size_t)rj * a.ldh + i] = silu(gs) * us;
+          }
+        }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
 }
 
-// y_j[r] = h_j . Wd[r] for every token j of the slot; routed results go to yd (or are
-// weighted and atomically added into acc), shared results to shy.
-__global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a, int n_slots) {
-  extern __shared__ __align__(16) float hs[];                   // [ntok, L]
-  __shared__ int tok_s[kMaxTok], row_s[kMaxTok];
-  __shared__ float wt_s[kMaxTok];
-  Slot sl;
-  const bool shared_slot = (int)blockIdx.y >= n_slots;
-  // Routing metadata comes from the router kernel, which finished before the gate/up kernel
-  // passed its own wait; only the SwiGLU outputs need this kernel's wait below.
-  const bool active = resolve_slot(a, blockIdx.y, n_slots, true, sl, tok_s, row_s);
-  const int row_base = blockIdx.x * kDnRows;
-  if (!active || row_base >= sl.nrows) return;
-  __syncthreads();
-  const int L = shared_slot ? a.S : a.I;        // contraction length
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int ntok = sl.ntok, chunks = L / 8;
-  const int r0 = row_base + wid * kDnRowsPerWarp;
-  // stream this warp's weight rows first: they do not depend on the gate/up results
-  // (contraction <= 1024 elements: each lane holds at most 4 chunks of each of its rows)
-  uint4 wv[kDnRowsPerWarp][4];
-#pragma unroll
-  for (int rr = 0; rr < kDnRowsPerWarp; ++rr) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int c = q * 32 + lane;
-      if (r0 + rr < sl.nrows && c < chunks)
-        wv[rr][q] = ld_stream(reinterpret_cast<const uint4*>(sl.w0 + (size_t)(r0 + rr) * L) + c);
+// ------------------------------------------------------------------ down
+
+// y_j[r] = h_j . Wd[r] for every token j of the slot. Item = kDownRows consecutive rows of
+// Wd_e (or of the shared down weights); routed results go to yd, or are weighted and
+// atomically added into acc; shared results go to shy.
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_down_kernel(DecodeArgs a, int stages, int item_bytes) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)stages * item_bytes);
+  uint64_t* empty = full + kMaxStages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = a.H;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers);
     }
-  }
-  pdl_wait();       // SwiGLU outputs of the gate/up kernel
-  pdl_trigger();
-  for (int i = threadIdx.x; i < sl.ntok * (L / 4); i += blockDim.x) {
-    int j = i / (L / 4), c = i % (L / 4);
-    reinterpret_cast<float4*>(hs)[j * (L / 4) + c] =
-        __ldcg(reinterpret_cast<const float4*>(a.hd + (size_t)row_s[j] * a.ldh) + c);
-  }
-  if (!shared_slot && a.acc) {
-    for (int j = threadIdx.x; j < sl.ntok; j += blockDim.x)
-      wt_s[j] = a.w[a.sorted_pairs[row_s[j]]];
+    fence_mbarrier_init();
   }
   __syncthreads();
+  // Routing metadata comes from the router kernel, which finished before the gate/up kernel
+  // passed its own wait, so the weights can stream before this kernel's wait; only the
+  // consumers read the SwiGLU outputs and wait for them.
+  const int per_slot = H / kDownRows;
+  const int routed = (int)__ldcg(&a.hdr->num_active) * per_slot;
+  const int total = routed + (a.S > 0 ? per_slot : 0);
+  int i0, i1;
+  item_range(total, i0, i1);
+
+  if (warp == 0) {
+    pdl_trigger();
+    if (lane == 0) {
+      bool ok = true;
+      int issued = 0;
+      for (int it = i0; it < i1; ++it, ++issued) {
+        const int k = it - i0, s = k % stages;
+        if (!mbar_wait(&empty[s], ((k / stages) & 1) ^ 1, a.hdr)) { ok = false; break; }
+        const __nv_bfloat16* src;
+        uint32_t bytes;
+        if (it < routed) {
+          const int e = (int)__ldcg(a.active + it / per_slot);
+          src = a.wd + ((size_t)e * H + (size_t)(it % per_slot) * kDownRows) * a.I;
+          bytes = (uint32_t)(kDownRows * a.I * 2);
+        } else {
+          src = a.sd + (size_t)(it - routed) * kDownRows * a.S;
+          bytes = (uint32_t)(kDownRows * a.S * 2);
+        }
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_load(ring + (size_t)s * item_bytes, src, bytes, &full[s]);
+      }
+      if (!ok)
+        for (int k = issued > stages ? issued - stages : 0; k < issued; ++k)
+          mbar_wait(&full[k % stages], (k / stages) & 1, nullptr);
+    }
+  } else {
+    pdl_wait();     // SwiGLU outputs of the gate/up kernel
+    pdl_trigger();
+    const int cw = warp - 1;
+    int cur_slot = -2, ntok = 0, tok = 0, orow = 0;
+    float wt = 0.0f;
+    for (int it = i0; it < i1; ++it) {
+      const int k = it - i0, s = k % stages;
+      const bool shared_item = it >= routed;
+      const int slot = shared_item ? -1 : it / per_slot;
+      const int rbase = (shared_item ? it - routed : it % per_slot) * kDownRows;
+      const int L = shared_item ? a.S : a.I;
+      if (slot != cur_slot) {
+        cur_slot = slot;
+        if (!shared_item) {
+          ntok = expert_tokens(a, (int)__ldcg(a.active + slot), lane, tok, orow);
+          if (a.acc && lane < ntok) wt = a.w[__ldcg(a.sorted_pairs + orow)];
+        } else {
+          ntok = a.N;
+          tok = lane;
+          orow = a.te + lane;
+        }
+      }
+      if (!mbar_wait(&full[s], (k / stages) & 1, a.hdr)) break;
+      const uint8_t* stage = ring + (size_t)s * item_bytes;
+#pragma unroll 1
+      for (int rr = 0; rr < kDownRows / kConsumers; ++rr) {
+        const int rl = cw * (kDownRows / kConsumers) + rr;
+        const uint4* wr = reinterpret_cast<const uint4*>(stage + (size_t)rl * L * 2);
+        float acc[kMaxTok];
 #pragma unroll
-  for (int rr = 0; rr < kDnRowsPerWarp; ++rr) {
-    const int r = r0 + rr;
-    if (r >= sl.nrows) break;
-    float acc[kMaxTok];
+        for (int j = 0; j < kMaxTok; ++j) acc[j] = 0.0f;
+        for (int c = lane; c < L / 8; c += 32) {
+          float wf[8];
+          bf16x8_to_f32(wr[c], wf);
 #pragma unroll
-    for (int j = 0; j < kMaxTok; ++j) acc[j] = 0.0f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int c = q * 32 + lane;
-      if (c < chunks) {
-        float wf[8];
-        bf16x8_to_f32(wv[rr][q], wf);
+          for (int j = 0; j < kMaxTok; ++j) {
+            if (j < ntok) {
+              const int rj = __shfl_sync(0xffffffffu, orow, j);
+              const float4* hp =
+                  reinterpret_cast<const float4*>(a.hd + (size_t)rj * a.ldh) + 2 * c;
+              const float4 h0 = hp[0], h1 = hp[1];
+              acc[j] = fmaf(wf[0], h0.x, acc[j]);
+              acc[j] = fmaf(wf[1], h0.y, acc[j]);
+              acc[j] = fmaf(wf[2], h0.z, acc[j]);
+              acc[j] = fmaf(wf[3], h0.w, acc[j]);
+              acc[j] = fmaf(wf[4], h1.x, acc[j]);
+              acc[j] = fmaf(wf[5], h1.y, acc[j]);
+              acc[j] = fmaf(wf[6], h1.z, acc[j]);
+              acc[j] = fmaf(wf[7], h1.w, acc[j]);
+            }
+          }
+        }
+        const int r = rbase + rl;
 #pragma unroll
         for (int j = 0; j < kMaxTok; ++j) {
           if (j < ntok) {
-            const float4 h0 = reinterpret_cast<const float4*>(hs + j * L)[2 * c];
-            const float4 h1 = reinterpret_cast<const float4*>(hs + j * L)[2 * c + 1];
-            acc[j] = fmaf(wf[0], h0.x, acc[j]);
-            acc[j] = fmaf(wf[1], h0.y, acc[j]);
-            acc[j] = fmaf(wf[2], h0.z, acc[j]);
-            acc[j] = fmaf(wf[3], h0.w, acc[j]);
-            acc[j] = fmaf(wf[4], h1.x, acc[j]);
-            acc[j] = fmaf(wf[5], h1.y, acc[j]);
-            acc[j] = fmaf(wf[6], h1.z, acc[j]);
-            acc[j] = fmaf(wf[7], h1.w, acc[j]);
+            const float y = warp_sum(acc[j]);
+            const int tj = __shfl_sync(0xffffffffu, tok, j);
+            const int rj = __shfl_sync(0xffffffffu, orow, j);
+            const float wj = __shfl_sync(0xffffffffu, wt, j);
+            if (lane == 0) {
+              if (shared_item) a.shy[(size_t)tj * H + r] = y;
+              else if (a.acc) atomicAdd(a.acc + (size_t)tj * H + r, wj * y);
+              else a.yd[(size_t)rj * H + r] = y;
+            }
           }
         }
       }
-    }
-#pragma unroll
-    for (int j = 0; j < kMaxTok; ++j) {
-      if (j < ntok) {
-        const float y = warp_sum(acc[j]);
-        if (lane == 0) {
-          if (shared_slot) {
-            a.shy[(size_t)tok_s[j] * a.H + r] = y;
-          } else if (a.acc) {
-            atomicAdd(a.acc + (size_t)tok_s[j] * a.H + r, wt_s[j] * y);
-          } else {
-            a.yd[(size_t)row_s[j] * a.H + r] = y;
-          }
-        }
-      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
+}
+
+int sm_count() {
+  static int cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
 }
 
 }  // namespace
 
 cudaError_t launch_decode_gateup(const DecodeArgs& a, cudaStream_t st) {
-  const int n_slots = a.te < a.E ? a.te : a.E;
-  const int maxrows = a.I > a.S ? a.I : a.S;
-  dim3 grid((maxrows + kGuRows - 1) / kGuRows, n_slots + 1);
-  const int maxtok = a.N < kMaxTok ? a.N : kMaxTok;
-  size_t sm = (size_t)maxtok * a.H * 2;
-  if (sm > 32 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(decode_gateup_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    if (e != cudaSuccess) return e;
-  }
-  return launch_dependent(decode_gateup_kernel, grid, dim3(256), sm, st, a, n_slots);
+  const int xbytes = (a.N * a.H * 2 + 127) & ~127;
+  // row pairs per item: the most (<= 8, one per consumer warp) that keep 3 stages in budget
+  int rp = 8;
+  while (rp > 1 && (a.I % rp || (a.S && a.S % rp) ||
+                    (size_t)xbytes + 3 * (size_t)rp * 4 * a.H + 1024 > (size_t)kSmemBudget))
+    rp >>= 1;
+  const int item = rp * 4 * a.H;
+  int stages = (kSmemBudget - 1024 - xbytes) / item;
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 1) return cudaErrorInvalidValue;
+  const size_t sm = (size_t)xbytes + (size_t)stages * item + 2 * kMaxStages * 8;
+  cudaError_t e = cudaFuncSetAttribute(decode_gateup_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(decode_gateup_kernel, dim3(sm_count()), dim3(kThreads), sm, st, a, rp,
+                          stages, item, xbytes);
 }
 
 cudaError_t launch_decode_down(const DecodeArgs& a, cudaStream_t st) {
-  const int n_slots = a.te < a.E ? a.te : a.E;
-  dim3 grid((a.H + kDnRows - 1) / kDnRows, n_slots + 1);
-  const int maxtok = a.N < kMaxTok ? a.N : kMaxTok;
-  const int maxl = a.I > a.S ? a.I : a.S;
-  size_t sm = (size_t)maxtok * maxl * 4;
-  if (sm > 32 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(decode_down_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    if (e != cudaSuccess) return e;
-  }
-  return launch_dependent(decode_down_kernel, grid, dim3(256), sm, st, a, n_slots);
+  if (a.H % kDownRows) return cudaErrorInvalidValue;
+  const int L = a.I > a.S ? a.I : a.S;
+  const int item = kDownRows * L * 2;
+  int stages = (kSmemBudget - 1024) / item;
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 1) return cudaErrorInvalidValue;
+  const size_t sm = (size_t)stages * item + 2 * kMaxStages * 8;
+  cudaError_t e = cudaFuncSetAttribute(decode_down_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(decode_down_kernel, dim3(sm_count()), dim3(kThreads), sm, st, a, stages,
+                          item);
 }
 
 }  // namespace moe

@@ -195,16 +195,28 @@ __global__ void __launch_bounds__(256) router_small_kernel(RouteArgs a, SortArgs
 #pragma unroll
     for (int t = 0; t < kRouterTok; ++t) acc[t] = 0.0f;
     const uint4* wrow = reinterpret_cast<const uint4*>(a.router_w + (size_t)r * H);
-    for (int c = lane; c < chunks; c += 32) {
-      float wf[8];
-      bf16x8_to_f32(wrow[c], wf);
+    for (int c0 = 0; c0 < chunks; c0 += 256) {
+      uint4 wv[8];            // all of this lane's loads in flight before any arithmetic
 #pragma unroll
-      for (int t = 0; t < kRouterTok; ++t) {
-        if (t < ntok) {
-          float xf[8];
-          bf16x8_to_f32(reinterpret_cast<const uint4*>(xs)[t * chunks + c], xf);
+      for (int q = 0; q < 8; ++q) {
+        const int c = c0 + q * 32 + lane;
+        if (c < chunks) wv[q] = __ldg(wrow + c);
+      }
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[t] = fmaf(wf[i], xf[i], acc[t]);
+      for (int q = 0; q < 8; ++q) {
+        const int c = c0 + q * 32 + lane;
+        if (c < chunks) {
+          float wf[8];
+          bf16x8_to_f32(wv[q], wf);
+#pragma unroll
+          for (int t = 0; t < kRouterTok; ++t) {
+            if (t < ntok) {
+              float xf[8];
+              bf16x8_to_f32(reinterpret_cast<const uint4*>(xs)[t * chunks + c], xf);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) acc[t] = fmaf(wf[i], xf[i], acc[t]);
+            }
+          }
         }
       }
     }
