@@ -122,7 +122,9 @@ def kernels_per_step(B, cfg):
                                             and cfg.weight_dtype == 0)
     if decode:
         return 4            # fused router + top-K + sort, gate/up, down, combine
-    return 8 + (2 if cfg.shared_inter else 0)   # router, top-K, 3 sort, [2 shared], 2 GEMM, combine
+    # router, top-K, 3 sort, gate/up GEMM, down GEMM, combine; FP8 experts run the bf16 shared
+    # expert in two launches of its own
+    return 8 + (2 if cfg.shared_inter and cfg.weight_dtype == 1 else 0)
 
 
 def barrier():
@@ -231,6 +233,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the zero-expert, FP8 and tiny workloads")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--profile-only", choices=["decode", "prefill", "fp8", "zero_expert"],
                     help="run one workload's timing loop only (for ncu captures); prints a "
@@ -349,6 +353,30 @@ def main():
             "min_expert_rows": int(p["rs"]["counts"].min()),
             "clocks": p["clocks"]}
         line["gpu_launches"] += p["launches_per_step"] * max(3, args.steps // 2)
+    if not args.no_extra:
+        extra = {}
+        for shp in (I.ZERO_EXPERT, I.FP8_PREFILL, I.TINY):
+            x = time_ours(B, shp, max(3, args.steps // 2), warmup, dev, peaks, with_e2e=False)
+            xa = x["alg"]
+            fp8 = shp.weight_dtype == I.WDTYPE_FP8_E4M3_B128
+            tpeak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+            gu = x["stage_ms"]["gate_up"]
+            extra[shp.name] = {
+                "value": shp.num_tokens / (x["ms"] / 1000.0), "unit": "tokens/s",
+                "ms_per_step": x["ms"],
+                "stage_us": {k: 1000 * v for k, v in x["stage_ms"].items()},
+                "gate_up_tflops": xa["gate_up_flops"] / (gu / 1000.0) / 1e12,
+                "gate_up_tensor_frac": xa["gate_up_flops"] / (gu / 1000.0) / 1e12 / tpeak,
+                "gate_up_hbm_frac": xa["gate_up_bytes"] / (gu / 1000.0) / 1e9 / peaks["hbm_gbs"],
+                "tensor_peak_tflops": tpeak,
+                "tensor_peak_src": "2 x measured bf16 (nominal fp8:bf16 ratio)" if fp8 else "measured bf16",
+                "step_hbm_frac": xa["bytes"] / (x["ms"] / 1000.0) / 1e9 / peaks["hbm_gbs"],
+                "step_tensor_frac": xa["flops"] / (x["ms"] / 1000.0) / 1e12 / tpeak,
+                "Z": x["rs"]["Z"], "distinct_experts": x["rs"]["distinct"]}
+            line["gpu_launches"] += x["launches_per_step"] * max(3, args.steps // 2)
+            del x
+            torch.cuda.empty_cache()
+        line["other_workloads"] = extra
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_oracle_tokens_per_s(r["inp"])
     if world > 1:

@@ -24,7 +24,7 @@ constexpr int kSmallRouterMaxTokens = 64;
 
 enum Region {
   R_HDR, R_LOGITS, R_IDX, R_W, R_ZSUM, R_BLK, R_LRANK, R_OFFS, R_P2R, R_SPAIRS, R_ACTIVE,
-  R_TILES, R_XP, R_XS, R_HH, R_HS, R_Y, R_SHH, R_SHY, R_HD, R_YD, R_ACC, R_NUM
+  R_TILES, R_STOK, R_XP, R_XS, R_HH, R_HS, R_Y, R_SHH, R_SHY, R_HD, R_YD, R_ACC, R_NUM
 };
 
 struct Layout {
@@ -96,13 +96,14 @@ Layout make_layout(const moe_config_t* c) {
     sz[R_BLK] = (size_t)L.nblk * E * 4;
     sz[R_LRANK] = te * 4;
     sz[R_TILES] = (size_t)L.max_mtiles * 16;
+    sz[R_STOK] = te * 4;                 // token of each sorted row (bf16 rows are gathered
+                                         // straight from x by the gate/up GEMM)
     if (c->weight_dtype == MOE_W_FP8_E4M3_B128) {
       sz[R_XP] = te * H;                 // E4M3 codes of the gathered rows
       sz[R_XS] = (H / 128) * te * 4;     // their 1x128 scales, [H/128, te]
       sz[R_HH] = te * I;                 // E4M3 codes of the SwiGLU intermediate
       sz[R_HS] = (I / 128) * te * 4;
     } else {
-      sz[R_XP] = te * H * 2;
       sz[R_HH] = te * I * 2;
     }
     sz[R_Y] = te * H * 2;
@@ -280,6 +281,7 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
   sa.sorted_pairs = P.at<uint32_t>(R_SPAIRS);
   sa.active = P.at<uint32_t>(R_ACTIVE);
   sa.tiles = P.at<int4>(R_TILES);
+  sa.sorted_tok = P.at<uint32_t>(R_STOK);
   sa.hdr = hdr;
 
   CK(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
@@ -291,26 +293,26 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
     CK(launch_router_small(ra, sa, false, st));
   } else {
     // router logits on the tensor cores: [N,H] x [R,H]^T -> fp32 [N,R]
-    CUtensorMap ma, mb;
-    if (!make_map_bf16(&ma, x, c->hidden, c->num_tokens, 128) ||
-        !make_map_bf16(&mb, w->router_w, c->hidden, c->router_width, 128))
+    CUtensorMap maps[2][3];
+    if (!make_map_bf16(&maps[0][0], x, c->hidden, c->num_tokens, 128) ||
+        !make_map_bf16(&maps[0][1], w->router_w, c->hidden, c->router_width, 128))
       return MOE_ERR_CUDA;
+    maps[0][2] = maps[0][1];
     GemmArgs g{};
-    g.dense_m = c->num_tokens;
-    g.max_mtiles = (c->num_tokens + 127) / 128;
-    g.n_tiles = (c->router_width + 127) / 128;
-    g.num_kb = c->hidden / 64;
-    g.b_rows_per_expert = 0;
-    g.out = ra.logits;
-    g.ldo = c->router_width;
-    g.n_valid = c->router_width;
+    g.nprob = 1;
+    g.p[0].dense_m = c->num_tokens;
+    g.p[0].max_mtiles = (c->num_tokens + 127) / 128;
+    g.p[0].n_tiles = (c->router_width + 127) / 128;
+    g.p[0].num_kb = c->hidden / 64;
+    g.p[0].out = ra.logits;
+    g.p[0].ldo = c->router_width;
+    g.p[0].n_valid = c->router_width;
     g.status = hdr;
-    CK(launch_gemm_bf16(kGemmStoreF32, 128, ma, mb, mb, g, num_sms(), st));
+    CK(launch_gemm_bf16(kGemmStoreF32, 128, false, maps, g, num_sms(), st));
   }
   CK(launch_topk(ra, st));
   const bool fp8 = c->weight_dtype == MOE_W_FP8_E4M3_B128;
-  CK(launch_sort(sa, ra.x, c->hidden,
-                 gather && !fp8 ? P.at<__nv_bfloat16>(R_XP) : nullptr,
+  CK(launch_sort(sa, ra.x, c->hidden, nullptr,
                  gather && fp8 ? P.at<uint8_t>(R_XP) : nullptr,
                  gather && fp8 ? P.at<float>(R_XS) : nullptr, st));
   return MOE_OK;
@@ -324,29 +326,42 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
   WsHeader* hdr = P.at<WsHeader>(R_HDR);
   const int sms = num_sms();
   const int bn_h = (H % 256 == 0) ? 256 : 128;   // N-tile of the projections back to H
-  // shared expert: dense SwiGLU FFN on all N rows
-  MARK(MOE_STAGE_SHARED, 0);
+  const bool fp8 = c->weight_dtype == MOE_W_FP8_E4M3_B128;
+  // Shared expert: a dense SwiGLU FFN on all N rows. With bf16 experts it is problem 0 of the
+  // routed launches below; with FP8 experts it runs as its own bf16 launches here.
+  CUtensorMap sh_gu[3], sh_dn[3];
+  GemmProblem sh_gu_p{}, sh_dn_p{};
   if (S > 0) {
-    CUtensorMap ma, mg, mu, mh, md;
-    if (!make_map_bf16(&ma, x, H, N, 128) || !make_map_bf16(&mg, w->sh_gate, H, S, 128) ||
-        !make_map_bf16(&mu, w->sh_up, H, S, 128) ||
-        !make_map_bf16(&mh, P.at<void>(R_SHH), S, N, 128) ||
-        !make_map_bf16(&md, w->sh_down, S, H, bn_h))
+    if (!make_map_bf16(&sh_gu[0], x, H, N, fp8 ? 128 : 1) ||
+        !make_map_bf16(&sh_gu[1], w->sh_gate, H, S, 128) ||
+        !make_map_bf16(&sh_gu[2], w->sh_up, H, S, 128) ||
+        !make_map_bf16(&sh_dn[0], P.at<void>(R_SHH), S, N, 128) ||
+        !make_map_bf16(&sh_dn[1], w->sh_down, S, H, bn_h))
       return MOE_ERR_CUDA;
+    sh_dn[2] = sh_dn[1];
+    sh_gu_p.dense_m = N;
+    sh_gu_p.max_mtiles = (N + 127) / 128;
+    sh_gu_p.n_tiles = S / 128;
+    sh_gu_p.num_kb = H / 64;
+    sh_gu_p.out = P.at<void>(R_SHH);
+    sh_gu_p.ldo = S;
+    sh_dn_p = sh_gu_p;
+    sh_dn_p.n_tiles = H / bn_h;
+    sh_dn_p.num_kb = S / 64;
+    sh_dn_p.out = P.at<void>(R_SHY);
+    sh_dn_p.ldo = H;
+  }
+  MARK(MOE_STAGE_SHARED, 0);
+  if (S > 0 && fp8) {
+    CUtensorMap maps[2][3] = {{sh_gu[0], sh_gu[1], sh_gu[2]}, {sh_gu[0], sh_gu[1], sh_gu[2]}};
     GemmArgs g{};
-    g.dense_m = N;
-    g.max_mtiles = (N + 127) / 128;
-    g.n_tiles = S / 128;
-    g.num_kb = H / 64;
-    g.out = P.at<void>(R_SHH);
-    g.ldo = S;
+    g.nprob = 1;
+    g.p[0] = sh_gu_p;
     g.status = hdr;
-    CK(launch_gemm_bf16(kGemmSwiGLU, 256, ma, mg, mu, g, sms, st));
-    g.n_tiles = H / bn_h;
-    g.num_kb = S / 64;
-    g.out = P.at<void>(R_SHY);
-    g.ldo = H;
-    CK(launch_gemm_bf16(kGemmStoreBF16, bn_h, mh, md, md, g, sms, st));
+    CK(launch_gemm_bf16(kGemmSwiGLU, 256, false, maps, g, sms, st));
+    CUtensorMap dmaps[2][3] = {{sh_dn[0], sh_dn[1], sh_dn[2]}, {sh_dn[0], sh_dn[1], sh_dn[2]}};
+    g.p[0] = sh_dn_p;
+    CK(launch_gemm_bf16(kGemmStoreBF16, bn_h, false, dmaps, g, sms, st));
   }
   MARK(MOE_STAGE_SHARED, 1);
   // routed experts: grouped gate/up + SiLU*up, then grouped down, over the sorted rows
@@ -393,34 +408,59 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
     CK(launch_gemm_fp8(1, mh, md, md, g, sms, st));
     MARK(MOE_STAGE_DOWN, 1);
   } else {
-    CUtensorMap ma, mg, mu, mh, md;
+    // routed problem (plus the shared expert as problem 0 when present)
+    CUtensorMap gu[3], dn[3];
     const uint64_t rows = (uint64_t)L.te;
-    if (!make_map_bf16(&ma, P.at<void>(R_XP), H, rows, 128) ||
-        !make_map_bf16(&mg, w->w_gate, H, (uint64_t)E * I, 128) ||
-        !make_map_bf16(&mu, w->w_up, H, (uint64_t)E * I, 128) ||
-        !make_map_bf16(&mh, P.at<void>(R_HH), I, rows, 128) ||
-        !make_map_bf16(&md, w->w_down, I, (uint64_t)E * H, bn_h))
+    if (!make_map_bf16(&gu[0], x, H, (uint64_t)N, 1) ||
+        !make_map_bf16(&gu[1], w->w_gate, H, (uint64_t)E * I, 128) ||
+        !make_map_bf16(&gu[2], w->w_up, H, (uint64_t)E * I, 128) ||
+        !make_map_bf16(&dn[0], P.at<void>(R_HH), I, rows, 128) ||
+        !make_map_bf16(&dn[1], w->w_down, I, (uint64_t)E * H, bn_h))
       return MOE_ERR_CUDA;
+    dn[2] = dn[1];
+    GemmProblem rgu{};
+    rgu.tiles = P.at<int4>(R_TILES);
+    rgu.count = hdr;
+    rgu.max_mtiles = L.max_mtiles;
+    rgu.n_tiles = I / 128;
+    rgu.num_kb = H / 64;
+    rgu.b_rows_per_expert = I;
+    rgu.a_rows = P.at<uint32_t>(R_STOK);
+    rgu.out = P.at<void>(R_HH);
+    rgu.ldo = I;
+    GemmProblem rdn = rgu;
+    rdn.a_rows = nullptr;
+    rdn.n_tiles = H / bn_h;
+    rdn.num_kb = I / 64;
+    rdn.b_rows_per_expert = H;
+    rdn.out = P.at<void>(R_Y);
+    rdn.ldo = H;
     GemmArgs g{};
-    g.tiles = P.at<int4>(R_TILES);
-    g.hdr = hdr;
-    g.max_mtiles = L.max_mtiles;
-    g.n_tiles = I / 128;
-    g.num_kb = H / 64;
-    g.b_rows_per_expert = I;
-    g.out = P.at<void>(R_HH);
-    g.ldo = I;
     g.status = hdr;
+    CUtensorMap maps[2][3];
+    if (S > 0) {
+      g.nprob = 2;
+      g.p[0] = sh_gu_p;
+      g.p[1] = rgu;
+      for (int i = 0; i < 3; ++i) { maps[0][i] = sh_gu[i]; maps[1][i] = gu[i]; }
+    } else {
+      g.nprob = 1;
+      g.p[0] = rgu;
+      for (int i = 0; i < 3; ++i) maps[0][i] = maps[1][i] = gu[i];
+    }
     MARK(MOE_STAGE_GATE_UP, 0);
-    CK(launch_gemm_bf16(kGemmSwiGLU, 256, ma, mg, mu, g, sms, st));
+    CK(launch_gemm_bf16(kGemmSwiGLU, 256, true, maps, g, sms, st));
     MARK(MOE_STAGE_GATE_UP, 1);
-    g.n_tiles = H / bn_h;
-    g.num_kb = I / 64;
-    g.b_rows_per_expert = H;
-    g.out = P.at<void>(R_Y);
-    g.ldo = H;
+    if (S > 0) {
+      g.p[0] = sh_dn_p;
+      g.p[1] = rdn;
+      for (int i = 0; i < 3; ++i) { maps[0][i] = sh_dn[i]; maps[1][i] = dn[i]; }
+    } else {
+      g.p[0] = rdn;
+      for (int i = 0; i < 3; ++i) maps[0][i] = maps[1][i] = dn[i];
+    }
     MARK(MOE_STAGE_DOWN, 0);
-    CK(launch_gemm_bf16(kGemmStoreBF16, bn_h, mh, md, md, g, sms, st));
+    CK(launch_gemm_bf16(kGemmStoreBF16, bn_h, false, maps, g, sms, st));
     MARK(MOE_STAGE_DOWN, 1);
   }
   CombineArgs ca{};

@@ -62,14 +62,24 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(CombineArgs a) {
     load8(a.acc, 1, (size_t)t * H + h0, acc);
   }
   if (a.y) {
-    for (int k = 0; k < a.K; ++k) {
-      const uint32_t row = a.pair_to_row[t * a.K + k];
-      if (row == kNoRow) continue;
-      const float wk = a.w[t * a.K + k];
-      float yf[8];
-      load8(a.y, a.y_is_f32, (size_t)row * H + h0, yf);
+    // all of the token's expert rows in flight at once: 8 slots per round
+    for (int k0 = 0; k0 < a.K; k0 += 8) {
+      float yf[8][8];
+      float wk[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk, yf[i], acc[i]);
+      for (int u = 0; u < 8; ++u) {
+        const int k = k0 + u;
+        const uint32_t row = k < a.K ? a.pair_to_row[t * a.K + k] : kNoRow;
+        wk[u] = row != kNoRow ? a.w[t * a.K + k] : 0.0f;
+        if (row != kNoRow) load8(a.y, a.y_is_f32, (size_t)row * H + h0, yf[u]);
+        else
+#pragma unroll
+          for (int i = 0; i < 8; ++i) yf[u][i] = 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk[u], yf[u][i], acc[i]);
     }
   }
   {

@@ -131,8 +131,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint4* gr = reinterpret_cast<const uint4*>(st);
         const uint4* ur = reinterpret_cast<const uint4*>(st + half_bytes);
         float ag[kMaxTok], au[kMaxTok];
+        int tks[kMaxTok];     // token ids, gathered while the whole warp is converged
 #pragma unroll
-        for (int j = 0; j < kMaxTok; ++j) ag[j] = au[j] = 0.0f;
+        for (int j = 0; j < kMaxTok; ++j) {
+          ag[j] = au[j] = 0.0f;
+          tks[j] = __shfl_sync(0xffffffffu, tok, j);
+        }
         for (int c = lane; c < H / 8; c += 32) {
           float gf[8], uf[8];
           bf16x8_to_f32(gr[c], gf);
@@ -140,9 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < kMaxTok; ++j) {
             if (j < ntok) {
-              const int tj = __shfl_sync(0xffffffffu, tok, j);
               float xf[8];
-              bf16x8_to_f32(reinterpret_cast<const uint4*>(xs + (size_t)tj * H)[c], xf);
+              bf16x8_to_f32(reinterpret_cast<const uint4*>(xs + (size_t)tks[j] * H)[c], xf);
 #pragma unroll
               for (int q = 0; q < 8; ++q) {
                 ag[j] = fmaf(gf[q], xf[q], ag[j]);
@@ -252,17 +255,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rl = cw * (kDownRows / kConsumers) + rr;
         const uint4* wr = reinterpret_cast<const uint4*>(stage + (size_t)rl * L * 2);
         float acc[kMaxTok];
+        int rws[kMaxTok];     // SwiGLU rows, gathered while the whole warp is converged
 #pragma unroll
-        for (int j = 0; j < kMaxTok; ++j) acc[j] = 0.0f;
+        for (int j = 0; j < kMaxTok; ++j) {
+          acc[j] = 0.0f;
+          rws[j] = __shfl_sync(0xffffffffu, orow, j);
+        }
         for (int c = lane; c < L / 8; c += 32) {
           float wf[8];
           bf16x8_to_f32(wr[c], wf);
 #pragma unroll
           for (int j = 0; j < kMaxTok; ++j) {
             if (j < ntok) {
-              const int rj = __shfl_sync(0xffffffffu, orow, j);
               const float4* hp =
-                  reinterpret_cast<const float4*>(a.hd + (size_t)rj * a.ldh) + 2 * c;
+                  reinterpret_cast<const float4*>(a.hd + (size_t)rws[j] * a.ldh) + 2 * c;
               const float4 h0 = hp[0], h1 = hp[1];
               acc[j] = fmaf(wf[0], h0.x, acc[j]);
               acc[j] = fmaf(wf[1], h0.y, acc[j]);

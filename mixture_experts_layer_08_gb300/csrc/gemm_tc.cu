@@ -2,15 +2,20 @@
 //
 // D[rows of expert e, n-tile] = A[rows, K] . B_e[n-tile rows, K]^T over the expert-sorted
 // rows, with the epilogue fused: SiLU(gate) * up -> bf16 (gate/up projection), plain bf16
-// store (down projection, shared expert), or fp32 store (router logits).
+// store (down projection), or fp32 store (router logits). One launch may carry two problems
+// (the shared expert's dense FFN and the routed experts), so both fill the same persistent
+// grid.
 //
 // Pages: "metrale_model_layers/layers/moe/forward_prefill.rs" (`run_routed_grouped_gemm`:
 // grouped gate/up GEMM, activation and grouped down GEMM over the rows sorted by expert,
-// the sorted result left for the unpermute; the shared expert as a dense FFN on all rows).
+// the sorted result left for the unpermute; `run_shared_expert_prefill`: the shared expert
+// as a dense FFN on all rows).
 //
 // Design (one persistent CTA per SM, 192 threads):
 //   warp 0      TMA producer: A tile 128 x 64 and B tile BN x 64 (bf16, 128-byte swizzle)
-//               per stage into a ring of kStages stages.
+//               per stage into a ring of kStages stages. In gather launches every lane
+//               fetches 4 of the 128 A rows straight from the token rows of x (tile::gather4),
+//               so the expert-sorted copy of the input is never materialised.
 //   warp 1      allocates TMEM (2 x BN fp32 columns: two accumulators), one lane issues
 //               tcgen05.mma (M=128, N=BN, K=16) x 4 per stage and commits stage releases.
 //   warps 2-5   epilogue: tcgen05.ld of the finished accumulator (warp w reads TMEM lanes
@@ -39,27 +44,54 @@ struct Cfg {
   static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024 + 256;
 };
 
-__device__ __forceinline__ void tile_coords(const GemmArgs& g, int tile, int& e, int& row0,
-                                            int& row1, int& n) {
-  const int m = tile / g.n_tiles;
-  n = tile % g.n_tiles;
-  if (g.tiles) {
-    const int4 t = g.tiles[m];
-    e = t.x;
-    row0 = t.y;
-    row1 = t.z;
-  } else {
-    e = 0;
-    row0 = m * kBM;
-    row1 = min(g.dense_m, row0 + kBM);
-  }
+// Per-tile view of the problem it belongs to (selected without dynamic param indexing).
+struct Tile {
+  int p, e, row0, row1, n, num_kb, b_rows_per_expert;
+  const uint32_t* a_rows;
+  void* out;
+  int ldo, n_valid;
+};
+
+__device__ __forceinline__ int problem_mtiles(const GemmProblem& q) {
+  return q.tiles ? (int)q.count->num_mtiles : (q.dense_m + kBM - 1) / kBM;
 }
 
-template <int BN, int MODE>
+__device__ __forceinline__ void tile_of(const GemmArgs& g, int tot0, int tile, Tile& t) {
+  const bool second = tile >= tot0;
+  const GemmProblem& q0 = g.p[0];
+  const GemmProblem& q1 = g.p[1];
+  const int local = second ? tile - tot0 : tile;
+  const int n_tiles = second ? q1.n_tiles : q0.n_tiles;
+  const int4* tiles = second ? q1.tiles : q0.tiles;
+  const int m = local / n_tiles;
+  t.p = second ? 1 : 0;
+  t.n = local % n_tiles;
+  if (tiles) {
+    const int4 v = tiles[m];
+    t.e = v.x;
+    t.row0 = v.y;
+    t.row1 = v.z;
+  } else {
+    t.e = 0;
+    t.row0 = m * kBM;
+    t.row1 = min(second ? q1.dense_m : q0.dense_m, t.row0 + kBM);
+  }
+  t.num_kb = second ? q1.num_kb : q0.num_kb;
+  t.b_rows_per_expert = second ? q1.b_rows_per_expert : q0.b_rows_per_expert;
+  t.a_rows = second ? q1.a_rows : q0.a_rows;
+  t.out = second ? q1.out : q0.out;
+  t.ldo = second ? q1.ldo : q0.ldo;
+  t.n_valid = second ? q1.n_valid : q0.n_valid;
+}
+
+template <int BN, int MODE, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tm_a,
-                     const __grid_constant__ CUtensorMap tm_b0,
-                     const __grid_constant__ CUtensorMap tm_b1, const GemmArgs g) {
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tm_a0,
+                     const __grid_constant__ CUtensorMap tm_b00,
+                     const __grid_constant__ CUtensorMap tm_b01,
+                     const __grid_constant__ CUtensorMap tm_a1,
+                     const __grid_constant__ CUtensorMap tm_b10,
+                     const __grid_constant__ CUtensorMap tm_b11, const GemmArgs g) {
   using C = Cfg<BN>;
   constexpr int S = C::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -89,9 +121,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain, 1);
     fence_mbarrier_init();
-    tma_prefetch_desc(&tm_a);
-    tma_prefetch_desc(&tm_b0);
-    if (MODE == kGemmSwiGLU) tma_prefetch_desc(&tm_b1);
+    tma_prefetch_desc(&tm_a0);
+    tma_prefetch_desc(&tm_b00);
+    if (MODE == kGemmSwiGLU) tma_prefetch_desc(&tm_b01);
+    if (g.nprob > 1) {
+      tma_prefetch_desc(&tm_a1);
+      tma_prefetch_desc(&tm_b10);
+      if (MODE == kGemmSwiGLU) tma_prefetch_desc(&tm_b11);
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
@@ -99,10 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int num_m = g.tiles ? (int)g.hdr->num_mtiles : (g.dense_m + kBM - 1) / kBM;
-  const int total = num_m * g.n_tiles;
+  const int tot0 = problem_mtiles(g.p[0]) * g.p[0].n_tiles;
+  const int total = tot0 + (g.nprob > 1 ? problem_mtiles(g.p[1]) * g.p[1].n_tiles : 0);
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------ TMA producer
     int s = 0;
     uint32_t ph = 0;
@@ -110,21 +147,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     constexpr int b_rows = MODE == kGemmSwiGLU ? BN / 2 : BN;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      int e, row0, row1, n;
-      tile_coords(g, tile, e, row0, row1, n);
-      const int brow = e * g.b_rows_per_expert + n * b_rows;
-      for (int kb = 0; kb < g.num_kb; ++kb) {
-        if (!mbar_wait(&empty[s], ph ^ 1, hdr)) { ok = false; break; }
-        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-        tma_load_2d(sA + s * kATileBytes, &tm_a, kb * kBK, row0, &full[s]);
-        tma_load_2d(sB + s * C::kBTileBytes, &tm_b0, kb * kBK, brow, &full[s]);
-        if (MODE == kGemmSwiGLU)
-          tma_load_2d(sB + s * C::kBTileBytes + (BN / 2) * 128, &tm_b1, kb * kBK, brow, &full[s]);
+      Tile t;
+      tile_of(g, tot0, tile, t);
+      const CUtensorMap* ma = t.p ? &tm_a1 : &tm_a0;
+      const CUtensorMap* mb0 = t.p ? &tm_b10 : &tm_b00;
+      const CUtensorMap* mb1 = t.p ? &tm_b11 : &tm_b01;
+      const int brow = t.e * t.b_rows_per_expert + t.n * b_rows;
+      int tok[4] = {0, 0, 0, 0};
+      if (GATHER) {
+        // rows past the tile's end repeat its last row; their results are never stored
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = min(t.row0 + lane * 4 + j, t.row1 - 1);
+          tok[j] = t.a_rows ? (int)__ldg(t.a_rows + r) : r;
+        }
+      }
+      for (int kb = 0; kb < t.num_kb; ++kb) {
+        if (lane == 0) {
+          ok = mbar_wait(&empty[s], ph ^ 1, hdr);
+          if (ok) {
+            mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+            tma_load_2d(sB + s * C::kBTileBytes, mb0, kb * kBK, brow, &full[s]);
+            if (MODE == kGemmSwiGLU)
+              tma_load_2d(sB + s * C::kBTileBytes + (BN / 2) * 128, mb1, kb * kBK, brow, &full[s]);
+            if (!GATHER) tma_load_2d(sA + s * kATileBytes, ma, kb * kBK, t.row0, &full[s]);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if (GATHER)
+          tma_gather4(sA + s * kATileBytes + lane * 512, ma, kb * kBK, tok[0], tok[1], tok[2],
+                      tok[3], &full[s]);
         ++issued;
         if (++s == S) { s = 0; ph ^= 1; }
       }
     }
-    if (!ok) {
+    if (!ok && lane == 0) {
       // let the copies already issued land before the CTA can exit
       for (long long i = issued > S ? issued - S : 0; i < issued; ++i)
         mbar_wait(&full[i % S], (uint32_t)((i / S) & 1), nullptr);
@@ -137,11 +195,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int it = 0;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+      Tile t;
+      tile_of(g, tot0, tile, t);
       const int acc = it & 1;
       if (!mbar_wait(&tempty[acc], ((it >> 1) & 1) ^ 1, hdr)) { ok = false; break; }
       tc_fence_after();
       const uint32_t d = tmem_base + acc * BN;
-      for (int kb = 0; kb < g.num_kb; ++kb) {
+      for (int kb = 0; kb < t.num_kb; ++kb) {
         if (!mbar_wait(&full[s], ph, hdr)) { ok = false; break; }
         tc_fence_after();
         const uint32_t a0 = smem_u32(sA + s * kATileBytes);
@@ -165,17 +225,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r_local = q * 32 + lane;
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-      int e, row0, row1, n;
-      tile_coords(g, tile, e, row0, row1, n);
+      Tile t;
+      tile_of(g, tot0, tile, t);
       const int acc = it & 1;
       if (!mbar_wait(&tfull[acc], (it >> 1) & 1, hdr)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      const int row = row0 + r_local;
-      const bool valid = row < row1;
+      const int row = t.row0 + r_local;
+      const bool valid = row < t.row1;
       if (MODE == kGemmSwiGLU) {
         __nv_bfloat16* orow =
-            static_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + n * (BN / 2);
+            static_cast<__nv_bfloat16*>(t.out) + (size_t)row * t.ldo + t.n * (BN / 2);
 #pragma unroll 1
         for (int c = 0; c < BN / 2; c += 32) {
           float gv[32], uv[32];
@@ -195,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if (MODE == kGemmStoreBF16) {
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + n * BN;
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(t.out) + (size_t)row * t.ldo + t.n * BN;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           float v[32];
@@ -214,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        float* orow = static_cast<float*>(g.out) + (size_t)row * g.ldo;
+        float* orow = static_cast<float*>(t.out) + (size_t)row * t.ldo;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           float v[32];
@@ -222,8 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (valid) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              const int col = n * BN + c + j;
-              if (col < g.n_valid) orow[col] = v[j];
+              const int col = t.n * BN + c + j;
+              if (col < t.n_valid) orow[col] = v[j];
             }
           }
         }
@@ -241,33 +301,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int MODE>
-cudaError_t launch_t(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                     const GemmArgs& g, int num_sms, cudaStream_t st) {
+template <int BN, int MODE, bool GATHER>
+cudaError_t launch_t(const CUtensorMap maps[2][3], const GemmArgs& g, int num_sms,
+                     cudaStream_t st) {
   using C = Cfg<BN>;
-  auto kern = gemm_bf16_kernel<BN, MODE>;
+  auto kern = gemm_bf16_kernel<BN, MODE, GATHER>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int max_tiles = g.max_mtiles * g.n_tiles;
+  int max_tiles = g.p[0].max_mtiles * g.p[0].n_tiles;
+  if (g.nprob > 1) max_tiles += g.p[1].max_mtiles * g.p[1].n_tiles;
   int grid = max_tiles < num_sms ? max_tiles : num_sms;
   if (grid < 1) grid = 1;
-  kern<<<grid, kThreads, C::kSmemBytes, st>>>(a, b0, b1, g);
+  const int j = g.nprob > 1 ? 1 : 0;   // unused maps of a one-problem launch repeat problem 0's
+  kern<<<grid, kThreads, C::kSmemBytes, st>>>(maps[0][0], maps[0][1], maps[0][2], maps[j][0],
+                                              maps[j][1], maps[j][2], g);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_bf16(int mode, int bn, const CUtensorMap& a, const CUtensorMap& b0,
-                             const CUtensorMap& b1, const GemmArgs& g, int num_sms,
-                             cudaStream_t st) {
+cudaError_t launch_gemm_bf16(int mode, int bn, bool gather, const CUtensorMap maps[2][3],
+                             const GemmArgs& g, int num_sms, cudaStream_t st) {
+  if (g.nprob < 1 || g.nprob > 2) return cudaErrorInvalidValue;
+  if (gather) {
+    if (bn == 256 && mode == kGemmSwiGLU) return launch_t<256, kGemmSwiGLU, true>(maps, g, num_sms, st);
+    return cudaErrorInvalidValue;
+  }
   if (bn == 256) {
-    if (mode == kGemmSwiGLU) return launch_t<256, kGemmSwiGLU>(a, b0, b1, g, num_sms, st);
-    if (mode == kGemmStoreBF16) return launch_t<256, kGemmStoreBF16>(a, b0, b1, g, num_sms, st);
+    if (mode == kGemmSwiGLU) return launch_t<256, kGemmSwiGLU, false>(maps, g, num_sms, st);
+    if (mode == kGemmStoreBF16) return launch_t<256, kGemmStoreBF16, false>(maps, g, num_sms, st);
   } else if (bn == 128) {
-    if (mode == kGemmSwiGLU) return launch_t<128, kGemmSwiGLU>(a, b0, b1, g, num_sms, st);
-    if (mode == kGemmStoreBF16) return launch_t<128, kGemmStoreBF16>(a, b0, b1, g, num_sms, st);
-    if (mode == kGemmStoreF32) return launch_t<128, kGemmStoreF32>(a, b0, b1, g, num_sms, st);
+    if (mode == kGemmSwiGLU) return launch_t<128, kGemmSwiGLU, false>(maps, g, num_sms, st);
+    if (mode == kGemmStoreBF16) return launch_t<128, kGemmStoreBF16, false>(maps, g, num_sms, st);
+    if (mode == kGemmStoreF32) return launch_t<128, kGemmStoreF32, false>(maps, g, num_sms, st);
   }
   return cudaErrorInvalidValue;
 }

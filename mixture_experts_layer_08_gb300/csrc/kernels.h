@@ -54,6 +54,7 @@ struct SortArgs {
   uint32_t* sorted_pairs;          // [te]
   uint32_t* active;                // [E] experts with rows, ascending
   int4* tiles;                     // [max m-tiles] (expert, row0, row1, 0)
+  uint32_t* sorted_tok;            // [te] token of each sorted row, or null
   WsHeader* hdr;
 };
 
@@ -115,24 +116,35 @@ cudaError_t launch_bounded_wait_selftest(WsHeader* hdr, long long limit_cycles, 
 // tcgen05 grouped GEMM. Epilogue modes.
 enum GemmMode { kGemmSwiGLU = 0, kGemmStoreBF16 = 1, kGemmStoreF32 = 2 };
 
-struct GemmArgs {
-  const int4* tiles;               // m-tile list, or null for a dense problem
-  const WsHeader* hdr;             // number of m-tiles when `tiles` is given
-  int dense_m;                     // rows of the dense problem
+// One GEMM problem of a launch: rows grouped into 128-row m-tiles (from a device-built list,
+// or dense), each m-tile times n_tiles output tiles.
+struct GemmProblem {
+  const int4* tiles;               // m-tile list (expert, row0, row1, 0), or null: dense
+  const WsHeader* count;           // its num_mtiles (when `tiles` is given)
+  int dense_m;                     // rows of a dense problem
   int max_mtiles;                  // upper bound on m-tiles (grid sizing)
   int n_tiles;                     // output tiles along N per m-tile
   int num_kb;                      // contraction blocks of 64 (bf16)
   int b_rows_per_expert;           // rows of one expert in the B tensor map
+  const uint32_t* a_rows;          // gather launches: source row of each A row (null: the row
+                                   // itself); the A map's box is then {64, 1}
   void* out;
   int ldo;                         // elements
   int n_valid;                     // valid output columns (fp32 store mode)
+};
+
+// Up to two problems share one persistent launch (problem 0's tiles first), e.g. the shared
+// expert and the routed experts.
+struct GemmArgs {
+  GemmProblem p[2];
+  int nprob;
   WsHeader* status;
 };
-// A: [rows, K] bf16 map, box {64, 128}; B0 (and B1 for SwiGLU): [rows, K] bf16, box {64,
-// BN/2 (SwiGLU) or BN}.
-cudaError_t launch_gemm_bf16(int mode, int bn, const CUtensorMap& a, const CUtensorMap& b0,
-                             const CUtensorMap& b1, const GemmArgs& g, int num_sms,
-                             cudaStream_t st);
+
+// maps[i] = {A, B0, B1} of problem i. A: [rows, K] bf16, box {64, 128} (or {64, 1} when
+// gathering); B0 (and B1 for SwiGLU): [rows, K] bf16, box {64, BN/2 (SwiGLU) or BN}.
+cudaError_t launch_gemm_bf16(int mode, int bn, bool gather, const CUtensorMap maps[2][3],
+                             const GemmArgs& g, int num_sms, cudaStream_t st);
 
 // FP8 (E4M3, block-scaled) grouped GEMM over the expert-sorted rows. mode 0: gate/up with
 // SwiGLU and 1x128 E4M3 quantisation of the intermediate; mode 1: down projection to bf16.

@@ -363,11 +363,12 @@ __global__ void __launch_bounds__(256) sort_scatter_kernel(SortArgs s, const __n
     return;
   }
   uint32_t row = s.blk_counts[(size_t)(j / kSortBlock) * s.E + e] + s.local_rank[j];
+  const int t = j / s.K;
   if (lane == 0) {
     s.pair_to_row[j] = row;
     s.sorted_pairs[row] = (uint32_t)j;
+    if (s.sorted_tok) s.sorted_tok[row] = (uint32_t)t;
   }
-  const int t = j / s.K;
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
   if (xp) {
     uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)row * H);
