@@ -24,7 +24,7 @@ constexpr int kSmallRouterMaxTokens = 64;
 
 enum Region {
   R_HDR, R_LOGITS, R_IDX, R_W, R_ZSUM, R_BLK, R_LRANK, R_OFFS, R_P2R, R_SPAIRS, R_ACTIVE,
-  R_TILES, R_STOK, R_XP, R_XS, R_HH, R_HS, R_Y, R_SHH, R_SHY, R_HD, R_YD, R_ACC, R_NUM
+  R_TILES, R_XP, R_XS, R_HH, R_HS, R_Y, R_SHH, R_SHY, R_HD, R_YD, R_ACC, R_NUM
 };
 
 struct Layout {
@@ -96,14 +96,13 @@ Layout make_layout(const moe_config_t* c) {
     sz[R_BLK] = (size_t)L.nblk * E * 4;
     sz[R_LRANK] = te * 4;
     sz[R_TILES] = (size_t)L.max_mtiles * 16;
-    sz[R_STOK] = te * 4;                 // token of each sorted row (bf16 rows are gathered
-                                         // straight from x by the gate/up GEMM)
     if (c->weight_dtype == MOE_W_FP8_E4M3_B128) {
       sz[R_XP] = te * H;                 // E4M3 codes of the gathered rows
       sz[R_XS] = (H / 128) * te * 4;     // their 1x128 scales, [H/128, te]
       sz[R_HH] = te * I;                 // E4M3 codes of the SwiGLU intermediate
       sz[R_HS] = (I / 128) * te * 4;
     } else {
+      sz[R_XP] = te * H * 2;             // x rows in expert-sorted order
       sz[R_HH] = te * I * 2;
     }
     sz[R_Y] = te * H * 2;
@@ -281,7 +280,6 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
   sa.sorted_pairs = P.at<uint32_t>(R_SPAIRS);
   sa.active = P.at<uint32_t>(R_ACTIVE);
   sa.tiles = P.at<int4>(R_TILES);
-  sa.sorted_tok = P.at<uint32_t>(R_STOK);
   sa.hdr = hdr;
 
   CK(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
@@ -308,11 +306,11 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
     g.p[0].ldo = c->router_width;
     g.p[0].n_valid = c->router_width;
     g.status = hdr;
-    CK(launch_gemm_bf16(kGemmStoreF32, 128, false, maps, g, num_sms(), st));
+    CK(launch_gemm_bf16(kGemmStoreF32, 128, maps, g, num_sms(), st));
   }
   CK(launch_topk(ra, st));
   const bool fp8 = c->weight_dtype == MOE_W_FP8_E4M3_B128;
-  CK(launch_sort(sa, ra.x, c->hidden, nullptr,
+  CK(launch_sort(sa, ra.x, c->hidden, gather && !fp8 ? P.at<__nv_bfloat16>(R_XP) : nullptr,
                  gather && fp8 ? P.at<uint8_t>(R_XP) : nullptr,
                  gather && fp8 ? P.at<float>(R_XS) : nullptr, st));
   return MOE_OK;
@@ -332,7 +330,7 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
   CUtensorMap sh_gu[3], sh_dn[3];
   GemmProblem sh_gu_p{}, sh_dn_p{};
   if (S > 0) {
-    if (!make_map_bf16(&sh_gu[0], x, H, N, fp8 ? 128 : 1) ||
+    if (!make_map_bf16(&sh_gu[0], x, H, N, 128) ||
         !make_map_bf16(&sh_gu[1], w->sh_gate, H, S, 128) ||
         !make_map_bf16(&sh_gu[2], w->sh_up, H, S, 128) ||
         !make_map_bf16(&sh_dn[0], P.at<void>(R_SHH), S, N, 128) ||
@@ -358,10 +356,10 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
     g.nprob = 1;
     g.p[0] = sh_gu_p;
     g.status = hdr;
-    CK(launch_gemm_bf16(kGemmSwiGLU, 256, false, maps, g, sms, st));
+    CK(launch_gemm_bf16(kGemmSwiGLU, 256, maps, g, sms, st));
     CUtensorMap dmaps[2][3] = {{sh_dn[0], sh_dn[1], sh_dn[2]}, {sh_dn[0], sh_dn[1], sh_dn[2]}};
     g.p[0] = sh_dn_p;
-    CK(launch_gemm_bf16(kGemmStoreBF16, bn_h, false, dmaps, g, sms, st));
+    CK(launch_gemm_bf16(kGemmStoreBF16, bn_h, dmaps, g, sms, st));
   }
   MARK(MOE_STAGE_SHARED, 1);
   // routed experts: grouped gate/up + SiLU*up, then grouped down, over the sorted rows
@@ -411,7 +409,7 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
     // routed problem (plus the shared expert as problem 0 when present)
     CUtensorMap gu[3], dn[3];
     const uint64_t rows = (uint64_t)L.te;
-    if (!make_map_bf16(&gu[0], x, H, (uint64_t)N, 1) ||
+    if (!make_map_bf16(&gu[0], P.at<void>(R_XP), H, rows, 128) ||
         !make_map_bf16(&gu[1], w->w_gate, H, (uint64_t)E * I, 128) ||
         !make_map_bf16(&gu[2], w->w_up, H, (uint64_t)E * I, 128) ||
         !make_map_bf16(&dn[0], P.at<void>(R_HH), I, rows, 128) ||
@@ -425,11 +423,9 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
     rgu.n_tiles = I / 128;
     rgu.num_kb = H / 64;
     rgu.b_rows_per_expert = I;
-    rgu.a_rows = P.at<uint32_t>(R_STOK);
     rgu.out = P.at<void>(R_HH);
     rgu.ldo = I;
     GemmProblem rdn = rgu;
-    rdn.a_rows = nullptr;
     rdn.n_tiles = H / bn_h;
     rdn.num_kb = I / 64;
     rdn.b_rows_per_expert = H;
@@ -449,7 +445,7 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
       for (int i = 0; i < 3; ++i) maps[0][i] = maps[1][i] = gu[i];
     }
     MARK(MOE_STAGE_GATE_UP, 0);
-    CK(launch_gemm_bf16(kGemmSwiGLU, 256, true, maps, g, sms, st));
+    CK(launch_gemm_bf16(kGemmSwiGLU, 256, maps, g, sms, st));
     MARK(MOE_STAGE_GATE_UP, 1);
     if (S > 0) {
       g.p[0] = sh_dn_p;
@@ -460,7 +456,7 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
       for (int i = 0; i < 3; ++i) maps[0][i] = maps[1][i] = dn[i];
     }
     MARK(MOE_STAGE_DOWN, 0);
-    CK(launch_gemm_bf16(kGemmStoreBF16, bn_h, false, maps, g, sms, st));
+    CK(launch_gemm_bf16(kGemmStoreBF16, bn_h, maps, g, sms, st));
     MARK(MOE_STAGE_DOWN, 1);
   }
   CombineArgs ca{};

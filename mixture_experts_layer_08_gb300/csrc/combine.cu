@@ -15,19 +15,35 @@ namespace {
 
 constexpr int kCombThreads = 256;
 
-__device__ __forceinline__ void load8(const void* base, int is_f32, size_t off, float* f) {
-  if (is_f32) {
+template <bool F32>
+struct Row8;      // 8 consecutive outputs of one row, loaded raw then widened
+
+template <>
+struct Row8<false> {
+  uint4 v;
+  __device__ __forceinline__ void load(const void* base, size_t off) {
+    v = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + off);
+  }
+  __device__ __forceinline__ void widen(float* f) const { bf16x8_to_f32(v, f); }
+};
+
+template <>
+struct Row8<true> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const void* base, size_t off) {
     const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
-    const float4 a = p[0], b = p[1];
+    a = p[0];
+    b = p[1];
+  }
+  __device__ __forceinline__ void widen(float* f) const {
     f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
     f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-  } else {
-    bf16x8_to_f32(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + off),
-                  f);
   }
-}
+};
 
-// Block (t, part): 8 consecutive outputs per thread of token t.
+// Block (t, part): 8 consecutive outputs per thread of token t. YF32 / SF32: the expert rows
+// and the shared-expert row are fp32 (decode chain) or bf16 (grouped chain).
+template <bool YF32, bool SF32>
 __global__ void __launch_bounds__(kCombThreads) combine_kernel(CombineArgs a) {
   __shared__ float red[kCombThreads / 32];
   const int t = blockIdx.x;
@@ -59,27 +75,33 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(CombineArgs a) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
   if (a.acc) {
-    load8(a.acc, 1, (size_t)t * H + h0, acc);
+    Row8<true> r;
+    r.load(a.acc, (size_t)t * H + h0);
+    r.widen(acc);
   }
   if (a.y) {
-    // all of the token's expert rows in flight at once: 8 slots per round
-    for (int k0 = 0; k0 < a.K; k0 += 8) {
-      float yf[8][8];
-      float wk[8];
+    // 4 expert rows in flight per round, loaded before any of them is used
+    for (int k0 = 0; k0 < a.K; k0 += 4) {
+      Row8<YF32> rows[4];
+      float wk[4];
+      bool live[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 4; ++u) {
         const int k = k0 + u;
         const uint32_t row = k < a.K ? a.pair_to_row[t * a.K + k] : kNoRow;
-        wk[u] = row != kNoRow ? a.w[t * a.K + k] : 0.0f;
-        if (row != kNoRow) load8(a.y, a.y_is_f32, (size_t)row * H + h0, yf[u]);
-        else
-#pragma unroll
-          for (int i = 0; i < 8; ++i) yf[u][i] = 0.0f;
+        live[u] = row != kNoRow;     // identity-expert slots have no expert row
+        wk[u] = live[u] ? a.w[t * a.K + k] : 0.0f;
+        if (live[u]) rows[u].load(a.y, (size_t)row * H + h0);
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
+      for (int u = 0; u < 4; ++u) {
+        if (live[u]) {
+          float yf[8];
+          rows[u].widen(yf);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk[u], yf[u][i], acc[i]);
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk[u], yf[i], acc[i]);
+        }
+      }
     }
   }
   {
@@ -90,8 +112,10 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(CombineArgs a) {
     for (int i = 0; i < 8; ++i) acc[i] = fmaf(z, xf[i], acc[i]);
   }
   if (a.shy) {
+    Row8<SF32> r;
+    r.load(a.shy, (size_t)t * H + h0);
     float sf[8];
-    load8(a.shy, a.shy_is_f32, (size_t)t * H + h0, sf);
+    r.widen(sf);
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = fmaf(gamma, sf[i], acc[i]);
   }
@@ -121,7 +145,9 @@ cudaError_t launch_bounded_wait_selftest(WsHeader* hdr, long long limit_cycles, 
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
   dim3 grid(a.N, (a.H / 8 + kCombThreads - 1) / kCombThreads);
-  combine_kernel<<<grid, kCombThreads, 0, st>>>(a);
+  if (a.y_is_f32 != a.shy_is_f32 && a.shy) return cudaErrorInvalidValue;
+  if (a.y_is_f32) combine_kernel<true, true><<<grid, kCombThreads, 0, st>>>(a);
+  else combine_kernel<false, false><<<grid, kCombThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
 

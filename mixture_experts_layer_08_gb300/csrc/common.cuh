@@ -147,20 +147,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// Row gather: 4 rows (ids y0..y3) x 64 bf16 columns starting at column x of a 2D tensor map
-// whose box is {64, 1}, written as 4 consecutive 128-byte rows (swizzled by destination
-// address like a tiled load), completing transaction bytes on `bar`.
-__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, int32_t x,
-                                            int32_t y0, int32_t y1, int32_t y2, int32_t y3,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
-      "r"(smem_u32(bar))
-      : "memory");
-}
-
 // 1D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16), completing
 // transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,

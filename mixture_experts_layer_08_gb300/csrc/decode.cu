@@ -23,7 +23,8 @@ namespace {
 constexpr int kMaxTok = 16;          // tokens per expert the decode chain handles
 constexpr int kConsumers = 8;        // consumer warps
 constexpr int kThreads = 32 * (1 + kConsumers);
-constexpr int kSmemBudget = 224 * 1024;   // of the 227 KB a block may opt into
+constexpr int kSmemBudget = 214 * 1024;   // dynamic part; + RouteMeta, of the 227 KB allowed
+constexpr int kMaxPairs = 512;        // N * K of the decode chain (16 tokens x top-32)
 constexpr int kMaxStages = 4;
 constexpr int kDownRows = 32;        // down-projection rows per item (4 per consumer warp)
 
@@ -34,15 +35,45 @@ __device__ __forceinline__ void item_range(int total, int& i0, int& i1) {
   i1 = (int)((total * (b + 1)) / G);
 }
 
-// Token list of a routed expert: lane j < ntok gets the token id and sorted row of the j-th
-// pair routed to it. Routing metadata is read through L2 (written by an earlier kernel).
-__device__ __forceinline__ int expert_tokens(const DecodeArgs& a, int e, int lane, int& tok,
-                                             int& row) {
-  const int r0 = (int)__ldcg(a.offsets + e), r1 = (int)__ldcg(a.offsets + e + 1);
-  const int ntok = r1 - r0;
-  tok = 0;
+// Routing of the batch, copied to shared memory once per block so the streaming loops
+// never wait on a dependent global load: expert, first sorted row and row count of every
+// active slot, and the token of every sorted row.
+struct RouteMeta {
+  int n_active;
+  int slot_e[kMaxPairs];
+  int slot_r0[kMaxPairs];
+  int slot_n[kMaxPairs];
+  int row_tok[kMaxPairs];
+};
+
+// All threads of the block; routing metadata is read through L2 (an earlier kernel wrote it).
+__device__ void load_route_meta(const DecodeArgs& a, RouteMeta& m) {
+  const int n_active = (int)__ldcg(&a.hdr->num_active);
+  for (int s = threadIdx.x; s < n_active; s += blockDim.x) {
+    const int e = (int)__ldcg(a.active + s);
+    const int r0 = (int)__ldcg(a.offsets + e);
+    m.slot_e[s] = e;
+    m.slot_r0[s] = r0;
+    m.slot_n[s] = (int)__ldcg(a.offsets + e + 1) - r0;
+  }
+  for (int r = threadIdx.x; r < a.te; r += blockDim.x)
+    m.row_tok[r] = (int)(__ldcg(a.sorted_pairs + r) / (uint32_t)a.K);
+  if (threadIdx.x == 0) m.n_active = n_active;
+  __syncthreads();
+}
+
+// Token list of slot `slot` (-1: the shared expert): lane j < ntok gets the token id and the
+// intermediate row of the j-th token.
+__device__ __forceinline__ int slot_tokens(const DecodeArgs& a, const RouteMeta& m, int slot,
+                                           int lane, int& tok, int& row) {
+  if (slot < 0) {
+    tok = lane;
+    row = a.te + lane;
+    return a.N;
+  }
+  const int r0 = m.slot_r0[slot], ntok = m.slot_n[slot];
   row = r0 + lane;
-  if (lane < ntok) tok = (int)(__ldcg(a.sorted_pairs + r0 + lane) / (uint32_t)a.K);
+  tok = lane < ntok ? m.row_tok[r0 + lane] : 0;
   return ntok;
 }
 
@@ -53,6 +84,7 @@ __device__ __forceinline__ int expert_tokens(const DecodeArgs& a, int e, int lan
 __global__ void __launch_bounds__(kThreads, 1)
     decode_gateup_kernel(DecodeArgs a, int rp, int stages, int item_bytes, int xbytes) {
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ RouteMeta meta;
   const int H = a.H, N = a.N;
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);             // [N, H]
   uint8_t* ring = smem + xbytes;
@@ -73,9 +105,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   pdl_wait();       // routing of the router kernel
   pdl_trigger();    // the down projection may start streaming its weights
+  load_route_meta(a, meta);
 
   const int per_slot = a.I / rp;
-  const int routed = (int)__ldcg(&a.hdr->num_active) * per_slot;
+  const int routed = meta.n_active * per_slot;
   const int total = routed + (a.S > 0 ? a.S / rp : 0);
   int i0, i1;
   item_range(total, i0, i1);
@@ -90,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&empty[s], ((k / stages) & 1) ^ 1, a.hdr)) { ok = false; break; }
         const __nv_bfloat16 *g, *u;
         if (it < routed) {
-          const int e = (int)__ldcg(a.active + it / per_slot);
+          const int e = meta.slot_e[it / per_slot];
           const size_t r = (size_t)e * a.I + (size_t)(it % per_slot) * rp;
           g = a.wg + r * H;
           u = a.wu + r * H;
@@ -117,13 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i = (it < routed ? (it % per_slot) : (it - routed)) * rp + cw;
       if (slot != cur_slot) {
         cur_slot = slot;
-        if (slot >= 0) {
-          ntok = expert_tokens(a, (int)__ldcg(a.active + slot), lane, tok, orow);
-        } else {
-          ntok = N;
-          tok = lane;
-          orow = a.te + lane;
-        }
+        ntok = slot_tokens(a, meta, slot, lane, tok, orow);
       }
       if (!mbar_wait(&full[s], (k / stages) & 1, a.hdr)) break;
       if (cw < rp) {
@@ -178,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(kThreads, 1)
     decode_down_kernel(DecodeArgs a, int stages, int item_bytes) {
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ RouteMeta meta;
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)stages * item_bytes);
   uint64_t* empty = full + kMaxStages;
@@ -190,12 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbarrier_init();
   }
-  __syncthreads();
   // Routing metadata comes from the router kernel, which finished before the gate/up kernel
   // passed its own wait, so the weights can stream before this kernel's wait; only the
   // consumers read the SwiGLU outputs and wait for them.
+  load_route_meta(a, meta);
   const int per_slot = H / kDownRows;
-  const int routed = (int)__ldcg(&a.hdr->num_active) * per_slot;
+  const int routed = meta.n_active * per_slot;
   const int total = routed + (a.S > 0 ? per_slot : 0);
   int i0, i1;
   item_range(total, i0, i1);
@@ -211,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const __nv_bfloat16* src;
         uint32_t bytes;
         if (it < routed) {
-          const int e = (int)__ldcg(a.active + it / per_slot);
+          const int e = meta.slot_e[it / per_slot];
           src = a.wd + ((size_t)e * H + (size_t)(it % per_slot) * kDownRows) * a.I;
           bytes = (uint32_t)(kDownRows * a.I * 2);
         } else {
@@ -239,14 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int L = shared_item ? a.S : a.I;
       if (slot != cur_slot) {
         cur_slot = slot;
-        if (!shared_item) {
-          ntok = expert_tokens(a, (int)__ldcg(a.active + slot), lane, tok, orow);
-          if (a.acc && lane < ntok) wt = a.w[__ldcg(a.sorted_pairs + orow)];
-        } else {
-          ntok = a.N;
-          tok = lane;
-          orow = a.te + lane;
-        }
+        ntok = slot_tokens(a, meta, slot, lane, tok, orow);
+        if (!shared_item && a.acc && lane < ntok) wt = a.w[__ldcg(a.sorted_pairs + orow)];
       }
       if (!mbar_wait(&full[s], (k / stages) & 1, a.hdr)) break;
       const uint8_t* stage = ring + (size_t)s * item_bytes;
@@ -319,6 +341,7 @@ int sm_count() {
 }  // namespace
 
 cudaError_t launch_decode_gateup(const DecodeArgs& a, cudaStream_t st) {
+  if (a.te > kMaxPairs) return cudaErrorInvalidValue;
   const int xbytes = (a.N * a.H * 2 + 127) & ~127;
   // row pairs per item: the most (<= 8, one per consumer warp) that keep 3 stages in budget
   int rp = 8;
@@ -338,7 +361,7 @@ cudaError_t launch_decode_gateup(const DecodeArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_decode_down(const DecodeArgs& a, cudaStream_t st) {
-  if (a.H % kDownRows) return cudaErrorInvalidValue;
+  if (a.H % kDownRows || a.te > kMaxPairs) return cudaErrorInvalidValue;
   const int L = a.I > a.S ? a.I : a.S;
   const int item = kDownRows * L * 2;
   int stages = (kSmemBudget - 1024) / item;

@@ -13,9 +13,8 @@
 //
 // Design (one persistent CTA per SM, 192 threads):
 //   warp 0      TMA producer: A tile 128 x 64 and B tile BN x 64 (bf16, 128-byte swizzle)
-//               per stage into a ring of kStages stages. In gather launches every lane
-//               fetches 4 of the 128 A rows straight from the token rows of x (tile::gather4),
-//               so the expert-sorted copy of the input is never materialised.
+//               per stage into a ring of kStages stages. (A 4-row TMA gather straight from
+//               the token rows measured 3x slower than reading an expert-sorted copy.)
 //   warp 1      allocates TMEM (2 x BN fp32 columns: two accumulators), one lane issues
 //               tcgen05.mma (M=128, N=BN, K=16) x 4 per stage and commits stage releases.
 //   warps 2-5   epilogue: tcgen05.ld of the finished accumulator (warp w reads TMEM lanes
@@ -47,7 +46,6 @@ struct Cfg {
 // Per-tile view of the problem it belongs to (selected without dynamic param indexing).
 struct Tile {
   int p, e, row0, row1, n, num_kb, b_rows_per_expert;
-  const uint32_t* a_rows;
   void* out;
   int ldo, n_valid;
 };
@@ -78,13 +76,12 @@ __device__ __forceinline__ void tile_of(const GemmArgs& g, int tot0, int tile, T
   }
   t.num_kb = second ? q1.num_kb : q0.num_kb;
   t.b_rows_per_expert = second ? q1.b_rows_per_expert : q0.b_rows_per_expert;
-  t.a_rows = second ? q1.a_rows : q0.a_rows;
   t.out = second ? q1.out : q0.out;
   t.ldo = second ? q1.ldo : q0.ldo;
   t.n_valid = second ? q1.n_valid : q0.n_valid;
 }
 
-template <int BN, int MODE, bool GATHER>
+template <int BN, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tm_a0,
                      const __grid_constant__ CUtensorMap tm_b00,
@@ -139,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tot0 = problem_mtiles(g.p[0]) * g.p[0].n_tiles;
   const int total = tot0 + (g.nprob > 1 ? problem_mtiles(g.p[1]) * g.p[1].n_tiles : 0);
 
-  if (warp == 0) {
+  if (warp == 0 && lane == 0) {
     // ------------------------------------------------ TMA producer
     int s = 0;
     uint32_t ph = 0;
@@ -153,36 +150,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* mb0 = t.p ? &tm_b10 : &tm_b00;
       const CUtensorMap* mb1 = t.p ? &tm_b11 : &tm_b01;
       const int brow = t.e * t.b_rows_per_expert + t.n * b_rows;
-      int tok[4] = {0, 0, 0, 0};
-      if (GATHER) {
-        // rows past the tile's end repeat its last row; their results are never stored
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = min(t.row0 + lane * 4 + j, t.row1 - 1);
-          tok[j] = t.a_rows ? (int)__ldg(t.a_rows + r) : r;
-        }
-      }
       for (int kb = 0; kb < t.num_kb; ++kb) {
-        if (lane == 0) {
-          ok = mbar_wait(&empty[s], ph ^ 1, hdr);
-          if (ok) {
-            mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-            tma_load_2d(sB + s * C::kBTileBytes, mb0, kb * kBK, brow, &full[s]);
-            if (MODE == kGemmSwiGLU)
-              tma_load_2d(sB + s * C::kBTileBytes + (BN / 2) * 128, mb1, kb * kBK, brow, &full[s]);
-            if (!GATHER) tma_load_2d(sA + s * kATileBytes, ma, kb * kBK, t.row0, &full[s]);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        if (GATHER)
-          tma_gather4(sA + s * kATileBytes + lane * 512, ma, kb * kBK, tok[0], tok[1], tok[2],
-                      tok[3], &full[s]);
+        if (!mbar_wait(&empty[s], ph ^ 1, hdr)) { ok = false; break; }
+        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+        tma_load_2d(sA + s * kATileBytes, ma, kb * kBK, t.row0, &full[s]);
+        tma_load_2d(sB + s * C::kBTileBytes, mb0, kb * kBK, brow, &full[s]);
+        if (MODE == kGemmSwiGLU)
+          tma_load_2d(sB + s * C::kBTileBytes + (BN / 2) * 128, mb1, kb * kBK, brow, &full[s]);
         ++issued;
         if (++s == S) { s = 0; ph ^= 1; }
       }
     }
-    if (!ok && lane == 0) {
+    if (!ok) {
       // let the copies already issued land before the CTA can exit
       for (long long i = issued > S ? issued - S : 0; i < issued; ++i)
         mbar_wait(&full[i % S], (uint32_t)((i / S) & 1), nullptr);
@@ -301,11 +280,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int MODE, bool GATHER>
+template <int BN, int MODE>
 cudaError_t launch_t(const CUtensorMap maps[2][3], const GemmArgs& g, int num_sms,
                      cudaStream_t st) {
   using C = Cfg<BN>;
-  auto kern = gemm_bf16_kernel<BN, MODE, GATHER>;
+  auto kern = gemm_bf16_kernel<BN, MODE>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -321,20 +300,16 @@ cudaError_t launch_t(const CUtensorMap maps[2][3], const GemmArgs& g, int num_sm
 
 }  // namespace
 
-cudaError_t launch_gemm_bf16(int mode, int bn, bool gather, const CUtensorMap maps[2][3],
-                             const GemmArgs& g, int num_sms, cudaStream_t st) {
+cudaError_t launch_gemm_bf16(int mode, int bn, const CUtensorMap maps[2][3], const GemmArgs& g,
+                             int num_sms, cudaStream_t st) {
   if (g.nprob < 1 || g.nprob > 2) return cudaErrorInvalidValue;
-  if (gather) {
-    if (bn == 256 && mode == kGemmSwiGLU) return launch_t<256, kGemmSwiGLU, true>(maps, g, num_sms, st);
-    return cudaErrorInvalidValue;
-  }
   if (bn == 256) {
-    if (mode == kGemmSwiGLU) return launch_t<256, kGemmSwiGLU, false>(maps, g, num_sms, st);
-    if (mode == kGemmStoreBF16) return launch_t<256, kGemmStoreBF16, false>(maps, g, num_sms, st);
+    if (mode == kGemmSwiGLU) return launch_t<256, kGemmSwiGLU>(maps, g, num_sms, st);
+    if (mode == kGemmStoreBF16) return launch_t<256, kGemmStoreBF16>(maps, g, num_sms, st);
   } else if (bn == 128) {
-    if (mode == kGemmSwiGLU) return launch_t<128, kGemmSwiGLU, false>(maps, g, num_sms, st);
-    if (mode == kGemmStoreBF16) return launch_t<128, kGemmStoreBF16, false>(maps, g, num_sms, st);
-    if (mode == kGemmStoreF32) return launch_t<128, kGemmStoreF32, false>(maps, g, num_sms, st);
+    if (mode == kGemmSwiGLU) return launch_t<128, kGemmSwiGLU>(maps, g, num_sms, st);
+    if (mode == kGemmStoreBF16) return launch_t<128, kGemmStoreBF16>(maps, g, num_sms, st);
+    if (mode == kGemmStoreF32) return launch_t<128, kGemmStoreF32>(maps, g, num_sms, st);
   }
   return cudaErrorInvalidValue;
 }

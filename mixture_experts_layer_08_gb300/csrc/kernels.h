@@ -54,7 +54,6 @@ struct SortArgs {
   uint32_t* sorted_pairs;          // [te]
   uint32_t* active;                // [E] experts with rows, ascending
   int4* tiles;                     // [max m-tiles] (expert, row0, row1, 0)
-  uint32_t* sorted_tok;            // [te] token of each sorted row, or null
   WsHeader* hdr;
 };
 
@@ -126,8 +125,6 @@ struct GemmProblem {
   int n_tiles;                     // output tiles along N per m-tile
   int num_kb;                      // contraction blocks of 64 (bf16)
   int b_rows_per_expert;           // rows of one expert in the B tensor map
-  const uint32_t* a_rows;          // gather launches: source row of each A row (null: the row
-                                   // itself); the A map's box is then {64, 1}
   void* out;
   int ldo;                         // elements
   int n_valid;                     // valid output columns (fp32 store mode)
@@ -141,10 +138,10 @@ struct GemmArgs {
   WsHeader* status;
 };
 
-// maps[i] = {A, B0, B1} of problem i. A: [rows, K] bf16, box {64, 128} (or {64, 1} when
-// gathering); B0 (and B1 for SwiGLU): [rows, K] bf16, box {64, BN/2 (SwiGLU) or BN}.
-cudaError_t launch_gemm_bf16(int mode, int bn, bool gather, const CUtensorMap maps[2][3],
-                             const GemmArgs& g, int num_sms, cudaStream_t st);
+// maps[i] = {A, B0, B1} of problem i. A: [rows, K] bf16, box {64, 128}; B0 (and B1 for
+// SwiGLU): [rows, K] bf16, box {64, BN/2 (SwiGLU) or BN}.
+cudaError_t launch_gemm_bf16(int mode, int bn, const CUtensorMap maps[2][3], const GemmArgs& g,
+                             int num_sms, cudaStream_t st);
 
 // FP8 (E4M3, block-scaled) grouped GEMM over the expert-sorted rows. mode 0: gate/up with
 // SwiGLU and 1x128 E4M3 quantisation of the intermediate; mode 1: down projection to bf16.

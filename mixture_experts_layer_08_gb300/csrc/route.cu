@@ -367,7 +367,6 @@ __global__ void __launch_bounds__(256) sort_scatter_kernel(SortArgs s, const __n
   if (lane == 0) {
     s.pair_to_row[j] = row;
     s.sorted_pairs[row] = (uint32_t)j;
-    if (s.sorted_tok) s.sorted_tok[row] = (uint32_t)t;
   }
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
   if (xp) {
