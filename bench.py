@@ -122,9 +122,11 @@ def kernels_per_step(B, cfg):
                                             and cfg.weight_dtype == 0)
     if decode:
         return 4            # fused router + top-K + sort, gate/up, down, combine
-    # router, top-K, 3 sort, gate/up GEMM, down GEMM, combine; FP8 experts run the bf16 shared
-    # expert in two launches of its own
-    return 8 + (2 if cfg.shared_inter and cfg.weight_dtype == 1 else 0)
+    # router, top-K, 3 sort, gate/up GEMM, down GEMM, combine; FP8 experts add the token-row
+    # quantiser and run the bf16 shared expert in two launches of its own
+    if cfg.weight_dtype == 1:
+        return 9 + (2 if cfg.shared_inter else 0)
+    return 8
 
 
 def barrier():

@@ -24,7 +24,7 @@ constexpr int kSmallRouterMaxTokens = 64;
 
 enum Region {
   R_HDR, R_LOGITS, R_IDX, R_W, R_ZSUM, R_BLK, R_LRANK, R_OFFS, R_P2R, R_SPAIRS, R_ACTIVE,
-  R_TILES, R_XP, R_XS, R_HH, R_HS, R_Y, R_SHH, R_SHY, R_HD, R_YD, R_ACC, R_NUM
+  R_TILES, R_XQT, R_XST, R_XP, R_XS, R_HH, R_HS, R_Y, R_SHH, R_SHY, R_HD, R_YD, R_ACC, R_NUM
 };
 
 struct Layout {
@@ -61,7 +61,11 @@ moe_status_t validate_config(const moe_config_t* c) {
   if (c->hidden % 128 || c->inter % 128 || c->shared_inter % 128) return MOE_ERR_UNSUPPORTED;
   if (c->top_k > 32 || c->router_width > 1024 || c->num_experts > 1024) return MOE_ERR_UNSUPPORTED;
   // FP8 experts: the down projection's N-tile is 256 wide
-  if (c->weight_dtype == MOE_W_FP8_E4M3_B128 && c->hidden % 256) return MOE_ERR_UNSUPPORTED;
+  // FP8 experts: the down projection's N-tile is 256 wide; each tile keeps the scales of at
+  // most 32 K blocks of 128
+  if (c->weight_dtype == MOE_W_FP8_E4M3_B128 &&
+      (c->hidden % 256 || c->hidden > 4096 || c->inter > 4096))
+    return MOE_ERR_UNSUPPORTED;
   const int path = resolve_path(c);
   if (path == MOE_PATH_DECODE &&
       (c->weight_dtype != MOE_W_BF16 || c->num_tokens > kDecodeMaxTokens || c->inter > 1024 ||
@@ -97,6 +101,8 @@ Layout make_layout(const moe_config_t* c) {
     sz[R_LRANK] = te * 4;
     sz[R_TILES] = (size_t)L.max_mtiles * 16;
     if (c->weight_dtype == MOE_W_FP8_E4M3_B128) {
+      sz[R_XQT] = N * H;                 // E4M3 codes of each token row
+      sz[R_XST] = (H / 128) * N * 4;     // and their scales
       sz[R_XP] = te * H;                 // E4M3 codes of the gathered rows
       sz[R_XS] = (H / 128) * te * 4;     // their 1x128 scales, [H/128, te]
       sz[R_HH] = te * I;                 // E4M3 codes of the SwiGLU intermediate
@@ -110,7 +116,7 @@ Layout make_layout(const moe_config_t* c) {
     sz[R_SHY] = S ? N * H * 2 : 0;
   } else {
     const size_t L2 = I > S ? I : S;
-    sz[R_HD] = (te + N) * L2 * 4;
+    sz[R_HD] = (te + N) * 2 * L2 * 4;   // gate and up dot products of every row
     if (c->deterministic) sz[R_YD] = te * H * 4;
     else sz[R_ACC] = N * H * 4;
     sz[R_SHY] = S ? N * H * 4 : 0;
@@ -280,6 +286,9 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
   sa.sorted_pairs = P.at<uint32_t>(R_SPAIRS);
   sa.active = P.at<uint32_t>(R_ACTIVE);
   sa.tiles = P.at<int4>(R_TILES);
+  sa.xq_tok = P.at<uint8_t>(R_XQT);
+  sa.xs_tok = P.at<float>(R_XST);
+  sa.N = c->num_tokens;
   sa.hdr = hdr;
 
   CK(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
@@ -310,6 +319,9 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
   }
   CK(launch_topk(ra, st));
   const bool fp8 = c->weight_dtype == MOE_W_FP8_E4M3_B128;
+  if (gather && fp8)
+    CK(launch_quant_rows(ra.x, c->num_tokens, c->hidden, P.at<uint8_t>(R_XQT),
+                         P.at<float>(R_XST), st));
   CK(launch_sort(sa, ra.x, c->hidden, gather && !fp8 ? P.at<__nv_bfloat16>(R_XP) : nullptr,
                  gather && fp8 ? P.at<uint8_t>(R_XP) : nullptr,
                  gather && fp8 ? P.at<float>(R_XS) : nullptr, st));

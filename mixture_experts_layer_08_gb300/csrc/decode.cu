@@ -9,11 +9,14 @@
 // routed down projections weighted and FP32-atomic-added into a [N,H] accumulator zeroed
 // first, then a finalize that casts to BF16 and blends the shared expert).
 //
-// Both kernels are persistent (one block per SM) and split the work into items: a few
-// consecutive weight rows of one slot, contiguous in memory. Warp 0 streams items into a
-// shared-memory ring with 1D bulk copies (150-200 KB in flight per SM, enough to keep HBM
-// busy); 8 consumer warps take the dot products against the slot's token vectors. Each block
-// owns a contiguous range of items, so a slot's token list changes rarely within a block.
+// Both kernels are persistent (one block per SM) and split the work into items: consecutive
+// weight rows of one slot, contiguous in memory. Warp 0 streams items into a shared-memory
+// ring with 1D bulk copies (up to ~200 KB in flight per SM, enough to keep HBM busy);
+// 16 consumer warps take one weight row each per item, with the inner loop specialised on
+// the slot's token count, so enough independent warps hide the arithmetic latency. The gate
+// kernel writes raw gate and up dot products; the down kernel forms SiLU(gate) * up when it
+// stages a slot's intermediate vectors in shared memory. Each block owns a contiguous range
+// of items, so a slot changes rarely within a block.
 #include "kernels.h"
 
 namespace moe {
@@ -21,12 +24,12 @@ namespace moe {
 namespace {
 
 constexpr int kMaxTok = 16;          // tokens per expert the decode chain handles
-constexpr int kConsumers = 8;        // consumer warps
+constexpr int kConsumers = 16;       // consumer warps
 constexpr int kThreads = 32 * (1 + kConsumers);
-constexpr int kSmemBudget = 214 * 1024;   // dynamic part; + RouteMeta, of the 227 KB allowed
-constexpr int kMaxPairs = 512;        // N * K of the decode chain (16 tokens x top-32)
+constexpr int kSmemBudget = 212 * 1024;   // dynamic part; + RouteMeta, of the 227 KB allowed
 constexpr int kMaxStages = 4;
-constexpr int kDownRows = 32;        // down-projection rows per item (4 per consumer warp)
+constexpr int kMaxPairs = 512;       // N * K of the decode chain (16 tokens x top-32)
+constexpr int kDownRows = 32;        // down-projection rows per item (2 per consumer warp)
 
 // Contiguous, balanced share [i0, i1) of `total` items for this block.
 __device__ __forceinline__ void item_range(int total, int& i0, int& i1) {
@@ -62,27 +65,92 @@ __device__ void load_route_meta(const DecodeArgs& a, RouteMeta& m) {
   __syncthreads();
 }
 
-// Token list of slot `slot` (-1: the shared expert): lane j < ntok gets the token id and the
-// intermediate row of the j-th token.
-__device__ __forceinline__ int slot_tokens(const DecodeArgs& a, const RouteMeta& m, int slot,
-                                           int lane, int& tok, int& row) {
+// Tokens of slot `slot` (-1: the shared expert): first intermediate row and count.
+__device__ __forceinline__ int slot_rows(const DecodeArgs& a, const RouteMeta& m, int slot,
+                                         int& r0) {
   if (slot < 0) {
-    tok = lane;
-    row = a.te + lane;
+    r0 = a.te;
     return a.N;
   }
-  const int r0 = m.slot_r0[slot], ntok = m.slot_n[slot];
-  row = r0 + lane;
-  tok = lane < ntok ? m.row_tok[r0 + lane] : 0;
-  return ntok;
+  r0 = m.slot_r0[slot];
+  return m.slot_n[slot];
+}
+
+__device__ __forceinline__ int token_of_row(const DecodeArgs& a, const RouteMeta& m, int row) {
+  return row >= a.te ? row - a.te : m.row_tok[row];
+}
+
+// Dot products of one bf16 weight row (shared memory) with NT token rows of x (shared
+// memory); only the first `ntok` results are meaningful. Lane-strided 16-byte chunks.
+template <int NT>
+__device__ __forceinline__ void row_dots(const uint4* w, const __nv_bfloat16* xs, int H,
+                                         const int* tk, int lane, float* out) {
+  float acc[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) acc[j] = 0.0f;
+  const uint4* xr[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) xr[j] = reinterpret_cast<const uint4*>(xs + (size_t)tk[j] * H);
+  for (int c = lane; c < H / 8; c += 32) {
+    float wf[8];
+    bf16x8_to_f32(w[c], wf);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      float xf[8];
+      bf16x8_to_f32(xr[j][c], xf);
+      float p0 = wf[0] * xf[0], p1 = wf[1] * xf[1];
+      p0 = fmaf(wf[2], xf[2], p0);
+      p1 = fmaf(wf[3], xf[3], p1);
+      p0 = fmaf(wf[4], xf[4], p0);
+      p1 = fmaf(wf[5], xf[5], p1);
+      p0 = fmaf(wf[6], xf[6], p0);
+      p1 = fmaf(wf[7], xf[7], p1);
+      acc[j] += p0 + p1;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NT; ++j) out[j] = warp_sum(acc[j]);
+}
+
+// Dot products of one bf16 weight row (shared memory) with NT fp32 vectors hs[j * L ...]
+// (shared memory; rows past `ntok` repeat the last valid one and are discarded).
+template <int NT>
+__device__ __forceinline__ void row_dots_h(const uint4* w, const float* hs, int L, int ntok,
+                                           int lane, float* out) {
+  float acc[NT];
+  const float4* hr[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    acc[j] = 0.0f;
+    hr[j] = reinterpret_cast<const float4*>(hs + (size_t)min(j, ntok - 1) * L);
+  }
+#pragma unroll 1
+  for (int c = lane; c < L / 8; c += 32) {
+    float wf[8];
+    bf16x8_to_f32(w[c], wf);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const float4 h0 = hr[j][2 * c], h1 = hr[j][2 * c + 1];
+      float p0 = wf[0] * h0.x, p1 = wf[1] * h0.y;
+      p0 = fmaf(wf[2], h0.z, p0);
+      p1 = fmaf(wf[3], h0.w, p1);
+      p0 = fmaf(wf[4], h1.x, p0);
+      p1 = fmaf(wf[5], h1.y, p1);
+      p0 = fmaf(wf[6], h1.z, p0);
+      p1 = fmaf(wf[7], h1.w, p1);
+      acc[j] += p0 + p1;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NT; ++j) out[j] = warp_sum(acc[j]);
 }
 
 // ------------------------------------------------------------------ gate/up
 
-// hd[row_j, i] = SiLU(x_j . Wg[i]) * (x_j . Wu[i]) for every token j of the slot.
-// Item = `rp` consecutive row pairs of one slot: rp gate rows then rp up rows in the stage.
+// hd[row_j, i] = x_j . Wg[i] and hd[row_j, ldh + i] = x_j . Wu[i] for every token j of the
+// slot. Item = `ri` consecutive rows of one slot's gate or up matrix.
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_gateup_kernel(DecodeArgs a, int rp, int stages, int item_bytes, int xbytes) {
+    decode_gateup_kernel(DecodeArgs a, int ri, int stages, int item_bytes, int xbytes) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteMeta meta;
   const int H = a.H, N = a.N;
@@ -102,17 +170,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the block input is not produced by the router: stage it before waiting on the router
   for (int i = threadIdx.x; i < N * H / 8; i += blockDim.x)
     reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(a.x)[i];
-  __syncthreads();
   pdl_wait();       // routing of the router kernel
   pdl_trigger();    // the down projection may start streaming its weights
-  load_route_meta(a, meta);
+  load_route_meta(a, meta);   // (ends with a block barrier: x is staged too)
 
-  const int per_slot = a.I / rp;
+  // items per slot: the gate rows in chunks of ri, then the up rows
+  const int per_slot = 2 * (a.I / ri);
   const int routed = meta.n_active * per_slot;
-  const int total = routed + (a.S > 0 ? a.S / rp : 0);
+  const int total = routed + (a.S > 0 ? 2 * (a.S / ri) : 0);
   int i0, i1;
   item_range(total, i0, i1);
-  const uint32_t half_bytes = (uint32_t)(rp * H * 2);
+  const uint32_t bytes = (uint32_t)(ri * H * 2);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -121,21 +189,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = i0; it < i1; ++it, ++issued) {
         const int k = it - i0, s = k % stages;
         if (!mbar_wait(&empty[s], ((k / stages) & 1) ^ 1, a.hdr)) { ok = false; break; }
-        const __nv_bfloat16 *g, *u;
+        const __nv_bfloat16* src;
         if (it < routed) {
           const int e = meta.slot_e[it / per_slot];
-          const size_t r = (size_t)e * a.I + (size_t)(it % per_slot) * rp;
-          g = a.wg + r * H;
-          u = a.wu + r * H;
+          const int j = it % per_slot, half = a.I / ri;
+          src = (j < half ? a.wg : a.wu) + ((size_t)e * a.I + (size_t)(j % half) * ri) * H;
         } else {
-          const size_t r = (size_t)(it - routed) * rp;
-          g = a.sg + r * H;
-          u = a.su + r * H;
+          const int j = it - routed, half = a.S / ri;
+          src = (j < half ? a.sg : a.su) + (size_t)(j % half) * ri * H;
         }
-        uint8_t* dst = ring + (size_t)s * item_bytes;
-        mbar_arrive_expect_tx(&full[s], 2 * half_bytes);
-        bulk_load(dst, g, half_bytes, &full[s]);
-        bulk_load(dst + half_bytes, u, half_bytes, &full[s]);
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_load(ring + (size_t)s * item_bytes, src, bytes, &full[s]);
       }
       if (!ok)   // let the copies already issued land before the block can exit
         for (int k = issued > stages ? issued - stages : 0; k < issued; ++k)
@@ -143,52 +207,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int cw = warp - 1;
-    int cur_slot = -2, ntok = 0, tok = 0, orow = 0;
+    int cur_slot = -2, ntok = 0, r0 = 0;
+    int tk[kMaxTok];
+#pragma unroll
+    for (int j = 0; j < kMaxTok; ++j) tk[j] = 0;
     for (int it = i0; it < i1; ++it) {
       const int k = it - i0, s = k % stages;
-      const int slot = it < routed ? it / per_slot : -1;
-      const int i = (it < routed ? (it % per_slot) : (it - routed)) * rp + cw;
+      const bool routed_item = it < routed;
+      const int slot = routed_item ? it / per_slot : -1;
+      const int j = routed_item ? it % per_slot : it - routed;
+      const int half = (routed_item ? a.I : a.S) / ri;
+      const int col = (j < half ? 0 : a.ldh) + (j % half) * ri + cw;   // hd column
       if (slot != cur_slot) {
         cur_slot = slot;
-        ntok = slot_tokens(a, meta, slot, lane, tok, orow);
+        ntok = slot_rows(a, meta, slot, r0);
+#pragma unroll
+        for (int q = 0; q < kMaxTok; ++q)
+          tk[q] = q < ntok ? token_of_row(a, meta, r0 + q) : tk[0];
       }
       if (!mbar_wait(&full[s], (k / stages) & 1, a.hdr)) break;
-      if (cw < rp) {
-        const uint8_t* st = ring + (size_t)s * item_bytes + (size_t)cw * H * 2;
-        const uint4* gr = reinterpret_cast<const uint4*>(st);
-        const uint4* ur = reinterpret_cast<const uint4*>(st + half_bytes);
-        float ag[kMaxTok], au[kMaxTok];
-        int tks[kMaxTok];     // token ids, gathered while the whole warp is converged
+      if (cw < ri) {
+        const uint4* w = reinterpret_cast<const uint4*>(ring + (size_t)s * item_bytes +
+                                                        (size_t)cw * H * 2);
+        float d[kMaxTok];
+        if (ntok <= 1) row_dots<1>(w, xs, H, tk, lane, d);
+        else if (ntok <= 2) row_dots<2>(w, xs, H, tk, lane, d);
+        else if (ntok <= 4) row_dots<4>(w, xs, H, tk, lane, d);
+        else if (ntok <= 8) row_dots<8>(w, xs, H, tk, lane, d);
+        else row_dots<16>(w, xs, H, tk, lane, d);
+        if (lane < ntok) {
+          // lane j stores token j's result (d[] is warp-uniform after the reduction)
+          float v = d[0];
 #pragma unroll
-        for (int j = 0; j < kMaxTok; ++j) {
-          ag[j] = au[j] = 0.0f;
-          tks[j] = __shfl_sync(0xffffffffu, tok, j);
-        }
-        for (int c = lane; c < H / 8; c += 32) {
-          float gf[8], uf[8];
-          bf16x8_to_f32(gr[c], gf);
-          bf16x8_to_f32(ur[c], uf);
-#pragma unroll
-          for (int j = 0; j < kMaxTok; ++j) {
-            if (j < ntok) {
-              float xf[8];
-              bf16x8_to_f32(reinterpret_cast<const uint4*>(xs + (size_t)tks[j] * H)[c], xf);
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                ag[j] = fmaf(gf[q], xf[q], ag[j]);
-                au[j] = fmaf(uf[q], xf[q], au[j]);
-              }
-            }
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < kMaxTok; ++j) {
-          if (j < ntok) {
-            const float gs = warp_sum(ag[j]);
-            const float us = warp_sum(au[j]);
-            const int rj = __shfl_sync(0xffffffffu, orow, j);
-            if (lane == 0) a.hd[(size_t)rj * a.ldh + i] = silu(gs) * us;
-          }
+          for (int q = 1; q < kMaxTok; ++q)
+            if (lane == q) v = d[q];
+          a.hd[(size_t)(r0 + lane) * (2 * a.ldh) + col] = v;
         }
       }
       __syncwarp();
@@ -199,14 +252,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ down
 
-// y_j[r] = h_j . Wd[r] for every token j of the slot. Item = kDownRows consecutive rows of
-// Wd_e (or of the shared down weights); routed results go to yd, or are weighted and
-// atomically added into acc; shared results go to shy.
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// y_j[r] = h_j . Wd[r] for every token j of the slot, h_j = SiLU(gate_j) * up_j. Item =
+// kDownRows consecutive rows of Wd_e (or of the shared down weights); routed results go to
+// yd, or are weighted and atomically added into acc; shared results go to shy.
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_down_kernel(DecodeArgs a, int stages, int item_bytes) {
+    decode_down_kernel(DecodeArgs a, int stages, int item_bytes, int hbytes) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteMeta meta;
-  uint8_t* ring = smem;
+  float* hs = reinterpret_cast<float*>(smem);                  // [ntok, L] of the current slot
+  uint8_t* ring = smem + hbytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)stages * item_bytes);
   uint64_t* empty = full + kMaxStages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -220,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // Routing metadata comes from the router kernel, which finished before the gate/up kernel
   // passed its own wait, so the weights can stream before this kernel's wait; only the
-  // consumers read the SwiGLU outputs and wait for them.
+  // consumers read the gate/up results and wait for them.
   load_route_meta(a, meta);
   const int per_slot = H / kDownRows;
   const int routed = meta.n_active * per_slot;
@@ -254,73 +312,65 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(&full[k % stages], (k / stages) & 1, nullptr);
     }
   } else {
-    pdl_wait();     // SwiGLU outputs of the gate/up kernel
+    pdl_wait();     // gate/up results of the previous kernel
     pdl_trigger();
-    const int cw = warp - 1;
-    int cur_slot = -2, ntok = 0, tok = 0, orow = 0;
-    float wt = 0.0f;
+    const int cw = warp - 1, ct = threadIdx.x - 32;
+    int cur_slot = -2, ntok = 0, r0 = 0, L = a.I;
+    bool live = true;   // false after a timed-out wait: keep pace (barriers), skip the work
     for (int it = i0; it < i1; ++it) {
       const int k = it - i0, s = k % stages;
       const bool shared_item = it >= routed;
       const int slot = shared_item ? -1 : it / per_slot;
       const int rbase = (shared_item ? it - routed : it % per_slot) * kDownRows;
-      const int L = shared_item ? a.S : a.I;
       if (slot != cur_slot) {
+        // every consumer warp walks the same items, so they all change slot together
+        named_sync(1, 32 * kConsumers);
         cur_slot = slot;
-        ntok = slot_tokens(a, meta, slot, lane, tok, orow);
-        if (!shared_item && a.acc && lane < ntok) wt = a.w[__ldcg(a.sorted_pairs + orow)];
+        ntok = slot_rows(a, meta, slot, r0);
+        L = shared_item ? a.S : a.I;
+        for (int i = ct; i < ntok * L; i += 32 * kConsumers) {
+          const int j = i / L, c = i % L;
+          const float* hr = a.hd + (size_t)(r0 + j) * (2 * a.ldh);
+          hs[j * L + c] = silu(__ldcg(hr + c)) * __ldcg(hr + a.ldh + c);
+        }
+        named_sync(1, 32 * kConsumers);
       }
-      if (!mbar_wait(&full[s], (k / stages) & 1, a.hdr)) break;
-      const uint8_t* stage = ring + (size_t)s * item_bytes;
+      if (live && !mbar_wait(&full[s], (k / stages) & 1, a.hdr)) live = false;
+      if (live) {
+        const uint8_t* stage = ring + (size_t)s * item_bytes;
 #pragma unroll 1
-      for (int rr = 0; rr < kDownRows / kConsumers; ++rr) {
-        const int rl = cw * (kDownRows / kConsumers) + rr;
-        const uint4* wr = reinterpret_cast<const uint4*>(stage + (size_t)rl * L * 2);
-        float acc[kMaxTok];
-        int rws[kMaxTok];     // SwiGLU rows, gathered while the whole warp is converged
+        for (int rr = 0; rr < kDownRows / kConsumers; ++rr) {
+          const int rl = cw * (kDownRows / kConsumers) + rr;
+          const uint4* wr = reinterpret_cast<const uint4*>(stage + (size_t)rl * L * 2);
+          const int r = rbase + rl;
+          // groups of up to 4 tokens: each group's results are stored before the next
+          for (int j0 = 0; j0 < ntok; j0 += 4) {
+            const int nt = min(4, ntok - j0);
+            float acc[4];
+            const float* hg = hs + (size_t)j0 * L;
+            if (nt == 1) row_dots_h<1>(wr, hg, L, nt, lane, acc);
+            else if (nt == 2) row_dots_h<2>(wr, hg, L, nt, lane, acc);
+            else row_dots_h<4>(wr, hg, L, nt, lane, acc);
+            if (lane < nt) {
+              float y = acc[0];
 #pragma unroll
-        for (int j = 0; j < kMaxTok; ++j) {
-          acc[j] = 0.0f;
-          rws[j] = __shfl_sync(0xffffffffu, orow, j);
-        }
-        for (int c = lane; c < L / 8; c += 32) {
-          float wf[8];
-          bf16x8_to_f32(wr[c], wf);
-#pragma unroll
-          for (int j = 0; j < kMaxTok; ++j) {
-            if (j < ntok) {
-              const float4* hp =
-                  reinterpret_cast<const float4*>(a.hd + (size_t)rws[j] * a.ldh) + 2 * c;
-              const float4 h0 = hp[0], h1 = hp[1];
-              acc[j] = fmaf(wf[0], h0.x, acc[j]);
-              acc[j] = fmaf(wf[1], h0.y, acc[j]);
-              acc[j] = fmaf(wf[2], h0.z, acc[j]);
-              acc[j] = fmaf(wf[3], h0.w, acc[j]);
-              acc[j] = fmaf(wf[4], h1.x, acc[j]);
-              acc[j] = fmaf(wf[5], h1.y, acc[j]);
-              acc[j] = fmaf(wf[6], h1.z, acc[j]);
-              acc[j] = fmaf(wf[7], h1.w, acc[j]);
-            }
-          }
-        }
-        const int r = rbase + rl;
-#pragma unroll
-        for (int j = 0; j < kMaxTok; ++j) {
-          if (j < ntok) {
-            const float y = warp_sum(acc[j]);
-            const int tj = __shfl_sync(0xffffffffu, tok, j);
-            const int rj = __shfl_sync(0xffffffffu, orow, j);
-            const float wj = __shfl_sync(0xffffffffu, wt, j);
-            if (lane == 0) {
-              if (shared_item) a.shy[(size_t)tj * H + r] = y;
-              else if (a.acc) atomicAdd(a.acc + (size_t)tj * H + r, wj * y);
-              else a.yd[(size_t)rj * H + r] = y;
+              for (int q = 1; q < 4; ++q)
+                if (lane == q) y = acc[q];
+              const int j = j0 + lane, row = r0 + j;
+              if (shared_item) {
+                a.shy[(size_t)j * H + r] = y;
+              } else if (a.acc) {
+                const int t = meta.row_tok[row];
+                atomicAdd(a.acc + (size_t)t * H + r, a.w[__ldcg(a.sorted_pairs + row)] * y);
+              } else {
+                a.yd[(size_t)row * H + r] = y;
+              }
             }
           }
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      if (lane == 0 && live) mbar_arrive(&empty[s]);
     }
   }
 }
@@ -343,12 +393,12 @@ int sm_count() {
 cudaError_t launch_decode_gateup(const DecodeArgs& a, cudaStream_t st) {
   if (a.te > kMaxPairs) return cudaErrorInvalidValue;
   const int xbytes = (a.N * a.H * 2 + 127) & ~127;
-  // row pairs per item: the most (<= 8, one per consumer warp) that keep 3 stages in budget
-  int rp = 8;
-  while (rp > 1 && (a.I % rp || (a.S && a.S % rp) ||
-                    (size_t)xbytes + 3 * (size_t)rp * 4 * a.H + 1024 > (size_t)kSmemBudget))
-    rp >>= 1;
-  const int item = rp * 4 * a.H;
+  // rows per item: the most (<= 16, one per consumer warp) that keep 3 stages in budget
+  int ri = kConsumers;
+  while (ri > 1 && (a.I % ri || (a.S && a.S % ri) ||
+                    (size_t)xbytes + 3 * (size_t)ri * 2 * a.H + 1024 > (size_t)kSmemBudget))
+    ri >>= 1;
+  const int item = ri * 2 * a.H;
   int stages = (kSmemBudget - 1024 - xbytes) / item;
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 1) return cudaErrorInvalidValue;
@@ -356,23 +406,25 @@ cudaError_t launch_decode_gateup(const DecodeArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(decode_gateup_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  return launch_dependent(decode_gateup_kernel, dim3(sm_count()), dim3(kThreads), sm, st, a, rp,
+  return launch_dependent(decode_gateup_kernel, dim3(sm_count()), dim3(kThreads), sm, st, a, ri,
                           stages, item, xbytes);
 }
 
 cudaError_t launch_decode_down(const DecodeArgs& a, cudaStream_t st) {
   if (a.H % kDownRows || a.te > kMaxPairs) return cudaErrorInvalidValue;
   const int L = a.I > a.S ? a.I : a.S;
+  const int maxtok = a.N < kMaxTok ? a.N : kMaxTok;
+  const int hbytes = (maxtok * L * 4 + 127) & ~127;
   const int item = kDownRows * L * 2;
-  int stages = (kSmemBudget - 1024) / item;
+  int stages = (kSmemBudget - 1024 - hbytes) / item;
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 1) return cudaErrorInvalidValue;
-  const size_t sm = (size_t)stages * item + 2 * kMaxStages * 8;
+  const size_t sm = (size_t)hbytes + (size_t)stages * item + 2 * kMaxStages * 8;
   cudaError_t e = cudaFuncSetAttribute(decode_down_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   return launch_dependent(decode_down_kernel, dim3(sm_count()), dim3(kThreads), sm, st, a, stages,
-                          item);
+                          item, hbytes);
 }
 
 }  // namespace moe

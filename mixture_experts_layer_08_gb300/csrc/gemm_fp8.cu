@@ -27,12 +27,16 @@ constexpr int kThreads = 320;
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 128;                    // fp8 elements = bytes per swizzle row
-constexpr int kStages = 4;
+constexpr int kStages = 3;
+constexpr int kMaxKb = 32;                  // K blocks of 128 per tile (K <= 4096)
+constexpr int kEpi = 256;                   // promotion / epilogue threads
 constexpr int kATile = kBM * kBK;           // 16 KB
 constexpr int kBTile = kBN * kBK;           // 32 KB
 constexpr int kStageBytes = kATile + kBTile;
 constexpr int kTmemCols = 2 * kBN;          // two partial buffers
-constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024 + 256 + 2 * 2 * 128 * 4;
+constexpr size_t kScaleBytes = (size_t)kMaxKb * kEpi * 4 + (size_t)8 * kMaxKb * 2 * 4;
+constexpr size_t kSmemBytes =
+    (size_t)kStages * kStageBytes + 1024 + 256 + 2 * 2 * 128 * 4 + kScaleBytes;
 
 // Hands this thread's row amax to the warp that owns the other column half of the same row
 // and returns the partner's; `seq` tags the tile so values of different tiles never mix.
@@ -73,6 +77,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   float* amax_s = reinterpret_cast<float*>(smem + kStages * kStageBytes + 256);  // [2][128]
   uint32_t* seq_s = reinterpret_cast<uint32_t*>(amax_s + 2 * 128);                  // [2][128]
+  // per tile: each promotion thread's row scale for every K block ([kb][thread]), and each
+  // epilogue warp's weight-block scales ([warp][kb][gate/up])
+  float* sa_s = reinterpret_cast<float*>(seq_s + 2 * 128);
+  float* sb_s = sa_s + kMaxKb * kEpi;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WsHeader* hdr = g.status;
@@ -169,21 +177,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int e = t.x;
       const int row = t.y + r_local;
       const bool valid = row < t.z;
+      // this tile's scales into shared memory, loads in flight together: every promotion
+      // step below then reads them without a global round trip
+      const int et = threadIdx.x - 64, ew = et >> 5;
+      for (int kb = 0; kb < g.num_kb; ++kb)
+        sa_s[kb * kEpi + et] = valid ? __ldg(g.sa + (size_t)kb * g.sa_stride + row) : 0.0f;
+      if (lane < g.num_kb) {
+        float b0, b1;
+        if (MODE == 0) {
+          const size_t bi = ((size_t)e * g.b_blocks_per_expert + n) * g.num_kb + lane;
+          b0 = __ldg(g.sb0 + bi);
+          b1 = __ldg(g.sb1 + bi);
+        } else {
+          const size_t bi =
+              ((size_t)e * g.b_blocks_per_expert + 2 * n + half) * g.num_kb + lane;
+          b0 = b1 = __ldg(g.sb0 + bi);
+        }
+        sb_s[(ew * kMaxKb + lane) * 2] = b0;
+        sb_s[(ew * kMaxKb + lane) * 2 + 1] = b1;
+      }
+      __syncwarp();
       float acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
       for (int kb = 0; kb < g.num_kb; ++kb, ++pc) {
         const uint32_t slot = pc & 1;
-        const float sa = valid ? g.sa[(size_t)kb * g.sa_stride + row] : 0.0f;
-        float s0, s1;
-        if (MODE == 0) {
-          const size_t bi = ((size_t)e * g.b_blocks_per_expert + n) * g.num_kb + kb;
-          s0 = sa * g.sb0[bi];
-          s1 = sa * g.sb1[bi];
-        } else {
-          const size_t bi = ((size_t)e * g.b_blocks_per_expert + 2 * n + half) * g.num_kb + kb;
-          s0 = s1 = sa * g.sb0[bi];
-        }
+        const float sa = sa_s[kb * kEpi + et];
+        const float s0 = sa * sb_s[(ew * kMaxKb + kb) * 2];
+        const float s1 = sa * sb_s[(ew * kMaxKb + kb) * 2 + 1];
         if (!mbar_wait(&pfull[slot], (pc >> 1) & 1, hdr)) { ok = false; break; }
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + slot * kBN;
@@ -201,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&pempty[slot]);
       }
+      __syncwarp();     // the next tile rewrites this warp's scales
       if (!ok) break;
       if (MODE == 0) {
         // h = SiLU(gate) * up for 64 columns; quantise each row's 128-wide group (two warps)

@@ -54,6 +54,9 @@ struct SortArgs {
   uint32_t* sorted_pairs;          // [te]
   uint32_t* active;                // [E] experts with rows, ascending
   int4* tiles;                     // [max m-tiles] (expert, row0, row1, 0)
+  const uint8_t* xq_tok;           // FP8 experts: E4M3 codes of each token row [N, H]
+  const float* xs_tok;             // and their 1x128 scales [H/128, N]
+  int N;
   WsHeader* hdr;
 };
 
@@ -64,9 +67,12 @@ cudaError_t launch_router_small(const RouteArgs& a, const SortArgs& s, bool fuse
                                 cudaStream_t st);
 // Scoring + top-K + weights, one warp per token.
 cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st);
+// Per 1x128 E4M3 quantisation of the token rows (FP8 experts): codes [N,H], scales [H/128,N].
+cudaError_t launch_quant_rows(const __nv_bfloat16* x, int N, int H, uint8_t* q, float* sc,
+                              cudaStream_t st);
 // Stable counting sort of the (token, slot) pairs by expert (count / scan / scatter) and the
 // m-tile list of the grouped GEMM. Scatter also gathers x rows (bf16) into `xp` when given,
-// or quantises them per 1x128 to E4M3 into `xq` + `xs` (kb-major scales [H/128, te]).
+// or the quantised token rows (s.xq_tok / s.xs_tok) into `xq` + `xs` (scales [H/128, te]).
 cudaError_t launch_sort(const SortArgs& s, const __nv_bfloat16* x, int H, __nv_bfloat16* xp,
                         uint8_t* xq, float* xs, cudaStream_t st);
 
@@ -80,9 +86,9 @@ struct DecodeArgs {
   const uint32_t* active;
   const float* w;                  // routing weights [N,K]
   int N, H, E, K, I, S, te;
-  float* hd;                       // [te + N, max(I,S)] fp32 SwiGLU outputs (row = sorted row,
-                                   // shared rows te + t)
-  int ldh;
+  float* hd;                       // [te + N, 2*ldh] fp32 gate (cols < ldh) and up dot products
+                                   // (row = sorted row, shared rows te + t)
+  int ldh;                         // max(I, S)
   float* yd;                       // [te, H] fp32 (deterministic) or null
   float* acc;                      // [N, H] fp32 atomic accumulator or null
   float* shy;                      // [N, H] fp32 shared expert output

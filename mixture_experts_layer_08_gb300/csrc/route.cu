@@ -374,40 +374,61 @@ __global__ void __launch_bounds__(256) sort_scatter_kernel(SortArgs s, const __n
     for (int c = lane; c < H / 8; c += 32) dst[c] = src[c];
   }
   if (xq) {
-    // 1x128 groups: 16 lanes x 8 values; amax, scale = amax/448 (1 if 0), code = e4m3(v/scale)
-    const int te_stride = s.te;
-    for (int c0 = 0; c0 < H / 8; c0 += 32) {
-      const int c = c0 + lane;
-      const bool on = c < H / 8;
-      float f[8];
+    // E4M3 codes and 1x128 scales of the token row (quantised once per token)
+    const uint4* qsrc = reinterpret_cast<const uint4*>(s.xq_tok + (size_t)t * H);
+    uint4* qdst = reinterpret_cast<uint4*>(xq + (size_t)row * H);
+    for (int c = lane; c < H / 16; c += 32) qdst[c] = qsrc[c];
+    for (int g = lane; g < H / 128; g += 32)
+      xsc[(size_t)g * s.te + row] = s.xs_tok[(size_t)g * s.N + t];
+  }
+}
+
+// One warp per token row: per 1x128 group, amax, scale = amax/448 (1 if 0) and the E4M3
+// code of value/scale (round to nearest even, saturating), all decided in fp32.
+// Codes [N, H]; scales [H/128, N].
+__global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* x, int N, int H,
+                                                         uint8_t* q, float* sc) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= N) return;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  for (int c0 = 0; c0 < H / 8; c0 += 32) {
+    const int c = c0 + lane;
+    const bool on = c < H / 8;
+    float f[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) f[i] = 0.0f;
-      if (on) bf16x8_to_f32(src[c], f);
-      float am = 0.0f;
+    for (int i = 0; i < 8; ++i) f[i] = 0.0f;
+    if (on) bf16x8_to_f32(src[c], f);
+    float am = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
+    for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-      const float sc = am > 0.0f ? __fdiv_rn(am, 448.0f) : 1.0f;
-      uint32_t lo = 0, hi = 0;
+    for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    const float s = am > 0.0f ? __fdiv_rn(am, 448.0f) : 1.0f;
+    uint32_t lo = 0, hi = 0;
 #pragma unroll
-      for (int i = 0; i < 4; i += 2) {
-        lo |= (uint32_t)__nv_cvt_float2_to_fp8x2(
-                  make_float2(__fdiv_rn(f[i], sc), __fdiv_rn(f[i + 1], sc)), __NV_SATFINITE,
-                  __NV_E4M3) << (8 * i);
-        hi |= (uint32_t)__nv_cvt_float2_to_fp8x2(
-                  make_float2(__fdiv_rn(f[4 + i], sc), __fdiv_rn(f[5 + i], sc)), __NV_SATFINITE,
-                  __NV_E4M3) << (8 * i);
-      }
-      if (on) {
-        reinterpret_cast<uint2*>(xq + (size_t)row * H)[c] = make_uint2(lo, hi);
-        if ((lane & 15) == 0) xsc[(size_t)(c / 16) * te_stride + row] = sc;
-      }
+    for (int i = 0; i < 4; i += 2) {
+      lo |= (uint32_t)__nv_cvt_float2_to_fp8x2(
+                make_float2(__fdiv_rn(f[i], s), __fdiv_rn(f[i + 1], s)), __NV_SATFINITE,
+                __NV_E4M3) << (8 * i);
+      hi |= (uint32_t)__nv_cvt_float2_to_fp8x2(
+                make_float2(__fdiv_rn(f[4 + i], s), __fdiv_rn(f[5 + i], s)), __NV_SATFINITE,
+                __NV_E4M3) << (8 * i);
+    }
+    if (on) {
+      reinterpret_cast<uint2*>(q + (size_t)t * H)[c] = make_uint2(lo, hi);
+      if ((lane & 15) == 0) sc[(size_t)(c / 16) * N + t] = s;
     }
   }
 }
 
 }  // namespace
+
+cudaError_t launch_quant_rows(const __nv_bfloat16* x, int N, int H, uint8_t* q, float* sc,
+                              cudaStream_t st) {
+  quant_rows_kernel<<<(N + 7) / 8, 256, 0, st>>>(x, N, H, q, sc);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_router_small(const RouteArgs& a, const SortArgs& s, bool fuse_tail,
                                 cudaStream_t st) {
