@@ -69,15 +69,29 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(CombineArgs a) {
     gamma = 1.0f / (1.0f + expf(-d));
   }
   const int c = blockIdx.y * kCombThreads + threadIdx.x;    // chunk of 8 outputs
-  if (c >= H / 8) return;
+  const bool on = c < H / 8;
   const size_t h0 = (size_t)c * 8;
+  // Everything produced before the expert projections (routing, x) is read before waiting on
+  // the previous kernel: it finished at least two launches back.
   float acc[8];
+  {
+    const float z = a.zsum[t];
+    float xf[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int i = 0; i < 8; ++i) xf[i] = 0.0f;
+    if (on) bf16x8_to_f32(reinterpret_cast<const uint4*>(xt)[c], xf);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = z * xf[i];
+  }
+  pdl_wait();     // expert outputs of the previous kernel
+  if (!on) return;
   if (a.acc) {
     Row8<true> r;
     r.load(a.acc, (size_t)t * H + h0);
-    r.widen(acc);
+    float f[8];
+    r.widen(f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += f[i];
   }
   if (a.y) {
     // 4 expert rows in flight per round, loaded before any of them is used
@@ -103,13 +117,6 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(CombineArgs a) {
         }
       }
     }
-  }
-  {
-    const float z = a.zsum[t];
-    float xf[8];
-    bf16x8_to_f32(reinterpret_cast<const uint4*>(xt)[c], xf);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = fmaf(z, xf[i], acc[i]);
   }
   if (a.shy) {
     Row8<SF32> r;
@@ -146,9 +153,8 @@ cudaError_t launch_bounded_wait_selftest(WsHeader* hdr, long long limit_cycles, 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
   dim3 grid(a.N, (a.H / 8 + kCombThreads - 1) / kCombThreads);
   if (a.y_is_f32 != a.shy_is_f32 && a.shy) return cudaErrorInvalidValue;
-  if (a.y_is_f32) combine_kernel<true, true><<<grid, kCombThreads, 0, st>>>(a);
-  else combine_kernel<false, false><<<grid, kCombThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  if (a.y_is_f32) return launch_dependent(combine_kernel<true, true>, grid, dim3(kCombThreads), 0, st, a);
+  return launch_dependent(combine_kernel<false, false>, grid, dim3(kCombThreads), 0, st, a);
 }
 
 }  // namespace moe

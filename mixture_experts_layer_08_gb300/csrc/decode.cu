@@ -80,31 +80,31 @@ __device__ __forceinline__ int token_of_row(const DecodeArgs& a, const RouteMeta
   return row >= a.te ? row - a.te : m.row_tok[row];
 }
 
-// Dot products of one bf16 weight row (shared memory) with NT token rows of x (shared
+// Dot products of one bf16 weight row (shared memory) with NT fp32 token rows of x (shared
 // memory); only the first `ntok` results are meaningful. Lane-strided 16-byte chunks.
 template <int NT>
-__device__ __forceinline__ void row_dots(const uint4* w, const __nv_bfloat16* xs, int H,
-                                         const int* tk, int lane, float* out) {
+__device__ __forceinline__ void row_dots(const uint4* w, const float* xs, int H, const int* tk,
+                                         int lane, float* out) {
   float acc[NT];
+  const float4* xr[NT];
 #pragma unroll
-  for (int j = 0; j < NT; ++j) acc[j] = 0.0f;
-  const uint4* xr[NT];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) xr[j] = reinterpret_cast<const uint4*>(xs + (size_t)tk[j] * H);
+  for (int j = 0; j < NT; ++j) {
+    acc[j] = 0.0f;
+    xr[j] = reinterpret_cast<const float4*>(xs + (size_t)tk[j] * H);
+  }
   for (int c = lane; c < H / 8; c += 32) {
     float wf[8];
     bf16x8_to_f32(w[c], wf);
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      float xf[8];
-      bf16x8_to_f32(xr[j][c], xf);
-      float p0 = wf[0] * xf[0], p1 = wf[1] * xf[1];
-      p0 = fmaf(wf[2], xf[2], p0);
-      p1 = fmaf(wf[3], xf[3], p1);
-      p0 = fmaf(wf[4], xf[4], p0);
-      p1 = fmaf(wf[5], xf[5], p1);
-      p0 = fmaf(wf[6], xf[6], p0);
-      p1 = fmaf(wf[7], xf[7], p1);
+      const float4 x0 = xr[j][2 * c], x1 = xr[j][2 * c + 1];
+      float p0 = wf[0] * x0.x, p1 = wf[1] * x0.y;
+      p0 = fmaf(wf[2], x0.z, p0);
+      p1 = fmaf(wf[3], x0.w, p1);
+      p0 = fmaf(wf[4], x1.x, p0);
+      p1 = fmaf(wf[5], x1.y, p1);
+      p0 = fmaf(wf[6], x1.z, p0);
+      p1 = fmaf(wf[7], x1.w, p1);
       acc[j] += p0 + p1;
     }
   }
@@ -112,37 +112,44 @@ __device__ __forceinline__ void row_dots(const uint4* w, const __nv_bfloat16* xs
   for (int j = 0; j < NT; ++j) out[j] = warp_sum(acc[j]);
 }
 
-// Dot products of one bf16 weight row (shared memory) with NT fp32 vectors hs[j * L ...]
-// (shared memory; rows past `ntok` repeat the last valid one and are discarded).
+// Dot products of two bf16 weight rows (shared memory) with NT fp32 vectors hs[j * L ...]
+// (shared memory; rows past `ntok` repeat the last valid one and are discarded). Each h chunk
+// is loaded once for both rows. out0/out1: results of row 0 / row 1.
 template <int NT>
-__device__ __forceinline__ void row_dots_h(const uint4* w, const float* hs, int L, int ntok,
-                                           int lane, float* out) {
-  float acc[NT];
+__device__ __forceinline__ void row2_dots_h(const uint4* w0, const uint4* w1, const float* hs,
+                                            int L, int ntok, int lane, float* out0,
+                                            float* out1) {
+  float a0[NT], a1[NT];
   const float4* hr[NT];
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
-    acc[j] = 0.0f;
+    a0[j] = a1[j] = 0.0f;
     hr[j] = reinterpret_cast<const float4*>(hs + (size_t)min(j, ntok - 1) * L);
   }
 #pragma unroll 1
   for (int c = lane; c < L / 8; c += 32) {
-    float wf[8];
-    bf16x8_to_f32(w[c], wf);
+    float f0[8], f1[8];
+    bf16x8_to_f32(w0[c], f0);
+    bf16x8_to_f32(w1[c], f1);
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       const float4 h0 = hr[j][2 * c], h1 = hr[j][2 * c + 1];
-      float p0 = wf[0] * h0.x, p1 = wf[1] * h0.y;
-      p0 = fmaf(wf[2], h0.z, p0);
-      p1 = fmaf(wf[3], h0.w, p1);
-      p0 = fmaf(wf[4], h1.x, p0);
-      p1 = fmaf(wf[5], h1.y, p1);
-      p0 = fmaf(wf[6], h1.z, p0);
-      p1 = fmaf(wf[7], h1.w, p1);
-      acc[j] += p0 + p1;
+      const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+      float p0 = f0[0] * hv[0], p1 = f1[0] * hv[0];
+#pragma unroll
+      for (int q = 1; q < 8; ++q) {
+        p0 = fmaf(f0[q], hv[q], p0);
+        p1 = fmaf(f1[q], hv[q], p1);
+      }
+      a0[j] += p0;
+      a1[j] += p1;
     }
   }
 #pragma unroll
-  for (int j = 0; j < NT; ++j) out[j] = warp_sum(acc[j]);
+  for (int j = 0; j < NT; ++j) {
+    out0[j] = warp_sum(a0[j]);
+    out1[j] = warp_sum(a1[j]);
+  }
 }
 
 // ------------------------------------------------------------------ gate/up
@@ -154,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteMeta meta;
   const int H = a.H, N = a.N;
-  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);             // [N, H]
+  float* xs = reinterpret_cast<float*>(smem);                               // [N, H] fp32
   uint8_t* ring = smem + xbytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)stages * item_bytes);
   uint64_t* empty = full + kMaxStages;
@@ -167,9 +174,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbarrier_init();
   }
-  // the block input is not produced by the router: stage it before waiting on the router
-  for (int i = threadIdx.x; i < N * H / 8; i += blockDim.x)
-    reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(a.x)[i];
+  // the block input is not produced by the router: stage it (widened to fp32) before waiting
+  for (int i = threadIdx.x; i < N * H / 8; i += blockDim.x) {
+    float f[8];
+    bf16x8_to_f32(reinterpret_cast<const uint4*>(a.x)[i], f);
+    reinterpret_cast<float4*>(xs)[2 * i] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4*>(xs)[2 * i + 1] = make_float4(f[4], f[5], f[6], f[7]);
+  }
   pdl_wait();       // routing of the router kernel
   pdl_trigger();    // the down projection may start streaming its weights
   load_route_meta(a, meta);   // (ends with a block barrier: x is staged too)
@@ -208,9 +219,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     const int cw = warp - 1;
     int cur_slot = -2, ntok = 0, r0 = 0;
-    int tk[kMaxTok];
-#pragma unroll
-    for (int j = 0; j < kMaxTok; ++j) tk[j] = 0;
     for (int it = i0; it < i1; ++it) {
       const int k = it - i0, s = k % stages;
       const bool routed_item = it < routed;
@@ -221,27 +229,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (slot != cur_slot) {
         cur_slot = slot;
         ntok = slot_rows(a, meta, slot, r0);
-#pragma unroll
-        for (int q = 0; q < kMaxTok; ++q)
-          tk[q] = q < ntok ? token_of_row(a, meta, r0 + q) : tk[0];
       }
       if (!mbar_wait(&full[s], (k / stages) & 1, a.hdr)) break;
       if (cw < ri) {
         const uint4* w = reinterpret_cast<const uint4*>(ring + (size_t)s * item_bytes +
                                                         (size_t)cw * H * 2);
-        float d[kMaxTok];
-        if (ntok <= 1) row_dots<1>(w, xs, H, tk, lane, d);
-        else if (ntok <= 2) row_dots<2>(w, xs, H, tk, lane, d);
-        else if (ntok <= 4) row_dots<4>(w, xs, H, tk, lane, d);
-        else if (ntok <= 8) row_dots<8>(w, xs, H, tk, lane, d);
-        else row_dots<16>(w, xs, H, tk, lane, d);
-        if (lane < ntok) {
-          // lane j stores token j's result (d[] is warp-uniform after the reduction)
-          float v = d[0];
+        // groups of up to 4 tokens: each group's results are stored before the next
+        for (int j0 = 0; j0 < ntok; j0 += 4) {
+          const int nt = min(4, ntok - j0);
+          int tg[4];          // the group's tokens; past ntok, repeats of a valid one
 #pragma unroll
-          for (int q = 1; q < kMaxTok; ++q)
-            if (lane == q) v = d[q];
-          a.hd[(size_t)(r0 + lane) * (2 * a.ldh) + col] = v;
+          for (int u = 0; u < 4; ++u) tg[u] = token_of_row(a, meta, r0 + j0 + min(u, nt - 1));
+          float d[4];
+          if (nt == 1) row_dots<1>(w, xs, H, tg, lane, d);
+          else if (nt == 2) row_dots<2>(w, xs, H, tg, lane, d);
+          else row_dots<4>(w, xs, H, tg, lane, d);
+          if (lane < nt) {
+            float v = d[0];
+#pragma unroll
+            for (int q = 1; q < 4; ++q)
+              if (lane == q) v = d[q];
+            a.hd[(size_t)(r0 + j0 + lane) * (2 * a.ldh) + col] = v;
+          }
         }
       }
       __syncwarp();
@@ -338,33 +347,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (live && !mbar_wait(&full[s], (k / stages) & 1, a.hdr)) live = false;
       if (live) {
         const uint8_t* stage = ring + (size_t)s * item_bytes;
-#pragma unroll 1
-        for (int rr = 0; rr < kDownRows / kConsumers; ++rr) {
-          const int rl = cw * (kDownRows / kConsumers) + rr;
-          const uint4* wr = reinterpret_cast<const uint4*>(stage + (size_t)rl * L * 2);
-          const int r = rbase + rl;
-          // groups of up to 4 tokens: each group's results are stored before the next
-          for (int j0 = 0; j0 < ntok; j0 += 4) {
-            const int nt = min(4, ntok - j0);
-            float acc[4];
-            const float* hg = hs + (size_t)j0 * L;
-            if (nt == 1) row_dots_h<1>(wr, hg, L, nt, lane, acc);
-            else if (nt == 2) row_dots_h<2>(wr, hg, L, nt, lane, acc);
-            else row_dots_h<4>(wr, hg, L, nt, lane, acc);
-            if (lane < nt) {
-              float y = acc[0];
+        static_assert(kDownRows == 2 * kConsumers, "two down rows per consumer warp");
+        const int rl = 2 * cw;
+        const uint4* w0 = reinterpret_cast<const uint4*>(stage + (size_t)rl * L * 2);
+        const uint4* w1 = reinterpret_cast<const uint4*>(stage + (size_t)(rl + 1) * L * 2);
+        // groups of up to 4 tokens: each group's results are stored before the next
+        for (int j0 = 0; j0 < ntok; j0 += 4) {
+          const int nt = min(4, ntok - j0);
+          float y0[4], y1[4];
+          const float* hg = hs + (size_t)j0 * L;
+          if (nt == 1) row2_dots_h<1>(w0, w1, hg, L, nt, lane, y0, y1);
+          else if (nt == 2) row2_dots_h<2>(w0, w1, hg, L, nt, lane, y0, y1);
+          else row2_dots_h<4>(w0, w1, hg, L, nt, lane, y0, y1);
+          if (lane < 2 * nt) {
+            // lanes 0..nt-1: row rl for token j0+lane; lanes nt..2nt-1: row rl+1
+            const int q = lane < nt ? lane : lane - nt;
+            float y = 0.0f;
 #pragma unroll
-              for (int q = 1; q < 4; ++q)
-                if (lane == q) y = acc[q];
-              const int j = j0 + lane, row = r0 + j;
-              if (shared_item) {
-                a.shy[(size_t)j * H + r] = y;
-              } else if (a.acc) {
-                const int t = meta.row_tok[row];
-                atomicAdd(a.acc + (size_t)t * H + r, a.w[__ldcg(a.sorted_pairs + row)] * y);
-              } else {
-                a.yd[(size_t)row * H + r] = y;
-              }
+            for (int u = 0; u < 4; ++u)
+              if (q == u) y = lane < nt ? y0[u] : y1[u];
+            const int r = rbase + rl + (lane < nt ? 0 : 1);
+            const int j = j0 + q, row = r0 + j;
+            if (shared_item) {
+              a.shy[(size_t)j * H + r] = y;
+            } else if (a.acc) {
+              const int t = meta.row_tok[row];
+              atomicAdd(a.acc + (size_t)t * H + r, a.w[__ldcg(a.sorted_pairs + row)] * y);
+            } else {
+              a.yd[(size_t)row * H + r] = y;
             }
           }
         }
@@ -392,7 +402,7 @@ int sm_count() {
 
 cudaError_t launch_decode_gateup(const DecodeArgs& a, cudaStream_t st) {
   if (a.te > kMaxPairs) return cudaErrorInvalidValue;
-  const int xbytes = (a.N * a.H * 2 + 127) & ~127;
+  const int xbytes = (a.N * a.H * 4 + 127) & ~127;
   // rows per item: the most (<= 16, one per consumer warp) that keep 3 stages in budget
   int ri = kConsumers;
   while (ri > 1 && (a.I % ri || (a.S && a.S % ri) ||
