@@ -80,31 +80,32 @@ __device__ __forceinline__ int token_of_row(const DecodeArgs& a, const RouteMeta
   return row >= a.te ? row - a.te : m.row_tok[row];
 }
 
-// Dot products of one bf16 weight row (shared memory) with NT fp32 token rows of x (shared
+// Dot products of one bf16 weight row (shared memory) with NT bf16 token rows of x (shared
 // memory); only the first `ntok` results are meaningful. Lane-strided 16-byte chunks.
 template <int NT>
-__device__ __forceinline__ void row_dots(const uint4* w, const float* xs, int H, const int* tk,
-                                         int lane, float* out) {
+__device__ __forceinline__ void row_dots(const uint4* w, const __nv_bfloat16* xs, int H,
+                                         const int* tk, int lane, float* out) {
   float acc[NT];
-  const float4* xr[NT];
+  const uint4* xr[NT];
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
     acc[j] = 0.0f;
-    xr[j] = reinterpret_cast<const float4*>(xs + (size_t)tk[j] * H);
+    xr[j] = reinterpret_cast<const uint4*>(xs + (size_t)tk[j] * H);
   }
   for (int c = lane; c < H / 8; c += 32) {
     float wf[8];
     bf16x8_to_f32(w[c], wf);
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      const float4 x0 = xr[j][2 * c], x1 = xr[j][2 * c + 1];
-      float p0 = wf[0] * x0.x, p1 = wf[1] * x0.y;
-      p0 = fmaf(wf[2], x0.z, p0);
-      p1 = fmaf(wf[3], x0.w, p1);
-      p0 = fmaf(wf[4], x1.x, p0);
-      p1 = fmaf(wf[5], x1.y, p1);
-      p0 = fmaf(wf[6], x1.z, p0);
-      p1 = fmaf(wf[7], x1.w, p1);
+      float xf[8];
+      bf16x8_to_f32(xr[j][c], xf);
+      float p0 = wf[0] * xf[0], p1 = wf[1] * xf[1];
+      p0 = fmaf(wf[2], xf[2], p0);
+      p1 = fmaf(wf[3], xf[3], p1);
+      p0 = fmaf(wf[4], xf[4], p0);
+      p1 = fmaf(wf[5], xf[5], p1);
+      p0 = fmaf(wf[6], xf[6], p0);
+      p1 = fmaf(wf[7], xf[7], p1);
       acc[j] += p0 + p1;
     }
   }
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteMeta meta;
   const int H = a.H, N = a.N;
-  float* xs = reinterpret_cast<float*>(smem);                               // [N, H] fp32
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);             // [N, H]
   uint8_t* ring = smem + xbytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)stages * item_bytes);
   uint64_t* empty = full + kMaxStages;
@@ -174,13 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbarrier_init();
   }
-  // the block input is not produced by the router: stage it (widened to fp32) before waiting
-  for (int i = threadIdx.x; i < N * H / 8; i += blockDim.x) {
-    float f[8];
-    bf16x8_to_f32(reinterpret_cast<const uint4*>(a.x)[i], f);
-    reinterpret_cast<float4*>(xs)[2 * i] = make_float4(f[0], f[1], f[2], f[3]);
-    reinterpret_cast<float4*>(xs)[2 * i + 1] = make_float4(f[4], f[5], f[6], f[7]);
-  }
+  // the block input is not produced by the router: stage it before waiting on the router
+  for (int i = threadIdx.x; i < N * H / 8; i += blockDim.x)
+    reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(a.x)[i];
   pdl_wait();       // routing of the router kernel
   pdl_trigger();    // the down projection may start streaming its weights
   load_route_meta(a, meta);   // (ends with a block barrier: x is staged too)
@@ -402,7 +399,7 @@ int sm_count() {
 
 cudaError_t launch_decode_gateup(const DecodeArgs& a, cudaStream_t st) {
   if (a.te > kMaxPairs) return cudaErrorInvalidValue;
-  const int xbytes = (a.N * a.H * 4 + 127) & ~127;
+  const int xbytes = (a.N * a.H * 2 + 127) & ~127;
   // rows per item: the most (<= 16, one per consumer warp) that keep 3 stages in budget
   int ri = kConsumers;
   while (ri > 1 && (a.I % ri || (a.S && a.S % ri) ||
