@@ -110,7 +110,8 @@ def algorithmic(inp, rs):
               + 2 * s.num_tokens * H * 2 + (H * 2 if s.shared_gated else 0))
     flops_routed = 6.0 * rs["Z"] * H * I_
     flops = flops_routed + 6.0 * s.num_tokens * H * S + 2.0 * s.num_tokens * H * R
-    gate_up_flops = 4.0 * rs["Z"] * H * I_
+    # the gate/up launch also runs the shared expert's gate/up projection (bf16 experts)
+    gate_up_flops = 4.0 * rs["Z"] * H * I_ + 4.0 * s.num_tokens * H * S
     gate_up_bytes = rs["distinct"] * 2 * I_ * H * wb + (2 * S * H * 2)
     return {"bytes": bytes_, "flops": flops, "gate_up_flops": gate_up_flops,
             "gate_up_bytes": gate_up_bytes, "expert_bytes": expert_bytes}

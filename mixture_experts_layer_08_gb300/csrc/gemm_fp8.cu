@@ -34,7 +34,6 @@ constexpr int kATile = kBM * kBK;           // 16 KB
 constexpr int kBTile = kBN * kBK;           // 32 KB
 constexpr int kStageBytes = kATile + kBTile;
 constexpr int kTmemCols = 2 * kBN;          // two partial buffers
-constexpr int kPrefetch = 6;                // K blocks of weights requested into L2 ahead
 constexpr size_t kScaleBytes = (size_t)kMaxKb * kEpi * 4 + (size_t)8 * kMaxKb * 2 * 4;
 constexpr size_t kSmemBytes =
     (size_t)kStages * kStageBytes + 1024 + 256 + 2 * 2 * 128 * 4 + kScaleBytes;
@@ -118,26 +117,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long issued = 0;
     bool ok = true;
     constexpr int b_rows = MODE == 0 ? kBN / 2 : kBN;
-    // weight tiles kPrefetch K blocks ahead (into the next tile) are requested into L2 early
-    int pf_tile = blockIdx.x, pf_kb = 0, pf_brow = 0;
-    if (pf_tile < total) {
-      const int4 t = g.tiles[pf_tile / g.n_tiles];
-      pf_brow = t.x * g.b_rows_per_expert + (pf_tile % g.n_tiles) * b_rows;
-    }
-    auto prefetch_next = [&]() {
-      if (pf_tile >= total) return;
-      tma_prefetch_l2_2d(&tm_b0, pf_kb * kBK, pf_brow);
-      if (MODE == 0) tma_prefetch_l2_2d(&tm_b1, pf_kb * kBK, pf_brow);
-      if (++pf_kb == g.num_kb) {
-        pf_kb = 0;
-        pf_tile += gridDim.x;
-        if (pf_tile < total) {
-          const int4 t = g.tiles[pf_tile / g.n_tiles];
-          pf_brow = t.x * g.b_rows_per_expert + (pf_tile % g.n_tiles) * b_rows;
-        }
-      }
-    };
-    for (int i = 0; i < kPrefetch; ++i) prefetch_next();
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const int m = tile / g.n_tiles, n = tile % g.n_tiles;
       const int4 t = g.tiles[m];
@@ -148,7 +127,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sA + s * kATile, &tm_a, kb * kBK, t.y, &full[s]);
         tma_load_2d(sB + s * kBTile, &tm_b0, kb * kBK, brow, &full[s]);
         if (MODE == 0) tma_load_2d(sB + s * kBTile + (kBN / 2) * kBK, &tm_b1, kb * kBK, brow, &full[s]);
-        prefetch_next();
         ++issued;
         if (++s == kStages) { s = 0; ph ^= 1; }
       }

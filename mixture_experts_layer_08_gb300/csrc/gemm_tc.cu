@@ -33,7 +33,6 @@ constexpr int kThreads = 192;
 constexpr int kBM = 128;
 constexpr int kBK = 64;                 // bf16 elements per 128-byte swizzle row
 constexpr int kATileBytes = kBM * 128;  // 16 KB
-constexpr int kPrefetch = 8;            // K blocks of weights requested into L2 ahead of use
 
 template <int BN>
 struct Cfg {
@@ -144,25 +143,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long issued = 0;
     bool ok = true;
     constexpr int b_rows = MODE == kGemmSwiGLU ? BN / 2 : BN;
-    // The weight tiles this CTA needs kPrefetch K blocks from now (running into its next
-    // tile) are requested into L2 early, so DRAM latency hides behind the smem ring.
-    int pf_tile = blockIdx.x, pf_kb = 0;
-    Tile pf;
-    if (pf_tile < total) tile_of(g, tot0, pf_tile, pf);
-    auto prefetch_next = [&]() {
-      if (pf_tile >= total) return;
-      const CUtensorMap* pb0 = pf.p ? &tm_b10 : &tm_b00;
-      const CUtensorMap* pb1 = pf.p ? &tm_b11 : &tm_b01;
-      const int prow = pf.e * pf.b_rows_per_expert + pf.n * b_rows;
-      tma_prefetch_l2_2d(pb0, pf_kb * kBK, prow);
-      if (MODE == kGemmSwiGLU) tma_prefetch_l2_2d(pb1, pf_kb * kBK, prow);
-      if (++pf_kb == pf.num_kb) {
-        pf_kb = 0;
-        pf_tile += gridDim.x;
-        if (pf_tile < total) tile_of(g, tot0, pf_tile, pf);
-      }
-    };
-    for (int i = 0; i < kPrefetch; ++i) prefetch_next();
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       Tile t;
       tile_of(g, tot0, tile, t);
@@ -177,7 +157,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sB + s * C::kBTileBytes, mb0, kb * kBK, brow, &full[s]);
         if (MODE == kGemmSwiGLU)
           tma_load_2d(sB + s * C::kBTileBytes + (BN / 2) * 128, mb1, kb * kBK, brow, &full[s]);
-        prefetch_next();
         ++issued;
         if (++s == S) { s = 0; ph ^= 1; }
       }

@@ -88,8 +88,8 @@ __device__ void route_token_warp(const float* L, const float* logit_bias, const 
 
 // ------------------------------------------------------------------ small-N router
 
-constexpr int kRouterWarps = 8;      // router columns per block
-constexpr int kRouterTok = 16;       // tokens per block
+constexpr int kRouterWarps = 4;      // router columns per block (one per warp)
+constexpr int kRouterTok = 16;       // most tokens per block
 
 // Block-wide exclusive scan of one value per thread (blockDim.x <= 1024, multiple of 32).
 __device__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_tot, uint32_t* total) {
@@ -172,14 +172,16 @@ __device__ void sort_in_block(const uint32_t* idx_s, int te, int E, int K, uint3
   }
 }
 
-__global__ void __launch_bounds__(256) router_small_kernel(RouteArgs a, SortArgs s,
-                                                           int fuse_tail) {
+// NT: tokens per block (a power of two >= the block's token count, <= 16).
+template <int NT>
+__global__ void __launch_bounds__(32 * kRouterWarps) router_small_kernel(RouteArgs a, SortArgs s,
+                                                                         int fuse_tail) {
   extern __shared__ __align__(16) uint8_t smem[];
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);     // [tok, H]
   pdl_trigger();    // the next kernel may launch now and wait for this one's results
   const int H = a.H, R = a.R;
-  const int tok0 = blockIdx.y * kRouterTok;
-  const int ntok = min(kRouterTok, a.N - tok0);
+  const int tok0 = blockIdx.y * NT;
+  const int ntok = min(NT, a.N - tok0);
   // stage the block's tokens in shared memory (16-byte chunks)
   const int chunks = H / 8;
   for (int i = threadIdx.x; i < ntok * chunks; i += blockDim.x) {
@@ -191,9 +193,9 @@ __global__ void __launch_bounds__(256) router_small_kernel(RouteArgs a, SortArgs
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int r = blockIdx.x * kRouterWarps + wid;
   if (r < R) {
-    float acc[kRouterTok];
+    float acc[NT];
 #pragma unroll
-    for (int t = 0; t < kRouterTok; ++t) acc[t] = 0.0f;
+    for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
     const uint4* wrow = reinterpret_cast<const uint4*>(a.router_w + (size_t)r * H);
     for (int c0 = 0; c0 < chunks; c0 += 256) {
       uint4 wv[8];            // all of this lane's loads in flight before any arithmetic
@@ -209,23 +211,20 @@ __global__ void __launch_bounds__(256) router_small_kernel(RouteArgs a, SortArgs
           float wf[8];
           bf16x8_to_f32(wv[q], wf);
 #pragma unroll
-          for (int t = 0; t < kRouterTok; ++t) {
-            if (t < ntok) {
-              float xf[8];
-              bf16x8_to_f32(reinterpret_cast<const uint4*>(xs)[t * chunks + c], xf);
+          for (int t = 0; t < NT; ++t) {
+            // rows past ntok repeat the block's first token (computed, never stored)
+            float xf[8];
+            bf16x8_to_f32(reinterpret_cast<const uint4*>(xs)[(t < ntok ? t : 0) * chunks + c], xf);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) acc[t] = fmaf(wf[i], xf[i], acc[t]);
-            }
+            for (int i = 0; i < 8; ++i) acc[t] = fmaf(wf[i], xf[i], acc[t]);
           }
         }
       }
     }
 #pragma unroll
-    for (int t = 0; t < kRouterTok; ++t) {
-      if (t < ntok) {
-        float v = warp_sum(acc[t]);
-        if (lane == 0) a.logits[(size_t)(tok0 + t) * R + r] = v;
-      }
+    for (int t = 0; t < NT; ++t) {
+      const float v = warp_sum(acc[t]);
+      if (lane == 0 && t < ntok) a.logits[(size_t)(tok0 + t) * R + r] = v;
     }
   }
   if (!fuse_tail) return;
@@ -430,21 +429,32 @@ cudaError_t launch_quant_rows(const __nv_bfloat16* x, int N, int H, uint8_t* q, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_router_small(const RouteArgs& a, const SortArgs& s, bool fuse_tail,
-                                cudaStream_t st) {
-  dim3 grid((a.R + kRouterWarps - 1) / kRouterWarps, (a.N + kRouterTok - 1) / kRouterTok);
-  size_t sm_x = (size_t)kRouterTok * a.H * 2;
+template <int NT>
+cudaError_t launch_router_small_t(const RouteArgs& a, const SortArgs& s, bool fuse_tail,
+                                  cudaStream_t st) {
+  dim3 grid((a.R + kRouterWarps - 1) / kRouterWarps, (a.N + NT - 1) / NT);
+  size_t sm_x = (size_t)NT * a.H * 2;
   size_t sm_tail = fuse_tail ? (size_t)2 * kRouterWarps * a.R * 4 + (size_t)a.N * a.K * 4 +
                                    (size_t)a.E * 4 + 40 * 4
                              : 0;
   size_t sm = sm_x > sm_tail ? sm_x : sm_tail;
   if (sm > 32 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(router_small_kernel,
+    cudaError_t e = cudaFuncSetAttribute(router_small_kernel<NT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
   }
-  router_small_kernel<<<grid, 256, sm, st>>>(a, s, fuse_tail ? 1 : 0);
+  router_small_kernel<NT><<<grid, 32 * kRouterWarps, sm, st>>>(a, s, fuse_tail ? 1 : 0);
   return cudaGetLastError();
+}
+
+cudaError_t launch_router_small(const RouteArgs& a, const SortArgs& s, bool fuse_tail,
+                                cudaStream_t st) {
+  if (fuse_tail && a.N > kRouterTok) return cudaErrorInvalidValue;
+  if (a.N <= 1) return launch_router_small_t<1>(a, s, fuse_tail, st);
+  if (a.N <= 2) return launch_router_small_t<2>(a, s, fuse_tail, st);
+  if (a.N <= 4) return launch_router_small_t<4>(a, s, fuse_tail, st);
+  if (a.N <= 8) return launch_router_small_t<8>(a, s, fuse_tail, st);
+  return launch_router_small_t<16>(a, s, fuse_tail, st);
 }
 
 cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st) {
