@@ -19,11 +19,10 @@ using namespace moe;
 
 namespace {
 
-constexpr int kDecodeMaxTokens = 16;
 constexpr int kSmallRouterMaxTokens = 64;
 
 enum Region {
-  R_HDR, R_LOGITS, R_IDX, R_W, R_ZSUM, R_BLK, R_LRANK, R_OFFS, R_P2R, R_SPAIRS, R_ACTIVE,
+  R_HDR, R_SYNC, R_LOGITS, R_IDX, R_W, R_ZSUM, R_BLK, R_LRANK, R_OFFS, R_P2R, R_SPAIRS, R_ACTIVE,
   R_TILES, R_XQT, R_XST, R_XP, R_XS, R_HH, R_HS, R_Y, R_SHH, R_SHY, R_HD, R_YD, R_ACC, R_NUM
 };
 
@@ -69,7 +68,7 @@ moe_status_t validate_config(const moe_config_t* c) {
   const int path = resolve_path(c);
   if (path == MOE_PATH_DECODE &&
       (c->weight_dtype != MOE_W_BF16 || c->num_tokens > kDecodeMaxTokens || c->inter > 1024 ||
-       c->shared_inter > 1024))
+       c->shared_inter > 1024 || c->hidden > 8192))
     return MOE_ERR_UNSUPPORTED;
   const long long te = (long long)c->num_tokens * c->top_k;
   if (te > (1ll << 30) || (long long)c->num_tokens * c->hidden > (1ll << 40))
@@ -115,6 +114,7 @@ Layout make_layout(const moe_config_t* c) {
     sz[R_SHH] = N * S * 2;
     sz[R_SHY] = S ? N * H * 2 : 0;
   } else {
+    sz[R_SYNC] = (kDecodeMaxPairs + 1) * 4;   // per-slot gate/up row counts, zeroed with hdr
     const size_t L2 = I > S ? I : S;
     sz[R_HD] = (te + N) * 2 * L2 * 4;   // gate and up dot products of every row
     if (c->deterministic) sz[R_YD] = te * H * 4;
@@ -291,7 +291,8 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
   sa.N = c->num_tokens;
   sa.hdr = hdr;
 
-  CK(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
+  // header (and, on the decode chain, the per-slot counters right after it) start at zero
+  CK(cudaMemsetAsync(hdr, 0, L.off[R_SYNC] + L.size[R_SYNC], st));
   if (L.path == MOE_PATH_DECODE) {
     CK(launch_router_small(ra, sa, true, st));
     return MOE_OK;
@@ -522,12 +523,13 @@ moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const voi
   d.hdr = P.at<WsHeader>(R_HDR);
   MARK(MOE_STAGE_SHARED, 0);
   MARK(MOE_STAGE_SHARED, 1);
-  MARK(MOE_STAGE_GATE_UP, 0);
+  d.h_cnt = P.at<uint32_t>(R_SYNC);
   if (d.acc) CK(cudaMemsetAsync(d.acc, 0, (size_t)N * H * 4, st));
-  CK(launch_decode_gateup(d, st));
+  // gate/up and down run in one persistent launch; its time is reported as the gate/up stage
+  MARK(MOE_STAGE_GATE_UP, 0);
+  CK(launch_decode_ffn(d, st));
   MARK(MOE_STAGE_GATE_UP, 1);
   MARK(MOE_STAGE_DOWN, 0);
-  CK(launch_decode_down(d, st));
   MARK(MOE_STAGE_DOWN, 1);
   CombineArgs ca{};
   ca.x = d.x;

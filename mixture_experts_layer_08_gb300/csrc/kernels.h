@@ -76,7 +76,11 @@ cudaError_t launch_quant_rows(const __nv_bfloat16* x, int N, int H, uint8_t* q, 
 cudaError_t launch_sort(const SortArgs& s, const __nv_bfloat16* x, int H, __nv_bfloat16* xp,
                         uint8_t* xq, float* xs, cudaStream_t st);
 
-// Decode chain: gate/up GEMV (+ SiLU*up) over the active experts and the shared expert.
+// Decode chain limits: tokens per forward and (token, slot) pairs.
+constexpr int kDecodeMaxTokens = 16;
+constexpr int kDecodeMaxPairs = 512;
+
+// Decode chain: gate/up and down GEMVs over the active experts and the shared expert.
 struct DecodeArgs {
   const __nv_bfloat16* x;          // [N,H]
   const __nv_bfloat16 *wg, *wu, *wd;   // [E,I,H], [E,I,H], [E,H,I]
@@ -92,10 +96,12 @@ struct DecodeArgs {
   float* yd;                       // [te, H] fp32 (deterministic) or null
   float* acc;                      // [N, H] fp32 atomic accumulator or null
   float* shy;                      // [N, H] fp32 shared expert output
+  uint32_t* h_cnt;                 // [kDecodeMaxPairs + 1] gate/up rows written per slot (the
+                                   // last entry: shared expert), zero on entry
   WsHeader* hdr;
 };
-cudaError_t launch_decode_gateup(const DecodeArgs& a, cudaStream_t st);
-cudaError_t launch_decode_down(const DecodeArgs& a, cudaStream_t st);
+// One cooperative launch: gate/up dots into hd, then SiLU(gate)*up and the down dots.
+cudaError_t launch_decode_ffn(const DecodeArgs& a, cudaStream_t st);
 
 // out[t] = sum_k w[t,k] * Y[pair_to_row[t,k]] (+ acc[t]) + zsum[t] * x[t] + gamma_t * shy[t]
 struct CombineArgs {
