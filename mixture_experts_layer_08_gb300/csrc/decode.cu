@@ -246,9 +246,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(DecodeArgs a, P
   const int cw = warp - 1, ct = threadIdx.x - 32;
   bool live = true;    // false after a timed-out wait: keep pace (barriers), skip the work
   int k = 0;
-  // gate/up: hd[row_j, i] = x_j . Wg[i], hd[row_j, ldh + i] = x_j . Wu[i]
+  // gate/up: hd[row_j, i] = x_j . Wg[i], hd[row_j, ldh + i] = x_j . Wu[i]. Rows written are
+  // counted per slot and published (fence, then one atomic) when the slot changes, so no fence
+  // sits between an item and the release of its ring stage.
   {
-    int cur_slot = -2, ntok = 0, r0 = 0;
+    int cur_slot = -2, ntok = 0, r0 = 0, pend = 0;
+    auto publish = [&]() {
+      if (pend == 0) return;
+      __threadfence();
+      __syncwarp();
+      if (lane == 0)
+        atomicAdd(a.h_cnt + (cur_slot < 0 ? kDecodeMaxPairs : cur_slot), (uint32_t)pend);
+      pend = 0;
+    };
     for (; k < ngu; ++k) {
       const int s = k % stages, it = g0 + k;
       const bool routed_item = it < gu_routed;
@@ -257,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(DecodeArgs a, P
       const int half = (routed_item ? a.I : a.S) / ri;
       const int col = (j < half ? 0 : a.ldh) + (j % half) * ri + cw;   // hd column
       if (slot != cur_slot) {
+        publish();
         cur_slot = slot;
         ntok = slot_rows(a, meta, slot, r0);
       }
@@ -282,14 +293,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(DecodeArgs a, P
             a.hd[(size_t)(r0 + j0 + lane) * (2 * a.ldh) + col] = v;
           }
         }
-        // publish this row: its values are visible before the slot's count moves
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) atomicAdd(a.h_cnt + (slot < 0 ? kDecodeMaxPairs : slot), 1u);
+        ++pend;
       }
       __syncwarp();
       if (lane == 0 && live) mbar_arrive(&empty[s]);
     }
+    publish();
   }
   // down: y_j[r] = h_j . Wd[r], h_j = SiLU(gate_j) * up_j
   {
