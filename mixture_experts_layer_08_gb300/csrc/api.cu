@@ -22,8 +22,9 @@ namespace {
 constexpr int kSmallRouterMaxTokens = 64;
 
 enum Region {
-  R_HDR, R_SYNC, R_LOGITS, R_IDX, R_W, R_ZSUM, R_BLK, R_LRANK, R_OFFS, R_P2R, R_SPAIRS, R_ACTIVE,
-  R_TILES, R_XQT, R_XST, R_XP, R_XS, R_HH, R_HS, R_Y, R_SHH, R_SHY, R_HD, R_YD, R_ACC, R_NUM
+  // the decode chain's accumulators follow the header so one memset clears them all
+  R_HDR, R_SYNC, R_HD, R_YD, R_ACC, R_SHY, R_LOGITS, R_IDX, R_W, R_ZSUM, R_BLK, R_LRANK, R_OFFS,
+  R_P2R, R_SPAIRS, R_ACTIVE, R_TILES, R_XQT, R_XST, R_XP, R_XS, R_HH, R_HS, R_Y, R_SHH, R_NUM
 };
 
 struct Layout {
@@ -114,9 +115,9 @@ Layout make_layout(const moe_config_t* c) {
     sz[R_SHH] = N * S * 2;
     sz[R_SHY] = S ? N * H * 2 : 0;
   } else {
-    sz[R_SYNC] = (kDecodeMaxPairs + 1) * 4;   // per-slot gate/up row counts, zeroed with hdr
+    sz[R_SYNC] = (kDecodeMaxPairs + 1) * 4;   // per-slot gate/up item counts
     const size_t L2 = I > S ? I : S;
-    sz[R_HD] = (te + N) * 2 * L2 * 4;   // gate and up dot products of every row
+    sz[R_HD] = (te + N) * 2 * L2 * 4;   // gate and up products of every row
     if (c->deterministic) sz[R_YD] = te * H * 4;
     else sz[R_ACC] = N * H * 4;
     sz[R_SHY] = S ? N * H * 4 : 0;
@@ -291,8 +292,10 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
   sa.N = c->num_tokens;
   sa.hdr = hdr;
 
-  // header (and, on the decode chain, the per-slot counters right after it) start at zero
-  CK(cudaMemsetAsync(hdr, 0, L.off[R_SYNC] + L.size[R_SYNC], st));
+  // header (and, on the decode chain, the per-slot counters and fp32 accumulators right after
+  // it) start at zero
+  const int last_zero = L.path == MOE_PATH_DECODE ? R_SHY : R_HDR;
+  CK(cudaMemsetAsync(hdr, 0, L.off[last_zero] + L.size[last_zero], st));
   if (L.path == MOE_PATH_DECODE) {
     CK(launch_router_small(ra, sa, true, st));
     return MOE_OK;
@@ -496,14 +499,26 @@ moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const voi
                         const Ptrs& P, cudaStream_t st, const Marks& M) {
   const Layout& L = *P.L;
   const int N = c->num_tokens, H = c->hidden, S = c->shared_inter;
+  const int E = c->num_experts, I = c->inter;
   DecodeArgs d{};
   d.x = static_cast<const __nv_bfloat16*>(x);
-  d.wg = static_cast<const __nv_bfloat16*>(w->w_gate);
-  d.wu = static_cast<const __nv_bfloat16*>(w->w_up);
-  d.wd = static_cast<const __nv_bfloat16*>(w->w_down);
-  d.sg = static_cast<const __nv_bfloat16*>(w->sh_gate);
-  d.su = static_cast<const __nv_bfloat16*>(w->sh_up);
-  d.sd = static_cast<const __nv_bfloat16*>(w->sh_down);
+  CUtensorMap maps[kDmNum];
+  const uint32_t bw = kDecodeBoxRowsW;
+  if (!make_map_bf16(&maps[kDmWg], w->w_gate, H, (uint64_t)E * I, bw) ||
+      !make_map_bf16(&maps[kDmWu], w->w_up, H, (uint64_t)E * I, bw) ||
+      !make_map_bf16(&maps[kDmWd], w->w_down, I, (uint64_t)E * H, bw) ||
+      !make_map_bf16(&maps[kDmX], x, H, N, kDecodeBoxRowsX))
+    return MOE_ERR_CUDA;
+  if (S > 0) {
+    if (!make_map_bf16(&maps[kDmSg], w->sh_gate, H, S, bw) ||
+        !make_map_bf16(&maps[kDmSu], w->sh_up, H, S, bw) ||
+        !make_map_bf16(&maps[kDmSd], w->sh_down, S, H, bw))
+      return MOE_ERR_CUDA;
+  } else {   // never read without a shared expert
+    maps[kDmSg] = maps[kDmWg];
+    maps[kDmSu] = maps[kDmWu];
+    maps[kDmSd] = maps[kDmWd];
+  }
   d.offsets = P.at<uint32_t>(R_OFFS);
   d.sorted_pairs = P.at<uint32_t>(R_SPAIRS);
   d.active = P.at<uint32_t>(R_ACTIVE);
@@ -524,10 +539,9 @@ moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const voi
   MARK(MOE_STAGE_SHARED, 0);
   MARK(MOE_STAGE_SHARED, 1);
   d.h_cnt = P.at<uint32_t>(R_SYNC);
-  if (d.acc) CK(cudaMemsetAsync(d.acc, 0, (size_t)N * H * 4, st));
   // gate/up and down run in one persistent launch; its time is reported as the gate/up stage
   MARK(MOE_STAGE_GATE_UP, 0);
-  CK(launch_decode_ffn(d, st));
+  CK(launch_decode_ffn(d, maps, st));
   MARK(MOE_STAGE_GATE_UP, 1);
   MARK(MOE_STAGE_DOWN, 0);
   MARK(MOE_STAGE_DOWN, 1);

@@ -80,28 +80,31 @@ cudaError_t launch_sort(const SortArgs& s, const __nv_bfloat16* x, int H, __nv_b
 constexpr int kDecodeMaxTokens = 16;
 constexpr int kDecodeMaxPairs = 512;
 
-// Decode chain: gate/up and down GEMVs over the active experts and the shared expert.
+// Decode chain: gate/up and down projections of the active experts and the shared expert as
+// skinny tensor-core GEMMs (weights as the 128-row A operand, the batch's tokens as N = 16).
 struct DecodeArgs {
   const __nv_bfloat16* x;          // [N,H]
-  const __nv_bfloat16 *wg, *wu, *wd;   // [E,I,H], [E,I,H], [E,H,I]
-  const __nv_bfloat16 *sg, *su, *sd;   // [S,H], [S,H], [H,S] or null
   const uint32_t* offsets;
   const uint32_t* sorted_pairs;
   const uint32_t* active;
   const float* w;                  // routing weights [N,K]
   int N, H, E, K, I, S, te;
-  float* hd;                       // [te + N, 2*ldh] fp32 gate (cols < ldh) and up dot products
-                                   // (row = sorted row, shared rows te + t)
+  float* hd;                       // [te + N, 2*ldh] fp32 gate (cols < ldh) and up products
+                                   // (row = sorted row, shared rows te + t); zero on entry
   int ldh;                         // max(I, S)
-  float* yd;                       // [te, H] fp32 (deterministic) or null
-  float* acc;                      // [N, H] fp32 atomic accumulator or null
-  float* shy;                      // [N, H] fp32 shared expert output
-  uint32_t* h_cnt;                 // [kDecodeMaxPairs + 1] gate/up rows written per slot (the
-                                   // last entry: shared expert), zero on entry
+  float* yd;                       // [te, H] fp32 (deterministic), zero on entry, or null
+  float* acc;                      // [N, H] fp32 atomic accumulator, zero on entry, or null
+  float* shy;                      // [N, H] fp32 shared expert output, zero on entry
+  uint32_t* h_cnt;                 // [kDecodeMaxPairs + 1] gate/up work items finished per slot
+                                   // (the last entry: shared expert), zero on entry
   WsHeader* hdr;
 };
-// One cooperative launch: gate/up dots into hd, then SiLU(gate)*up and the down dots.
-cudaError_t launch_decode_ffn(const DecodeArgs& a, cudaStream_t st);
+// Tensor maps (bf16, box {64, rows}, 128-byte swizzle) the decode kernel streams from.
+enum DecodeMap { kDmWg = 0, kDmWu, kDmSg, kDmSu, kDmWd, kDmSd, kDmX, kDmNum };
+// Box rows of each map: 128 for the weights, 16 for x.
+constexpr int kDecodeBoxRowsW = 128, kDecodeBoxRowsX = 16;
+// One cooperative launch: gate/up products into hd, then SiLU(gate)*up and the down products.
+cudaError_t launch_decode_ffn(const DecodeArgs& a, const CUtensorMap* maps, cudaStream_t st);
 
 // out[t] = sum_k w[t,k] * Y[pair_to_row[t,k]] (+ acc[t]) + zsum[t] * x[t] + gamma_t * shy[t]
 struct CombineArgs {
