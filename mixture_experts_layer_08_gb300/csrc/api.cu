@@ -503,16 +503,17 @@ moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const voi
   DecodeArgs d{};
   d.x = static_cast<const __nv_bfloat16*>(x);
   CUtensorMap maps[kDmNum];
-  const uint32_t bw = kDecodeBoxRowsW;
-  if (!make_map_bf16(&maps[kDmWg], w->w_gate, H, (uint64_t)E * I, bw) ||
-      !make_map_bf16(&maps[kDmWu], w->w_up, H, (uint64_t)E * I, bw) ||
-      !make_map_bf16(&maps[kDmWd], w->w_down, I, (uint64_t)E * H, bw) ||
+  int bg = 0, bd = 0;
+  decode_tile_rows(H, I, S, &bg, &bd);
+  if (!make_map_bf16(&maps[kDmWg], w->w_gate, H, (uint64_t)E * I, bg) ||
+      !make_map_bf16(&maps[kDmWu], w->w_up, H, (uint64_t)E * I, bg) ||
+      !make_map_bf16(&maps[kDmWd], w->w_down, I, (uint64_t)E * H, bd) ||
       !make_map_bf16(&maps[kDmX], x, H, N, kDecodeBoxRowsX))
     return MOE_ERR_CUDA;
   if (S > 0) {
-    if (!make_map_bf16(&maps[kDmSg], w->sh_gate, H, S, bw) ||
-        !make_map_bf16(&maps[kDmSu], w->sh_up, H, S, bw) ||
-        !make_map_bf16(&maps[kDmSd], w->sh_down, S, H, bw))
+    if (!make_map_bf16(&maps[kDmSg], w->sh_gate, H, S, bg) ||
+        !make_map_bf16(&maps[kDmSu], w->sh_up, H, S, bg) ||
+        !make_map_bf16(&maps[kDmSd], w->sh_down, S, H, bd))
       return MOE_ERR_CUDA;
   } else {   // never read without a shared expert
     maps[kDmSg] = maps[kDmWg];

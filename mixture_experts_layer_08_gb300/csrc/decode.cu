@@ -10,27 +10,29 @@
 // projections weighted and FP32-atomic-added into an [N,H] accumulator zeroed first, then a
 // finalize that casts to BF16 and blends the shared expert).
 //
-// Shape of the work. A weight tile is 128 rows of one projection of one slot (the A operand,
-// M = 128); the batch is the B operand (N = 16, tokens zero-padded): x itself for gate/up,
-// SiLU(gate)*up of the slot's tokens for down. A work item is one tile times 128 of its
-// contraction columns (32 KB of weights). Items are numbered slot-major; every block takes a
-// contiguous, balanced range of the gate/up items and then of the down items, so a block's
-// consecutive items of one tile form a run that accumulates in TMEM. The grid of each phase is
-// capped so that no tile is split over more than two blocks: the two fp32 partial sums then
-// meet in a zeroed buffer through atomic adds, and a + b == b + a makes the result
-// independent of their order.
+// Shape of the work. The weights are the wide B operand: a tile is BN (256, or 128 when a
+// dimension is not a multiple of 256) rows of one projection of one slot, so every MMA reads
+// its weights at the full-rate N. The batch is the A operand (M = 128): rows 0..15 hold the
+// tokens (x for gate/up, SiLU(gate)*up of the slot's tokens for down), rows 16..127 read
+// whatever shared memory follows and only produce accumulator rows that are never read. A
+// work item is one tile times one 64-column swizzle box of its contraction (BN x 128 bytes).
+// Items are numbered slot-major; every block takes a contiguous, balanced range of the gate/up
+// items and then of the down items, so a block's consecutive items of one tile form a run
+// that accumulates in TMEM. The grid of each phase is capped so that no tile is split over
+// more than two blocks: the two fp32 partial sums then meet in a zeroed buffer through atomic
+// adds, and a + b == b + a makes the result independent of their order.
 //
 // Roles (192 threads, one block per SM, all blocks resident):
-//   warp 0     TMA producer: per item two 128x64 weight boxes (+ two 16x64 x boxes on gate/up)
-//              into a ring of 36 KB stages.
-//   warp 1     allocates 32 TMEM columns (two 16-column accumulators); one lane issues
-//              tcgen05.mma (M=128, N=16, K=16) x 8 per item and commits stage releases and
-//              finished runs.
-//   warps 2-5  epilogue: tcgen05.ld of a finished run, fp32 atomic adds of each token's column
-//              into the gate/up buffer (then one count per run for the slot) or into the down
-//              output; before the first down run of a slot, wait for the slot's gate/up count
-//              (other blocks; bounded spin) and build SiLU(gate)*up in shared memory as the
-//              bf16 B operand (128-byte swizzle).
+//   warp 0     TMA producer: per item one BN x 64 weight box (+ one 16 x 64 box of x on
+//              gate/up) into a ring of stages.
+//   warp 1     allocates all 512 TMEM columns (two accumulators of up to 256 columns); one
+//              lane issues tcgen05.mma (M=128, N=BN, K=16) x 4 per item and commits stage
+//              releases and finished runs.
+//   warps 2-5  epilogue. Warp 4 (TMEM lanes 0..31 = the token rows) drains a finished run:
+//              fp32 atomic adds of each token's row into the gate/up buffer (then one count
+//              per run for the slot) or into the down output. Before the first down run of a
+//              slot, all four wait for the slot's gate/up count (other blocks; bounded spin)
+//              and build SiLU(gate)*up of its tokens as the bf16 A operand (128-byte swizzle).
 #include "kernels.h"
 
 namespace moe {
@@ -38,20 +40,21 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kM = 128;                  // weight rows per tile (MMA M)
-constexpr int kNB = 16;                  // MMA N: the batch's tokens, zero-padded
-constexpr int kKC = 128;                 // contraction columns per item (two 64-column boxes)
-constexpr int kABytes = kM * kKC * 2;    // 32 KB
-constexpr int kXBytes = kNB * kKC * 2;   // 4 KB
-constexpr int kStageBytes = kABytes + kXBytes;
+constexpr int kBox = 64;                  // contraction columns per item (one 128-byte row)
+constexpr int kMaxBN = 256;
+constexpr int kWBytes = kMaxBN * 128;     // weight box of a stage, 32 KB
+constexpr int kTokBytes = 16 * 128;       // token rows of one contraction box, 2 KB
 constexpr int kMaxStages = 8;
-constexpr int kTmemCols = 32;            // two accumulators of kNB columns
+constexpr int kTmemCols = 512;            // two accumulators of up to 256 columns
 constexpr int kEpiThreads = 128;
+constexpr int kDrainWarp = 4;             // warp % 4 == 0: TMEM lanes 0..31
+constexpr int kStageLd = 68;              // drain staging row stride (floats; 16-byte rows)
 constexpr int kSmemLimit = 227 * 1024;
 
 struct Plan {
   int stages;
-  int hbytes;   // B operand of the down projection: [16 rows, max(I, S)] bf16, swizzled
+  int bn_g, bn_d;   // weight rows per tile: gate/up, down
+  int hbytes;       // down-projection A operand: max(I, S) / 64 boxes of 16 rows x 128 bytes
 };
 
 // Routing of the batch, copied to shared memory once per block: expert, first sorted row and
@@ -82,19 +85,19 @@ __device__ void load_route_meta(const DecodeArgs& a, RouteMeta& m) {
 
 // Item numbering of both phases.
 struct Geo {
-  int nIt, nSt;     // 128-row tiles of one gate (or up) projection: routed, shared
-  int Pg;           // items per gate/up tile (H / 128)
-  int nHt;          // 128-row tiles of a down projection (H / 128)
-  int Pdr, Pds;     // items per down tile: routed (I / 128), shared (S / 128)
+  int nIt, nSt;     // weight tiles of one gate (or up) projection: routed, shared
+  int Pg;           // items per gate/up tile (H / 64)
+  int nHt;          // weight tiles of a down projection
+  int Pdr, Pds;     // items per down tile: routed (I / 64), shared (S / 64)
   int na;           // active routed slots
   int g_rt, g_items, d_ritems, d_items;
-  __device__ void init(const DecodeArgs& a, int n_active) {
-    nIt = a.I / kM;
-    nSt = a.S / kM;
-    Pg = a.H / kKC;
-    nHt = a.H / kM;
-    Pdr = a.I / kKC;
-    Pds = a.S / kKC;
+  __device__ void init(const DecodeArgs& a, const Plan& pl, int n_active) {
+    nIt = a.I / pl.bn_g;
+    nSt = a.S / pl.bn_g;
+    Pg = a.H / kBox;
+    nHt = a.H / pl.bn_d;
+    Pdr = a.I / kBox;
+    Pds = a.S / kBox;
     na = n_active;
     g_rt = na * 2 * nIt;
     g_items = (g_rt + (a.S ? 2 * nSt : 0)) * Pg;
@@ -156,15 +159,6 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   return v;
 }
 
-// v[c] for a warp-uniform column c < 16 (no dynamic register indexing).
-__device__ __forceinline__ float pick16(const float* v, int c) {
-  float r = v[0];
-#pragma unroll
-  for (int i = 1; i < 16; ++i)
-    if (c == i) r = v[i];
-  return r;
-}
-
 __device__ __forceinline__ int slot_rows(const DecodeArgs& a, const RouteMeta& m, int slot,
                                          int& r0) {
   if (slot < 0) {
@@ -187,18 +181,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ RouteMeta meta;
   __shared__ uint64_t bars[2 * kMaxStages + 6];
   __shared__ uint32_t tmem_slot;
-  // 1024-byte alignment for the 128-byte swizzle atoms
+  __shared__ __align__(16) float stage_rows[16 * kStageLd];   // drain staging, 16 rows x 64
+  // 1024-byte alignment for the 128-byte swizzle atoms. Layout: token boxes of the stages,
+  // the down-projection A operand, the weight ring (the A descriptors' rows 16..127 read on
+  // into what follows, always inside this allocation).
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int stages = pl.stages;
-  uint8_t* ring = smem;
-  uint8_t* hb = smem + (size_t)stages * kStageBytes;   // down-projection B operand
+  uint8_t* xtok = smem;                                   // [stages][16 x 128 B]
+  uint8_t* hb = xtok + (size_t)stages * kTokBytes;        // [max(I,S)/64][16 x 128 B]
+  uint8_t* ring = hb + pl.hbytes;                         // [stages][BN x 128 B]
   uint64_t* full = bars;
   uint64_t* empty = bars + kMaxStages;
-  uint64_t* afull = bars + 2 * kMaxStages;             // [2] run accumulated
-  uint64_t* aempty = afull + 2;                        // [2] run drained
-  uint64_t* bfull = aempty + 2;                        // down B operand built
-  uint64_t* drain = bfull + 1;                         // every MMA complete
+  uint64_t* afull = bars + 2 * kMaxStages;                // [2] run accumulated
+  uint64_t* aempty = afull + 2;                           // [2] run drained
+  uint64_t* bfull = aempty + 2;                           // down A operand built
+  uint64_t* drain = bfull + 1;                            // every MMA complete
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WsHeader* hdr = a.hdr;
 
@@ -209,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&afull[i], 1);
-      mbar_init(&aempty[i], 4);   // lane 0 of each epilogue warp
+      mbar_init(&aempty[i], 1);   // the draining warp's lane 0
     }
     mbar_init(bfull, 1);
     mbar_init(drain, 1);
@@ -232,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = tmem_slot;
 
   Geo geo;
-  geo.init(a, meta.n_active);
+  geo.init(a, pl, meta.n_active);
   int g0, g1, d0, d1;
   phase_range(geo.g_items, geo.Pg, g0, g1);
   phase_range(geo.d_items, geo.Pdr > geo.Pds ? geo.Pdr : geo.Pds, d0, d1);
@@ -249,13 +247,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool down = k >= ng;
         int tile, kc, slot, lt;
         geo.item(down, down ? d0 + (k - ng) : g0 + k, tile, kc, slot, lt);
-        uint8_t* st = ring + (size_t)s * kStageBytes;
-        const CUtensorMap* m;
-        int row;
+        uint8_t* wst = ring + (size_t)s * kWBytes;
         if (!down) {
           const int nt = slot >= 0 ? geo.nIt : geo.nSt;
           const bool up = lt >= nt;
-          const int r = (up ? lt - nt : lt) * kM;
+          const int r = (up ? lt - nt : lt) * pl.bn_g;
+          const CUtensorMap* m;
+          int row;
           if (slot >= 0) {
             m = up ? &tm_wu : &tm_wg;
             row = (int)meta.slot_e[slot] * a.I + r;
@@ -263,16 +261,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             m = up ? &tm_su : &tm_sg;
             row = r;
           }
-          mbar_arrive_expect_tx(&full[s], kStageBytes);
-          tma_load_2d(st + kABytes, &tm_x, kc * kKC, 0, &full[s]);
-          tma_load_2d(st + kABytes + kXBytes / 2, &tm_x, kc * kKC + 64, 0, &full[s]);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(pl.bn_g * 128 + kTokBytes));
+          tma_load_2d(xtok + (size_t)s * kTokBytes, &tm_x, kc * kBox, 0, &full[s]);
+          tma_load_2d(wst, m, kc * kBox, row, &full[s]);
         } else {
-          m = slot >= 0 ? &tm_wd : &tm_sd;
-          row = (slot >= 0 ? (int)meta.slot_e[slot] * a.H : 0) + lt * kM;
-          mbar_arrive_expect_tx(&full[s], kABytes);
+          const CUtensorMap* m = slot >= 0 ? &tm_wd : &tm_sd;
+          const int row = (slot >= 0 ? (int)meta.slot_e[slot] * a.H : 0) + lt * pl.bn_d;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(pl.bn_d * 128));
+          tma_load_2d(wst, m, kc * kBox, row, &full[s]);
         }
-        tma_load_2d(st, m, kc * kKC, row, &full[s]);
-        tma_load_2d(st + kABytes / 2, m, kc * kKC + 64, row, &full[s]);
         ++issued;
         if (++s == stages) { s = 0; ph ^= 1; }
       }
@@ -283,11 +280,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_make(kM, kNB, 1, 1);
+      const uint32_t idesc_g = idesc_make(128, pl.bn_g, 1, 1);
+      const uint32_t idesc_d = idesc_make(128, pl.bn_d, 1, 1);
       int s = 0, run = -1, prev_tile = -1, bslot = -2, nb = 0;
       uint32_t ph = 0;
       bool prev_down = false, ok = true, first = false;
-      const uint32_t hb_addr = smem_u32(hb);
       for (int k = 0; k < nitems && ok; ++k) {
         const bool down = k >= ng;
         int tile, kc, slot, lt;
@@ -308,16 +305,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!mbar_wait(&full[s], ph, hdr)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)((run & 1) * kNB);
-        const uint32_t a0 = smem_u32(ring + (size_t)s * kStageBytes);
-        const uint32_t b0 = down ? hb_addr + (uint32_t)kc * 2 * 2048 : a0 + kABytes;
+        const uint32_t d = tmem_base + (uint32_t)((run & 1) * kMaxBN);
+        const uint32_t a0 = down ? smem_u32(hb) + (uint32_t)kc * kTokBytes
+                                 : smem_u32(xtok) + (uint32_t)s * kTokBytes;
+        const uint32_t b0 = smem_u32(ring) + (uint32_t)s * kWBytes;
+        const uint32_t idesc = down ? idesc_d : idesc_g;
 #pragma unroll
-        for (int kk = 0; kk < kKC / 16; ++kk) {
-          const uint32_t ka = (uint32_t)(kk >> 2) * (kM * 128) + (uint32_t)(kk & 3) * 32;
-          const uint32_t kb = (uint32_t)(kk >> 2) * (kNB * 128) + (uint32_t)(kk & 3) * 32;
-          tc_mma_bf16(d, sdesc_k_sw128(a0 + ka), sdesc_k_sw128(b0 + kb), idesc,
+        for (int kk = 0; kk < kBox / 16; ++kk)
+          tc_mma_bf16(d, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
                       (first && kk == 0) ? 0u : 1u);
-        }
         first = false;
         tc_commit(&empty[s]);
         if (++s == stages) { s = 0; ph ^= 1; }
@@ -329,64 +325,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------ epilogue
-    const int q = warp & 3;                 // TMEM lane quadrant of this warp
-    const int row_l = q * 32 + lane;        // weight row within the tile
     const int et = threadIdx.x - 64;        // 0..127
-    const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16);
+    const bool drainer = warp == kDrainWarp;
     int run = -1, prev_tile = -1, bslot = -2;
     bool prev_down = false;
     // the run being accumulated: phase, slot, tile within the slot, items
     bool r_down = false;
     int r_slot = 0, r_lt = 0, r_len = 0;
     bool ok = true;
+    // Warp 4 drains a finished run: TMEM lane j < 16 holds accumulator row j (token j of x on
+    // gate/up, the slot's j-th token on down) across the tile's BN columns. 64 columns at a
+    // time go through shared memory so that every row's partial sums leave as coalesced
+    // 32-lane atomic adds.
     auto drain_run = [&]() {
       if (!ok) return;
       if (!mbar_wait(&afull[run & 1], ((uint32_t)run >> 1) & 1, hdr)) { ok = false; return; }
       tc_fence_after();
-      float v[16];
-      tmem_ld16(tq + (uint32_t)((run & 1) * kNB), v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&aempty[run & 1]);
       int r0;
       const int ntok = slot_rows(a, meta, r_slot, r0);
+      const uint32_t tacc = tmem_base + (uint32_t)((run & 1) * kMaxBN);
+      float* dst = nullptr;      // output row of accumulator row `lane` (lanes < 16)
+      float scale = 1.0f;
+      int bn;
       if (!r_down) {
+        bn = pl.bn_g;
+        int row = -1;            // sorted row of (slot, token lane)
+        if (r_slot < 0) {
+          if (lane < a.N) row = a.te + lane;
+        } else {
+          for (int j = 0; j < ntok; ++j)
+            if ((int)meta.row_tok[r0 + j] == lane) row = r0 + j;
+        }
         const int nt = r_slot >= 0 ? geo.nIt : geo.nSt;
-        const int col = (r_lt < nt ? 0 : a.ldh) + (r_lt < nt ? r_lt : r_lt - nt) * kM + row_l;
-        for (int jj = 0; jj < ntok; ++jj) {
-          const int row = r0 + jj;
-          const int t = row >= a.te ? row - a.te : (int)meta.row_tok[row];
-          atomicAdd(a.hd + (size_t)row * (2 * a.ldh) + col, pick16(v, t));
-        }
-        // publish: the slot's count moves only after every partial sum of the run landed
-        __threadfence();
-        named_sync(1, kEpiThreads);
-        if (et == 0) {
-          __threadfence();
-          atomicAdd(a.h_cnt + (r_slot < 0 ? kDecodeMaxPairs : r_slot), (uint32_t)r_len);
-        }
+        const int col = (r_lt < nt ? 0 : a.ldh) + (r_lt < nt ? r_lt : r_lt - nt) * bn;
+        if (row >= 0) dst = a.hd + (size_t)row * (2 * a.ldh) + col;
       } else {
-        const int r = r_lt * kM + row_l;
-        for (int jj = 0; jj < ntok; ++jj) {
-          const float y = pick16(v, jj);
-          const int row = r0 + jj;
+        bn = pl.bn_d;
+        const int c0 = r_lt * bn;
+        if (lane < ntok) {
+          const int row = r0 + lane;
           if (r_slot < 0) {
-            atomicAdd(a.shy + (size_t)jj * a.H + r, y);
+            dst = a.shy + (size_t)lane * a.H + c0;
           } else if (a.acc) {
-            const uint32_t pair = __ldcg(a.sorted_pairs + row);
-            atomicAdd(a.acc + (size_t)meta.row_tok[row] * a.H + r, a.w[pair] * y);
+            scale = a.w[__ldcg(a.sorted_pairs + row)];
+            dst = a.acc + (size_t)meta.row_tok[row] * a.H + c0;
           } else {
-            atomicAdd(a.yd + (size_t)row * a.H + r, y);
+            dst = a.yd + (size_t)row * a.H + c0;
           }
         }
       }
+      const uint32_t rows = __ballot_sync(0xffffffffu, dst != nullptr);
+#pragma unroll 1
+      for (int c = 0; c < bn; c += 64) {
+        float v[64];
+        tmem_ld32_nowait(tacc + (uint32_t)c, v);
+        tmem_ld32_nowait(tacc + (uint32_t)c + 32, v + 32);
+        tmem_wait_ld();
+        if (lane < 16 && dst) {
+          float4* st = reinterpret_cast<float4*>(stage_rows + lane * kStageLd);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            st[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+        __syncwarp();
+        for (uint32_t m = rows; m; m &= m - 1) {
+          const int j = __ffs(m) - 1;
+          float* dj = reinterpret_cast<float*>(
+              __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(dst), j));
+          const float sj = __shfl_sync(0xffffffffu, scale, j);
+          atomicAdd(dj + c + lane, sj * stage_rows[j * kStageLd + lane]);
+          atomicAdd(dj + c + 32 + lane, sj * stage_rows[j * kStageLd + 32 + lane]);
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&aempty[run & 1]);
+      if (!r_down) {
+        // publish: the slot's count moves only after every partial sum of the run landed
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          atomicAdd(a.h_cnt + (r_slot < 0 ? kDecodeMaxPairs : r_slot), (uint32_t)r_len);
+        }
+      }
     };
-    // SiLU(gate) * up of the slot's tokens as the bf16 B operand [16 rows, L], 128-byte swizzle:
-    // row j's 16-byte chunk c of K-block kb at kb * 2048 + j * 128 + ((c ^ (j & 7)) * 16).
-    auto build_b = [&](int slot) {
-      const uint32_t target =
-          (uint32_t)((slot >= 0 ? 2 * geo.nIt : 2 * geo.nSt) * geo.Pg);
-      if (et == 0) {
+    // SiLU(gate) * up of the slot's tokens as the bf16 A operand, 16 rows per 64-column box
+    // with the 128-byte swizzle: row j's 16-byte chunk c of box kb at
+    // kb * 2048 + j * 128 + ((c ^ (j & 7)) * 16).
+    auto build_a = [&](int slot) {
+      const uint32_t target = (uint32_t)((slot >= 0 ? 2 * geo.nIt : 2 * geo.nSt) * geo.Pg);
+      if (drainer && lane == 0) {   // (after this warp published the block's own gate/up runs)
         const uint32_t* cnt = a.h_cnt + (slot < 0 ? kDecodeMaxPairs : slot);
         if (ld_acquire(cnt) < target) {
           const long long t0 = clock64();
@@ -404,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ntok = slot_rows(a, meta, slot, r0);
       const int L = slot >= 0 ? a.I : a.S;
       const int cpr = L / 8;   // 16-byte chunks per row
-      for (int id = et; id < kNB * cpr; id += kEpiThreads) {
+      for (int id = et; id < 16 * cpr; id += kEpiThreads) {
         const int j = id / cpr, c = id - j * cpr;
         uint4 o = make_uint4(0u, 0u, 0u, 0u);
         if (j < ntok) {
@@ -418,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           o.z = pack_bf16x2(silu(g1v.x) * u1.x, silu(g1v.y) * u1.y);
           o.w = pack_bf16x2(silu(g1v.z) * u1.z, silu(g1v.w) * u1.w);
         }
-        *reinterpret_cast<uint4*>(hb + (size_t)(c >> 3) * 2048 + j * 128 +
+        *reinterpret_cast<uint4*>(hb + (size_t)(c >> 3) * kTokBytes + j * 128 +
                                   (((c & 7) ^ (j & 7)) << 4)) = o;
       }
       fence_proxy_async_smem();
@@ -430,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int tile, kc, slot, lt;
       geo.item(down, down ? d0 + (k - ng) : g0 + k, tile, kc, slot, lt);
       if (run < 0 || down != prev_down || tile != prev_tile) {
-        if (run >= 0) drain_run();
+        if (run >= 0 && drainer) drain_run();
         ++run;
         prev_down = down;
         prev_tile = tile;
@@ -438,15 +468,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         r_slot = slot;
         r_lt = lt;
         r_len = 0;
-        // the MMAs of every earlier run are complete (drained): the B buffer is free
+        // the MMAs of every earlier run are complete (drained): the A buffer is free
         if (down && slot != bslot) {
-          build_b(slot);
+          build_a(slot);
           bslot = slot;
         }
       }
       ++r_len;
     }
-    if (run >= 0) drain_run();
+    if (run >= 0 && drainer) drain_run();
   }
   tc_fence_before();
   __syncthreads();
@@ -472,19 +502,27 @@ int sm_count() {
 
 }  // namespace
 
+// Weight rows per tile of each phase; the tensor maps of the weights use them as box rows.
+void decode_tile_rows(int H, int I, int S, int* bn_g, int* bn_d) {
+  *bn_g = (I % 256 == 0 && S % 256 == 0) ? 256 : 128;
+  *bn_d = H % 256 == 0 ? 256 : 128;
+}
+
 cudaError_t launch_decode_ffn(const DecodeArgs& a, const CUtensorMap* maps, cudaStream_t st) {
   if (a.te > kDecodeMaxPairs || a.N > kDecodeMaxTokens || a.N < 1 || !a.h_cnt ||
-      a.H % kKC || a.I % kKC || a.S % kKC)
+      a.H % 128 || a.I % 128 || a.S % 128)
     return cudaErrorInvalidValue;
   const int L = a.I > a.S ? a.I : a.S;
   Plan pl{};
-  pl.hbytes = L * kNB * 2;
-  const int fixed = 1024 + pl.hbytes;   // alignment slack + B operand
+  decode_tile_rows(a.H, a.I, a.S, &pl.bn_g, &pl.bn_d);
+  pl.hbytes = (L / kBox) * kTokBytes;
+  const int per_stage = kTokBytes + kWBytes;
+  const int fixed = 1024 + pl.hbytes;   // alignment slack + down A operand
   // (the static shared memory -- routing metadata, barriers -- stays within the 8 KB margin)
-  pl.stages = (kSmemLimit - 8192 - fixed) / kStageBytes;
+  pl.stages = (kSmemLimit - 8192 - fixed) / per_stage;
   if (pl.stages > kMaxStages) pl.stages = kMaxStages;
   if (pl.stages < 2) return cudaErrorInvalidValue;
-  const size_t sm = (size_t)fixed + (size_t)pl.stages * kStageBytes;
+  const size_t sm = (size_t)fixed + (size_t)pl.stages * per_stage;
   cudaError_t e =
       cudaFuncSetAttribute(decode_ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;

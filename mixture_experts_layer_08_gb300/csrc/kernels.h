@@ -81,7 +81,7 @@ constexpr int kDecodeMaxTokens = 16;
 constexpr int kDecodeMaxPairs = 512;
 
 // Decode chain: gate/up and down projections of the active experts and the shared expert as
-// skinny tensor-core GEMMs (weights as the 128-row A operand, the batch's tokens as N = 16).
+// skinny tensor-core GEMMs (weights as the wide B operand, the batch's tokens as A rows).
 struct DecodeArgs {
   const __nv_bfloat16* x;          // [N,H]
   const uint32_t* offsets;
@@ -101,8 +101,9 @@ struct DecodeArgs {
 };
 // Tensor maps (bf16, box {64, rows}, 128-byte swizzle) the decode kernel streams from.
 enum DecodeMap { kDmWg = 0, kDmWu, kDmSg, kDmSu, kDmWd, kDmSd, kDmX, kDmNum };
-// Box rows of each map: 128 for the weights, 16 for x.
-constexpr int kDecodeBoxRowsW = 128, kDecodeBoxRowsX = 16;
+// Box rows: x 16; gate/up weights (Wg, Wu, Sg, Su) *bn_g; down weights (Wd, Sd) *bn_d.
+constexpr int kDecodeBoxRowsX = 16;
+void decode_tile_rows(int H, int I, int S, int* bn_g, int* bn_d);
 // One cooperative launch: gate/up products into hd, then SiLU(gate)*up and the down products.
 cudaError_t launch_decode_ffn(const DecodeArgs& a, const CUtensorMap* maps, cudaStream_t st);
 
