@@ -292,10 +292,8 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
   sa.N = c->num_tokens;
   sa.hdr = hdr;
 
-  // header (and, on the decode chain, the per-slot counters and fp32 accumulators right after
-  // it) start at zero
-  const int last_zero = L.path == MOE_PATH_DECODE ? R_SHY : R_HDR;
-  CK(cudaMemsetAsync(hdr, 0, L.off[last_zero] + L.size[last_zero], st));
+  // the header starts at zero
+  CK(cudaMemsetAsync(hdr, 0, L.off[R_HDR] + L.size[R_HDR], st));
   if (L.path == MOE_PATH_DECODE) {
     CK(launch_router_small(ra, sa, true, st));
     return MOE_OK;
@@ -495,13 +493,51 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
   return MOE_OK;
 }
 
+// The decode chain: one memset of the header and the fp32 accumulators, one cooperative kernel
+// (router, top-K, sort, projections, combine). Its time is reported as the gate/up stage.
 moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const void* x, void* out,
-                        const Ptrs& P, cudaStream_t st, const Marks& M) {
+                        const Ptrs& P, const uint32_t* forced, cudaStream_t st, const Marks& M) {
   const Layout& L = *P.L;
   const int N = c->num_tokens, H = c->hidden, S = c->shared_inter;
   const int E = c->num_experts, I = c->inter;
+  WsHeader* hdr = P.at<WsHeader>(R_HDR);
+  MARK(MOE_STAGE_ROUTE, 0);
+  CK(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));   // the kernel clears its accumulators
+  MARK(MOE_STAGE_ROUTE, 1);
   DecodeArgs d{};
   d.x = static_cast<const __nv_bfloat16*>(x);
+  d.router_w = static_cast<const __nv_bfloat16*>(w->router_w);
+  d.logit_bias = w->router_logit_bias;
+  d.corr_bias = c->scoring == MOE_SCORING_SOFTMAX_BIAS ? w->correction_bias : nullptr;
+  d.forced = forced;
+  d.sh_gate_vec = S > 0 ? static_cast<const __nv_bfloat16*>(w->sh_gate_vec) : nullptr;
+  d.N = N;
+  d.H = H;
+  d.E = E;
+  d.R = c->router_width;
+  d.K = c->top_k;
+  d.I = I;
+  d.S = S;
+  d.te = L.te;
+  d.scoring = c->scoring;
+  d.norm = c->norm_topk_prob;
+  d.scale = c->routed_scaling_factor;
+  d.logits = P.at<float>(R_LOGITS);
+  d.idx = P.at<uint32_t>(R_IDX);
+  d.w = P.at<float>(R_W);
+  d.zsum = P.at<float>(R_ZSUM);
+  d.offsets = P.at<uint32_t>(R_OFFS);
+  d.sorted_pairs = P.at<uint32_t>(R_SPAIRS);
+  d.pair_to_row = P.at<uint32_t>(R_P2R);
+  d.active = P.at<uint32_t>(R_ACTIVE);
+  d.hd = P.at<float>(R_HD);
+  d.ldh = I > S ? I : S;
+  d.yd = P.at<float>(R_YD);
+  d.acc = P.at<float>(R_ACC);
+  d.shy = P.at<float>(R_SHY);
+  d.h_cnt = P.at<uint32_t>(R_SYNC);
+  d.hdr = hdr;
+  d.out = static_cast<__nv_bfloat16*>(out);
   CUtensorMap maps[kDmNum];
   int bg = 0, bd = 0;
   decode_tile_rows(H, I, S, &bg, &bd);
@@ -520,49 +556,14 @@ moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const voi
     maps[kDmSu] = maps[kDmWu];
     maps[kDmSd] = maps[kDmWd];
   }
-  d.offsets = P.at<uint32_t>(R_OFFS);
-  d.sorted_pairs = P.at<uint32_t>(R_SPAIRS);
-  d.active = P.at<uint32_t>(R_ACTIVE);
-  d.w = P.at<float>(R_W);
-  d.N = N;
-  d.H = H;
-  d.E = c->num_experts;
-  d.K = c->top_k;
-  d.I = c->inter;
-  d.S = S;
-  d.te = L.te;
-  d.hd = P.at<float>(R_HD);
-  d.ldh = c->inter > S ? c->inter : S;
-  d.yd = P.at<float>(R_YD);
-  d.acc = P.at<float>(R_ACC);
-  d.shy = P.at<float>(R_SHY);
-  d.hdr = P.at<WsHeader>(R_HDR);
   MARK(MOE_STAGE_SHARED, 0);
   MARK(MOE_STAGE_SHARED, 1);
-  d.h_cnt = P.at<uint32_t>(R_SYNC);
-  // gate/up and down run in one persistent launch; its time is reported as the gate/up stage
   MARK(MOE_STAGE_GATE_UP, 0);
-  CK(launch_decode_ffn(d, maps, st));
+  CK(launch_decode_forward(d, maps, st));
   MARK(MOE_STAGE_GATE_UP, 1);
   MARK(MOE_STAGE_DOWN, 0);
   MARK(MOE_STAGE_DOWN, 1);
-  CombineArgs ca{};
-  ca.x = d.x;
-  ca.pair_to_row = P.at<uint32_t>(R_P2R);
-  ca.w = d.w;
-  ca.zsum = P.at<float>(R_ZSUM);
-  ca.y = d.yd;
-  ca.y_is_f32 = 1;
-  ca.acc = d.acc;
-  ca.shy = S > 0 ? d.shy : nullptr;
-  ca.shy_is_f32 = 1;
-  ca.sh_gate_vec = static_cast<const __nv_bfloat16*>(w->sh_gate_vec);
-  ca.N = N;
-  ca.H = H;
-  ca.K = c->top_k;
-  ca.out = static_cast<__nv_bfloat16*>(out);
   MARK(MOE_STAGE_COMBINE, 0);
-  CK(launch_combine(ca, st));
   MARK(MOE_STAGE_COMBINE, 1);
   return MOE_OK;
 }
@@ -595,12 +596,15 @@ moe_status_t forward_impl(const moe_config_t* cfg, const moe_weights_t* weights,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Ptrs P{static_cast<uint8_t*>(workspace), &L};
   Marks M{events, st};
-  MARK(MOE_STAGE_ROUTE, 0);
-  s = run_routing(cfg, weights, x, P, forced_idx, L.path == MOE_PATH_GROUPED, st);
-  if (s != MOE_OK) return s;
-  MARK(MOE_STAGE_ROUTE, 1);
-  s = L.path == MOE_PATH_GROUPED ? run_grouped(cfg, weights, x, out, P, st, M)
-                                 : run_decode(cfg, weights, x, out, P, st, M);
+  if (L.path == MOE_PATH_GROUPED) {
+    MARK(MOE_STAGE_ROUTE, 0);
+    s = run_routing(cfg, weights, x, P, forced_idx, true, st);
+    if (s != MOE_OK) return s;
+    MARK(MOE_STAGE_ROUTE, 1);
+    s = run_grouped(cfg, weights, x, out, P, st, M);
+  } else {
+    s = run_decode(cfg, weights, x, out, P, forced_idx, st, M);
+  }
   if (s != MOE_OK) return s;
   const size_t te = (size_t)L.te;
   if (topk_idx_out)

@@ -16,10 +16,12 @@ namespace moe {
 // Workspace header: the first 256 bytes of every workspace.
 struct WsHeader {
   int32_t status;          // MOE_OK or MOE_ERR_DEVICE_TIMEOUT, written by kernels
-  uint32_t done_blocks;    // "last block" counter of the fused decode router
+  uint32_t done_blocks;    // "last block" counter of the small router's fused tail; grid
+                           // barrier counter of the fused decode kernel
   uint32_t num_active;     // distinct experts with at least one routed row
   uint32_t num_mtiles;     // 128-row tiles of the grouped GEMM (sum over experts)
-  uint32_t pad[60];
+  float gate_dot[16];      // fused decode kernel: x[t] . g of the shared-expert gate, t < 16
+  uint32_t pad[44];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

@@ -1,14 +1,27 @@
-// Decode chain (few tokens): the expert projections of the whole batch as skinny GEMMs on the
-// 5th-generation tensor cores, in one persistent, cooperatively launched kernel that streams
-// the weights of every expert the batch touches -- gate and up rows, then down rows -- from
-// HBM once, for all the tokens routed to it. The shared expert is one more slot.
+// Decode chain (few tokens): the whole block forward in one persistent, cooperatively launched
+// kernel -- router, top-K and sort, the expert projections as skinny GEMMs on the
+// 5th-generation tensor cores, and the weighted combine -- streaming the weights of every
+// expert the batch touches from HBM once, for all the tokens routed to it. The shared expert
+// is one more slot.
 //
-// Pages: "spark_model/layers/moe/forward.rs" (`forward`: fused gate/up projection for the K
-// routed experts plus the shared expert, fused SiLU and down projection, weighted sum and
-// sigmoid-gated shared blend, all on device with no host synchronisation) and
+// Pages: "spark_model/layers/moe/forward.rs" (`forward`: gate GEMM, softmax + correction-bias
+// top-K, fused gate/up projection for the K routed experts plus the shared expert, fused SiLU
+// and down projection, weighted sum + sigmoid-gated shared blend + identity-expert add, all on
+// device with no host synchronisation; the single-CTA fused gate+top-K it rejects is replaced
+// by router rows spread over every block and a per-block top-K) and
 // "metrale_model_layers/layers/moe/forward_atomic_c4.rs" (few-row decode: routed down
 // projections weighted and FP32-atomic-added into an [N,H] accumulator zeroed first, then a
 // finalize that casts to BF16 and blends the shared expert).
+//
+// Phases, separated by two grid barriers (all blocks are resident: a bounded spin on a
+// counter in the workspace header):
+//   0  router logits: one warp per router row, rows spread over the blocks;
+//   1  every block routes the whole batch into its own shared memory (softmax, top-K,
+//      renormalisation, identity-expert sums, shared-expert gate, stable sort by expert);
+//      block 0 also writes the routing to the workspace;
+//   2  gate/up then down projections (below);
+//   3  out[t] = bf16(sum_k w * y[row(t,k)] (or the atomic accumulator) + zsum * x + gamma * Sh),
+//      output chunks spread over the blocks.
 //
 // Shape of the work. The weights are the wide B operand: a tile is BN (256, or 128 when a
 // dimension is not a multiple of 256) rows of one projection of one slot, so every MMA reads
@@ -34,12 +47,14 @@
 //              slot, all four wait for the slot's gate/up count (other blocks; bounded spin)
 //              and build SiLU(gate)*up of its tokens as the bf16 A operand (128-byte swizzle).
 #include "kernels.h"
+#include "route_dev.cuh"
 
 namespace moe {
 
 namespace {
 
 constexpr int kThreads = 192;
+constexpr int kWarps = kThreads / 32;
 constexpr int kBox = 64;                  // contraction columns per item (one 128-byte row)
 constexpr int kMaxBN = 256;
 constexpr int kWBytes = kMaxBN * 128;     // weight box of a stage, 32 KB
@@ -57,40 +72,487 @@ struct Plan {
   int hbytes;       // down-projection A operand: max(I, S) / 64 boxes of 16 rows x 128 bytes
 };
 
-// Routing of the batch, copied to shared memory once per block: expert, first sorted row and
-// row count of every active slot, and the token of every sorted row.
-struct RouteMeta {
-  int n_active;
-  uint16_t slot_e[kDecodeMaxPairs];
-  uint16_t slot_r0[kDecodeMaxPairs];
-  uint16_t slot_n[kDecodeMaxPairs];
-  uint16_t row_tok[kDecodeMaxPairs];
+constexpr uint16_t kNoRow16 = 0xFFFF;
+
+// Routing of the batch; every block computes its own copy in shared memory.
+struct Routing {
+  int n_active;                          // active (expert, rows) slots
+  int rows;                              // routed rows (pairs on real experts)
+  uint16_t slot_e[kDecodeMaxPairs];      // expert of each active slot
+  uint16_t slot_r0[kDecodeMaxPairs];     // its first sorted row
+  uint16_t slot_n[kDecodeMaxPairs];      // its row count
+  uint16_t row_tok[kDecodeMaxPairs];     // token of each sorted row
+  uint16_t row_pair[kDecodeMaxPairs];    // (token, slot) pair of each sorted row
+  uint16_t pair_row[kDecodeMaxPairs];    // sorted row of each pair, kNoRow16: identity expert
+  float w[kDecodeMaxPairs];              // routing weight of each pair
+  float zsum[kDecodeMaxTokens];          // identity-expert weight sum of each token
+  float gamma[kDecodeMaxTokens];         // shared-expert blend weight of each token
 };
 
-// All threads of the block; routing metadata is read through L2 (an earlier kernel wrote it).
-__device__ void load_route_meta(const DecodeArgs& a, RouteMeta& m) {
-  const int n_active = (int)__ldcg(&a.hdr->num_active);
-  for (int s = threadIdx.x; s < n_active; s += blockDim.x) {
-    const int e = (int)__ldcg(a.active + s);
-    const int r0 = (int)__ldcg(a.offsets + e);
-    m.slot_e[s] = (uint16_t)e;
-    m.slot_r0[s] = (uint16_t)r0;
-    m.slot_n[s] = (uint16_t)((int)__ldcg(a.offsets + e + 1) - r0);
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier of the co-resident blocks: the header counter reaches `target` (the number
+// of blocks times the barriers passed so far). Bounded: a timeout is reported and the block
+// carries on (its results are then not used).
+__device__ void grid_barrier(WsHeader* hdr, uint32_t target) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    atomicAdd(&hdr->done_blocks, 1u);
+    if (ld_acquire(&hdr->done_blocks) < target) {
+      const long long t0 = clock64();
+      while (ld_acquire(&hdr->done_blocks) < target) {
+        if (clock64() - t0 > kSpinLimitCycles) {
+          report_timeout(hdr);
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+    __threadfence();
   }
-  for (int r = threadIdx.x; r < a.te; r += blockDim.x)
-    m.row_tok[r] = (uint16_t)(__ldcg(a.sorted_pairs + r) / (uint32_t)a.K);
-  if (threadIdx.x == 0) m.n_active = n_active;
   __syncthreads();
 }
 
-// Item numbering of both phases.
-struct Geo {
+// Phase 0: logits[t, r] = x[t] . Wr[r] for every token, and the shared-gate products
+// x[t] . g (the gate vector as one more row, R), one row per block at a time with the
+// contraction spread over all its threads. x (and g) are staged in shared memory when they fit
+// (`scratch`), else read from global memory; the block's first row is loaded before the
+// staging so the two latencies overlap.
+__device__ void router_rows(const DecodeArgs& a, uint8_t* scratch, size_t scratch_bytes,
+                            float* red) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int chunks = a.H / 8;
+  const bool gated = a.S > 0 && a.sh_gate_vec;
+  const int rows = a.R + (gated ? 1 : 0);
+  auto row_ptr = [&](int r) {
+    return reinterpret_cast<const uint4*>(r < a.R ? a.router_w + (size_t)r * a.H : a.sh_gate_vec);
+  };
+  constexpr int kPer = 8;   // chunks per thread per pass (H <= 8 * 8 * kThreads)
+  uint4 wv[kPer];
+  const int r_first = blockIdx.x;
+  if (r_first < rows) {
+    const uint4* wr = row_ptr(r_first);
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int c = q * kThreads + tid;
+      if (c < chunks) wv[q] = __ldg(wr + c);
+    }
+  }
+  const size_t xbytes = (size_t)a.N * a.H * 2;
+  const __nv_bfloat16* xs = a.x;
+  if (xbytes <= scratch_bytes) {
+    uint4* d = reinterpret_cast<uint4*>(scratch);
+    const uint4* sx = reinterpret_cast<const uint4*>(a.x);
+    const int n = (int)(xbytes / 16);
+    for (int i0 = 0; i0 < n; i0 += 8 * kThreads) {
+      uint4 tmp[8];   // eight loads in flight per thread
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kThreads + tid;
+        if (i < n) tmp[u] = __ldg(sx + i);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kThreads + tid;
+        if (i < n) d[i] = tmp[u];
+      }
+    }
+    __syncthreads();
+    xs = reinterpret_cast<const __nv_bfloat16*>(scratch);
+  }
+  for (int r = r_first; r < rows; r += gridDim.x) {
+    float acc[kDecodeMaxTokens];
+#pragma unroll
+    for (int t = 0; t < kDecodeMaxTokens; ++t) acc[t] = 0.0f;
+    const uint4* wr = row_ptr(r);
+    for (int c0 = 0; c0 < chunks; c0 += kPer * kThreads) {
+      if (r != r_first || c0 != 0) {   // (the first pass was loaded above)
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+          const int c = c0 + q * kThreads + tid;
+          if (c < chunks) wv[q] = __ldg(wr + c);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        const int c = c0 + q * kThreads + tid;
+        if (c < chunks) {
+          float wf[8];
+          bf16x8_to_f32(wv[q], wf);
+#pragma unroll
+          for (int t = 0; t < kDecodeMaxTokens; ++t) {
+            if (t < a.N) {
+              float xf[8];
+              bf16x8_to_f32(reinterpret_cast<const uint4*>(xs + (size_t)t * a.H)[c], xf);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) acc[t] = fmaf(wf[i], xf[i], acc[t]);
+            }
+          }
+        }
+      }
+    }
+    // block reduction: per token, the warps' sums in shared memory
+#pragma unroll
+    for (int t = 0; t < kDecodeMaxTokens; ++t) {
+      if (t < a.N) {
+        const float v = warp_sum(acc[t]);
+        if (lane == 0) red[t * kWarps + warp] = v;
+      }
+    }
+    __syncthreads();
+    if (tid < a.N) {
+      float v = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) v += red[tid * kWarps + w];
+      if (r < a.R) a.logits[(size_t)tid * a.R + r] = v;
+      else a.hdr->gate_dot[tid] = v;
+    }
+    __syncthreads();
+  }
+}
+
+// Sorts the warp's 32 * VPL (score, id) keys best first (higher score, lower id on a tie) with a
+// bitonic network; lane l holds positions l * VPL .. l * VPL + VPL - 1. The stage loops stay
+// rolled: this code runs once per launch, so its size (instruction fetch) costs more than its
+// loop overhead.
+template <int VPL>
+__device__ __forceinline__ void bitonic_best_first(float (&v)[VPL], int (&ix)[VPL]) {
+  const int lane = threadIdx.x & 31;
+  constexpr int n = 32 * VPL;
+#pragma unroll 1
+  for (int k = 2; k <= n; k <<= 1) {
+#pragma unroll 1
+    for (int dist = k >> 1; dist > 0; dist >>= 1) {
+      if (dist < VPL) {
+#pragma unroll
+        for (int d = 1; d < VPL; d <<= 1) {
+          if (dist == d) {
+#pragma unroll
+            for (int j = 0; j < VPL; ++j) {
+              const int jj = j ^ d;
+              if (jj > j) {   // the pair (j, jj) of this lane, j the lower position
+                const bool up = ((lane * VPL + j) & k) == 0;
+                const bool hi_better = ranks_before(v[jj], ix[jj], v[j], ix[j]);
+                if (up == hi_better) {   // the lower position keeps the better key when up
+                  const float tv = v[j];
+                  v[j] = v[jj];
+                  v[jj] = tv;
+                  const int ti = ix[j];
+                  ix[j] = ix[jj];
+                  ix[jj] = ti;
+                }
+              }
+            }
+          }
+        }
+      } else {
+        const int lm = dist / VPL;
+        const bool lower = (lane & lm) == 0;
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+          const float ov = __shfl_xor_sync(0xffffffffu, v[j], lm);
+          const int oi = __shfl_xor_sync(0xffffffffu, ix[j], lm);
+          const bool up = ((lane * VPL + j) & k) == 0;
+          const bool other_better = ranks_before(ov, oi, v[j], ix[j]);
+          // lower position: keeps the better key when up; upper position: the worse one
+          if ((lower == up) == other_better) {
+            v[j] = ov;
+            ix[j] = oi;
+          }
+        }
+      }
+    }
+  }
+}
+
+// Top-K of one token by one warp: softmax in registers, selection by a bitonic sort of the
+// selection scores (R <= 32 * VPL), weights from the unbiased probabilities. `p_w`: per-warp
+// shared scratch of R floats.
+template <int VPL>
+__device__ void topk_sort_warp(const DecodeArgs& a, int t, float* p_w, uint32_t* idx_s,
+                               Routing& rt) {
+  const int lane = threadIdx.x & 31;
+  const int R = a.R, K = a.K;
+  const float* L = a.logits + (size_t)t * R;
+  const bool gated = a.S > 0 && a.sh_gate_vec;
+  const float gd = gated ? __ldcg(&a.hdr->gate_dot[t]) : 0.0f;   // (used at the end)
+  float v[VPL];
+  int ix[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int r = lane * VPL + j;
+    v[j] = r < R ? __ldcg(L + r) : 0.0f;
+  }
+  float mx = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int r = lane * VPL + j;
+    if (r < R) {
+      if (a.logit_bias) v[j] += a.logit_bias[r];
+      mx = fmaxf(mx, v[j]);
+    }
+  }
+  mx = warp_max(mx);
+  float den = 0.0f;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int r = lane * VPL + j;
+    if (r < R) {
+      v[j] = expf(v[j] - mx);
+      den += v[j];
+    }
+  }
+  den = warp_sum(den);
+  const bool biased = a.scoring == MOE_SCORING_SOFTMAX_BIAS && a.corr_bias;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int r = lane * VPL + j;
+    ix[j] = r;   // (padding keys: -inf with ids >= R, ordered after every real column)
+    if (r < R) {
+      const float pr = v[j] / den;
+      p_w[r] = pr;
+      v[j] = pr + (biased ? a.corr_bias[r] : 0.0f);
+    } else {
+      v[j] = -INFINITY;
+    }
+  }
+  uint32_t* idx_t = idx_s + t * K;
+  if (a.forced) {
+    if (lane < K) idx_t[lane] = a.forced[(size_t)t * K + lane];
+  } else {
+    bitonic_best_first<VPL>(v, ix);
+#pragma unroll
+    for (int j = 0; j < VPL; ++j)
+      if (lane * VPL + j < K) idx_t[lane * VPL + j] = (uint32_t)ix[j];
+  }
+  __syncwarp();
+  // weights: unbiased probabilities of the chosen ids, renormalised over all K slots
+  const uint32_t my_idx = lane < K ? idx_t[lane] : 0u;
+  float wk = lane < K ? p_w[my_idx < (uint32_t)R ? my_idx : 0u] : 0.0f;
+  const float sum = warp_sum(wk);
+  if (a.norm) wk = wk / sum;
+  wk *= a.scale;
+  float z = (lane < K && (int)my_idx >= a.E) ? wk : 0.0f;
+  z = warp_sum(z);
+  if (lane < K) rt.w[t * K + lane] = wk;
+  if (lane == 0) {
+    rt.zsum[t] = z;
+    // shared-expert blend weight sigmoid(x[t] . g), or 1 without a gate
+    rt.gamma[t] = gated ? 1.0f / (1.0f + expf(-gd)) : 1.0f;
+  }
+}
+
+// Wide routers (R > 256): K rounds of a warp arg-max (route_token_warp_reg), then the same
+// weights and blend gate.
+__device__ void topk_rounds_warp(const DecodeArgs& a, int t, uint32_t* idx_s, Routing& rt) {
+  const int lane = threadIdx.x & 31;
+  route_token_warp_fast(a.logits + (size_t)t * a.R, a.logit_bias, a.corr_bias, a.R, a.E, a.K,
+                        a.scoring, a.norm, a.scale,
+                        a.forced ? a.forced + (size_t)t * a.K : nullptr, idx_s + t * a.K,
+                        rt.w + t * a.K, rt.zsum + t);
+  if (lane == 0) {
+    const bool gated = a.S > 0 && a.sh_gate_vec;
+    rt.gamma[t] = gated ? 1.0f / (1.0f + expf(-__ldcg(&a.hdr->gate_dot[t]))) : 1.0f;
+  }
+}
+
+// Phase 1: the block's own copy of the routing. `scratch`: dynamic shared memory not yet in use.
+// The stable sort by expert takes a few block-wide steps: ranks of equal experts inside each
+// 32-pair chunk (match) and per-chunk counts; per expert, its first row (block scan) and each
+// chunk's first row; then every pair's row.
+__device__ void route_block(const DecodeArgs& a, Routing& rt, uint8_t* scratch) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int R = a.R, E = a.E, K = a.K, te = a.te;
+  const int nch = (te + 31) / 32;                                      // 32-pair chunks
+  uint32_t* idx_s = reinterpret_cast<uint32_t*>(scratch);              // [te]
+  uint32_t* lrank_s = idx_s + te;                                      // [te]
+  uint32_t* chunk_s = lrank_s + te;                                    // [nch][E]
+  uint32_t* base_s = chunk_s + (size_t)nch * E;                        // [E] first rows
+  uint32_t* scan_s = base_s + E;                                       // [33]
+  float* p_s = reinterpret_cast<float*>(scan_s + 40);                  // [warps][R]
+  for (int i = tid; i < nch * E; i += blockDim.x) chunk_s[i] = 0;
+  for (int t = warp; t < a.N; t += kWarps) {
+    if (R <= 128) topk_sort_warp<4>(a, t, p_s + warp * R, idx_s, rt);
+    else if (R <= 256) topk_sort_warp<8>(a, t, p_s + warp * R, idx_s, rt);
+    else topk_rounds_warp(a, t, idx_s, rt);
+    __syncwarp();
+  }
+  __syncthreads();
+  // ranks inside each chunk, and the chunk's count of every expert (its group's last lane)
+  for (int j0 = 0; j0 < te; j0 += kThreads) {
+    const int j = j0 + tid;
+    const uint32_t e = j < te ? idx_s[j] : 0xFFFFFFFFu;
+    const bool real = j < te && (int)e < E;
+    const uint32_t m = __match_any_sync(0xffffffffu, real ? e : 0xFFFFFFFFu);
+    if (j < te) lrank_s[j] = (uint32_t)__popc(m & ((1u << lane) - 1u));
+    if (real && (m >> lane) == 1u) chunk_s[(size_t)(j >> 5) * E + e] = (uint32_t)__popc(m);
+  }
+  __syncthreads();
+  // per expert: rows (sum over chunks), first row and slot (block scans), each chunk's first row
+  uint32_t carry_rows = 0, carry_slots = 0;
+  for (int e0 = 0; e0 < E; e0 += kThreads) {
+    const int e = e0 + tid;
+    uint32_t tot = 0;
+    if (e < E)
+      for (int c = 0; c < nch; ++c) tot += chunk_s[(size_t)c * E + e];
+    const uint32_t off = block_excl_scan(tot, scan_s, &scan_s[32]);
+    const uint32_t tot_rows = scan_s[32];
+    __syncthreads();
+    const uint32_t sl = block_excl_scan(tot > 0 ? 1u : 0u, scan_s, &scan_s[32]);
+    const uint32_t tot_slots = scan_s[32];
+    __syncthreads();
+    if (e < E) {
+      uint32_t row = carry_rows + off;
+      base_s[e] = row;
+      if (tot > 0) {
+        rt.slot_e[carry_slots + sl] = (uint16_t)e;
+        rt.slot_r0[carry_slots + sl] = (uint16_t)row;
+        rt.slot_n[carry_slots + sl] = (uint16_t)tot;
+      }
+      for (int c = 0; c < nch; ++c) {
+        const uint32_t n = chunk_s[(size_t)c * E + e];
+        chunk_s[(size_t)c * E + e] = row;
+        row += n;
+      }
+    }
+    carry_rows += tot_rows;
+    carry_slots += tot_slots;
+  }
+  if (tid == 0) {
+    rt.n_active = (int)carry_slots;
+    rt.rows = (int)carry_rows;
+  }
+  __syncthreads();
+  for (int j = tid; j < te; j += kThreads) {
+    const uint32_t e = idx_s[j];
+    if ((int)e >= E) {
+      rt.pair_row[j] = kNoRow16;
+      continue;
+    }
+    const uint32_t row = chunk_s[(size_t)(j >> 5) * E + e] + lrank_s[j];
+    rt.pair_row[j] = (uint16_t)row;
+    rt.row_pair[row] = (uint16_t)j;
+    rt.row_tok[row] = (uint16_t)(j / K);
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int j = tid; j < te; j += blockDim.x) {
+      a.idx[j] = idx_s[j];
+      a.w[j] = rt.w[j];
+      a.pair_to_row[j] = rt.pair_row[j] == kNoRow16 ? kNoRow : (uint32_t)rt.pair_row[j];
+    }
+    for (int r = tid; r < rt.rows; r += blockDim.x) a.sorted_pairs[r] = rt.row_pair[r];
+    for (int e = tid; e < E; e += blockDim.x) a.offsets[e] = base_s[e];
+    for (int sl = tid; sl < rt.n_active; sl += blockDim.x) a.active[sl] = rt.slot_e[sl];
+    for (int t = tid; t < a.N; t += blockDim.x) a.zsum[t] = rt.zsum[t];
+    if (tid == 0) {
+      a.offsets[E] = (uint32_t)rt.rows;
+      a.hdr->num_active = (uint32_t)rt.n_active;
+    }
+  }
+  // the scratch is about to be overwritten by bulk copies (async proxy)
+  fence_proxy_async_smem();
+  __syncthreads();
+}
+
+// Phase 3: 8 consecutive outputs per thread, chunks spread over the blocks.
+__device__ void combine_chunks(const DecodeArgs& a, const Routing& rt) {
+  const int C8 = a.H / 8, Q = a.N * C8;
+  for (int q = blockIdx.x + gridDim.x * threadIdx.x; q < Q; q += gridDim.x * blockDim.x) {
+    const int t = q / C8, c = q - t * C8;
+    const size_t o8 = (size_t)t * a.H + (size_t)c * 8;
+    float acc[8], xf[8];
+    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(a.x + o8)), xf);
+    const float z = rt.zsum[t];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = z * xf[i];
+    if (a.acc) {
+      const float4* p = reinterpret_cast<const float4*>(a.acc + o8);
+      const float4 u = __ldcg(p), v = __ldcg(p + 1);
+      acc[0] += u.x; acc[1] += u.y; acc[2] += u.z; acc[3] += u.w;
+      acc[4] += v.x; acc[5] += v.y; acc[6] += v.z; acc[7] += v.w;
+    } else {
+      for (int k0 = 0; k0 < a.K; k0 += 8) {   // 8 expert rows in flight per round
+        float4 y0[8], y1[8];
+        float wk[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int k = k0 + u;
+          const uint16_t row = k < a.K ? rt.pair_row[t * a.K + k] : kNoRow16;
+          wk[u] = 0.0f;
+          if (row != kNoRow16) {
+            wk[u] = rt.w[t * a.K + k];
+            const float4* p = reinterpret_cast<const float4*>(a.yd + (size_t)row * a.H + c * 8);
+            y0[u] = __ldcg(p);
+            y1[u] = __ldcg(p + 1);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int k = k0 + u;
+          if (k < a.K && rt.pair_row[t * a.K + k] != kNoRow16) {
+            acc[0] = fmaf(wk[u], y0[u].x, acc[0]);
+            acc[1] = fmaf(wk[u], y0[u].y, acc[1]);
+            acc[2] = fmaf(wk[u], y0[u].z, acc[2]);
+            acc[3] = fmaf(wk[u], y0[u].w, acc[3]);
+            acc[4] = fmaf(wk[u], y1[u].x, acc[4]);
+            acc[5] = fmaf(wk[u], y1[u].y, acc[5]);
+            acc[6] = fmaf(wk[u], y1[u].z, acc[6]);
+            acc[7] = fmaf(wk[u], y1[u].w, acc[7]);
+          }
+        }
+      }
+    }
+    if (a.S > 0) {
+      const float g = rt.gamma[t];
+      const float4* p = reinterpret_cast<const float4*>(a.shy + o8);
+      const float4 u = __ldcg(p), v = __ldcg(p + 1);
+      acc[0] = fmaf(g, u.x, acc[0]); acc[1] = fmaf(g, u.y, acc[1]);
+      acc[2] = fmaf(g, u.z, acc[2]); acc[3] = fmaf(g, u.w, acc[3]);
+      acc[4] = fmaf(g, v.x, acc[4]); acc[5] = fmaf(g, v.y, acc[5]);
+      acc[6] = fmaf(g, v.z, acc[6]); acc[7] = fmaf(g, v.w, acc[7]);
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(a.out + o8) = o;
+  }
+}
+
+// The block's work items: all gate/up items first, then the down items. Within a phase, items
+// are numbered slot-major (a slot's tiles, each tile's contraction boxes in order) and every
+// block takes a contiguous, balanced range. The grid of each phase is capped so that no tile
+// is split over more than two blocks: the two fp32 partial sums of a tile then meet in a
+// zeroed buffer through atomic adds, and a + b == b + a makes the result independent of their
+// order (deterministic).
+struct Sched {
   int nIt, nSt;     // weight tiles of one gate (or up) projection: routed, shared
   int Pg;           // items per gate/up tile (H / 64)
   int nHt;          // weight tiles of a down projection
   int Pdr, Pds;     // items per down tile: routed (I / 64), shared (S / 64)
   int na;           // active routed slots
   int g_rt, g_items, d_ritems, d_items;
+  int g0, ng, d0, total;   // this block's ranges
+  static __device__ __forceinline__ void range(int n, int per_tile, int& i0, int& cnt) {
+    int G = gridDim.x;
+    int cap = n / per_tile;
+    if (cap < 1) cap = 1;
+    if (G > cap) G = cap;
+    const int b = blockIdx.x;
+    if (b >= G) {
+      i0 = cnt = 0;
+      return;
+    }
+    i0 = (int)((long long)n * b / G);
+    cnt = (int)((long long)n * (b + 1) / G) - i0;
+  }
   __device__ void init(const DecodeArgs& a, const Plan& pl, int n_active) {
     nIt = a.I / pl.bn_g;
     nSt = a.S / pl.bn_g;
@@ -103,11 +565,18 @@ struct Geo {
     g_items = (g_rt + (a.S ? 2 * nSt : 0)) * Pg;
     d_ritems = na * nHt * Pdr;
     d_items = d_ritems + (a.S ? nHt * Pds : 0);
+    int nd;
+    range(g_items, Pg, g0, ng);
+    range(d_items, Pdr > Pds ? Pdr : Pds, d0, nd);
+    total = ng + nd;
   }
-  // slot: active slot index, or -1 for the shared expert; lt: tile within the slot's
-  // projection(s) (gate/up: gate tiles first, then up tiles)
-  __device__ void item(bool down, int it, int& tile, int& kc, int& slot, int& lt) const {
+  // this block's k-th item: phase, tile (unique within gate/up or within down), contraction
+  // box kc, slot (-1: shared expert), tile within the slot's projection(s) (gate/up: gate tiles
+  // first, then up tiles)
+  __device__ void item(int k, bool& down, int& tile, int& kc, int& slot, int& lt) const {
+    down = k >= ng;
     if (!down) {
+      const int it = g0 + k;
       tile = it / Pg;
       kc = it - tile * Pg;
       if (tile < g_rt) {
@@ -117,49 +586,45 @@ struct Geo {
         slot = -1;
         lt = tile - g_rt;
       }
-    } else if (it < d_ritems) {
-      tile = it / Pdr;
-      kc = it - tile * Pdr;
-      slot = tile / nHt;
-      lt = tile - slot * nHt;
     } else {
-      const int j = it - d_ritems;
-      lt = j / Pds;
-      kc = j - lt * Pds;
-      tile = na * nHt + lt;
-      slot = -1;
+      const int it = d0 + (k - ng);
+      if (it < d_ritems) {
+        tile = it / Pdr;
+        kc = it - tile * Pdr;
+        slot = tile / nHt;
+        lt = tile - slot * nHt;
+      } else {
+        const int j = it - d_ritems;
+        lt = j / Pds;
+        kc = j - lt * Pds;
+        tile = na * nHt + lt;
+        slot = -1;
+      }
     }
   }
 };
 
-// Contiguous share [i0, i1) of `total` items for this block. At most total / per_tile blocks
-// take part, so every block holds at least one tile's worth of items and no tile is split over
-// more than two blocks.
-__device__ __forceinline__ void phase_range(int total, int per_tile, int& i0, int& i1) {
-  int G = gridDim.x;
-  int cap = total / per_tile;
-  if (cap < 1) cap = 1;
-  if (G > cap) G = cap;
-  const int b = blockIdx.x;
-  if (b >= G) {
-    i0 = i1 = 0;
-    return;
-  }
-  i0 = (int)((long long)total * b / G);
-  i1 = (int)((long long)total * (b + 1) / G);
+// Phase 0 also clears the fp32 accumulators the projections add into (the grid barrier before
+// phase 2 orders it before every add).
+__device__ void zero_accumulators(const DecodeArgs& a) {
+  const size_t nth = (size_t)gridDim.x * blockDim.x, tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  auto zero16 = [&](void* p, size_t bytes) {   // bytes: a multiple of 16
+    uint4* q = reinterpret_cast<uint4*>(p);
+    for (size_t i = tid; i < bytes / 16; i += nth) q[i] = make_uint4(0u, 0u, 0u, 0u);
+  };
+  zero16(a.hd, (size_t)(a.te + a.N) * 2 * a.ldh * 4);
+  if (a.yd) zero16(a.yd, (size_t)a.te * a.H * 4);
+  if (a.acc) zero16(a.acc, (size_t)a.N * a.H * 4);
+  if (a.S > 0) zero16(a.shy, (size_t)a.N * a.H * 4);
+  for (size_t i = tid; i < (size_t)kDecodeMaxPairs + 1; i += nth) a.h_cnt[i] = 0u;
 }
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 
-__device__ __forceinline__ int slot_rows(const DecodeArgs& a, const RouteMeta& m, int slot,
+__device__ __forceinline__ int slot_rows(const DecodeArgs& a, const Routing& m, int slot,
                                          int& r0) {
   if (slot < 0) {
     r0 = a.te;
@@ -170,33 +635,36 @@ __device__ __forceinline__ int slot_rows(const DecodeArgs& a, const RouteMeta& m
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_ffn_kernel(const __grid_constant__ CUtensorMap tm_wg,
-                      const __grid_constant__ CUtensorMap tm_wu,
-                      const __grid_constant__ CUtensorMap tm_sg,
-                      const __grid_constant__ CUtensorMap tm_su,
-                      const __grid_constant__ CUtensorMap tm_wd,
-                      const __grid_constant__ CUtensorMap tm_sd,
-                      const __grid_constant__ CUtensorMap tm_x, const DecodeArgs a, const Plan pl) {
+    decode_forward_kernel(const __grid_constant__ CUtensorMap tm_wg,
+                          const __grid_constant__ CUtensorMap tm_wu,
+                          const __grid_constant__ CUtensorMap tm_sg,
+                          const __grid_constant__ CUtensorMap tm_su,
+                          const __grid_constant__ CUtensorMap tm_wd,
+                          const __grid_constant__ CUtensorMap tm_sd,
+                          const __grid_constant__ CUtensorMap tm_x, const DecodeArgs a,
+                          const Plan pl) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ RouteMeta meta;
-  __shared__ uint64_t bars[2 * kMaxStages + 6];
+  __shared__ Routing meta;
+  __shared__ uint64_t bars[2 * kMaxStages + 8];
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(16) float stage_rows[16 * kStageLd];   // drain staging, 16 rows x 64
-  // 1024-byte alignment for the 128-byte swizzle atoms. Layout: token boxes of the stages,
-  // the down-projection A operand, the weight ring (the A descriptors' rows 16..127 read on
-  // into what follows, always inside this allocation).
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ float red_s[kDecodeMaxTokens * kWarps];           // router block reductions
+  // 1024-byte alignment for the 128-byte swizzle atoms. Layout: token boxes of the stages, two
+  // buffers of the down-projection A operand, the weight ring (the A descriptors' rows 16..127
+  // read on into what follows, always inside this allocation). An offset from the __shared__
+  // array keeps the shared address space visible to the compiler.
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   const int stages = pl.stages;
   uint8_t* xtok = smem;                                   // [stages][16 x 128 B]
-  uint8_t* hb = xtok + (size_t)stages * kTokBytes;        // [max(I,S)/64][16 x 128 B]
-  uint8_t* ring = hb + pl.hbytes;                         // [stages][BN x 128 B]
+  uint8_t* hb = xtok + (size_t)stages * kTokBytes;        // [2][max(I,S)/64][16 x 128 B]
+  uint8_t* ring = hb + 2 * (size_t)pl.hbytes;             // [stages][BN x 128 B]
   uint64_t* full = bars;
   uint64_t* empty = bars + kMaxStages;
   uint64_t* afull = bars + 2 * kMaxStages;                // [2] run accumulated
   uint64_t* aempty = afull + 2;                           // [2] run drained
-  uint64_t* bfull = aempty + 2;                           // down A operand built
-  uint64_t* drain = bfull + 1;                            // every MMA complete
+  uint64_t* bfull = aempty + 2;                           // [2] down A operand built
+  uint64_t* drain = bfull + 2;                            // every MMA complete
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WsHeader* hdr = a.hdr;
 
@@ -208,8 +676,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&afull[i], 1);
       mbar_init(&aempty[i], 1);   // the draining warp's lane 0
+      mbar_init(&bfull[i], 1);
     }
-    mbar_init(bfull, 1);
     mbar_init(drain, 1);
     fence_mbarrier_init();
     tma_prefetch_desc(&tm_wg);
@@ -222,19 +690,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_sd);
     }
   }
-  pdl_trigger();   // the combine kernel may launch and wait for this one
   if (warp == 1) tmem_alloc(&tmem_slot, kTmemCols);
-  tc_fence_before();
-  load_route_meta(a, meta);   // (ends with a block barrier)
+  // ---- phases 0 and 1: router logits (spread over the grid) and zeroed accumulators, then
+  // each block's routing
+  router_rows(a, smem, (size_t)stages * (kTokBytes + kWBytes), red_s);
+  zero_accumulators(a);
+  grid_barrier(hdr, gridDim.x);
+  route_block(a, meta, smem);   // (ends with a block barrier)
   tc_fence_after();
   const uint32_t tmem_base = tmem_slot;
 
-  Geo geo;
-  geo.init(a, pl, meta.n_active);
-  int g0, g1, d0, d1;
-  phase_range(geo.g_items, geo.Pg, g0, g1);
-  phase_range(geo.d_items, geo.Pdr > geo.Pds ? geo.Pdr : geo.Pds, d0, d1);
-  const int ng = g1 - g0, nitems = ng + (d1 - d0);
+  // ---- phase 2: the projections
+  Sched sc;
+  sc.init(a, pl, meta.n_active);
+  const int nitems = sc.total;
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -244,12 +713,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int k = 0; k < nitems; ++k) {
         if (!mbar_wait(&empty[s], ph ^ 1, hdr)) { ok = false; break; }
-        const bool down = k >= ng;
+        bool down;
         int tile, kc, slot, lt;
-        geo.item(down, down ? d0 + (k - ng) : g0 + k, tile, kc, slot, lt);
+        sc.item(k, down, tile, kc, slot, lt);
         uint8_t* wst = ring + (size_t)s * kWBytes;
         if (!down) {
-          const int nt = slot >= 0 ? geo.nIt : geo.nSt;
+          const int nt = slot >= 0 ? sc.nIt : sc.nSt;
           const bool up = lt >= nt;
           const int r = (up ? lt - nt : lt) * pl.bn_g;
           const CUtensorMap* m;
@@ -283,20 +752,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_g = idesc_make(128, pl.bn_g, 1, 1);
       const uint32_t idesc_d = idesc_make(128, pl.bn_d, 1, 1);
       int s = 0, run = -1, prev_tile = -1, bslot = -2, nb = 0;
-      uint32_t ph = 0;
+      uint32_t ph = 0, hb_cur = 0;
       bool prev_down = false, ok = true, first = false;
       for (int k = 0; k < nitems && ok; ++k) {
-        const bool down = k >= ng;
+        bool down;
         int tile, kc, slot, lt;
-        geo.item(down, down ? d0 + (k - ng) : g0 + k, tile, kc, slot, lt);
+        sc.item(k, down, tile, kc, slot, lt);
         if (run < 0 || down != prev_down || tile != prev_tile) {
           if (run >= 0) tc_commit(&afull[run & 1]);
           ++run;
           prev_down = down;
           prev_tile = tile;
           if (!mbar_wait(&aempty[run & 1], (((uint32_t)run >> 1) & 1) ^ 1, hdr)) { ok = false; break; }
-          if (down && slot != bslot) {
-            if (!mbar_wait(bfull, (uint32_t)nb & 1, hdr)) { ok = false; break; }
+          if (down && slot != bslot) {   // the epilogue's nb-th build, in buffer nb % 2
+            if (!mbar_wait(&bfull[nb & 1], (uint32_t)(nb >> 1) & 1, hdr)) { ok = false; break; }
+            hb_cur = smem_u32(hb) + (uint32_t)(nb & 1) * (uint32_t)pl.hbytes;
             ++nb;
             bslot = slot;
           }
@@ -306,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&full[s], ph, hdr)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)((run & 1) * kMaxBN);
-        const uint32_t a0 = down ? smem_u32(hb) + (uint32_t)kc * kTokBytes
+        const uint32_t a0 = down ? hb_cur + (uint32_t)kc * kTokBytes
                                  : smem_u32(xtok) + (uint32_t)s * kTokBytes;
         const uint32_t b0 = smem_u32(ring) + (uint32_t)s * kWBytes;
         const uint32_t idesc = down ? idesc_d : idesc_g;
@@ -327,47 +797,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ epilogue
     const int et = threadIdx.x - 64;        // 0..127
     const bool drainer = warp == kDrainWarp;
-    int run = -1, prev_tile = -1, bslot = -2;
+    int run = -1, prev_tile = -1, bslot = -2, nb = 0;
     bool prev_down = false;
-    // the run being accumulated: phase, slot, tile within the slot, items
-    bool r_down = false;
-    int r_slot = 0, r_lt = 0, r_len = 0;
+    // the run being accumulated (phase, slot, tile within the slot, items) and whether the
+    // previous one was drained already
+    bool r_down = false, drained = true;
+    int r_slot = 0, r_lt = 0, r_len = 0, r_idx = -1;
     bool ok = true;
     // Warp 4 drains a finished run: TMEM lane j < 16 holds accumulator row j (token j of x on
     // gate/up, the slot's j-th token on down) across the tile's BN columns. 64 columns at a
     // time go through shared memory so that every row's partial sums leave as coalesced
     // 32-lane atomic adds.
-    auto drain_run = [&]() {
+    auto drain_run = [&](int rr, bool rdown, int rslot, int rlt, int rlen) {
       if (!ok) return;
-      if (!mbar_wait(&afull[run & 1], ((uint32_t)run >> 1) & 1, hdr)) { ok = false; return; }
+      if (!mbar_wait(&afull[rr & 1], ((uint32_t)rr >> 1) & 1, hdr)) { ok = false; return; }
       tc_fence_after();
       int r0;
-      const int ntok = slot_rows(a, meta, r_slot, r0);
-      const uint32_t tacc = tmem_base + (uint32_t)((run & 1) * kMaxBN);
+      const int ntok = slot_rows(a, meta, rslot, r0);
+      const uint32_t tacc = tmem_base + (uint32_t)((rr & 1) * kMaxBN);
       float* dst = nullptr;      // output row of accumulator row `lane` (lanes < 16)
       float scale = 1.0f;
       int bn;
-      if (!r_down) {
+      if (!rdown) {
         bn = pl.bn_g;
         int row = -1;            // sorted row of (slot, token lane)
-        if (r_slot < 0) {
+        if (rslot < 0) {
           if (lane < a.N) row = a.te + lane;
         } else {
           for (int j = 0; j < ntok; ++j)
             if ((int)meta.row_tok[r0 + j] == lane) row = r0 + j;
         }
-        const int nt = r_slot >= 0 ? geo.nIt : geo.nSt;
-        const int col = (r_lt < nt ? 0 : a.ldh) + (r_lt < nt ? r_lt : r_lt - nt) * bn;
+        const int nt = rslot >= 0 ? sc.nIt : sc.nSt;
+        const int col = (rlt < nt ? 0 : a.ldh) + (rlt < nt ? rlt : rlt - nt) * bn;
         if (row >= 0) dst = a.hd + (size_t)row * (2 * a.ldh) + col;
       } else {
         bn = pl.bn_d;
-        const int c0 = r_lt * bn;
+        const int c0 = rlt * bn;
         if (lane < ntok) {
           const int row = r0 + lane;
-          if (r_slot < 0) {
+          if (rslot < 0) {
             dst = a.shy + (size_t)lane * a.H + c0;
           } else if (a.acc) {
-            scale = a.w[__ldcg(a.sorted_pairs + row)];
+            scale = meta.w[meta.row_pair[row]];
             dst = a.acc + (size_t)meta.row_tok[row] * a.H + c0;
           } else {
             dst = a.yd + (size_t)row * a.H + c0;
@@ -400,23 +871,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&aempty[run & 1]);
-      if (!r_down) {
+      if (lane == 0) mbar_arrive(&aempty[rr & 1]);
+      if (!rdown) {
         // publish: the slot's count moves only after every partial sum of the run landed
         __threadfence();
         __syncwarp();
         if (lane == 0) {
           __threadfence();
-          atomicAdd(a.h_cnt + (r_slot < 0 ? kDecodeMaxPairs : r_slot), (uint32_t)r_len);
+          atomicAdd(a.h_cnt + (rslot < 0 ? kDecodeMaxPairs : rslot), (uint32_t)rlen);
         }
       }
     };
-    // SiLU(gate) * up of the slot's tokens as the bf16 A operand, 16 rows per 64-column box
-    // with the 128-byte swizzle: row j's 16-byte chunk c of box kb at
+    auto drain_current = [&]() {
+      if (drainer && !drained && r_idx >= 0) drain_run(r_idx, r_down, r_slot, r_lt, r_len);
+      drained = true;
+    };
+    // SiLU(gate) * up of the slot's tokens as the bf16 A operand (buffer nb % 2), 16 rows per
+    // 64-column box with the 128-byte swizzle: row j's 16-byte chunk c of box kb at
     // kb * 2048 + j * 128 + ((c ^ (j & 7)) * 16).
-    auto build_a = [&](int slot) {
-      const uint32_t target = (uint32_t)((slot >= 0 ? 2 * geo.nIt : 2 * geo.nSt) * geo.Pg);
-      if (drainer && lane == 0) {   // (after this warp published the block's own gate/up runs)
+    auto build_a = [&](int slot, uint8_t* buf) {
+      const uint32_t target = (uint32_t)((slot >= 0 ? 2 * sc.nIt : 2 * sc.nSt) * sc.Pg);
+      if (drainer && lane == 0) {
         const uint32_t* cnt = a.h_cnt + (slot < 0 ? kDecodeMaxPairs : slot);
         if (ld_acquire(cnt) < target) {
           const long long t0 = clock64();
@@ -448,35 +923,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           o.z = pack_bf16x2(silu(g1v.x) * u1.x, silu(g1v.y) * u1.y);
           o.w = pack_bf16x2(silu(g1v.z) * u1.z, silu(g1v.w) * u1.w);
         }
-        *reinterpret_cast<uint4*>(hb + (size_t)(c >> 3) * kTokBytes + j * 128 +
+        *reinterpret_cast<uint4*>(buf + (size_t)(c >> 3) * 2048 + j * 128 +
                                   (((c & 7) ^ (j & 7)) << 4)) = o;
       }
       fence_proxy_async_smem();
       named_sync(1, kEpiThreads);
-      if (et == 0) mbar_arrive(bfull);
+      if (et == 0) mbar_arrive(&bfull[nb & 1]);
     };
     for (int k = 0; k < nitems; ++k) {
-      const bool down = k >= ng;
+      bool down;
       int tile, kc, slot, lt;
-      geo.item(down, down ? d0 + (k - ng) : g0 + k, tile, kc, slot, lt);
+      sc.item(k, down, tile, kc, slot, lt);
       if (run < 0 || down != prev_down || tile != prev_tile) {
-        if (run >= 0 && drainer) drain_run();
         ++run;
         prev_down = down;
         prev_tile = tile;
+        if (down && slot != bslot) {
+          // The previous gate/up run is published first (the count may wait on it). Otherwise
+          // the next buffer is free -- the runs that read it, two slot changes back, are
+          // drained -- and the build overlaps the MMAs of the previous run.
+          if (!r_down) drain_current();
+          build_a(slot, hb + (size_t)(nb & 1) * pl.hbytes);
+          ++nb;
+          bslot = slot;
+        }
+        drain_current();
+        r_idx = run;
         r_down = down;
         r_slot = slot;
         r_lt = lt;
         r_len = 0;
-        // the MMAs of every earlier run are complete (drained): the A buffer is free
-        if (down && slot != bslot) {
-          build_a(slot);
-          bslot = slot;
-        }
+        drained = false;
       }
       ++r_len;
     }
-    if (run >= 0 && drainer) drain_run();
+    drain_current();
   }
   tc_fence_before();
   __syncthreads();
@@ -485,6 +966,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  // ---- phase 3: every block's partial sums have landed; combine
+  grid_barrier(hdr, 2 * gridDim.x);
+  combine_chunks(a, meta);
 }
 
 int sm_count() {
@@ -508,27 +992,31 @@ void decode_tile_rows(int H, int I, int S, int* bn_g, int* bn_d) {
   *bn_d = H % 256 == 0 ? 256 : 128;
 }
 
-cudaError_t launch_decode_ffn(const DecodeArgs& a, const CUtensorMap* maps, cudaStream_t st) {
+cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, cudaStream_t st) {
   if (a.te > kDecodeMaxPairs || a.N > kDecodeMaxTokens || a.N < 1 || !a.h_cnt ||
-      a.H % 128 || a.I % 128 || a.S % 128)
+      a.H % 128 || a.I % 128 || a.S % 128 || a.R > 1024 || a.E > 1024 || a.K > 32)
     return cudaErrorInvalidValue;
   const int L = a.I > a.S ? a.I : a.S;
   Plan pl{};
   decode_tile_rows(a.H, a.I, a.S, &pl.bn_g, &pl.bn_d);
   pl.hbytes = (L / kBox) * kTokBytes;
   const int per_stage = kTokBytes + kWBytes;
-  const int fixed = 1024 + pl.hbytes;   // alignment slack + down A operand
-  // (the static shared memory -- routing metadata, barriers -- stays within the 8 KB margin)
-  pl.stages = (kSmemLimit - 8192 - fixed) / per_stage;
+  const int fixed = 1024 + 2 * pl.hbytes;   // alignment slack + two down A operands
+  // (the static shared memory -- routing, barriers, drain staging -- stays within 16 KB)
+  pl.stages = (kSmemLimit - 16384 - fixed) / per_stage;
   if (pl.stages > kMaxStages) pl.stages = kMaxStages;
   if (pl.stages < 2) return cudaErrorInvalidValue;
+  // the routing scratch of phase 1 lives in the (not yet used) dynamic region
+  const size_t scratch = (size_t)a.te * 8 + (size_t)((a.te + 31) / 32) * a.E * 4 +
+                         (size_t)a.E * 4 + 160 + (size_t)kWarps * a.R * 4;
+  if (scratch > (size_t)pl.stages * (kTokBytes + kWBytes)) return cudaErrorInvalidValue;
   const size_t sm = (size_t)fixed + (size_t)pl.stages * per_stage;
   cudaError_t e =
-      cudaFuncSetAttribute(decode_ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      cudaFuncSetAttribute(decode_forward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   // the down phase waits on other blocks' gate/up work: all blocks must be resident
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_ffn_kernel, kThreads, sm);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_forward_kernel, kThreads, sm);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
@@ -541,7 +1029,7 @@ cudaError_t launch_decode_ffn(const DecodeArgs& a, const CUtensorMap* maps, cuda
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_ffn_kernel, maps[kDmWg], maps[kDmWu], maps[kDmSg],
+  return cudaLaunchKernelEx(&cfg, decode_forward_kernel, maps[kDmWg], maps[kDmWu], maps[kDmSg],
                             maps[kDmSu], maps[kDmWd], maps[kDmSd], maps[kDmX], a, pl);
 }
 

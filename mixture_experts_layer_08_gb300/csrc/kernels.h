@@ -80,32 +80,46 @@ cudaError_t launch_sort(const SortArgs& s, const __nv_bfloat16* x, int H, __nv_b
 constexpr int kDecodeMaxTokens = 16;
 constexpr int kDecodeMaxPairs = 512;
 
-// Decode chain: gate/up and down projections of the active experts and the shared expert as
-// skinny tensor-core GEMMs (weights as the wide B operand, the batch's tokens as A rows).
+// Decode chain: the whole block forward of a few tokens in one cooperative launch -- router,
+// top-K and sort, gate/up and down projections of the active experts and the shared expert as
+// skinny tensor-core GEMMs (weights as the wide B operand, the tokens as A rows), combine.
 struct DecodeArgs {
   const __nv_bfloat16* x;          // [N,H]
-  const uint32_t* offsets;
-  const uint32_t* sorted_pairs;
-  const uint32_t* active;
-  const float* w;                  // routing weights [N,K]
-  int N, H, E, K, I, S, te;
-  float* hd;                       // [te + N, 2*ldh] fp32 gate (cols < ldh) and up products
-                                   // (row = sorted row, shared rows te + t); zero on entry
+  const __nv_bfloat16* router_w;   // [R,H]
+  const float* logit_bias;         // [R] or null
+  const float* corr_bias;          // [R] or null (selection only)
+  const uint32_t* forced;          // [N,K] or null
+  const __nv_bfloat16* sh_gate_vec;    // [H] or null
+  int N, H, E, R, K, I, S, te, scoring, norm;
+  float scale;
+  float* logits;                   // [N,R]
+  // routing results, written by block 0 for inspection and the top-K outputs
+  uint32_t* idx;                   // [N,K]
+  float* w;                        // [N,K]
+  float* zsum;                     // [N]
+  uint32_t* offsets;               // [E+1]
+  uint32_t* sorted_pairs;          // [te]
+  uint32_t* pair_to_row;           // [te]
+  uint32_t* active;                // [E]
+  // fp32 accumulators, cleared by the kernel
+  float* hd;                       // [te + N, 2*ldh] gate (cols < ldh) and up products
+                                   // (row = sorted row, shared rows te + t)
   int ldh;                         // max(I, S)
-  float* yd;                       // [te, H] fp32 (deterministic), zero on entry, or null
-  float* acc;                      // [N, H] fp32 atomic accumulator, zero on entry, or null
-  float* shy;                      // [N, H] fp32 shared expert output, zero on entry
+  float* yd;                       // [te, H] expert outputs (deterministic) or null
+  float* acc;                      // [N, H] atomic accumulator (atomic mode) or null
+  float* shy;                      // [N, H] shared expert output
   uint32_t* h_cnt;                 // [kDecodeMaxPairs + 1] gate/up work items finished per slot
-                                   // (the last entry: shared expert), zero on entry
-  WsHeader* hdr;
+                                   // (the last entry: shared expert)
+  WsHeader* hdr;                   // done_blocks (grid barriers) zero on entry
+  __nv_bfloat16* out;              // [N,H]
 };
 // Tensor maps (bf16, box {64, rows}, 128-byte swizzle) the decode kernel streams from.
 enum DecodeMap { kDmWg = 0, kDmWu, kDmSg, kDmSu, kDmWd, kDmSd, kDmX, kDmNum };
 // Box rows: x 16; gate/up weights (Wg, Wu, Sg, Su) *bn_g; down weights (Wd, Sd) *bn_d.
 constexpr int kDecodeBoxRowsX = 16;
 void decode_tile_rows(int H, int I, int S, int* bn_g, int* bn_d);
-// One cooperative launch: gate/up products into hd, then SiLU(gate)*up and the down products.
-cudaError_t launch_decode_ffn(const DecodeArgs& a, const CUtensorMap* maps, cudaStream_t st);
+// The decode forward as one cooperative launch.
+cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, cudaStream_t st);
 
 // out[t] = sum_k w[t,k] * Y[pair_to_row[t,k]] (+ acc[t]) + zsum[t] * x[t] + gamma_t * shy[t]
 struct CombineArgs {

@@ -10,114 +10,16 @@
 // into zero_accum; the single-CTA fused gate+top-K was too slow for 256 experts, so here
 // routing is one warp per token and the router spreads its columns over many blocks).
 #include "kernels.h"
+#include "route_dev.cuh"
 
 namespace moe {
 
 namespace {
 
-// Does candidate (va, ia) rank before (vb, ib)? Higher score first, lower id on a tie.
-__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
-
-// One warp routes one token. `L` is the token's fp32 logit row; `p` and `sel` are per-warp
-// shared scratch of R floats. Lane k < K writes slot k of idx/w; lane 0 writes zsum.
-__device__ void route_token_warp(const float* L, const float* logit_bias, const float* corr_bias,
-                                 int R, int E, int K, int scoring, int norm, float scale,
-                                 const uint32_t* forced, float* p, float* sel, uint32_t* idx_out,
-                                 float* w_out, float* zsum_out, uint32_t* idx_smem) {
-  const int lane = threadIdx.x & 31;
-  float mx = -INFINITY;
-  for (int r = lane; r < R; r += 32) {
-    float v = __ldcg(L + r) + (logit_bias ? logit_bias[r] : 0.0f);
-    p[r] = v;
-    mx = fmaxf(mx, v);
-  }
-  mx = warp_max(mx);
-  float den = 0.0f;
-  for (int r = lane; r < R; r += 32) {
-    float e = expf(p[r] - mx);
-    p[r] = e;
-    den += e;
-  }
-  den = warp_sum(den);
-  for (int r = lane; r < R; r += 32) {
-    float pr = p[r] / den;
-    p[r] = pr;
-    sel[r] = pr + ((scoring == MOE_SCORING_SOFTMAX_BIAS && corr_bias) ? corr_bias[r] : 0.0f);
-  }
-  __syncwarp();
-  uint32_t my_idx = 0;
-  for (int k = 0; k < K; ++k) {
-    int best;
-    if (forced) {
-      best = (int)forced[k];
-    } else {
-      float bv = -INFINITY;
-      best = 0x7fffffff;
-      for (int r = lane; r < R; r += 32) {
-        float v = sel[r];
-        if (ranks_before(v, r, bv, best)) { bv = v; best = r; }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        int oi = __shfl_xor_sync(0xffffffffu, best, o);
-        if (ranks_before(ov, oi, bv, best)) { bv = ov; best = oi; }
-      }
-      __syncwarp();
-      if (lane == 0) sel[best] = -INFINITY;   // taken
-      __syncwarp();
-    }
-    if (lane == k) my_idx = (uint32_t)best;
-  }
-  // weights: unbiased probabilities of the chosen ids, renormalised over all K slots
-  float wk = (lane < K) ? p[my_idx] : 0.0f;
-  float sum = warp_sum(wk);
-  if (norm) wk = wk / sum;
-  wk *= scale;
-  float z = (lane < K && (int)my_idx >= E) ? wk : 0.0f;
-  z = warp_sum(z);
-  if (lane < K) {
-    idx_out[lane] = my_idx;
-    w_out[lane] = wk;
-    if (idx_smem) idx_smem[lane] = my_idx;
-  }
-  if (lane == 0) *zsum_out = z;
-}
-
 // ------------------------------------------------------------------ small-N router
 
 constexpr int kRouterWarps = 4;      // router columns per block (one per warp)
 constexpr int kRouterTok = 16;       // most tokens per block
-
-// Block-wide exclusive scan of one value per thread (blockDim.x <= 1024, multiple of 32).
-__device__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_tot, uint32_t* total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  uint32_t inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    uint32_t n = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += n;
-  }
-  if (lane == 31) warp_tot[wid] = inc;
-  __syncthreads();
-  if (wid == 0) {
-    uint32_t t = lane < nw ? warp_tot[lane] : 0;
-    uint32_t ti = t;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      uint32_t n = __shfl_up_sync(0xffffffffu, ti, o);
-      if (lane >= o) ti += n;
-    }
-    if (lane < nw) warp_tot[lane] = ti - t;
-    if (lane == 31 && total) *total = ti;
-  }
-  __syncthreads();
-  uint32_t r = warp_tot[wid] + inc - v;
-  __syncthreads();
-  return r;
-}
 
 // Stable sort of te <= 1024 * k pairs inside one block (used by the fused decode tail).
 // idx_s: the pair expert ids in shared memory.
