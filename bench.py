@@ -113,10 +113,35 @@ def algorithmic(inp, rs):
     # the gate/up launch also runs the shared expert's gate/up projection (bf16 experts)
     gate_up_flops = 4.0 * rs["Z"] * H * I_ + 4.0 * s.num_tokens * H * S
     gate_up_bytes = rs["distinct"] * 2 * I_ * H * wb + (2 * S * H * 2)
-    # the decode chain's one streaming kernel reads every touched expert and the shared expert
-    ffn_bytes = rs["distinct"] * expert_bytes + 3 * S * H * 2
+    # the decode chain's one kernel reads every touched expert, the shared expert, the router
+    # and x, and writes out: all of the step's algorithmic bytes
+    ffn_bytes = bytes_
     return {"bytes": bytes_, "flops": flops, "gate_up_flops": gate_up_flops,
             "gate_up_bytes": gate_up_bytes, "ffn_bytes": ffn_bytes, "expert_bytes": expert_bytes}
+
+
+def measured_traffic(kernel, workload):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from the committed ncu
+    summary (profiles/traffic.json), or None when none was taken or the kernel's source has
+    changed since (the summary records the SHA-256 of the source file it measured)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    for e in rec.get("entries", []):
+        if e.get("kernel") != kernel or e.get("workload") != workload:
+            continue
+        src = os.path.join(ROOT, e["source"])
+        try:
+            with open(src, "rb") as f:
+                sha = hashlib.sha256(f.read()).hexdigest()
+        except OSError:
+            return None
+        return e["dram_bytes_per_launch"] if sha == e.get("source_sha256") else None
+    return None
 
 
 def kernels_per_step(B, cfg):
@@ -124,7 +149,7 @@ def kernels_per_step(B, cfg):
     decode = cfg.path == B.PATH_DECODE or (cfg.path == B.PATH_AUTO and cfg.num_tokens <= 16
                                             and cfg.weight_dtype == 0)
     if decode:
-        return 3            # router + top-K + sort, fused gate/up + down, combine
+        return 1            # router, top-K, sort, projections and combine in one kernel
     # router, top-K, 3 sort, gate/up GEMM, down GEMM, combine; FP8 experts add the token-row
     # quantiser and run the bf16 shared expert in two launches of its own
     if cfg.weight_dtype == 1:
@@ -314,10 +339,12 @@ def main():
         ms = float(t.item())
     value = world * shape.num_tokens / (ms / 1000.0)
     alg = r["alg"]
-    # dominant kernel of the decode chain: the fused gate/up + down weight-streaming kernel
-    # (timed as the gate/up stage), algorithmic bytes = every touched expert's weights once
+    # the decode chain's kernel (timed as the gate/up stage): router, top-K, sort, projections
+    # and combine; algorithmic bytes = every touched expert's weights once, the shared expert,
+    # the router, x and out
     gu_ms = r["stage_ms"]["gate_up"]
     gu_ach = alg["ffn_bytes"] / (gu_ms / 1000.0) / 1e9
+    traffic = measured_traffic("decode_forward_kernel", shape.name)
     step_ach = alg["bytes"] / (ms / 1000.0) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -328,9 +355,9 @@ def main():
                    "I": shape.inter, "S": shape.shared_inter, "parallelism": "replicas",
                    "l2": "flushed before every timed step (512 MiB write, untimed)",
                    "distinct_experts": r["rs"]["distinct"]},
-        "roofline": {"bound": "hbm", "kernel": "decode_ffn_kernel",
+        "roofline": {"bound": "hbm", "kernel": "decode_forward_kernel",
                      "achieved": gu_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": gu_ach / peaks["hbm_gbs"], "traffic": None,
+                     "frac": gu_ach / peaks["hbm_gbs"], "traffic": traffic,
                      "peak_src": peaks["src"],
                      "step_achieved_gbs": step_ach, "step_frac": step_ach / peaks["hbm_gbs"],
                      "algorithmic_bytes_per_launch": alg["ffn_bytes"],
