@@ -216,135 +216,19 @@ __device__ void router_rows(const DecodeArgs& a, uint8_t* scratch, size_t scratc
   }
 }
 
-// Sorts the warp's 32 * VPL (score, id) keys best first (higher score, lower id on a tie) with a
-// bitonic network; lane l holds positions l * VPL .. l * VPL + VPL - 1. The stage loops stay
-// rolled: this code runs once per launch, so its size (instruction fetch) costs more than its
-// loop overhead.
-template <int VPL>
-__device__ __forceinline__ void bitonic_best_first(float (&v)[VPL], int (&ix)[VPL]) {
-  const int lane = threadIdx.x & 31;
-  constexpr int n = 32 * VPL;
-#pragma unroll 1
-  for (int k = 2; k <= n; k <<= 1) {
-#pragma unroll 1
-    for (int dist = k >> 1; dist > 0; dist >>= 1) {
-      if (dist < VPL) {
-#pragma unroll
-        for (int d = 1; d < VPL; d <<= 1) {
-          if (dist == d) {
-#pragma unroll
-            for (int j = 0; j < VPL; ++j) {
-              const int jj = j ^ d;
-              if (jj > j) {   // the pair (j, jj) of this lane, j the lower position
-                const bool up = ((lane * VPL + j) & k) == 0;
-                const bool hi_better = ranks_before(v[jj], ix[jj], v[j], ix[j]);
-                if (up == hi_better) {   // the lower position keeps the better key when up
-                  const float tv = v[j];
-                  v[j] = v[jj];
-                  v[jj] = tv;
-                  const int ti = ix[j];
-                  ix[j] = ix[jj];
-                  ix[jj] = ti;
-                }
-              }
-            }
-          }
-        }
-      } else {
-        const int lm = dist / VPL;
-        const bool lower = (lane & lm) == 0;
-#pragma unroll
-        for (int j = 0; j < VPL; ++j) {
-          const float ov = __shfl_xor_sync(0xffffffffu, v[j], lm);
-          const int oi = __shfl_xor_sync(0xffffffffu, ix[j], lm);
-          const bool up = ((lane * VPL + j) & k) == 0;
-          const bool other_better = ranks_before(ov, oi, v[j], ix[j]);
-          // lower position: keeps the better key when up; upper position: the worse one
-          if ((lower == up) == other_better) {
-            v[j] = ov;
-            ix[j] = oi;
-          }
-        }
-      }
-    }
-  }
-}
-
-// Top-K of one token by one warp: softmax in registers, selection by a bitonic sort of the
-// selection scores (R <= 32 * VPL), weights from the unbiased probabilities. `p_w`: per-warp
-// shared scratch of R floats.
+// Top-K of one token by one warp (bitonic selection, route_dev.cuh), then the shared-expert
+// blend weight. `p_w`: per-warp shared scratch of R floats.
 template <int VPL>
 __device__ void topk_sort_warp(const DecodeArgs& a, int t, float* p_w, uint32_t* idx_s,
                                Routing& rt) {
   const int lane = threadIdx.x & 31;
-  const int R = a.R, K = a.K;
-  const float* L = a.logits + (size_t)t * R;
   const bool gated = a.S > 0 && a.sh_gate_vec;
   const float gd = gated ? __ldcg(&a.hdr->gate_dot[t]) : 0.0f;   // (used at the end)
-  float v[VPL];
-  int ix[VPL];
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int r = lane * VPL + j;
-    v[j] = r < R ? __ldcg(L + r) : 0.0f;
-  }
-  float mx = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int r = lane * VPL + j;
-    if (r < R) {
-      if (a.logit_bias) v[j] += a.logit_bias[r];
-      mx = fmaxf(mx, v[j]);
-    }
-  }
-  mx = warp_max(mx);
-  float den = 0.0f;
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int r = lane * VPL + j;
-    if (r < R) {
-      v[j] = expf(v[j] - mx);
-      den += v[j];
-    }
-  }
-  den = warp_sum(den);
-  const bool biased = a.scoring == MOE_SCORING_SOFTMAX_BIAS && a.corr_bias;
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int r = lane * VPL + j;
-    ix[j] = r;   // (padding keys: -inf with ids >= R, ordered after every real column)
-    if (r < R) {
-      const float pr = v[j] / den;
-      p_w[r] = pr;
-      v[j] = pr + (biased ? a.corr_bias[r] : 0.0f);
-    } else {
-      v[j] = -INFINITY;
-    }
-  }
-  uint32_t* idx_t = idx_s + t * K;
-  if (a.forced) {
-    if (lane < K) idx_t[lane] = a.forced[(size_t)t * K + lane];
-  } else {
-    bitonic_best_first<VPL>(v, ix);
-#pragma unroll
-    for (int j = 0; j < VPL; ++j)
-      if (lane * VPL + j < K) idx_t[lane * VPL + j] = (uint32_t)ix[j];
-  }
-  __syncwarp();
-  // weights: unbiased probabilities of the chosen ids, renormalised over all K slots
-  const uint32_t my_idx = lane < K ? idx_t[lane] : 0u;
-  float wk = lane < K ? p_w[my_idx < (uint32_t)R ? my_idx : 0u] : 0.0f;
-  const float sum = warp_sum(wk);
-  if (a.norm) wk = wk / sum;
-  wk *= a.scale;
-  float z = (lane < K && (int)my_idx >= a.E) ? wk : 0.0f;
-  z = warp_sum(z);
-  if (lane < K) rt.w[t * K + lane] = wk;
-  if (lane == 0) {
-    rt.zsum[t] = z;
-    // shared-expert blend weight sigmoid(x[t] . g), or 1 without a gate
-    rt.gamma[t] = gated ? 1.0f / (1.0f + expf(-gd)) : 1.0f;
-  }
+  route_token_warp_sort<VPL>(a.logits + (size_t)t * a.R, a.logit_bias, a.corr_bias, a.R, a.E,
+                             a.K, a.scoring, a.norm, a.scale,
+                             a.forced ? a.forced + (size_t)t * a.K : nullptr, p_w,
+                             idx_s + t * a.K, rt.w + t * a.K, rt.zsum + t);
+  if (lane == 0) rt.gamma[t] = gated ? 1.0f / (1.0f + expf(-gd)) : 1.0f;
 }
 
 // Wide routers (R > 256): K rounds of a warp arg-max (route_token_warp_reg), then the same

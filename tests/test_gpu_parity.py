@@ -47,6 +47,15 @@ SMALL = {
     "wide_small": I.PREFILL.with_(name="wide_small", num_tokens=1000, hidden=1024,
                                   num_experts=8, router_width=8, top_k=2, inter=384,
                                   shared_inter=128, zipf_s=0.0, shared_gated=True),
+    # decode-sized batches on both chains: identity experts and a router wider than 256 columns
+    # (the fused decode kernel's arg-max-rounds top-K), 128-row weight tiles (H, I, S not
+    # multiples of 256), a full 16-token batch
+    "zero_expert_decode": I.ZERO_EXPERT.with_(name="zero_expert_decode", num_tokens=9,
+                                              hidden=512, num_experts=256, router_width=384,
+                                              top_k=8, inter=256),
+    "odd_tiles_decode": I.DECODE.with_(name="odd_tiles_decode", num_tokens=16, hidden=384,
+                                       num_experts=24, router_width=24, top_k=3, inter=384,
+                                       shared_inter=128),
 }
 
 
