@@ -120,11 +120,20 @@ def algorithmic(inp, rs):
             "gate_up_bytes": gate_up_bytes, "ffn_bytes": ffn_bytes, "expert_bytes": expert_bytes}
 
 
+def sources_sha256(paths):
+    """SHA-256 over the bytes of the given repository files, in order."""
+    import hashlib
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def measured_traffic(kernel, workload):
     """DRAM bytes (read + write) per launch of `kernel` on `workload` from the committed ncu
-    summary (profiles/traffic.json), or None when none was taken or the kernel's source has
-    changed since (the summary records the SHA-256 of the source file it measured)."""
-    import hashlib
+    summary (profiles/traffic.json), or None when none was taken or the kernel's sources have
+    changed since (the summary records the SHA-256 of the source files it measured)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -134,13 +143,11 @@ def measured_traffic(kernel, workload):
     for e in rec.get("entries", []):
         if e.get("kernel") != kernel or e.get("workload") != workload:
             continue
-        src = os.path.join(ROOT, e["source"])
         try:
-            with open(src, "rb") as f:
-                sha = hashlib.sha256(f.read()).hexdigest()
-        except OSError:
+            sha = sources_sha256(e["sources"])
+        except (OSError, KeyError):
             return None
-        return e["dram_bytes_per_launch"] if sha == e.get("source_sha256") else None
+        return e["dram_bytes_per_launch"] if sha == e.get("sources_sha256") else None
     return None
 
 
@@ -155,6 +162,19 @@ def kernels_per_step(B, cfg):
     if cfg.weight_dtype == 1:
         return 9 + (2 if cfg.shared_inter else 0)
     return 8
+
+
+def replicas_value(ms_local, tokens_per_replica, device="cpu"):
+    """Independent replicas, one per rank: the job's time is the slowest rank's and its
+    throughput every rank's tokens over that time. Returns (ms, tokens/s)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    ms = ms_local
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * tokens_per_replica / (ms / 1000.0)
 
 
 def barrier():
@@ -212,6 +232,7 @@ def time_ours(B, shape, steps, warmup, dev, peaks, with_e2e=True):
            "clocks": clk.summary(), "wall_s": t_wall,
            "launches_per_step": kernels_per_step(B, blk.cfg)}
     if with_e2e:
+        res["graph"] = time_graph(B, blk, inp, out, flush, steps, warmup)
         hx = torch.empty(inp.x.shape, dtype=inp.x.dtype, pin_memory=True)
         hx.copy_(inp.x.cpu())
         ho = torch.empty(inp.x.shape, dtype=inp.x.dtype, pin_memory=True)
@@ -231,6 +252,35 @@ def time_ours(B, shape, steps, warmup, dev, peaks, with_e2e=True):
         res["e2e_ms"] = statistics.mean(e2e)
         res["io_bytes"] = hx.numel() * hx.element_size()
     return res
+
+
+def time_graph(B, blk, inp, out, flush, steps, warmup):
+    """The same forward captured once in a CUDA graph and replayed (L2 flushed before each
+    replay, outside the graph). Returns ms per replay, or the reason capture failed."""
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            B.moe_forward(blk.cfg, blk.weights, inp.x, out, blk.workspace, side)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            B.moe_forward(blk.cfg, blk.weights, inp.x, out, blk.workspace,
+                          torch.cuda.current_stream())
+        times = []
+        for i in range(warmup + steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            if i >= warmup:
+                times.append(a.elapsed_time(b))
+        return {"ms_per_step": statistics.mean(times)}
+    except Exception as exc:   # reported, not fatal: the stream-launched number stands
+        return {"error": f"{type(exc).__name__}: {exc}"[:300]}
 
 
 def cpu_oracle_tokens_per_s(inp, budget_s=12.0, max_tokens=None):
@@ -331,13 +381,7 @@ def main():
         return
 
     r = time_ours(B, shape, args.steps, warmup, dev, peaks)
-    ms = r["ms"]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=f"cuda:{dev}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * shape.num_tokens / (ms / 1000.0)
+    ms, value = replicas_value(r["ms"], shape.num_tokens, f"cuda:{dev}")
     alg = r["alg"]
     # the decode chain's kernel (timed as the gate/up stage): router, top-K, sort, projections
     # and combine; algorithmic bytes = every touched expert's weights once, the shared expert,
@@ -367,19 +411,27 @@ def main():
         "clocks": r["clocks"],
         "e2e": {"value": world * shape.num_tokens / (r["e2e_ms"] / 1000.0), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["io_bytes"], "d2h_bytes_per_step": r["io_bytes"]},
+        "graph_replay": (dict(r["graph"], value=world * shape.num_tokens /
+                              (r["graph"]["ms_per_step"] / 1000.0), unit="tokens/s")
+                         if "ms_per_step" in r["graph"] else r["graph"]),
     }
     if not args.no_prefill:
         p = time_ours(B, I.PREFILL, max(3, args.steps // 2), warmup, dev, peaks, with_e2e=False)
         pa = p["alg"]
         gu = p["stage_ms"]["gate_up"]
         gu_tf = pa["gate_up_flops"] / (gu / 1000.0) / 1e12
+        p_traffic = measured_traffic("gemm_bf16_kernel<256,SwiGLU>", I.PREFILL.name)
         line["prefill"] = {
             "workload": I.PREFILL.name, "value": I.PREFILL.num_tokens / (p["ms"] / 1000.0),
             "unit": "tokens/s", "ms_per_step": p["ms"],
             "stage_us": {k: 1000 * v for k, v in p["stage_ms"].items()},
             "roofline": {"bound": "tensor", "kernel": "gemm_bf16_kernel<256,SwiGLU>",
                          "achieved": gu_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": gu_tf / peaks["bf16_tflops"], "traffic": None,
+                         "frac": gu_tf / peaks["bf16_tflops"], "traffic": p_traffic,
+                         # the same launch against the HBM roofline: measured DRAM bytes
+                         # (ncu, one launch) over its CUDA-event time
+                         "hbm_frac": (p_traffic / (gu / 1000.0) / 1e9 / peaks["hbm_gbs"]
+                                      if p_traffic else None),
                          "step_tflops": pa["flops"] / (p["ms"] / 1000.0) / 1e12,
                          "step_frac": pa["flops"] / (p["ms"] / 1000.0) / 1e12 / peaks["bf16_tflops"]},
             "Z": p["rs"]["Z"], "max_expert_rows": int(p["rs"]["counts"].max()),

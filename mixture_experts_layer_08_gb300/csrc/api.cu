@@ -77,16 +77,6 @@ moe_status_t validate_config(const moe_config_t* c) {
   return MOE_OK;
 }
 
-// Contraction parts of the tensor-core router GEMM (N > kSmallRouterMaxTokens): enough
-// (m-tile, part) pairs to cover the SMs, each part at least four 64-wide blocks.
-int router_splits(const moe_config_t* c) {
-  const int tiles = ((c->num_tokens + 127) / 128) * ((c->router_width + 127) / 128);
-  const int kb = c->hidden / 64;
-  int s = 1;
-  while (s < 8 && tiles * s < 128 && kb % (2 * s) == 0 && kb / (2 * s) >= 4) s *= 2;
-  return s;
-}
-
 Layout make_layout(const moe_config_t* c) {
   Layout L{};
   const size_t N = c->num_tokens, H = c->hidden, E = c->num_experts, R = c->router_width;
@@ -98,7 +88,7 @@ Layout make_layout(const moe_config_t* c) {
   L.max_mtiles = (int)((te < E ? te : E) + te / 128);
   size_t sz[R_NUM] = {};
   sz[R_HDR] = sizeof(WsHeader);
-  sz[R_LOGITS] = N * R * 4 * (size_t)(N > (size_t)kSmallRouterMaxTokens ? router_splits(c) : 1);
+  sz[R_LOGITS] = N * R * 4;
   sz[R_IDX] = te * 4;
   sz[R_W] = te * 4;
   sz[R_ZSUM] = N * 4;
@@ -326,12 +316,6 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
     g.p[0].out = ra.logits;
     g.p[0].ldo = c->router_width;
     g.p[0].n_valid = c->router_width;
-    // a few output tiles only: split the contraction so the grid fills the GPU; the top-K
-    // kernel adds the partial logits in order
-    g.p[0].k_splits = router_splits(c);
-    g.p[0].split_stride = (size_t)c->num_tokens * c->router_width;
-    ra.logit_splits = g.p[0].k_splits;
-    ra.split_stride = g.p[0].split_stride;
     g.status = hdr;
     CK(launch_gemm_bf16(kGemmStoreF32, 128, maps, g, num_sms(), st));
   }

@@ -45,7 +45,7 @@ struct Cfg {
 
 // Per-tile view of the problem it belongs to (selected without dynamic param indexing).
 struct Tile {
-  int p, e, row0, row1, n, kb0, num_kb, b_rows_per_expert;
+  int p, e, row0, row1, n, num_kb, b_rows_per_expert;
   void* out;
   int ldo, n_valid;
 };
@@ -54,20 +54,14 @@ __device__ __forceinline__ int problem_mtiles(const GemmProblem& q) {
   return q.tiles ? (int)q.count->num_mtiles : (q.dense_m + kBM - 1) / kBM;
 }
 
-__device__ __forceinline__ int problem_splits(const GemmProblem& q) {
-  return q.k_splits > 1 ? q.k_splits : 1;
-}
-
 __device__ __forceinline__ void tile_of(const GemmArgs& g, int tot0, int tile, Tile& t) {
   const bool second = tile >= tot0;
   const GemmProblem& q0 = g.p[0];
   const GemmProblem& q1 = g.p[1];
   const int local = second ? tile - tot0 : tile;
   const int n_tiles = second ? q1.n_tiles : q0.n_tiles;
-  const int splits = problem_splits(second ? q1 : q0);
   const int4* tiles = second ? q1.tiles : q0.tiles;
-  const int ms = local / n_tiles;          // (m-tile, contraction part), n fastest
-  const int m = ms / splits, ks = ms - m * splits;
+  const int m = local / n_tiles;
   t.p = second ? 1 : 0;
   t.n = local % n_tiles;
   if (tiles) {
@@ -80,13 +74,9 @@ __device__ __forceinline__ void tile_of(const GemmArgs& g, int tot0, int tile, T
     t.row0 = m * kBM;
     t.row1 = min(second ? q1.dense_m : q0.dense_m, t.row0 + kBM);
   }
-  const int kb_all = second ? q1.num_kb : q0.num_kb;
-  t.num_kb = kb_all / splits;
-  t.kb0 = ks * t.num_kb;
+  t.num_kb = second ? q1.num_kb : q0.num_kb;
   t.b_rows_per_expert = second ? q1.b_rows_per_expert : q0.b_rows_per_expert;
   t.out = second ? q1.out : q0.out;
-  if (splits > 1)
-    t.out = static_cast<float*>(t.out) + (size_t)ks * (second ? q1.split_stride : q0.split_stride);
   t.ldo = second ? q1.ldo : q0.ldo;
   t.n_valid = second ? q1.n_valid : q0.n_valid;
 }
@@ -143,9 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int tot0 = problem_mtiles(g.p[0]) * problem_splits(g.p[0]) * g.p[0].n_tiles;
-  const int total =
-      tot0 + (g.nprob > 1 ? problem_mtiles(g.p[1]) * problem_splits(g.p[1]) * g.p[1].n_tiles : 0);
+  const int tot0 = problem_mtiles(g.p[0]) * g.p[0].n_tiles;
+  const int total = tot0 + (g.nprob > 1 ? problem_mtiles(g.p[1]) * g.p[1].n_tiles : 0);
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------ TMA producer
@@ -163,12 +152,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int brow = t.e * t.b_rows_per_expert + t.n * b_rows;
       for (int kb = 0; kb < t.num_kb; ++kb) {
         if (!mbar_wait(&empty[s], ph ^ 1, hdr)) { ok = false; break; }
-        const int kx = (t.kb0 + kb) * kBK;
         mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-        tma_load_2d(sA + s * kATileBytes, ma, kx, t.row0, &full[s]);
-        tma_load_2d(sB + s * C::kBTileBytes, mb0, kx, brow, &full[s]);
+        tma_load_2d(sA + s * kATileBytes, ma, kb * kBK, t.row0, &full[s]);
+        tma_load_2d(sB + s * C::kBTileBytes, mb0, kb * kBK, brow, &full[s]);
         if (MODE == kGemmSwiGLU)
-          tma_load_2d(sB + s * C::kBTileBytes + (BN / 2) * 128, mb1, kx, brow, &full[s]);
+          tma_load_2d(sB + s * C::kBTileBytes + (BN / 2) * 128, mb1, kb * kBK, brow, &full[s]);
         ++issued;
         if (++s == S) { s = 0; ph ^= 1; }
       }
@@ -300,9 +288,8 @@ cudaError_t launch_t(const CUtensorMap maps[2][3], const GemmArgs& g, int num_sm
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  auto splits = [](const GemmProblem& q) { return q.k_splits > 1 ? q.k_splits : 1; };
-  int max_tiles = g.p[0].max_mtiles * g.p[0].n_tiles * splits(g.p[0]);
-  if (g.nprob > 1) max_tiles += g.p[1].max_mtiles * g.p[1].n_tiles * splits(g.p[1]);
+  int max_tiles = g.p[0].max_mtiles * g.p[0].n_tiles;
+  if (g.nprob > 1) max_tiles += g.p[1].max_mtiles * g.p[1].n_tiles;
   int grid = max_tiles < num_sms ? max_tiles : num_sms;
   if (grid < 1) grid = 1;
   const int j = g.nprob > 1 ? 1 : 0;   // unused maps of a one-problem launch repeat problem 0's

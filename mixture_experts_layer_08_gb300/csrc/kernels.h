@@ -37,9 +37,7 @@ struct RouteArgs {
   const uint32_t* forced;          // [N,K] or null
   int N, H, E, R, K, scoring, norm;
   float scale;
-  float* logits;                   // [N,R], or logit_splits partial sums split_stride apart
-  int logit_splits;                // 0 or 1: one buffer
-  size_t split_stride;             // floats
+  float* logits;                   // [N,R]
   uint32_t* idx;                   // [N,K]
   float* w;                        // [N,K]
   float* zsum;                     // [N]
@@ -160,9 +158,6 @@ struct GemmProblem {
   void* out;
   int ldo;                         // elements
   int n_valid;                     // valid output columns (fp32 store mode)
-  int k_splits;                    // fp32 store mode: the contraction split in k_splits parts
-                                   // (0 or 1: none), part s written at out + s * split_stride
-  size_t split_stride;             // elements
 };
 
 // Up to two problems share one persistent launch (problem 0's tiles first), e.g. the shared

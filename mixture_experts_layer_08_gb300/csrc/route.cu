@@ -157,28 +157,18 @@ __global__ void __launch_bounds__(32 * kRouterWarps) router_small_kernel(RouteAr
   if (threadIdx.x == 0) a.hdr->done_blocks = 0;
 }
 
-// One warp per token, scores held in registers; the logits may arrive as partial sums.
+// One warp per token (with thousands of tokens in flight the shared-memory version keeps up
+// better than the register-resident ones, which win only for a lone warp).
 __global__ void __launch_bounds__(256) topk_kernel(RouteArgs a) {
-  __shared__ float p_s[8 * 256];   // per-warp probabilities (bitonic path: R <= 256)
+  extern __shared__ __align__(16) float sm[];
   const int wid = threadIdx.x >> 5;
   const int t = blockIdx.x * 8 + wid;
   if (t >= a.N) return;
-  const int splits = a.logit_splits > 1 ? a.logit_splits : 1;
-  const float* L = a.logits + (size_t)t * a.R;
-  const uint32_t* f = a.forced ? a.forced + (size_t)t * a.K : nullptr;
-  uint32_t* io = a.idx + (size_t)t * a.K;
-  float* wo = a.w + (size_t)t * a.K;
-  if (a.R <= 128)
-    route_token_warp_sort<4>(L, a.logit_bias, a.corr_bias, a.R, a.E, a.K, a.scoring, a.norm,
-                             a.scale, f, p_s + wid * 256, io, wo, a.zsum + t, splits,
-                             a.split_stride);
-  else if (a.R <= 256)
-    route_token_warp_sort<8>(L, a.logit_bias, a.corr_bias, a.R, a.E, a.K, a.scoring, a.norm,
-                             a.scale, f, p_s + wid * 256, io, wo, a.zsum + t, splits,
-                             a.split_stride);
-  else
-    route_token_warp_fast(L, a.logit_bias, a.corr_bias, a.R, a.E, a.K, a.scoring, a.norm,
-                          a.scale, f, io, wo, a.zsum + t, splits, a.split_stride);
+  float* p = sm + wid * 2 * a.R;
+  route_token_warp(a.logits + (size_t)t * a.R, a.logit_bias, a.corr_bias, a.R, a.E, a.K,
+                   a.scoring, a.norm, a.scale, a.forced ? a.forced + (size_t)t * a.K : nullptr,
+                   p, p + a.R, a.idx + (size_t)t * a.K, a.w + (size_t)t * a.K, a.zsum + t,
+                   nullptr);
 }
 
 // ------------------------------------------------------------------ large-N sort
@@ -372,7 +362,13 @@ cudaError_t launch_router_small(const RouteArgs& a, const SortArgs& s, bool fuse
 }
 
 cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st) {
-  topk_kernel<<<(a.N + 7) / 8, 256, 0, st>>>(a);
+  size_t sm = (size_t)8 * 2 * a.R * 4;
+  if (sm > 32 * 1024) {
+    cudaError_t e =
+        cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+  }
+  topk_kernel<<<(a.N + 7) / 8, 256, sm, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -98,30 +98,17 @@ __device__ void route_token_warp(const float* L, const float* logit_bias, const 
 // Register-resident variant of route_token_warp for R <= 32 * VPL: each lane holds the scores
 // of router columns lane, lane + 32, ...; K rounds of a warp arg-max (same order: higher
 // selection score first, lower id on a tie). Lane k < K writes slot k; lane 0 writes zsum.
-// The logits may come in `splits` partial sums `split_stride` floats apart (a split
-// contraction), added here in order.
 template <int VPL>
 __device__ void route_token_warp_reg(const float* L, const float* logit_bias,
                                      const float* corr_bias, int R, int E, int K, int scoring,
                                      int norm, float scale, const uint32_t* forced,
-                                     uint32_t* idx_out, float* w_out, float* zsum_out,
-                                     int splits = 1, size_t split_stride = 0) {
+                                     uint32_t* idx_out, float* w_out, float* zsum_out) {
   const int lane = threadIdx.x & 31;
   float v[VPL], sel[VPL];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int r = i * 32 + lane;
     v[i] = r < R ? __ldcg(L + r) : 0.0f;
-  }
-  for (int sp = 1; sp < splits; ++sp) {
-    float u[VPL];
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      const int r = i * 32 + lane;
-      u[i] = r < R ? __ldcg(L + (size_t)sp * split_stride + r) : 0.0f;
-    }
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) v[i] += u[i];
   }
   float mx = -INFINITY;
 #pragma unroll
@@ -213,20 +200,19 @@ __device__ __forceinline__ void route_token_warp_fast(const float* L, const floa
                                                       const float* corr_bias, int R, int E, int K,
                                                       int scoring, int norm, float scale,
                                                       const uint32_t* forced, uint32_t* idx_out,
-                                                      float* w_out, float* zsum_out,
-                                                      int splits = 1, size_t split_stride = 0) {
+                                                      float* w_out, float* zsum_out) {
   if (R <= 128)
     route_token_warp_reg<4>(L, logit_bias, corr_bias, R, E, K, scoring, norm, scale, forced,
-                            idx_out, w_out, zsum_out, splits, split_stride);
+                            idx_out, w_out, zsum_out);
   else if (R <= 256)
     route_token_warp_reg<8>(L, logit_bias, corr_bias, R, E, K, scoring, norm, scale, forced,
-                            idx_out, w_out, zsum_out, splits, split_stride);
+                            idx_out, w_out, zsum_out);
   else if (R <= 512)
     route_token_warp_reg<16>(L, logit_bias, corr_bias, R, E, K, scoring, norm, scale, forced,
-                             idx_out, w_out, zsum_out, splits, split_stride);
+                             idx_out, w_out, zsum_out);
   else
     route_token_warp_reg<32>(L, logit_bias, corr_bias, R, E, K, scoring, norm, scale, forced,
-                             idx_out, w_out, zsum_out, splits, split_stride);
+                             idx_out, w_out, zsum_out);
 }
 
 // Sorts the warp's 32 * VPL (score, id) keys best first (higher score, lower id on a tie) with a
@@ -285,15 +271,13 @@ __device__ __forceinline__ void bitonic_best_first(float (&v)[VPL], int (&ix)[VP
 
 // One warp routes one token: softmax in registers, selection by a bitonic sort of the
 // selection scores (R <= 32 * VPL; lane l holds columns l * VPL .. l * VPL + VPL - 1), weights
-// from the unbiased probabilities. The logits may come in `splits` partial sums
-// `split_stride` floats apart (added in order). `p_w`: per-warp shared scratch of R floats.
+// from the unbiased probabilities. `p_w`: per-warp shared scratch of R floats.
 // Lane k < K writes slot k of idx/w; lane 0 writes zsum.
 template <int VPL>
 __device__ void route_token_warp_sort(const float* L, const float* logit_bias,
                                       const float* corr_bias, int R, int E, int K, int scoring,
                                       int norm, float scale, const uint32_t* forced, float* p_w,
-                                      uint32_t* idx_out, float* w_out, float* zsum_out,
-                                      int splits = 1, size_t split_stride = 0) {
+                                      uint32_t* idx_out, float* w_out, float* zsum_out) {
   const int lane = threadIdx.x & 31;
   float v[VPL];
   int ix[VPL];
@@ -301,16 +285,6 @@ __device__ void route_token_warp_sort(const float* L, const float* logit_bias,
   for (int j = 0; j < VPL; ++j) {
     const int r = lane * VPL + j;
     v[j] = r < R ? __ldcg(L + r) : 0.0f;
-  }
-  for (int sp = 1; sp < splits; ++sp) {
-    float u[VPL];
-#pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      const int r = lane * VPL + j;
-      u[j] = r < R ? __ldcg(L + (size_t)sp * split_stride + r) : 0.0f;
-    }
-#pragma unroll
-    for (int j = 0; j < VPL; ++j) v[j] += u[j];
   }
   float mx = -INFINITY;
 #pragma unroll
