@@ -273,8 +273,22 @@ __global__ void __launch_bounds__(256) sort_scatter_kernel(SortArgs s, const __n
   }
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
   if (xp) {
+    // all of this lane's loads in flight before the stores; the copy is read once, by the
+    // GEMM, so it is written evict-first
     uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)row * H);
-    for (int c = lane; c < H / 8; c += 32) dst[c] = src[c];
+    for (int c0 = 0; c0 < H / 8; c0 += 8 * 32) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < H / 8) v[u] = __ldg(src + c);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < H / 8) __stcs(dst + c, v[u]);
+      }
+    }
   }
   if (xq) {
     // E4M3 codes and 1x128 scales of the token row (quantised once per token)
