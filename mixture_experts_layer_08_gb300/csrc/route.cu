@@ -294,7 +294,19 @@ __global__ void __launch_bounds__(256) sort_scatter_kernel(SortArgs s, const __n
     // E4M3 codes and 1x128 scales of the token row (quantised once per token)
     const uint4* qsrc = reinterpret_cast<const uint4*>(s.xq_tok + (size_t)t * H);
     uint4* qdst = reinterpret_cast<uint4*>(xq + (size_t)row * H);
-    for (int c = lane; c < H / 16; c += 32) qdst[c] = qsrc[c];
+    for (int c0 = 0; c0 < H / 16; c0 += 8 * 32) {
+      uint4 v[8];   // loads in flight before the stores; the copy is read once
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < H / 16) v[u] = __ldg(qsrc + c);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < H / 16) __stcs(qdst + c, v[u]);
+      }
+    }
     for (int g = lane; g < H / 128; g += 32)
       xsc[(size_t)g * s.te + row] = s.xs_tok[(size_t)g * s.N + t];
   }
@@ -309,32 +321,40 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* x,
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= N) return;
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-  for (int c0 = 0; c0 < H / 8; c0 += 32) {
-    const int c = c0 + lane;
-    const bool on = c < H / 8;
-    float f[8];
+  for (int c4 = 0; c4 < H / 8; c4 += 4 * 32) {
+    uint4 raw[4];   // four loads in flight before the first group is quantised
 #pragma unroll
-    for (int i = 0; i < 8; ++i) f[i] = 0.0f;
-    if (on) bf16x8_to_f32(src[c], f);
-    float am = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-    const float s = am > 0.0f ? __fdiv_rn(am, 448.0f) : 1.0f;
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int i = 0; i < 4; i += 2) {
-      lo |= (uint32_t)__nv_cvt_float2_to_fp8x2(
-                make_float2(__fdiv_rn(f[i], s), __fdiv_rn(f[i + 1], s)), __NV_SATFINITE,
-                __NV_E4M3) << (8 * i);
-      hi |= (uint32_t)__nv_cvt_float2_to_fp8x2(
-                make_float2(__fdiv_rn(f[4 + i], s), __fdiv_rn(f[5 + i], s)), __NV_SATFINITE,
-                __NV_E4M3) << (8 * i);
+    for (int u = 0; u < 4; ++u) {
+      const int c = c4 + u * 32 + lane;
+      raw[u] = c < H / 8 ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
     }
-    if (on) {
-      reinterpret_cast<uint2*>(q + (size_t)t * H)[c] = make_uint2(lo, hi);
-      if ((lane & 15) == 0) sc[(size_t)(c / 16) * N + t] = s;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (c4 + u * 32 >= H / 8) break;   // (warp-uniform)
+      const int c = c4 + u * 32 + lane;
+      const bool on = c < H / 8;
+      float f[8];
+      bf16x8_to_f32(raw[u], f);
+      float am = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      const float s = am > 0.0f ? __fdiv_rn(am, 448.0f) : 1.0f;
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int i = 0; i < 4; i += 2) {
+        lo |= (uint32_t)__nv_cvt_float2_to_fp8x2(
+                  make_float2(__fdiv_rn(f[i], s), __fdiv_rn(f[i + 1], s)), __NV_SATFINITE,
+                  __NV_E4M3) << (8 * i);
+        hi |= (uint32_t)__nv_cvt_float2_to_fp8x2(
+                  make_float2(__fdiv_rn(f[4 + i], s), __fdiv_rn(f[5 + i], s)), __NV_SATFINITE,
+                  __NV_E4M3) << (8 * i);
+      }
+      if (on) {
+        reinterpret_cast<uint2*>(q + (size_t)t * H)[c] = make_uint2(lo, hi);
+        if ((lane & 15) == 0) sc[(size_t)(c / 16) * N + t] = s;
+      }
     }
   }
 }
