@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdio>
+#include <map>
 #include <mutex>
 
 #include "kernels.h"
@@ -151,6 +152,24 @@ int num_sms() {
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+}  // namespace
+
+cudaError_t moe::ensure_dyn_smem(const void* func, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> have;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  size_t& cur = have[{dev, func}];
+  if (bytes <= cur) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) cur = bytes;
+  return e;
+}
+
+namespace {
 
 bool encode_fn() {
   std::lock_guard<std::mutex> lk(g_mu);

@@ -46,6 +46,9 @@
 //              per run for the slot) or into the down output. Before the first down run of a
 //              slot, all four wait for the slot's gate/up count (other blocks; bounded spin)
 //              and build SiLU(gate)*up of its tokens as the bf16 A operand (128-byte swizzle).
+#include <mutex>
+#include <set>
+
 #include "kernels.h"
 #include "route_dev.cuh"
 
@@ -895,14 +898,26 @@ cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, 
                          (size_t)a.E * 4 + 160 + (size_t)kWarps * a.R * 4;
   if (scratch > (size_t)pl.stages * (kTokBytes + kWBytes)) return cudaErrorInvalidValue;
   const size_t sm = (size_t)fixed + (size_t)pl.stages * per_stage;
-  cudaError_t e =
-      cudaFuncSetAttribute(decode_forward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(decode_forward_kernel), sm);
   if (e != cudaSuccess) return e;
-  // the down phase waits on other blocks' gate/up work: all blocks must be resident
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_forward_kernel, kThreads, sm);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  // the down phase waits on other blocks' gate/up work: all blocks must be resident (checked
+  // once per device and shared-memory size)
+  {
+    static std::mutex mu;
+    static std::set<std::pair<int, size_t>> ok;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ok.count({dev, sm})) {
+      int per_sm = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_forward_kernel, kThreads,
+                                                        sm);
+      if (e != cudaSuccess) return e;
+      if (per_sm < 1) return cudaErrorInvalidConfiguration;
+      ok.insert({dev, sm});
+    }
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sm_count());
   cfg.blockDim = dim3(kThreads);

@@ -285,8 +285,7 @@ cudaError_t launch_t(const CUtensorMap maps[2][3], const GemmArgs& g, int num_sm
                      cudaStream_t st) {
   using C = Cfg<BN>;
   auto kern = gemm_bf16_kernel<BN, MODE>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
+  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(kern), C::kSmemBytes);
   if (e != cudaSuccess) return e;
   int max_tiles = g.p[0].max_mtiles * g.p[0].n_tiles;
   if (g.nprob > 1) max_tiles += g.p[1].max_mtiles * g.p[1].n_tiles;

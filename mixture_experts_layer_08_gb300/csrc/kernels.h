@@ -80,6 +80,10 @@ cudaError_t launch_sort(const SortArgs& s, const __nv_bfloat16* x, int H, __nv_b
 constexpr int kDecodeMaxTokens = 16;
 constexpr int kDecodeMaxPairs = 512;
 
+// Raises `func`'s dynamic shared memory limit on the current device to at least `bytes`,
+// calling the runtime only when the limit has to grow (not on every launch).
+cudaError_t ensure_dyn_smem(const void* func, size_t bytes);
+
 // Decode chain: the whole block forward of a few tokens in one cooperative launch -- router,
 // top-K and sort, gate/up and down projections of the active experts and the shared expert as
 // skinny tensor-core GEMMs (weights as the wide B operand, the tokens as A rows), combine.

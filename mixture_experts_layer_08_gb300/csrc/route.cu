@@ -377,8 +377,7 @@ cudaError_t launch_router_small_t(const RouteArgs& a, const SortArgs& s, bool fu
                              : 0;
   size_t sm = sm_x > sm_tail ? sm_x : sm_tail;
   if (sm > 32 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(router_small_kernel<NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(router_small_kernel<NT>), sm);
     if (e != cudaSuccess) return e;
   }
   router_small_kernel<NT><<<grid, 32 * kRouterWarps, sm, st>>>(a, s, fuse_tail ? 1 : 0);
@@ -398,8 +397,7 @@ cudaError_t launch_router_small(const RouteArgs& a, const SortArgs& s, bool fuse
 cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st) {
   size_t sm = (size_t)8 * 2 * a.R * 4;
   if (sm > 32 * 1024) {
-    cudaError_t e =
-        cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(topk_kernel), sm);
     if (e != cudaSuccess) return e;
   }
   topk_kernel<<<(a.N + 7) / 8, 256, sm, st>>>(a);
@@ -411,8 +409,7 @@ cudaError_t launch_sort(const SortArgs& s, const __nv_bfloat16* x, int H, __nv_b
   const int nblk = (s.te + kSortBlock - 1) / kSortBlock;
   size_t sm = (size_t)32 * s.E * 4;
   if (sm > 32 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(sort_count_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(sort_count_kernel), sm);
     if (e != cudaSuccess) return e;
   }
   sort_count_kernel<<<nblk, kSortBlock, sm, st>>>(s);
