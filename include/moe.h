@@ -64,7 +64,9 @@ typedef enum {
 
 typedef enum {
   MOE_PATH_AUTO = 0,            /* decode chain for bf16 experts and num_tokens <= 16, else grouped */
-  MOE_PATH_DECODE = 1,          /* weight-streaming GEMV chain (bf16 experts, num_tokens <= 16) */
+  MOE_PATH_DECODE = 1,          /* one cooperative kernel: routing, tcgen05 projections streaming
+                                   each touched expert's weights once, combine (bf16 experts,
+                                   num_tokens <= 16, inter and shared_inter <= 1024) */
   MOE_PATH_GROUPED = 2          /* sort + tcgen05 grouped GEMM chain (any num_tokens) */
 } moe_path_t;
 
@@ -91,9 +93,10 @@ typedef struct {
   int32_t norm_topk_prob;          /* nonzero: renormalise the K weights to sum 1 */
   float routed_scaling_factor;     /* multiplies every routing weight */
   int32_t weight_dtype;  /* moe_wdtype_t */
-  int32_t deterministic; /* nonzero: bitwise run-to-run reproducible (slot-ordered reduction);
-                            0: the decode chain accumulates the routed down projections with
-                            FP32 atomics */
+  int32_t deterministic; /* nonzero: bitwise run-to-run reproducible (slot-ordered reduction;
+                            partial sums meet pairwise, a + b == b + a); 0: the decode chain
+                            accumulates the weighted routed down projections into [N,H] with
+                            FP32 atomics in any order */
   int32_t path;          /* moe_path_t */
 } moe_config_t;
 
@@ -146,8 +149,9 @@ MOE_API moe_status_t moe_route(const moe_config_t *cfg, const moe_weights_t *wei
                        uint32_t *idx_out, float *w_out, float *zsum_out, uint32_t *offsets_out,
                        uint32_t *sorted_pairs_out, uint32_t *pair_to_row_out);
 
-/* Stages of one forward, in launch order, for moe_forward_profiled. The decode chain runs the
- * shared expert inside its gate/up and down launches, so its SHARED stage is empty. */
+/* Stages of one forward, in launch order, for moe_forward_profiled. The decode chain is one
+ * kernel: its ROUTE stage is the memset of the workspace header, its GATE_UP stage the kernel
+ * (routing, both projections, the shared expert and the combine), the other stages empty. */
 typedef enum {
   MOE_STAGE_ROUTE = 0,     /* router GEMM, scoring + top-K, sort (+ gather of expert rows) */
   MOE_STAGE_SHARED = 1,    /* shared expert gate/up + down (grouped chain) */

@@ -180,6 +180,34 @@ def test_decode_and_grouped_chains_agree(B):
 
 
 @pytest.mark.parametrize("path", [1, 2], ids=["decode", "grouped"])
+def test_forward_replays_from_a_cuda_graph(B, path):
+    """A forward captured once into a CUDA graph replays to the stream-launched result, bit for
+    bit (deterministic mode), on both chains."""
+    shape = I.DECODE.with_(num_tokens=8) if path == 1 else SMALL["prefill_zipf_small"]
+    dev = I.make_inputs(shape).to("cuda")
+    cfg = B.make_config(shape, True, path)
+    w = B.make_weights(dev)
+    ws = B.alloc_workspace(cfg)
+    ref = torch.empty_like(dev.x)
+    B.moe_forward(cfg, w, dev.x, ref, ws)
+    out = torch.zeros_like(dev.x)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):     # first call outside the capture (sets kernel attributes)
+        B.moe_forward(cfg, w, dev.x, out, ws, side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        B.moe_forward(cfg, w, dev.x, out, ws, torch.cuda.current_stream())
+    for _ in range(2):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("path", [1, 2], ids=["decode", "grouped"])
 def test_deterministic_mode_is_bitwise_stable(B, path):
     inp = I.make_inputs(I.DECODE.with_(num_tokens=12) if path == 1 else SMALL["prefill_zipf_small"])
     first = run_gpu(B, inp, path)[0]
