@@ -102,9 +102,9 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
 // of blocks times the barriers passed so far). Bounded: a timeout is reported and the block
 // carries on (its results are then not used).
 __device__ void grid_barrier(WsHeader* hdr, uint32_t target) {
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
+    __threadfence();   // (cumulative: the block's writes, ordered before it by the block barrier)
     atomicAdd(&hdr->done_blocks, 1u);
     if (ld_acquire(&hdr->done_blocks) < target) {
       const long long t0 = clock64();
@@ -113,7 +113,6 @@ __device__ void grid_barrier(WsHeader* hdr, uint32_t target) {
           report_timeout(hdr);
           break;
         }
-        __nanosleep(32);
       }
     }
     __threadfence();
@@ -169,9 +168,6 @@ __device__ void router_rows(const DecodeArgs& a, uint8_t* scratch, size_t scratc
     xs = reinterpret_cast<const __nv_bfloat16*>(scratch);
   }
   for (int r = r_first; r < rows; r += gridDim.x) {
-    float acc[kDecodeMaxTokens];
-#pragma unroll
-    for (int t = 0; t < kDecodeMaxTokens; ++t) acc[t] = 0.0f;
     const uint4* wr = row_ptr(r);
     for (int c0 = 0; c0 < chunks; c0 += kPer * kThreads) {
       if (r != r_first || c0 != 0) {   // (the first pass was loaded above)
@@ -181,30 +177,25 @@ __device__ void router_rows(const DecodeArgs& a, uint8_t* scratch, size_t scratc
           if (c < chunks) wv[q] = __ldg(wr + c);
         }
       }
+      // tokens in a rolled loop (run-once code: its size costs more than the loop), the
+      // warps' partial sums of each token accumulated in shared memory
+#pragma unroll 1
+      for (int t = 0; t < a.N; ++t) {
+        const uint4* xt = reinterpret_cast<const uint4*>(xs + (size_t)t * a.H);
+        float acc = 0.0f;
 #pragma unroll
-      for (int q = 0; q < kPer; ++q) {
-        const int c = c0 + q * kThreads + tid;
-        if (c < chunks) {
-          float wf[8];
-          bf16x8_to_f32(wv[q], wf);
+        for (int q = 0; q < kPer; ++q) {
+          const int c = c0 + q * kThreads + tid;
+          if (c < chunks) {
+            float wf[8], xf[8];
+            bf16x8_to_f32(wv[q], wf);
+            bf16x8_to_f32(xt[c], xf);
 #pragma unroll
-          for (int t = 0; t < kDecodeMaxTokens; ++t) {
-            if (t < a.N) {
-              float xf[8];
-              bf16x8_to_f32(reinterpret_cast<const uint4*>(xs + (size_t)t * a.H)[c], xf);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) acc[t] = fmaf(wf[i], xf[i], acc[t]);
-            }
+            for (int i = 0; i < 8; ++i) acc = fmaf(wf[i], xf[i], acc);
           }
         }
-      }
-    }
-    // block reduction: per token, the warps' sums in shared memory
-#pragma unroll
-    for (int t = 0; t < kDecodeMaxTokens; ++t) {
-      if (t < a.N) {
-        const float v = warp_sum(acc[t]);
-        if (lane == 0) red[t * kWarps + warp] = v;
+        acc = warp_sum(acc);
+        if (lane == 0) red[t * kWarps + warp] = (c0 == 0 ? 0.0f : red[t * kWarps + warp]) + acc;
       }
     }
     __syncthreads();
@@ -217,21 +208,6 @@ __device__ void router_rows(const DecodeArgs& a, uint8_t* scratch, size_t scratc
     }
     __syncthreads();
   }
-}
-
-// Top-K of one token by one warp (bitonic selection, route_dev.cuh), then the shared-expert
-// blend weight. `p_w`: per-warp shared scratch of R floats.
-template <int VPL>
-__device__ void topk_sort_warp(const DecodeArgs& a, int t, float* p_w, uint32_t* idx_s,
-                               Routing& rt) {
-  const int lane = threadIdx.x & 31;
-  const bool gated = a.S > 0 && a.sh_gate_vec;
-  const float gd = gated ? __ldcg(&a.hdr->gate_dot[t]) : 0.0f;   // (used at the end)
-  route_token_warp_sort<VPL>(a.logits + (size_t)t * a.R, a.logit_bias, a.corr_bias, a.R, a.E,
-                             a.K, a.scoring, a.norm, a.scale,
-                             a.forced ? a.forced + (size_t)t * a.K : nullptr, p_w,
-                             idx_s + t * a.K, rt.w + t * a.K, rt.zsum + t);
-  if (lane == 0) rt.gamma[t] = gated ? 1.0f / (1.0f + expf(-gd)) : 1.0f;
 }
 
 // Wide routers (R > 256): K rounds of a warp arg-max (route_token_warp_reg), then the same
@@ -248,83 +224,253 @@ __device__ void topk_rounds_warp(const DecodeArgs& a, int t, uint32_t* idx_s, Ro
   }
 }
 
+// Top-K of one token by one warp (R <= 32 * VPL). Lane l owns router columns l, l + 32, ...:
+// softmax (probabilities into p_t[R], kept for the weights), selection score = probability
+// (+ the correction bias). Each score becomes a 64-bit key (order-preserving score bits above
+// the complemented column id), so one unsigned compare orders by higher score, then lower id.
+// Every lane sorts its VPL keys in registers; then K rounds of a warp max over the lanes' heads,
+// the winning lane dropping its head. Also the shared-expert blend weight. This code runs once
+// per launch with a cold instruction cache, where every instruction costs a fetch: the loops
+// after the loads stay rolled over shared scratch (`p_t`, `cb_t`: R floats; `key_t`: R keys).
+template <int VPL>
+__device__ void token_topk(const DecodeArgs& a, int t, float* p_t, float* cb_t,
+                           unsigned long long* key_t, uint32_t* idx_t, Routing& rt) {
+  const int lane = threadIdx.x & 31;
+  const int R = a.R;
+  const float* L = a.logits + (size_t)t * R;
+  const bool gated = a.S > 0 && a.sh_gate_vec;
+  const bool biased = a.scoring == MOE_SCORING_SOFTMAX_BIAS && a.corr_bias;
+  const float gd = gated ? __ldcg(&a.hdr->gate_dot[t]) : 0.0f;
+  float v[VPL], cb[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {   // every load in flight at once
+    const int r = i * 32 + lane;
+    v[i] = r < R ? __ldcg(L + r) : 0.0f;
+    cb[i] = (biased && r < R) ? a.corr_bias[r] : 0.0f;
+    if (a.logit_bias && r < R) v[i] += a.logit_bias[r];
+  }
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int r = i * 32 + lane;
+    if (r < R) {
+      p_t[r] = v[i];
+      cb_t[r] = cb[i];
+    }
+  }
+  float mx = -INFINITY;
+#pragma unroll 1
+  for (int r = lane; r < R; r += 32) mx = fmaxf(mx, p_t[r]);
+  mx = warp_max(mx);
+  float den = 0.0f;
+#pragma unroll 1
+  for (int r = lane; r < R; r += 32) {
+    const float e = expf(p_t[r] - mx);
+    p_t[r] = e;
+    den += e;
+  }
+  den = warp_sum(den);
+#pragma unroll 1
+  for (int r = lane; r < R; r += 32) {
+    const float pr = p_t[r] / den;
+    p_t[r] = pr;
+    const float sc = pr + cb_t[r];
+    const uint32_t bits = sc == 0.0f ? 0u : __float_as_uint(sc);   // -0 ties with +0
+    const uint32_t ord = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+    key_t[r] = ((unsigned long long)ord << 32) | (uint32_t)~(uint32_t)r;
+  }
+  if (lane == 0) rt.gamma[t] = gated ? 1.0f / (1.0f + expf(-gd)) : 1.0f;
+  if (a.forced) {
+    if (lane < a.K) idx_t[lane] = a.forced[(size_t)t * a.K + lane];
+    return;
+  }
+  unsigned long long key[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int r = i * 32 + lane;
+    key[i] = r < R ? key_t[r] : 0ull;   // padding: below every real key
+  }
+  // each lane's keys, largest first (odd-even transposition network)
+#pragma unroll
+  for (int pass = 0; pass < VPL; ++pass) {
+#pragma unroll
+    for (int i = pass & 1; i + 1 < VPL; i += 2) {
+      const unsigned long long hi = key[i] > key[i + 1] ? key[i] : key[i + 1];
+      const unsigned long long lo = key[i] > key[i + 1] ? key[i + 1] : key[i];
+      key[i] = hi;
+      key[i + 1] = lo;
+    }
+  }
+#pragma unroll 1
+  for (int k = 0; k < a.K; ++k) {
+    unsigned long long best = key[0];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long ob = __shfl_xor_sync(0xffffffffu, best, o);
+      best = ob > best ? ob : best;
+    }
+    if (key[0] == best) {   // keys are unique: exactly one lane
+#pragma unroll
+      for (int i = 0; i + 1 < VPL; ++i) key[i] = key[i + 1];
+      key[VPL - 1] = 0ull;
+    }
+    if (lane == k) idx_t[k] = ~(uint32_t)best;
+  }
+}
+
+// Weights of one token's K chosen columns (warp): unbiased probabilities, renormalised over all K
+// slots, times the scaling factor; the identity-expert sum.
+__device__ void token_weights(const DecodeArgs& a, int t, const float* p_t,
+                              const uint32_t* idx_t, Routing& rt) {
+  const int lane = threadIdx.x & 31;
+  const int K = a.K;
+  const uint32_t my_idx = lane < K ? idx_t[lane] : 0u;
+  float wk = lane < K ? p_t[my_idx < (uint32_t)a.R ? my_idx : 0u] : 0.0f;
+  const float sum = warp_sum(wk);
+  if (a.norm) wk = wk / sum;
+  wk *= a.scale;
+  float z = (lane < K && (int)my_idx >= a.E) ? wk : 0.0f;
+  z = warp_sum(z);
+  if (lane < K) rt.w[t * K + lane] = wk;
+  if (lane == 0) rt.zsum[t] = z;
+}
+
 // Phase 1: the block's own copy of the routing. `scratch`: dynamic shared memory not yet in use.
-// The stable sort by expert takes a few block-wide steps: ranks of equal experts inside each
-// 32-pair chunk (match) and per-chunk counts; per expert, its first row (block scan) and each
-// chunk's first row; then every pair's row.
+// Top-K: one warp per token (token_topk up to 256 router columns, else K arg-max rounds). Then the
+// stable sort of the pairs by expert: one warp when there are at most 32 pairs, else block-wide
+// (ranks inside 32-pair chunks by match, per-chunk counts, block scans over the experts).
 __device__ void route_block(const DecodeArgs& a, Routing& rt, uint8_t* scratch) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-  const int R = a.R, E = a.E, K = a.K, te = a.te;
+  const int R = a.R, E = a.E, K = a.K, te = a.te, N = a.N;
   const int nch = (te + 31) / 32;                                      // 32-pair chunks
   uint32_t* idx_s = reinterpret_cast<uint32_t*>(scratch);              // [te]
   uint32_t* lrank_s = idx_s + te;                                      // [te]
   uint32_t* chunk_s = lrank_s + te;                                    // [nch][E]
   uint32_t* base_s = chunk_s + (size_t)nch * E;                        // [E] first rows
   uint32_t* scan_s = base_s + E;                                       // [33]
-  float* p_s = reinterpret_cast<float*>(scan_s + 40);                  // [warps][R]
-  for (int i = tid; i < nch * E; i += blockDim.x) chunk_s[i] = 0;
-  for (int t = warp; t < a.N; t += kWarps) {
-    if (R <= 128) topk_sort_warp<4>(a, t, p_s + warp * R, idx_s, rt);
-    else if (R <= 256) topk_sort_warp<8>(a, t, p_s + warp * R, idx_s, rt);
-    else topk_rounds_warp(a, t, idx_s, rt);
+  unsigned long long* k_s =
+      reinterpret_cast<unsigned long long*>(scratch + (((size_t)(scan_s + 40 - idx_s) * 4 + 7) & ~(size_t)7));
+  float* p_s = reinterpret_cast<float*>(k_s + (size_t)N * R);             // [N][R]
+  float* cb_s = p_s + (size_t)N * R;                                        // [N][R]
+  if (te > 32)
+    for (int i = tid; i < nch * E; i += blockDim.x) chunk_s[i] = 0;
+  for (int t = warp; t < N; t += kWarps) {
+    const size_t o = (size_t)t * R;
+    if (R <= 128) token_topk<4>(a, t, p_s + o, cb_s + o, k_s + o, idx_s + t * K, rt);
+    else if (R <= 256) token_topk<8>(a, t, p_s + o, cb_s + o, k_s + o, idx_s + t * K, rt);
+    else topk_rounds_warp(a, t, idx_s, rt);   // (weights included)
     __syncwarp();
   }
   __syncthreads();
-  // ranks inside each chunk, and the chunk's count of every expert (its group's last lane)
-  for (int j0 = 0; j0 < te; j0 += kThreads) {
-    const int j = j0 + tid;
-    const uint32_t e = j < te ? idx_s[j] : 0xFFFFFFFFu;
-    const bool real = j < te && (int)e < E;
-    const uint32_t m = __match_any_sync(0xffffffffu, real ? e : 0xFFFFFFFFu);
-    if (j < te) lrank_s[j] = (uint32_t)__popc(m & ((1u << lane) - 1u));
-    if (real && (m >> lane) == 1u) chunk_s[(size_t)(j >> 5) * E + e] = (uint32_t)__popc(m);
+  // the weights (R <= 256) need only idx and p: they run beside the sort (warps 1.. when one
+  // warp sorts, else ahead of it)
+  if (R <= 256) {
+    const int w0 = te <= 32 ? 1 : 0;
+    for (int t = warp - w0; t >= 0 && t < N; t += kWarps - w0)
+      token_weights(a, t, p_s + (size_t)t * R, idx_s + t * K, rt);
   }
-  __syncthreads();
-  // per expert: rows (sum over chunks), first row and slot (block scans), each chunk's first row
-  uint32_t carry_rows = 0, carry_slots = 0;
-  for (int e0 = 0; e0 < E; e0 += kThreads) {
-    const int e = e0 + tid;
-    uint32_t tot = 0;
-    if (e < E)
-      for (int c = 0; c < nch; ++c) tot += chunk_s[(size_t)c * E + e];
-    const uint32_t off = block_excl_scan(tot, scan_s, &scan_s[32]);
-    const uint32_t tot_rows = scan_s[32];
-    __syncthreads();
-    const uint32_t sl = block_excl_scan(tot > 0 ? 1u : 0u, scan_s, &scan_s[32]);
-    const uint32_t tot_slots = scan_s[32];
-    __syncthreads();
-    if (e < E) {
-      uint32_t row = carry_rows + off;
-      base_s[e] = row;
-      if (tot > 0) {
-        rt.slot_e[carry_slots + sl] = (uint16_t)e;
-        rt.slot_r0[carry_slots + sl] = (uint16_t)row;
-        rt.slot_n[carry_slots + sl] = (uint16_t)tot;
+  if (te <= 32) {
+    // one warp: lane j holds pair j; row = pairs of smaller experts + earlier pairs of its own;
+    // slot = distinct smaller experts
+    if (warp == 0) {
+      const bool valid = lane < te;
+      const uint32_t e = valid ? idx_s[lane] : 0xFFFFFFFFu;
+      const bool real = valid && (int)e < E;
+      const uint32_t m = __match_any_sync(0xffffffffu, real ? e : 0xFFFFFFFFu);
+      const uint32_t lrank = (uint32_t)__popc(m & ((1u << lane) - 1u));
+      const uint32_t reals = __ballot_sync(0xffffffffu, real);
+      const uint32_t leaders = __ballot_sync(0xffffffffu, real && lrank == 0);
+      uint32_t before = 0, slot = 0;
+#pragma unroll 1
+      for (int i = 0; i < 32; ++i) {
+        const uint32_t ei = __shfl_sync(0xffffffffu, e, i);
+        if (((reals >> i) & 1u) && ei < e) {
+          ++before;
+          if ((leaders >> i) & 1u) ++slot;
+        }
       }
-      for (int c = 0; c < nch; ++c) {
-        const uint32_t n = chunk_s[(size_t)c * E + e];
-        chunk_s[(size_t)c * E + e] = row;
-        row += n;
+      if (real) {
+        const uint32_t row = before + lrank;
+        rt.pair_row[lane] = (uint16_t)row;
+        rt.row_pair[row] = (uint16_t)lane;
+        rt.row_tok[row] = (uint16_t)(lane / K);
+        if (lrank == 0) {
+          rt.slot_e[slot] = (uint16_t)e;
+          rt.slot_r0[slot] = (uint16_t)before;
+          rt.slot_n[slot] = (uint16_t)__popc(m);
+        }
+      } else if (valid) {
+        rt.pair_row[lane] = kNoRow16;
+      }
+      if (lane == 0) {
+        rt.n_active = __popc(leaders);
+        rt.rows = __popc(reals);
       }
     }
-    carry_rows += tot_rows;
-    carry_slots += tot_slots;
-  }
-  if (tid == 0) {
-    rt.n_active = (int)carry_slots;
-    rt.rows = (int)carry_rows;
-  }
-  __syncthreads();
-  for (int j = tid; j < te; j += kThreads) {
-    const uint32_t e = idx_s[j];
-    if ((int)e >= E) {
-      rt.pair_row[j] = kNoRow16;
-      continue;
+    __syncthreads();
+    if (blockIdx.x == 0)   // first row of every expert, for the workspace copy below
+      for (int e = tid; e < E; e += blockDim.x) {
+        uint32_t n = 0;
+        for (int j = 0; j < te; ++j) n += (idx_s[j] < (uint32_t)e) ? 1u : 0u;
+        base_s[e] = n;
+      }
+  } else {
+    // ranks inside each chunk, and the chunk's count of every expert (its group's last lane)
+    for (int j0 = 0; j0 < te; j0 += kThreads) {
+      const int j = j0 + tid;
+      const uint32_t e = j < te ? idx_s[j] : 0xFFFFFFFFu;
+      const bool real = j < te && (int)e < E;
+      const uint32_t m = __match_any_sync(0xffffffffu, real ? e : 0xFFFFFFFFu);
+      if (j < te) lrank_s[j] = (uint32_t)__popc(m & ((1u << lane) - 1u));
+      if (real && (m >> lane) == 1u) chunk_s[(size_t)(j >> 5) * E + e] = (uint32_t)__popc(m);
     }
-    const uint32_t row = chunk_s[(size_t)(j >> 5) * E + e] + lrank_s[j];
-    rt.pair_row[j] = (uint16_t)row;
-    rt.row_pair[row] = (uint16_t)j;
-    rt.row_tok[row] = (uint16_t)(j / K);
+    __syncthreads();
+    // per expert: rows (sum over chunks), first row and slot (block scans), each chunk's first
+    // row
+    uint32_t carry_rows = 0, carry_slots = 0;
+    for (int e0 = 0; e0 < E; e0 += kThreads) {
+      const int e = e0 + tid;
+      uint32_t tot = 0;
+      if (e < E)
+        for (int c = 0; c < nch; ++c) tot += chunk_s[(size_t)c * E + e];
+      const uint32_t off = block_excl_scan(tot, scan_s, &scan_s[32]);
+      const uint32_t tot_rows = scan_s[32];
+      __syncthreads();
+      const uint32_t sl = block_excl_scan(tot > 0 ? 1u : 0u, scan_s, &scan_s[32]);
+      const uint32_t tot_slots = scan_s[32];
+      __syncthreads();
+      if (e < E) {
+        uint32_t row = carry_rows + off;
+        base_s[e] = row;
+        if (tot > 0) {
+          rt.slot_e[carry_slots + sl] = (uint16_t)e;
+          rt.slot_r0[carry_slots + sl] = (uint16_t)row;
+          rt.slot_n[carry_slots + sl] = (uint16_t)tot;
+        }
+        for (int c = 0; c < nch; ++c) {
+          const uint32_t n = chunk_s[(size_t)c * E + e];
+          chunk_s[(size_t)c * E + e] = row;
+          row += n;
+        }
+      }
+      carry_rows += tot_rows;
+      carry_slots += tot_slots;
+    }
+    if (tid == 0) {
+      rt.n_active = (int)carry_slots;
+      rt.rows = (int)carry_rows;
+    }
+    __syncthreads();
+    for (int j = tid; j < te; j += kThreads) {
+      const uint32_t e = idx_s[j];
+      if ((int)e >= E) {
+        rt.pair_row[j] = kNoRow16;
+        continue;
+      }
+      const uint32_t row = chunk_s[(size_t)(j >> 5) * E + e] + lrank_s[j];
+      rt.pair_row[j] = (uint16_t)row;
+      rt.row_pair[row] = (uint16_t)j;
+      rt.row_tok[row] = (uint16_t)(j / K);
+    }
   }
   __syncthreads();
   if (blockIdx.x == 0) {
@@ -336,7 +482,7 @@ __device__ void route_block(const DecodeArgs& a, Routing& rt, uint8_t* scratch) 
     for (int r = tid; r < rt.rows; r += blockDim.x) a.sorted_pairs[r] = rt.row_pair[r];
     for (int e = tid; e < E; e += blockDim.x) a.offsets[e] = base_s[e];
     for (int sl = tid; sl < rt.n_active; sl += blockDim.x) a.active[sl] = rt.slot_e[sl];
-    for (int t = tid; t < a.N; t += blockDim.x) a.zsum[t] = rt.zsum[t];
+    for (int t = tid; t < N; t += blockDim.x) a.zsum[t] = rt.zsum[t];
     if (tid == 0) {
       a.offsets[E] = (uint32_t)rt.rows;
       a.hdr->num_active = (uint32_t)rt.n_active;
@@ -595,21 +741,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      int s = 0, issued = 0;
-      uint32_t ph = 0;
-      bool ok = true;
-      for (int k = 0; k < nitems; ++k) {
-        if (!mbar_wait(&empty[s], ph ^ 1, hdr)) { ok = false; break; }
-        bool down;
-        int tile, kc, slot, lt;
+      // the weight box of item k: its tensor map and coordinates
+      auto locate = [&](int k, bool& down, int& kc, const CUtensorMap*& m, int& row) {
+        int tile, slot, lt;
         sc.item(k, down, tile, kc, slot, lt);
-        uint8_t* wst = ring + (size_t)s * kWBytes;
         if (!down) {
           const int nt = slot >= 0 ? sc.nIt : sc.nSt;
           const bool up = lt >= nt;
           const int r = (up ? lt - nt : lt) * pl.bn_g;
-          const CUtensorMap* m;
-          int row;
           if (slot >= 0) {
             m = up ? &tm_wu : &tm_wg;
             row = (int)meta.slot_e[slot] * a.I + r;
@@ -617,15 +756,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             m = up ? &tm_su : &tm_sg;
             row = r;
           }
+        } else {
+          m = slot >= 0 ? &tm_wd : &tm_sd;
+          row = (slot >= 0 ? (int)meta.slot_e[slot] * a.H : 0) + lt * pl.bn_d;
+        }
+      };
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int k = 0; k < nitems; ++k) {
+        if (!mbar_wait(&empty[s], ph ^ 1, hdr)) { ok = false; break; }
+        bool down;
+        int kc, row;
+        const CUtensorMap* m;
+        locate(k, down, kc, m, row);
+        uint8_t* wst = ring + (size_t)s * kWBytes;
+        if (!down) {
           mbar_arrive_expect_tx(&full[s], (uint32_t)(pl.bn_g * 128 + kTokBytes));
           tma_load_2d(xtok + (size_t)s * kTokBytes, &tm_x, kc * kBox, 0, &full[s]);
-          tma_load_2d(wst, m, kc * kBox, row, &full[s]);
         } else {
-          const CUtensorMap* m = slot >= 0 ? &tm_wd : &tm_sd;
-          const int row = (slot >= 0 ? (int)meta.slot_e[slot] * a.H : 0) + lt * pl.bn_d;
           mbar_arrive_expect_tx(&full[s], (uint32_t)(pl.bn_d * 128));
-          tma_load_2d(wst, m, kc * kBox, row, &full[s]);
         }
+        tma_load_2d(wst, m, kc * kBox, row, &full[s]);
         ++issued;
         if (++s == stages) { s = 0; ph ^= 1; }
       }
@@ -787,7 +939,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               report_timeout(hdr);
               break;
             }
-            __nanosleep(64);
           }
         }
       }
@@ -796,20 +947,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ntok = slot_rows(a, meta, slot, r0);
       const int L = slot >= 0 ? a.I : a.S;
       const int cpr = L / 8;   // 16-byte chunks per row
-      for (int id = et; id < 16 * cpr; id += kEpiThreads) {
+      // (rows ntok..15 keep whatever they hold: an MMA row depends only on its own A row, and
+      // those accumulator rows are never drained)
+      for (int id = et; id < ntok * cpr; id += kEpiThreads) {
         const int j = id / cpr, c = id - j * cpr;
-        uint4 o = make_uint4(0u, 0u, 0u, 0u);
-        if (j < ntok) {
-          const float* hr = a.hd + (size_t)(r0 + j) * (2 * a.ldh) + c * 8;
-          const float4 g0v = __ldcg(reinterpret_cast<const float4*>(hr));
-          const float4 g1v = __ldcg(reinterpret_cast<const float4*>(hr + 4));
-          const float4 u0 = __ldcg(reinterpret_cast<const float4*>(hr + a.ldh));
-          const float4 u1 = __ldcg(reinterpret_cast<const float4*>(hr + a.ldh + 4));
-          o.x = pack_bf16x2(silu(g0v.x) * u0.x, silu(g0v.y) * u0.y);
-          o.y = pack_bf16x2(silu(g0v.z) * u0.z, silu(g0v.w) * u0.w);
-          o.z = pack_bf16x2(silu(g1v.x) * u1.x, silu(g1v.y) * u1.y);
-          o.w = pack_bf16x2(silu(g1v.z) * u1.z, silu(g1v.w) * u1.w);
-        }
+        uint4 o;
+        const float* hr = a.hd + (size_t)(r0 + j) * (2 * a.ldh) + c * 8;
+        const float4 g0v = __ldcg(reinterpret_cast<const float4*>(hr));
+        const float4 g1v = __ldcg(reinterpret_cast<const float4*>(hr + 4));
+        const float4 u0 = __ldcg(reinterpret_cast<const float4*>(hr + a.ldh));
+        const float4 u1 = __ldcg(reinterpret_cast<const float4*>(hr + a.ldh + 4));
+        o.x = pack_bf16x2(silu(g0v.x) * u0.x, silu(g0v.y) * u0.y);
+        o.y = pack_bf16x2(silu(g0v.z) * u0.z, silu(g0v.w) * u0.w);
+        o.z = pack_bf16x2(silu(g1v.x) * u1.x, silu(g1v.y) * u1.y);
+        o.w = pack_bf16x2(silu(g1v.z) * u1.z, silu(g1v.w) * u1.w);
         *reinterpret_cast<uint4*>(buf + (size_t)(c >> 3) * 2048 + j * 128 +
                                   (((c & 7) ^ (j & 7)) << 4)) = o;
       }
@@ -895,7 +1046,8 @@ cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, 
   if (pl.stages < 2) return cudaErrorInvalidValue;
   // the routing scratch of phase 1 lives in the (not yet used) dynamic region
   const size_t scratch = (size_t)a.te * 8 + (size_t)((a.te + 31) / 32) * a.E * 4 +
-                         (size_t)a.E * 4 + 160 + (size_t)kWarps * a.R * 4;
+                         (size_t)a.E * 4 + 160 +
+                         (a.R <= 256 ? 8 + (size_t)a.N * a.R * 16 : 0);
   if (scratch > (size_t)pl.stages * (kTokBytes + kWBytes)) return cudaErrorInvalidValue;
   const size_t sm = (size_t)fixed + (size_t)pl.stages * per_stage;
   cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(decode_forward_kernel), sm);
