@@ -4,8 +4,10 @@ Headline: the decode workload (N=4 tokens, H=2048, 128 experts of inter 768, top
 gated shared expert of inter 512), HBM-bound. The prefill workload (N=4096, Zipf-skewed
 routing) is measured in the same run and reported under "prefill" (tensor-bound).
 
-A step is one moe_forward over one batch with inputs resident in HBM; L2 is flushed (512 MiB
-write) before every timed step, outside the timed region. Times come from CUDA events on the
+A step is one moe_forward over one batch with inputs resident in HBM; L2 is flushed before every
+timed step, outside the timed region: a 512 MiB write, then a 512 MiB read, so that L2 holds no
+line of the workload and no dirty line (a write-only flush leaves ~126 MB of dirty lines whose
+write-back lands inside the next timed step; that variant is reported too, as "l2_write_only"). Times come from CUDA events on the
 launching stream. `--impl reference` times the CPU oracle instead (the only baseline there
 is). Multi-GPU runs are independent replicas (the block does not shard): value = all ranks'
 tokens / the slowest rank's time.
@@ -28,6 +30,22 @@ from mixture_experts_layer_08_gb300 import inputs as I  # noqa: E402
 
 METRIC = "MoE-layer tokens/s (prefill N=4096, decode N=4) and % tensor/HBM roofline"
 FLUSH_BYTES = 512 << 20
+
+
+class L2Flush:
+    """Evicts the workload from L2 between timed steps: a write of FLUSH_BYTES, then (unless
+    `dirty`) a read of as many bytes, which leaves L2 clean."""
+
+    def __init__(self, device, dirty=False):
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.acc = torch.empty((), dtype=torch.float32, device=device)
+        self.dirty = dirty
+
+    def __call__(self):
+        self.w.zero_()
+        if not self.dirty:
+            torch.sum(self.r, dim=0, out=self.acc)
 
 
 def load_peaks():
@@ -194,7 +212,7 @@ def time_ours(B, shape, steps, warmup, dev, peaks, with_e2e=True):
     torch.cuda.synchronize()
     rs = routing_stats(inp, idx.cpu().numpy())
     alg = algorithmic(inp, rs)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=f"cuda:{dev}")
+    flush = L2Flush(f"cuda:{dev}")
     stream = torch.cuda.current_stream()
     nst = len(B.STAGES)
 
@@ -202,7 +220,7 @@ def time_ours(B, shape, steps, warmup, dev, peaks, with_e2e=True):
         B.moe_forward_profiled(blk.cfg, blk.weights, inp.x, out, blk.workspace, events, stream)
 
     for _ in range(warmup):
-        flush.zero_()
+        flush()
         one([None] * (2 * nst))
     torch.cuda.synchronize()
     barrier()
@@ -217,7 +235,7 @@ def time_ours(B, shape, steps, warmup, dev, peaks, with_e2e=True):
     with ClockSampler(dev) as clk:
         t_wall0 = time.time()
         for i in range(steps):
-            flush.zero_()
+            flush()
             ev0[i].record()
             B.moe_forward(blk.cfg, blk.weights, inp.x, out, blk.workspace, stream)
             ev1[i].record()
@@ -225,6 +243,16 @@ def time_ours(B, shape, steps, warmup, dev, peaks, with_e2e=True):
         t_wall = time.time() - t_wall0
     step_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(steps)]
     ms = statistics.mean(step_ms)
+    # the same loop after a write-only flush (dirty L2)
+    dirty = L2Flush(f"cuda:{dev}", dirty=True)
+    for i in range(steps):
+        dirty()
+        ev0[i].record()
+        B.moe_forward(blk.cfg, blk.weights, inp.x, out, blk.workspace, stream)
+        ev1[i].record()
+    torch.cuda.synchronize()
+    ms_dirty = statistics.mean([ev0[i].elapsed_time(ev1[i]) for i in range(steps)])
+    del dirty
     # the stage breakdown: the same steps again, with the caller's events around every stage
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nst)] for _ in range(steps)]
     for row in ev:
@@ -232,7 +260,7 @@ def time_ours(B, shape, steps, warmup, dev, peaks, with_e2e=True):
             e.record()
     torch.cuda.synchronize()
     for i in range(steps):
-        flush.zero_()
+        flush()
         one(ev[i])
     torch.cuda.synchronize()
     stage_ms = {n: [] for n in B.STAGES}
@@ -240,7 +268,7 @@ def time_ours(B, shape, steps, warmup, dev, peaks, with_e2e=True):
         e = ev[i]
         for s, n in enumerate(B.STAGES):
             stage_ms[n].append(e[2 * s].elapsed_time(e[2 * s + 1]))
-    res = {"inp": inp, "rs": rs, "alg": alg, "ms": ms, "stage_ms": {k: statistics.mean(v)
+    res = {"inp": inp, "rs": rs, "alg": alg, "ms": ms, "ms_dirty": ms_dirty, "stage_ms": {k: statistics.mean(v)
                                                                      for k, v in stage_ms.items()},
            "clocks": clk.summary(), "wall_s": t_wall,
            "launches_per_step": kernels_per_step(B, blk.cfg)}
@@ -252,7 +280,7 @@ def time_ours(B, shape, steps, warmup, dev, peaks, with_e2e=True):
         dx = torch.empty_like(inp.x)
         e2e = []
         for i in range(warmup + steps):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             dx.copy_(hx, non_blocking=True)
@@ -283,7 +311,7 @@ def time_graph(B, blk, inp, out, flush, steps, warmup):
                           torch.cuda.current_stream())
         times = []
         for i in range(warmup + steps):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             g.replay()
@@ -410,7 +438,8 @@ def main():
         "config": {"workload": shape.name, "N": shape.num_tokens, "H": shape.hidden,
                    "E": shape.num_experts, "R": shape.router_width, "K": shape.top_k,
                    "I": shape.inter, "S": shape.shared_inter, "parallelism": "replicas",
-                   "l2": "flushed before every timed step (512 MiB write, untimed)",
+                   "l2": "flushed before every timed step (512 MiB write, then 512 MiB read; "
+                         "untimed)",
                    "distinct_experts": r["rs"]["distinct"]},
         "roofline": {"bound": "hbm", "kernel": "decode_forward_kernel",
                      "achieved": gu_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -419,8 +448,11 @@ def main():
                      "step_achieved_gbs": step_ach, "step_frac": step_ach / peaks["hbm_gbs"],
                      "algorithmic_bytes_per_launch": alg["ffn_bytes"],
                      "algorithmic_bytes_per_step": alg["bytes"]},
+        "l2_write_only": {"ms_per_step": r["ms_dirty"],
+                          "value": world * shape.num_tokens / (r["ms_dirty"] / 1000.0),
+                          "unit": "tokens/s"},
         "stage_us": {k: 1000 * v for k, v in r["stage_ms"].items()},
-        "gpu_launches": r["launches_per_step"] * args.steps,
+        "gpu_launches": r["launches_per_step"] * 2 * args.steps,
         "clocks": r["clocks"],
         "e2e": {"value": world * shape.num_tokens / (r["e2e_ms"] / 1000.0), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["io_bytes"], "d2h_bytes_per_step": r["io_bytes"]},
