@@ -215,137 +215,6 @@ __device__ __forceinline__ void route_token_warp_fast(const float* L, const floa
                              idx_out, w_out, zsum_out);
 }
 
-// Sorts the warp's 32 * VPL (score, id) keys best first (higher score, lower id on a tie) with a
-// bitonic network; lane l holds positions l * VPL .. l * VPL + VPL - 1. The stage loops stay
-// rolled: this code runs once per launch, so its size (instruction fetch) costs more than its
-// loop overhead.
-template <int VPL>
-__device__ __forceinline__ void bitonic_best_first(float (&v)[VPL], int (&ix)[VPL]) {
-  const int lane = threadIdx.x & 31;
-  constexpr int n = 32 * VPL;
-#pragma unroll 1
-  for (int k = 2; k <= n; k <<= 1) {
-#pragma unroll 1
-    for (int dist = k >> 1; dist > 0; dist >>= 1) {
-      if (dist < VPL) {
-#pragma unroll
-        for (int d = 1; d < VPL; d <<= 1) {
-          if (dist == d) {
-#pragma unroll
-            for (int j = 0; j < VPL; ++j) {
-              const int jj = j ^ d;
-              if (jj > j) {   // the pair (j, jj) of this lane, j the lower position
-                const bool up = ((lane * VPL + j) & k) == 0;
-                const bool hi_better = ranks_before(v[jj], ix[jj], v[j], ix[j]);
-                if (up == hi_better) {   // the lower position keeps the better key when up
-                  const float tv = v[j];
-                  v[j] = v[jj];
-                  v[jj] = tv;
-                  const int ti = ix[j];
-                  ix[j] = ix[jj];
-                  ix[jj] = ti;
-                }
-              }
-            }
-          }
-        }
-      } else {
-        const int lm = dist / VPL;
-        const bool lower = (lane & lm) == 0;
-#pragma unroll
-        for (int j = 0; j < VPL; ++j) {
-          const float ov = __shfl_xor_sync(0xffffffffu, v[j], lm);
-          const int oi = __shfl_xor_sync(0xffffffffu, ix[j], lm);
-          const bool up = ((lane * VPL + j) & k) == 0;
-          const bool other_better = ranks_before(ov, oi, v[j], ix[j]);
-          // lower position: keeps the better key when up; upper position: the worse one
-          if ((lower == up) == other_better) {
-            v[j] = ov;
-            ix[j] = oi;
-          }
-        }
-      }
-    }
-  }
-}
-
-// One warp routes one token: softmax in registers, selection by a bitonic sort of the
-// selection scores (R <= 32 * VPL; lane l holds columns l * VPL .. l * VPL + VPL - 1), weights
-// from the unbiased probabilities. `p_w`: per-warp shared scratch of R floats.
-// Lane k < K writes slot k of idx/w; lane 0 writes zsum.
-template <int VPL>
-__device__ void route_token_warp_sort(const float* L, const float* logit_bias,
-                                      const float* corr_bias, int R, int E, int K, int scoring,
-                                      int norm, float scale, const uint32_t* forced, float* p_w,
-                                      uint32_t* idx_out, float* w_out, float* zsum_out) {
-  const int lane = threadIdx.x & 31;
-  float v[VPL];
-  int ix[VPL];
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int r = lane * VPL + j;
-    v[j] = r < R ? __ldcg(L + r) : 0.0f;
-  }
-  float mx = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int r = lane * VPL + j;
-    if (r < R) {
-      if (logit_bias) v[j] += logit_bias[r];
-      mx = fmaxf(mx, v[j]);
-    }
-  }
-  mx = warp_max(mx);
-  float den = 0.0f;
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int r = lane * VPL + j;
-    if (r < R) {
-      v[j] = expf(v[j] - mx);
-      den += v[j];
-    }
-  }
-  den = warp_sum(den);
-  const bool biased = scoring == MOE_SCORING_SOFTMAX_BIAS && corr_bias;
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int r = lane * VPL + j;
-    ix[j] = r;   // (padding keys: -inf with ids >= R, ordered after every real column)
-    if (r < R) {
-      const float pr = v[j] / den;
-      p_w[r] = pr;
-      v[j] = pr + (biased ? corr_bias[r] : 0.0f);
-    } else {
-      v[j] = -INFINITY;
-    }
-  }
-  uint32_t my_idx = 0;
-  if (forced) {
-    if (lane < K) my_idx = forced[lane];
-  } else {
-    bitonic_best_first<VPL>(v, ix);
-    // position k sits in lane k / VPL, register k % VPL
-#pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      const int src = __shfl_sync(0xffffffffu, ix[j], (lane / VPL) & 31);
-      if (lane < K && lane % VPL == j) my_idx = (uint32_t)src;
-    }
-  }
-  __syncwarp();
-  // weights: unbiased probabilities of the chosen ids, renormalised over all K slots
-  float wk = lane < K ? p_w[my_idx < (uint32_t)R ? my_idx : 0u] : 0.0f;
-  const float sum = warp_sum(wk);
-  if (norm) wk = wk / sum;
-  wk *= scale;
-  float z = (lane < K && (int)my_idx >= E) ? wk : 0.0f;
-  z = warp_sum(z);
-  if (lane < K) {
-    idx_out[lane] = my_idx;
-    w_out[lane] = wk;
-  }
-  if (lane == 0) *zsum_out = z;
-}
-
 // Block-wide exclusive scan of one value per thread (blockDim.x <= 1024, multiple of 32).
 __device__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_tot, uint32_t* total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
