@@ -90,7 +90,13 @@ struct Routing {
   float w[kDecodeMaxPairs];              // routing weight of each pair
   float zsum[kDecodeMaxTokens];          // identity-expert weight sum of each token
   float gamma[kDecodeMaxTokens];         // shared-expert blend weight of each token
+  uint16_t idx[32];                      // chosen router column of each pair (split routing)
+  uint32_t bits[32];                     // experts in use, one bit each (split routing)
 };
+
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   uint32_t v;
@@ -332,6 +338,125 @@ __device__ void token_weights(const DecodeArgs& a, int t, const float* p_t,
   z = warp_sum(z);
   if (lane < K) rt.w[t * K + lane] = wk;
   if (lane == 0) rt.zsum[t] = z;
+}
+
+// Split routing, for at most 32 routed pairs and routers up to 256 wide. The projections need
+// only the experts in use, in ascending id (the weight stream of the gate/up items does not
+// depend on which tokens chose an expert), so the block's first part of the routing stops
+// there and the stream starts; the epilogue warps compute the rest beside it (route_rows_split).
+// Part one, all threads: per-token top-K (token_topk), the chosen columns and their
+// probabilities kept in static shared memory (the dynamic scratch becomes the weight ring), a
+// bit per expert in use, and each expert's slot = the number of experts in use below it.
+__device__ void route_active_split(const DecodeArgs& a, Routing& rt, uint8_t* scratch) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int R = a.R, K = a.K, N = a.N, te = a.te;
+  uint32_t* idx_s = reinterpret_cast<uint32_t*>(scratch);                  // [te]
+  unsigned long long* k_s = reinterpret_cast<unsigned long long*>(scratch + 128);
+  float* p_s = reinterpret_cast<float*>(k_s + (size_t)N * R);             // [N][R]
+  float* cb_s = p_s + (size_t)N * R;                                        // [N][R]
+  if (warp == kWarps - 1) rt.bits[lane] = 0u;
+  for (int t = warp; t < N; t += kWarps) {
+    const size_t o = (size_t)t * R;
+    if (R <= 128) token_topk<4>(a, t, p_s + o, cb_s + o, k_s + o, idx_s + t * K, rt);
+    else token_topk<8>(a, t, p_s + o, cb_s + o, k_s + o, idx_s + t * K, rt);
+    __syncwarp();
+    if (lane < K) {
+      const uint32_t c = idx_s[t * K + lane];
+      rt.idx[t * K + lane] = (uint16_t)c;
+      rt.w[t * K + lane] = p_s[o + (c < (uint32_t)R ? c : 0u)];   // (normalised later)
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t e = lane < te ? (uint32_t)rt.idx[lane] : 0xFFFFFFFFu;
+    const bool real = e < (uint32_t)a.E;
+    if (real) atomicOr(&rt.bits[e >> 5], 1u << (e & 31));
+    __syncwarp();
+    if (real) {   // (lanes of one expert write the same slot)
+      uint32_t sl = (uint32_t)__popc(rt.bits[e >> 5] & ((1u << (e & 31)) - 1u));
+#pragma unroll 1
+      for (uint32_t w = 0; w < (e >> 5); ++w) sl += (uint32_t)__popc(rt.bits[w]);
+      rt.slot_e[sl] = (uint16_t)e;
+    }
+    const int nw = (a.E + 31) >> 5;
+    const uint32_t n = __reduce_add_sync(0xffffffffu, lane < nw ? (uint32_t)__popc(rt.bits[lane]) : 0u);
+    if (lane == 0) rt.n_active = (int)n;
+  }
+  // the scratch is about to be overwritten by bulk copies (async proxy)
+  fence_proxy_async_smem();
+  __syncthreads();
+}
+
+// Part two, the 128 epilogue threads (named barrier 1) while the weight stream runs: the stable
+// sort of the pairs by expert (one warp: match, then a rolled count over the 32 lanes), the
+// routing weights (renormalised probabilities x scale, identity-expert sums), and block 0's copy
+// of the routing into the workspace.
+__device__ void route_rows_split(const DecodeArgs& a, Routing& rt) {
+  const int et = threadIdx.x - 64, wq = et >> 5, lane = threadIdx.x & 31;
+  const int E = a.E, K = a.K, te = a.te, N = a.N;
+  if (wq == 0) {
+    const bool valid = lane < te;
+    const uint32_t e = valid ? (uint32_t)rt.idx[lane] : 0xFFFFFFFFu;
+    const bool real = valid && (int)e < E;
+    const uint32_t m = __match_any_sync(0xffffffffu, real ? e : 0xFFFFFFFFu);
+    const uint32_t lrank = (uint32_t)__popc(m & ((1u << lane) - 1u));
+    const uint32_t reals = __ballot_sync(0xffffffffu, real);
+    uint32_t before = 0;
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t ei = __shfl_sync(0xffffffffu, e, i);
+      if (((reals >> i) & 1u) && ei < e) ++before;
+    }
+    if (real) {
+      const uint32_t row = before + lrank;
+      rt.pair_row[lane] = (uint16_t)row;
+      rt.row_pair[row] = (uint16_t)lane;
+      rt.row_tok[row] = (uint16_t)(lane / K);
+      if (lrank == 0) {
+        uint32_t sl = (uint32_t)__popc(rt.bits[e >> 5] & ((1u << (e & 31)) - 1u));
+#pragma unroll 1
+        for (uint32_t w = 0; w < (e >> 5); ++w) sl += (uint32_t)__popc(rt.bits[w]);
+        rt.slot_r0[sl] = (uint16_t)before;
+        rt.slot_n[sl] = (uint16_t)__popc(m);
+      }
+    } else if (valid) {
+      rt.pair_row[lane] = kNoRow16;
+    }
+    if (lane == 0) rt.rows = __popc(reals);
+  } else {
+    for (int t = wq - 1; t < N; t += 3) {
+      const uint32_t c = lane < K ? (uint32_t)rt.idx[t * K + lane] : 0u;
+      float wk = lane < K ? rt.w[t * K + lane] : 0.0f;
+      const float sum = warp_sum(wk);
+      if (a.norm) wk = wk / sum;
+      wk *= a.scale;
+      const float z = warp_sum((lane < K && (int)c >= E) ? wk : 0.0f);
+      if (lane < K) rt.w[t * K + lane] = wk;
+      if (lane == 0) rt.zsum[t] = z;
+    }
+  }
+  named_sync(1, kEpiThreads);
+  if (blockIdx.x == 0) {
+    for (int j = et; j < te; j += kEpiThreads) {
+      a.idx[j] = rt.idx[j];
+      a.w[j] = rt.w[j];
+      a.pair_to_row[j] = rt.pair_row[j] == kNoRow16 ? kNoRow : (uint32_t)rt.pair_row[j];
+    }
+    for (int r = et; r < rt.rows; r += kEpiThreads) a.sorted_pairs[r] = rt.row_pair[r];
+    for (int e = et; e < E; e += kEpiThreads) {   // first row of every expert
+      uint32_t n = 0;
+#pragma unroll 1
+      for (int j = 0; j < te; ++j) n += ((uint32_t)rt.idx[j] < (uint32_t)e) ? 1u : 0u;
+      a.offsets[e] = n;
+    }
+    for (int sl = et; sl < rt.n_active; sl += kEpiThreads) a.active[sl] = rt.slot_e[sl];
+    for (int t = et; t < N; t += kEpiThreads) a.zsum[t] = rt.zsum[t];
+    if (et == 0) {
+      a.offsets[E] = (uint32_t)rt.rows;
+      a.hdr->num_active = (uint32_t)rt.n_active;
+    }
+  }
+  named_sync(1, kEpiThreads);
 }
 
 // Phase 1: the block's own copy of the routing. `scratch`: dynamic shared memory not yet in use.
@@ -652,10 +777,6 @@ __device__ void zero_accumulators(const DecodeArgs& a) {
   for (size_t i = tid; i < (size_t)kDecodeMaxPairs + 1; i += nth) a.h_cnt[i] = 0u;
 }
 
-__device__ __forceinline__ void named_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 
 __device__ __forceinline__ int slot_rows(const DecodeArgs& a, const Routing& m, int slot,
                                          int& r0) {
@@ -729,7 +850,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   router_rows(a, smem, (size_t)stages * (kTokBytes + kWBytes), red_s);
   zero_accumulators(a);
   grid_barrier(hdr, gridDim.x);
-  route_block(a, meta, smem);   // (ends with a block barrier)
+  const bool split_routing = a.te <= 32 && a.R <= 256;
+  if (split_routing) route_active_split(a, meta, smem);   // (ends with a block barrier)
+  else route_block(a, meta, smem);                        // (ends with a block barrier)
   tc_fence_after();
   const uint32_t tmem_base = tmem_slot;
 
@@ -834,6 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------ epilogue
+    if (split_routing) route_rows_split(a, meta);
     const int et = threadIdx.x - 64;        // 0..127
     const bool drainer = warp == kDrainWarp;
     int run = -1, prev_tile = -1, bslot = -2, nb = 0;
@@ -1045,9 +1169,11 @@ cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, 
   if (pl.stages > kMaxStages) pl.stages = kMaxStages;
   if (pl.stages < 2) return cudaErrorInvalidValue;
   // the routing scratch of phase 1 lives in the (not yet used) dynamic region
-  const size_t scratch = (size_t)a.te * 8 + (size_t)((a.te + 31) / 32) * a.E * 4 +
-                         (size_t)a.E * 4 + 160 +
-                         (a.R <= 256 ? 8 + (size_t)a.N * a.R * 16 : 0);
+  const size_t scratch = a.te <= 32 && a.R <= 256
+                             ? 128 + (size_t)a.N * a.R * 16   // split routing
+                             : (size_t)a.te * 8 + (size_t)((a.te + 31) / 32) * a.E * 4 +
+                                   (size_t)a.E * 4 + 160 +
+                                   (a.R <= 256 ? 8 + (size_t)a.N * a.R * 16 : 0);
   if (scratch > (size_t)pl.stages * (kTokBytes + kWBytes)) return cudaErrorInvalidValue;
   const size_t sm = (size_t)fixed + (size_t)pl.stages * per_stage;
   cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(decode_forward_kernel), sm);
