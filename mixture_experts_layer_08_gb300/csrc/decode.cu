@@ -104,14 +104,20 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   return v;
 }
 
+// Adds `v` to a global counter after every write this thread has made or seen ordered before
+// (a release: acq_rel fence, then a relaxed reduction).
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("fence.acq_rel.gpu;\n\tred.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v)
+               : "memory");
+}
+
 // Grid-wide barrier of the co-resident blocks: the header counter reaches `target` (the number
 // of blocks times the barriers passed so far). Bounded: a timeout is reported and the block
 // carries on (its results are then not used).
 __device__ void grid_barrier(WsHeader* hdr, uint32_t target) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();   // (cumulative: the block's writes, ordered before it by the block barrier)
-    atomicAdd(&hdr->done_blocks, 1u);
+    red_release_add(&hdr->done_blocks, 1u);   // (the block's writes, ordered before by the barrier)
     if (ld_acquire(&hdr->done_blocks) < target) {
       const long long t0 = clock64();
       while (ld_acquire(&hdr->done_blocks) < target) {
@@ -121,7 +127,6 @@ __device__ void grid_barrier(WsHeader* hdr, uint32_t target) {
         }
       }
     }
-    __threadfence();
   }
   __syncthreads();
 }
@@ -1037,12 +1042,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&aempty[rr & 1]);
       if (!rdown) {
         // publish: the slot's count moves only after every partial sum of the run landed
-        __threadfence();
         __syncwarp();
-        if (lane == 0) {
-          __threadfence();
-          atomicAdd(a.h_cnt + (rslot < 0 ? kDecodeMaxPairs : rslot), (uint32_t)rlen);
-        }
+        if (lane == 0) red_release_add(a.h_cnt + (rslot < 0 ? kDecodeMaxPairs : rslot), (uint32_t)rlen);
       }
     };
     auto drain_current = [&]() {
