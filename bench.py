@@ -253,6 +253,22 @@ def time_ours(B, shape, steps, warmup, dev, peaks, with_e2e=True):
     torch.cuda.synchronize()
     ms_dirty = statistics.mean([ev0[i].elapsed_time(ev1[i]) for i in range(steps)])
     del dirty
+    # the same loop in the non-deterministic mode (routed down rows FP32-atomic-added into one
+    # accumulator per token), where the chain supports it
+    ms_atomic = None
+    if with_e2e:
+        blk_a = B.MoeBlock(inp, deterministic=False)
+        for _ in range(warmup):
+            flush()
+            B.moe_forward(blk_a.cfg, blk_a.weights, inp.x, out, blk_a.workspace, stream)
+        for i in range(steps):
+            flush()
+            ev0[i].record()
+            B.moe_forward(blk_a.cfg, blk_a.weights, inp.x, out, blk_a.workspace, stream)
+            ev1[i].record()
+        torch.cuda.synchronize()
+        ms_atomic = statistics.mean([ev0[i].elapsed_time(ev1[i]) for i in range(steps)])
+        del blk_a
     # the stage breakdown: the same steps again, with the caller's events around every stage
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nst)] for _ in range(steps)]
     for row in ev:
@@ -268,7 +284,7 @@ def time_ours(B, shape, steps, warmup, dev, peaks, with_e2e=True):
         e = ev[i]
         for s, n in enumerate(B.STAGES):
             stage_ms[n].append(e[2 * s].elapsed_time(e[2 * s + 1]))
-    res = {"inp": inp, "rs": rs, "alg": alg, "ms": ms, "ms_dirty": ms_dirty, "stage_ms": {k: statistics.mean(v)
+    res = {"inp": inp, "rs": rs, "alg": alg, "ms": ms, "ms_dirty": ms_dirty, "ms_atomic": ms_atomic, "stage_ms": {k: statistics.mean(v)
                                                                      for k, v in stage_ms.items()},
            "clocks": clk.summary(), "wall_s": t_wall,
            "launches_per_step": kernels_per_step(B, blk.cfg)}
@@ -451,8 +467,12 @@ def main():
         "l2_write_only": {"ms_per_step": r["ms_dirty"],
                           "value": world * shape.num_tokens / (r["ms_dirty"] / 1000.0),
                           "unit": "tokens/s"},
+        "atomic_accumulation": {"ms_per_step": r["ms_atomic"],
+                                "value": world * shape.num_tokens / (r["ms_atomic"] / 1000.0),
+                                "unit": "tokens/s",
+                                "note": "deterministic=0: down rows FP32-atomic-added per token"},
         "stage_us": {k: 1000 * v for k, v in r["stage_ms"].items()},
-        "gpu_launches": r["launches_per_step"] * 2 * args.steps,
+        "gpu_launches": r["launches_per_step"] * 3 * args.steps,
         "clocks": r["clocks"],
         "e2e": {"value": world * shape.num_tokens / (r["e2e_ms"] / 1000.0), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["io_bytes"], "d2h_bytes_per_step": r["io_bytes"]},
