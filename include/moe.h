@@ -12,6 +12,7 @@
  *
  *   L[t,:]   = x[t,:] . Wr^T (+ router_logit_bias)                       fp32 accumulate
  *   p[t,:]   = softmax(L[t,:]) over all R router columns                  fp32
+ *              (MOE_SCORING_SIGMOID_BIAS: p[t,r] = sigmoid(L[t,r]))
  *   idx[t,:] = top-K of p (or of p + correction_bias), ties to the lower id
  *   w[t,k]   = p[t,idx] (/ sum_k if norm_topk_prob) * routed_scaling_factor
  *   out[t,:] = sum_{k: idx<E} w[t,k] * (SiLU(x Wg_e^T) * (x Wu_e^T)) Wd_e^T
@@ -52,7 +53,12 @@ extern "C" {
 
 typedef enum {
   MOE_SCORING_SOFTMAX = 0,      /* p = softmax(L); select by p */
-  MOE_SCORING_SOFTMAX_BIAS = 1  /* p = softmax(L); select by p + correction_bias; weights from p */
+  MOE_SCORING_SOFTMAX_BIAS = 1, /* p = softmax(L); select by p + correction_bias; weights from p
+                                   ("spark_model/layers/moe/forward.rs", LongCat arm) */
+  MOE_SCORING_SIGMOID_BIAS = 2  /* p = sigmoid(L) per column; select by p + correction_bias;
+                                   weights from p, renormalised over the K chosen when
+                                   norm_topk_prob, times routed_scaling_factor (same page,
+                                   DeepSeek-V3 / MiniMax-M2 arm); router_width == num_experts */
 } moe_scoring_t;
 
 typedef enum {
@@ -85,7 +91,7 @@ typedef struct {
   int32_t num_experts;   /* E: SwiGLU experts, ids 0..E-1 */
   int32_t router_width;  /* R >= E: router columns; ids E..R-1 are identity experts.
                             R > E requires MOE_SCORING_SOFTMAX_BIAS (the pages wire identity
-                            experts only on that arm) */
+                            experts only on that arm); otherwise MOE_ERR_UNSUPPORTED */
   int32_t top_k;         /* K */
   int32_t inter;         /* I: routed expert intermediate size */
   int32_t shared_inter;  /* S: shared expert intermediate size, 0 = no shared expert */
@@ -103,7 +109,8 @@ typedef struct {
 typedef struct {
   const void *router_w;            /* bf16 [R,H] */
   const float *router_logit_bias;  /* nullable fp32 [R], added to the logits before softmax */
-  const float *correction_bias;    /* fp32 [R], MOE_SCORING_SOFTMAX_BIAS only (selection only) */
+  const float *correction_bias;    /* fp32 [R], required by the *_BIAS scorings (selection only),
+                                      ignored with MOE_SCORING_SOFTMAX */
   const void *w_gate;              /* [E,I,H] bf16 or E4M3 */
   const void *w_up;                /* [E,I,H] bf16 or E4M3 */
   const void *w_down;              /* [E,H,I] bf16 or E4M3 */

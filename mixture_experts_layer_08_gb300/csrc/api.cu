@@ -51,7 +51,8 @@ moe_status_t validate_config(const moe_config_t* c) {
       c->top_k <= 0 || c->inter <= 0 || c->shared_inter < 0)
     return MOE_ERR_INVALID_ARG;
   if (c->router_width < c->num_experts || c->top_k > c->router_width) return MOE_ERR_INVALID_ARG;
-  if (c->scoring != MOE_SCORING_SOFTMAX && c->scoring != MOE_SCORING_SOFTMAX_BIAS)
+  if (c->scoring != MOE_SCORING_SOFTMAX && c->scoring != MOE_SCORING_SOFTMAX_BIAS &&
+      c->scoring != MOE_SCORING_SIGMOID_BIAS)
     return MOE_ERR_INVALID_ARG;
   if (c->weight_dtype != MOE_W_BF16 && c->weight_dtype != MOE_W_FP8_E4M3_B128)
     return MOE_ERR_INVALID_ARG;
@@ -218,7 +219,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 moe_status_t validate_weights(const moe_config_t* c, const moe_weights_t* w) {
   if (!w || !w->router_w || !w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
-  if (c->scoring == MOE_SCORING_SOFTMAX_BIAS && !w->correction_bias) return MOE_ERR_INVALID_ARG;
+  if (c->scoring != MOE_SCORING_SOFTMAX && !w->correction_bias) return MOE_ERR_INVALID_ARG;
   if (c->weight_dtype == MOE_W_FP8_E4M3_B128 && (!w->s_gate || !w->s_up || !w->s_down))
     return MOE_ERR_INVALID_ARG;
   if (c->shared_inter > 0 && (!w->sh_gate || !w->sh_up || !w->sh_down)) return MOE_ERR_INVALID_ARG;
@@ -279,7 +280,7 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
   ra.x = static_cast<const __nv_bfloat16*>(x);
   ra.router_w = static_cast<const __nv_bfloat16*>(w->router_w);
   ra.logit_bias = w->router_logit_bias;
-  ra.corr_bias = c->scoring == MOE_SCORING_SOFTMAX_BIAS ? w->correction_bias : nullptr;
+  ra.corr_bias = c->scoring != MOE_SCORING_SOFTMAX ? w->correction_bias : nullptr;
   ra.forced = forced;
   ra.N = c->num_tokens;
   ra.H = c->hidden;
@@ -527,7 +528,7 @@ moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const voi
   d.x = static_cast<const __nv_bfloat16*>(x);
   d.router_w = static_cast<const __nv_bfloat16*>(w->router_w);
   d.logit_bias = w->router_logit_bias;
-  d.corr_bias = c->scoring == MOE_SCORING_SOFTMAX_BIAS ? w->correction_bias : nullptr;
+  d.corr_bias = c->scoring != MOE_SCORING_SOFTMAX ? w->correction_bias : nullptr;
   d.forced = forced;
   d.sh_gate_vec = S > 0 ? static_cast<const __nv_bfloat16*>(w->sh_gate_vec) : nullptr;
   d.N = N;

@@ -236,7 +236,7 @@ __device__ void topk_rounds_warp(const DecodeArgs& a, int t, uint32_t* idx_s, Ro
 }
 
 // Top-K of one token by one warp (R <= 32 * VPL). Lane l owns router columns l, l + 32, ...:
-// softmax (probabilities into p_t[R], kept for the weights), selection score = probability
+// softmax or sigmoid scores (into p_t[R], kept for the weights), selection score = score
 // (+ the correction bias). Each score becomes a 64-bit key (order-preserving score bits above
 // the complemented column id), so one unsigned compare orders by higher score, then lower id.
 // Every lane sorts its VPL keys in registers; then K rounds of a warp max over the lanes' heads,
@@ -250,7 +250,8 @@ __device__ void token_topk(const DecodeArgs& a, int t, float* p_t, float* cb_t,
   const int R = a.R;
   const float* L = a.logits + (size_t)t * R;
   const bool gated = a.S > 0 && a.sh_gate_vec;
-  const bool biased = a.scoring == MOE_SCORING_SOFTMAX_BIAS && a.corr_bias;
+  const bool biased = selection_biased(a.scoring) && a.corr_bias;
+  const bool sig = a.scoring == MOE_SCORING_SIGMOID_BIAS;
   const float gd = gated ? __ldcg(&a.hdr->gate_dot[t]) : 0.0f;
   float v[VPL], cb[VPL];
 #pragma unroll
@@ -268,21 +269,24 @@ __device__ void token_topk(const DecodeArgs& a, int t, float* p_t, float* cb_t,
       cb_t[r] = cb[i];
     }
   }
-  float mx = -INFINITY;
+  float den = 1.0f;
+  if (!sig) {
+    float mx = -INFINITY;
 #pragma unroll 1
-  for (int r = lane; r < R; r += 32) mx = fmaxf(mx, p_t[r]);
-  mx = warp_max(mx);
-  float den = 0.0f;
+    for (int r = lane; r < R; r += 32) mx = fmaxf(mx, p_t[r]);
+    mx = warp_max(mx);
+    den = 0.0f;
 #pragma unroll 1
-  for (int r = lane; r < R; r += 32) {
-    const float e = expf(p_t[r] - mx);
-    p_t[r] = e;
-    den += e;
+    for (int r = lane; r < R; r += 32) {
+      const float e = expf(p_t[r] - mx);
+      p_t[r] = e;
+      den += e;
+    }
+    den = warp_sum(den);
   }
-  den = warp_sum(den);
 #pragma unroll 1
   for (int r = lane; r < R; r += 32) {
-    const float pr = p_t[r] / den;
+    const float pr = sig ? sigmoid_score(p_t[r]) : p_t[r] / den;
     p_t[r] = pr;
     const float sc = pr + cb_t[r];
     const uint32_t bits = sc == 0.0f ? 0u : __float_as_uint(sc);   // -0 ties with +0

@@ -16,6 +16,14 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
   return va > vb || (va == vb && ia < ib);
 }
 
+// Does the scoring add the correction bias to the selection score (never to the weights)?
+__device__ __forceinline__ bool selection_biased(int scoring) {
+  return scoring == MOE_SCORING_SOFTMAX_BIAS || scoring == MOE_SCORING_SIGMOID_BIAS;
+}
+
+// The sigmoid arm's score: 1 / (1 + e^-x).
+__device__ __forceinline__ float sigmoid_score(float x) { return 1.0f / (1.0f + expf(-x)); }
+
 // One warp routes one token. `L` is the token's fp32 logit row; `p` and `sel` are per-warp
 // shared scratch of R floats. Lane k < K writes slot k of idx/w; lane 0 writes zsum.
 __device__ void route_token_warp(const float* L, const float* logit_bias, const float* corr_bias,
@@ -41,18 +49,27 @@ __device__ void route_token_warp(const float* L, const float* logit_bias, const 
       }
     }
   }
-  mx = warp_max(mx);
-  float den = 0.0f;
-  for (int r = lane; r < R; r += 32) {
-    float e = expf(p[r] - mx);
-    p[r] = e;
-    den += e;
-  }
-  den = warp_sum(den);
-  for (int r = lane; r < R; r += 32) {
-    float pr = p[r] / den;
-    p[r] = pr;
-    sel[r] = pr + ((scoring == MOE_SCORING_SOFTMAX_BIAS && corr_bias) ? corr_bias[r] : 0.0f);
+  const bool biased = selection_biased(scoring) && corr_bias;
+  if (scoring == MOE_SCORING_SIGMOID_BIAS) {
+    for (int r = lane; r < R; r += 32) {
+      const float pr = sigmoid_score(p[r]);
+      p[r] = pr;
+      sel[r] = pr + (biased ? corr_bias[r] : 0.0f);
+    }
+  } else {
+    mx = warp_max(mx);
+    float den = 0.0f;
+    for (int r = lane; r < R; r += 32) {
+      float e = expf(p[r] - mx);
+      p[r] = e;
+      den += e;
+    }
+    den = warp_sum(den);
+    for (int r = lane; r < R; r += 32) {
+      float pr = p[r] / den;
+      p[r] = pr;
+      sel[r] = pr + (biased ? corr_bias[r] : 0.0f);
+    }
   }
   __syncwarp();
   uint32_t my_idx = 0;
@@ -119,23 +136,27 @@ __device__ void route_token_warp_reg(const float* L, const float* logit_bias,
       mx = fmaxf(mx, v[i]);
     }
   }
-  mx = warp_max(mx);
-  float den = 0.0f;
+  const bool sig = scoring == MOE_SCORING_SIGMOID_BIAS;
+  float den = 1.0f;
+  if (!sig) {
+    mx = warp_max(mx);
+    den = 0.0f;
 #pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    const int r = i * 32 + lane;
-    if (r < R) {
-      v[i] = expf(v[i] - mx);
-      den += v[i];
+    for (int i = 0; i < VPL; ++i) {
+      const int r = i * 32 + lane;
+      if (r < R) {
+        v[i] = expf(v[i] - mx);
+        den += v[i];
+      }
     }
+    den = warp_sum(den);
   }
-  den = warp_sum(den);
-  const bool biased = scoring == MOE_SCORING_SOFTMAX_BIAS && corr_bias;
+  const bool biased = selection_biased(scoring) && corr_bias;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int r = i * 32 + lane;
     if (r < R) {
-      v[i] = v[i] / den;
+      v[i] = sig ? sigmoid_score(v[i]) : v[i] / den;
       sel[i] = v[i] + (biased ? corr_bias[r] : 0.0f);
     } else {
       sel[i] = -INFINITY;

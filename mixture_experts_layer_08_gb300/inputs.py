@@ -29,6 +29,7 @@ import torch
 
 SCORING_SOFTMAX = 0
 SCORING_SOFTMAX_BIAS = 1
+SCORING_SIGMOID_BIAS = 2
 
 WDTYPE_BF16 = 0
 WDTYPE_FP8_E4M3_B128 = 1
@@ -54,7 +55,7 @@ class MoeShape:
     routed_scaling_factor: float = 1.0
     weight_dtype: int = WDTYPE_BF16
     zipf_s: float = 0.0        # >0: skewed per-expert router-logit offsets
-    correction_bias_std: float = 0.0  # >0 with SCORING_SOFTMAX_BIAS
+    correction_bias_std: float = 0.0  # >0 with the *_BIAS scorings
     seed: int = 0
 
     def with_(self, **kw) -> "MoeShape":

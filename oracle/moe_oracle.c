@@ -111,7 +111,8 @@ void orc_quant_1x128(const float *v, int n, uint8_t *codes, float *scales, doubl
 
 typedef struct {
     int32_t num_tokens, hidden, num_experts, router_width, top_k, inter, shared_inter;
-    int32_t scoring;          /* 0 softmax, 1 softmax + selection-only correction bias */
+    int32_t scoring;          /* 0 softmax, 1 softmax + selection-only correction bias,
+                                 2 sigmoid + selection-only correction bias */
     int32_t norm_topk_prob;
     double routed_scaling_factor;
     int32_t weight_dtype;     /* 0 bf16, 1 E4M3 + fp32 128x128 block scales */
@@ -145,21 +146,28 @@ static int ranks_before(const double *sel, int a, int b) {
 }
 
 /* Scoring, top-K and weights of one token.
- * p = softmax(L) over all R columns; sel = p (+ correction bias); idx = K best by sel;
+ * p = softmax(L) over all R columns (scoring 2: p[r] = sigmoid(L[r]) = 1 / (1 + e^-L[r]),
+ * each column on its own, the decode page's sigmoid + correction-bias arm);
+ * sel = p (+ correction bias); idx = K best by sel;
  * w = p[idx] (/ sum if norm_topk_prob) * routed_scaling_factor; zsum = sum of w on ids >= E.
  * gap = sel of the K-th choice minus sel of the (K+1)-th (INFINITY when K == R). */
 static void route_token(const orc_config_t *c, const orc_weights_t *w, const double *L,
                         const int32_t *forced, int32_t *idx, double *wt, double *zsum,
                         double *gap, double *p, double *sel, char *taken) {
     int R = c->router_width, K = c->top_k, E = c->num_experts;
-    double mx = L[0];
-    for (int r = 1; r < R; ++r) if (L[r] > mx) mx = L[r];
-    double den = 0.0;
-    for (int r = 0; r < R; ++r) { p[r] = exp(L[r] - mx); den += p[r]; }
-    for (int r = 0; r < R; ++r) p[r] /= den;
+    if (c->scoring == 2) {
+        for (int r = 0; r < R; ++r) p[r] = 1.0 / (1.0 + exp(-L[r]));
+    } else {
+        double mx = L[0];
+        for (int r = 1; r < R; ++r) if (L[r] > mx) mx = L[r];
+        double den = 0.0;
+        for (int r = 0; r < R; ++r) { p[r] = exp(L[r] - mx); den += p[r]; }
+        for (int r = 0; r < R; ++r) p[r] /= den;
+    }
     for (int r = 0; r < R; ++r) {
         sel[r] = p[r];
-        if (c->scoring == 1 && w->correction_bias) sel[r] += (double)w->correction_bias[r];
+        if ((c->scoring == 1 || c->scoring == 2) && w->correction_bias)
+            sel[r] += (double)w->correction_bias[r];
     }
     for (int r = 0; r < R; ++r) taken[r] = 0;
     for (int k = 0; k < K; ++k) {

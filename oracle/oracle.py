@@ -267,11 +267,14 @@ def moe_forward_dense(inp, forced_idx=None):
     L = x @ _f64(inp.router_w).T
     if inp.router_logit_bias is not None:
         L = L + _f64(inp.router_logit_bias)[None, :]
-    L = L - L.max(axis=1, keepdims=True)
-    p = np.exp(L)
-    p = p / p.sum(axis=1, keepdims=True)
+    if s.scoring == 2:                     # sigmoid arm: each column scored on its own
+        p = 0.5 * (1.0 + np.tanh(0.5 * L))   # = 1 / (1 + e^-L), written differently
+    else:
+        L = L - L.max(axis=1, keepdims=True)
+        p = np.exp(L)
+        p = p / p.sum(axis=1, keepdims=True)
     sel = p.copy()
-    if s.scoring == 1 and inp.correction_bias is not None:
+    if s.scoring in (1, 2) and inp.correction_bias is not None:
         sel = sel + _f64(inp.correction_bias)[None, :]
     # K best by (score desc, index asc): lexsort with the index as the secondary key
     order = np.lexsort((np.broadcast_to(np.arange(R), sel.shape), -sel), axis=1)

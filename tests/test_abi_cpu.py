@@ -56,6 +56,8 @@ def _cfg(B, **kw):
     (dict(inter=96), 2),
     (dict(shared_inter=100), 2),
     (dict(router_width=12), 2),               # identity experts need softmax + bias scoring
+    (dict(router_width=12, scoring=2), 2),    # ... not the sigmoid + bias scoring
+    (dict(scoring=3), 1),                     # no such scoring
     (dict(top_k=33, router_width=64, num_experts=64), 2),
     (dict(router_width=2048, num_experts=2048, scoring=1), 2),
 ])

@@ -56,6 +56,23 @@ SMALL = {
     "odd_tiles_decode": I.DECODE.with_(name="odd_tiles_decode", num_tokens=16, hidden=384,
                                        num_experts=24, router_width=24, top_k=3, inter=384,
                                        shared_inter=128),
+    # sigmoid + correction-bias scoring: 32 routed pairs (the decode kernel's split routing),
+    # a router wider than 256 columns (arg-max rounds), and a grouped-chain batch
+    "sigmoid_bias_decode": I.DECODE.with_(name="sigmoid_bias_decode", hidden=512,
+                                          num_experts=64, router_width=64, inter=256,
+                                          shared_inter=256, scoring=I.SCORING_SIGMOID_BIAS,
+                                          correction_bias_std=0.05, routed_scaling_factor=2.5),
+    "sigmoid_wide_decode": I.DECODE.with_(name="sigmoid_wide_decode", num_tokens=3, hidden=256,
+                                          num_experts=320, router_width=320, top_k=4,
+                                          inter=128, shared_inter=0, shared_gated=False,
+                                          scoring=I.SCORING_SIGMOID_BIAS,
+                                          correction_bias_std=0.05, norm_topk_prob=False),
+    "sigmoid_bias_small": I.PREFILL.with_(name="sigmoid_bias_small", num_tokens=200,
+                                          hidden=512, num_experts=32, router_width=32,
+                                          top_k=6, inter=256, shared_inter=0, zipf_s=0.0,
+                                          scoring=I.SCORING_SIGMOID_BIAS,
+                                          correction_bias_std=0.05, norm_topk_prob=False,
+                                          routed_scaling_factor=1.5),
 }
 
 

@@ -188,6 +188,51 @@ def test_selection_scores_are_probabilities_plus_bias():
     np.testing.assert_allclose(r["sel"], want, rtol=1e-12, atol=1e-15)
 
 
+def test_sigmoid_topk_brute_force_with_bias():
+    """Sigmoid + bias arm: the chosen set is the unique K-subset ranking before every other
+    column under (sigmoid(L) + bias desc, index asc), sigmoid taken from torch; the selection
+    scores are those; the weights are the chosen unbiased scores, renormalised."""
+    shape = small(I.TINY, num_tokens=12, router_width=8, num_experts=8, top_k=3,
+                  scoring=I.SCORING_SIGMOID_BIAS, correction_bias_std=0.05,
+                  routed_scaling_factor=1.5)
+    inp = I.make_inputs(shape)
+    L = inp.x.double() @ inp.router_w.double().T
+    s = torch.sigmoid(L).numpy()
+    sel = s + inp.correction_bias.double().numpy()[None, :]
+    R, K = 8, 3
+    for impl in (O.moe_forward, O.moe_forward_dense):
+        r = impl(inp)
+        for t in range(shape.num_tokens):
+            def before(a, b):
+                return sel[t, a] > sel[t, b] or (sel[t, a] == sel[t, b] and a < b)
+            winners = [S for S in itertools.combinations(range(R), K)
+                       if all(before(a, b) for a in S for b in range(R) if b not in S)]
+            assert len(winners) == 1 and sorted(r["idx"][t]) == sorted(winners[0])
+            got = list(r["idx"][t])
+            assert all(before(got[i], got[i + 1]) for i in range(K - 1))
+            np.testing.assert_allclose(r["w"][t].sum(), 1.5, rtol=1e-13)
+            np.testing.assert_allclose(r["w"][t] / r["w"][t].sum(),
+                                       s[t, got] / s[t, got].sum(), rtol=1e-12)
+    np.testing.assert_allclose(O.moe_forward(inp, routing_only=True)["sel"], sel, rtol=1e-12,
+                               atol=1e-15)
+
+
+def test_sigmoid_without_bias_selects_by_logits():
+    """Sigmoid is increasing, so with a zero bias the K chosen columns are the K largest
+    logits (numpy argsort of the library matmul), the same set softmax scoring picks."""
+    shape = small(I.TINY, num_tokens=32, router_width=16, num_experts=16, top_k=4,
+                  scoring=I.SCORING_SIGMOID_BIAS)
+    inp = I.make_inputs(shape)
+    inp.correction_bias = torch.zeros(16)
+    L = (inp.x.double() @ inp.router_w.double().T).numpy()
+    order = np.lexsort((np.broadcast_to(np.arange(16), L.shape), -L), axis=1)[:, :4]
+    r = O.moe_forward(inp, routing_only=True)
+    np.testing.assert_array_equal(r["idx"], order)
+    soft = O.moe_forward(I.make_inputs(shape.with_(scoring=I.SCORING_SOFTMAX)),
+                         routing_only=True)
+    np.testing.assert_array_equal(np.sort(soft["idx"], 1), np.sort(r["idx"], 1))
+
+
 def test_gap_matches_sorted_scores_with_bias():
     shape = small(I.ZERO_EXPERT, num_tokens=32, hidden=256, num_experts=16, router_width=24,
                   inter=128)
