@@ -35,7 +35,8 @@ WDTYPE_BF16 = 0
 WDTYPE_FP8_E4M3_B128 = 1
 
 _TENSOR_IDS = {"x": 0, "router_w": 1, "w_gate": 2, "w_up": 3, "w_down": 4,
-               "sh_gate": 5, "sh_up": 6, "sh_down": 7, "sh_gate_vec": 8, "bias": 9}
+               "sh_gate": 5, "sh_up": 6, "sh_down": 7, "sh_gate_vec": 8, "bias": 9,
+               "norm_w": 10}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -56,6 +57,8 @@ class MoeShape:
     weight_dtype: int = WDTYPE_BF16
     zipf_s: float = 0.0        # >0: skewed per-expert router-logit offsets
     correction_bias_std: float = 0.0  # >0 with the *_BIAS scorings
+    pre_expert_norm: bool = False     # RMSNorm of the routed experts' input (weight ~ 1 + N(0, 0.1))
+    rms_norm_eps: float = 1e-6
     seed: int = 0
 
     def with_(self, **kw) -> "MoeShape":
@@ -127,6 +130,7 @@ class MoeInputs:
     sh_gate_vec: Optional[torch.Tensor] = None
     router_logit_bias: Optional[torch.Tensor] = None
     correction_bias: Optional[torch.Tensor] = None
+    pre_expert_norm_w: Optional[torch.Tensor] = None
 
     def tensors(self):
         return {k: v for k, v in dataclasses.asdict(self).items()
@@ -175,8 +179,11 @@ def make_inputs(shape: MoeShape, device="cpu", x_only_tokens: Optional[int] = No
         rlb = rlb.to(torch.float32).to(device)
     if shape.correction_bias_std > 0:
         cb = _randn(shape, "bias", (R,), shape.correction_bias_std, device)
+    nw = None
+    if shape.pre_expert_norm:
+        nw = (1.0 + _randn(shape, "norm_w", (H,), 0.1, device)).to(bf)
     return MoeInputs(shape=shape, x=x, router_w=router_w, **out, **sh,
-                     router_logit_bias=rlb, correction_bias=cb)
+                     router_logit_bias=rlb, correction_bias=cb, pre_expert_norm_w=nw)
 
 
 def l2_flush_bytes() -> int:

@@ -116,6 +116,7 @@ typedef struct {
     int32_t norm_topk_prob;
     double routed_scaling_factor;
     int32_t weight_dtype;     /* 0 bf16, 1 E4M3 + fp32 128x128 block scales */
+    double rms_norm_eps;      /* with pre_expert_norm_w: epsilon of the pre-expert RMSNorm */
 } orc_config_t;
 
 typedef struct {
@@ -126,6 +127,7 @@ typedef struct {
     const float *s_gate, *s_up, *s_down; /* [E,I/128,H/128], [E,I/128,H/128], [E,H/128,I/128] */
     const uint16_t *sh_gate, *sh_up, *sh_down; /* bf16 [S,H], [S,H], [H,S] */
     const uint16_t *sh_gate_vec;      /* bf16 [H] or NULL */
+    const uint16_t *pre_expert_norm_w; /* bf16 [H] or NULL: RMSNorm of the routed experts' input */
 } orc_weights_t;
 
 /* Router logits of one token, fp64: L[r] = sum_h x[h] * Wr[r,h] (+ logit bias[r]). */
@@ -252,6 +254,33 @@ static void shared_ffn(const orc_config_t *c, const orc_weights_t *w, const doub
     }
 }
 
+/* ---------------------------------------------------------------- pre-expert norm */
+
+/* Nearest bf16 (ties to even) of v taken to fp32 first: the normed copy of the pages is a
+ * bf16 buffer written from fp32 arithmetic. */
+static double round_bf16_via_f32(double v) {
+    float f = (float)v;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    u &= 0xFFFF0000u;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Routed experts' input with a pre-expert norm ("metrale_model_layers/layers/moe/
+ * forward_prefill.rs", `pre_expert_norm`: after routing, before expert dispatch; the router
+ * and the shared-expert blend keep reading the un-normed input):
+ * xn[h] = bf16( x[h] * g[h] / sqrt(mean_h x^2 + eps) ). */
+static void pre_expert_rms_norm(const orc_config_t *c, const uint16_t *g, const double *x,
+                                double *xn) {
+    int H = c->hidden;
+    double ss = 0.0;
+    for (int h = 0; h < H; ++h) ss += x[h] * x[h];
+    double inv = 1.0 / sqrt(ss / (double)H + c->rms_norm_eps);
+    for (int h = 0; h < H; ++h) xn[h] = round_bf16_via_f32(x[h] * orc_bf16_to_f64(g[h]) * inv);
+}
+
 /* ---------------------------------------------------------------- the block forward */
 
 /* Forward of the tokens listed in `tokens` (n_sel of them; NULL = all N in order).
@@ -294,11 +323,12 @@ int orc_moe_forward(const orc_config_t *c, const orc_weights_t *w, const uint16_
         route_token(c, w, L, forced_idx ? forced_idx + (size_t)t * K : NULL, idx, wt, &zsum,
                     &gap, p, sel, taken);
         if (!routing_only) {
+            /* the routed experts' input: x, or its pre-expert RMSNorm */
+            if (w->pre_expert_norm_w) pre_expert_rms_norm(c, w->pre_expert_norm_w, xt, xe);
+            else memcpy(xe, xt, sizeof(double) * H);
             if (c->weight_dtype == 1) {
-                for (int h = 0; h < H; ++h) x32[h] = (float)xt[h];
+                for (int h = 0; h < H; ++h) x32[h] = (float)xe[h];
                 quant_1x128(x32, H, xe, NULL, NULL);
-            } else {
-                memcpy(xe, xt, sizeof(double) * H);
             }
             for (int h = 0; h < H; ++h) acc[h] = 0.0;
             for (int k = 0; k < K; ++k) {

@@ -56,13 +56,16 @@ class _Config(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("inter", ctypes.c_int32),
                 ("shared_inter", ctypes.c_int32), ("scoring", ctypes.c_int32),
                 ("norm_topk_prob", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_double),
-                ("weight_dtype", ctypes.c_int32)]
+                ("weight_dtype", ctypes.c_int32), ("rms_norm_eps", ctypes.c_double)]
+
+
+_WEIGHTS = ("router_w", "router_logit_bias", "correction_bias", "w_gate", "w_up", "w_down",
+            "s_gate", "s_up", "s_down", "sh_gate", "sh_up", "sh_down", "sh_gate_vec",
+            "pre_expert_norm_w")
 
 
 class _Weights(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in (
-        "router_w", "router_logit_bias", "correction_bias", "w_gate", "w_up", "w_down",
-        "s_gate", "s_up", "s_down", "sh_gate", "sh_up", "sh_down", "sh_gate_vec")]
+    _fields_ = [(n, ctypes.c_void_p) for n in _WEIGHTS]
 
 
 def _load():
@@ -100,7 +103,7 @@ def _cfg(shape) -> _Config:
     return _Config(shape.num_tokens, shape.hidden, shape.num_experts, shape.router_width,
                    shape.top_k, shape.inter, shape.shared_inter, shape.scoring,
                    int(shape.norm_topk_prob), float(shape.routed_scaling_factor),
-                   shape.weight_dtype)
+                   shape.weight_dtype, float(shape.rms_norm_eps))
 
 
 def moe_forward(inp, tokens=None, forced_idx=None, routing_only: bool = False):
@@ -113,9 +116,7 @@ def moe_forward(inp, tokens=None, forced_idx=None, routing_only: bool = False):
     lib = _load()
     s = inp.shape
     keep: list = []
-    wts = _Weights(*[_host(getattr(inp, n), keep) for n in (
-        "router_w", "router_logit_bias", "correction_bias", "w_gate", "w_up", "w_down",
-        "s_gate", "s_up", "s_down", "sh_gate", "sh_up", "sh_down", "sh_gate_vec")])
+    wts = _Weights(*[_host(getattr(inp, n), keep) for n in _WEIGHTS])
     x = _host(inp.x, keep)
     if tokens is None:
         tok = None
@@ -287,14 +288,19 @@ def moe_forward_dense(inp, forced_idx=None):
     M = np.zeros((N, R))
     for k in range(K):
         M[np.arange(N), idx[:, k]] += w[:, k]
+    xr = x                                  # routed experts' input
+    if inp.pre_expert_norm_w is not None:   # RMSNorm, stored as bf16 like the pages' buffer
+        rms = np.sqrt(np.mean(x * x, axis=1, keepdims=True) + s.rms_norm_eps)
+        xr = x / rms * _f64(inp.pre_expert_norm_w)[None, :]
+        xr = torch.from_numpy(xr).to(torch.float32).to(torch.bfloat16).double().numpy()
     if s.weight_dtype == 1:
         Wg = _dequant_blocks(inp.w_gate, inp.s_gate)
         Wu = _dequant_blocks(inp.w_up, inp.s_up)
         Wd = _dequant_blocks(inp.w_down, inp.s_down)
-        xe = _quant_rows_np(x)
+        xe = _quant_rows_np(xr)
     else:
         Wg, Wu, Wd = _f64(inp.w_gate), _f64(inp.w_up), _f64(inp.w_down)
-        xe = x
+        xe = xr
     out = np.zeros_like(x)
     for e in range(E):
         if not M[:, e].any():

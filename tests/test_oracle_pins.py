@@ -47,7 +47,9 @@ def inputs_from_case(c):
     shape = I.MoeShape(c["name"], int(kv["N"]), int(kv["H"]), int(kv["E"]), int(kv["R"]),
                        int(kv["K"]), int(kv["I"]), shared_inter=int(kv["S"]),
                        scoring=int(kv["scoring"]), norm_topk_prob=bool(int(kv["norm"])),
-                       routed_scaling_factor=float(kv["scale"]))
+                       routed_scaling_factor=float(kv["scale"]),
+                       pre_expert_norm="pre_expert_norm_w" in c,
+                       rms_norm_eps=float(kv.get("eps", 1e-6)))
     bf = torch.bfloat16
     N, H, E, R, Ii, S = (shape.num_tokens, shape.hidden, shape.num_experts, shape.router_width,
                          shape.inter, shape.shared_inter)
@@ -63,6 +65,8 @@ def inputs_from_case(c):
               w_down=mat("w_down", E * H, Ii).reshape(E, H, Ii))
     if "correction_bias" in c:
         kw["correction_bias"] = torch.tensor(_rows(c["correction_bias"])[0], dtype=torch.float32)
+    if "pre_expert_norm_w" in c:
+        kw["pre_expert_norm_w"] = mat("pre_expert_norm_w", 1, H).reshape(H)
     if S:
         kw["sh_gate"] = mat("sh_gate", S, H)
         kw["sh_up"] = mat("sh_up", S, H)
@@ -322,7 +326,11 @@ def test_mixed_identity_and_zero_weight_experts():
     assert np.array_equal(r["out"], r["zsum"][:, None] * inp.x.double().numpy())
 
 
-@pytest.mark.parametrize("base", [I.TINY, I.DECODE, I.ZERO_EXPERT, I.PREFILL],
+@pytest.mark.parametrize("base", [I.TINY, I.DECODE, I.ZERO_EXPERT, I.PREFILL,
+                                  I.DECODE.with_(name="decode_prenorm", pre_expert_norm=True),
+                                  I.PREFILL.with_(name="sigmoid_prenorm", pre_expert_norm=True,
+                                                  scoring=I.SCORING_SIGMOID_BIAS,
+                                                  correction_bias_std=0.05, zipf_s=0.0)],
                          ids=lambda s: s.name)
 def test_loop_and_dense_formulations_agree(base):
     shape = base.with_(num_tokens=min(base.num_tokens, 24), hidden=256,
