@@ -173,13 +173,14 @@ def kernels_per_step(B, cfg):
     """Kernels of this library one forward launches (memsets are not kernels)."""
     decode = cfg.path == B.PATH_DECODE or (cfg.path == B.PATH_AUTO and cfg.num_tokens <= 16
                                             and cfg.weight_dtype == 0)
-    if decode:
-        return 1            # router, top-K, sort, projections and combine in one kernel
+    if decode:              # router, top-K, sort, projections and combine in one kernel (and
+        return 1 + (1 if cfg.pre_expert_norm else 0)   # the pre-expert norm's row kernel)
     # router, top-K, 3 sort, gate/up GEMM, down GEMM, combine; FP8 experts add the token-row
     # quantiser and run the bf16 shared expert in two launches of its own
+    norm = 1 if cfg.pre_expert_norm else 0
     if cfg.weight_dtype == 1:
-        return 9 + (2 if cfg.shared_inter else 0)
-    return 8
+        return 9 + (2 if cfg.shared_inter else 0) + norm
+    return 8 + norm
 
 
 def replicas_value(ms_local, tokens_per_replica, device="cpu"):
@@ -505,7 +506,7 @@ def main():
         line["gpu_launches"] += p["launches_per_step"] * max(3, args.steps // 2)
     if not args.no_extra:
         extra = {}
-        for shp in (I.ZERO_EXPERT, I.FP8_PREFILL, I.TINY):
+        for shp in (I.ZERO_EXPERT, I.FP8_PREFILL, I.TINY, I.DECODE_PRENORM):
             x = time_ours(B, shp, max(3, args.steps // 2), warmup, dev, peaks, with_e2e=False)
             xa = x["alg"]
             fp8 = shp.weight_dtype == I.WDTYPE_FP8_E4M3_B128

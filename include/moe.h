@@ -16,6 +16,7 @@
  *   idx[t,:] = top-K of p (or of p + correction_bias), ties to the lower id
  *   w[t,k]   = p[t,idx] (/ sum_k if norm_topk_prob) * routed_scaling_factor
  *   out[t,:] = sum_{k: idx<E} w[t,k] * (SiLU(x Wg_e^T) * (x Wu_e^T)) Wd_e^T
+ *                                   (x = its pre-expert RMSNorm here when pre_expert_norm)
  *            + (sum_{k: idx>=E} w[t,k]) * x[t,:]            identity ("zero-computation") experts
  *            + gamma_t * (SiLU(x Sg^T) * (x Su^T)) Sd^T      shared expert, gamma_t = sigmoid(x.g)
  *                                                             or 1 when g is NULL
@@ -104,6 +105,12 @@ typedef struct {
                             accumulates the weighted routed down projections into [N,H] with
                             FP32 atomics in any order */
   int32_t path;          /* moe_path_t */
+  int32_t pre_expert_norm; /* nonzero: the routed experts read RMSNorm(x) (weights
+                              pre_expert_norm_w), xn = bf16(x * g / sqrt(mean(x^2) + eps)),
+                              while the router, the shared expert and its gate and the identity
+                              experts read x ("metrale_model_layers/layers/moe/
+                              forward_prefill.rs", `pre_expert_norm`) */
+  float rms_norm_eps;      /* eps of that norm (>= 0) */
 } moe_config_t;
 
 typedef struct {
@@ -122,6 +129,7 @@ typedef struct {
   const void *sh_down;             /* bf16 [H,S] */
   const void *sh_gate_vec;         /* nullable bf16 [H]: shared blend weight sigmoid(x . g);
                                       NULL = weight 1 */
+  const void *pre_expert_norm_w;   /* bf16 [H], required iff pre_expert_norm */
 } moe_weights_t;
 
 /* Bytes of device workspace moe_forward / moe_route need for `cfg` (path resolved as in

@@ -41,11 +41,13 @@ class moe_config_t(ctypes.Structure):
                 ("shared_inter", ctypes.c_int32), ("scoring", ctypes.c_int32),
                 ("norm_topk_prob", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
                 ("weight_dtype", ctypes.c_int32), ("deterministic", ctypes.c_int32),
-                ("path", ctypes.c_int32)]
+                ("path", ctypes.c_int32), ("pre_expert_norm", ctypes.c_int32),
+                ("rms_norm_eps", ctypes.c_float)]
 
 
 _WEIGHT_FIELDS = ("router_w", "router_logit_bias", "correction_bias", "w_gate", "w_up", "w_down",
-                  "s_gate", "s_up", "s_down", "sh_gate", "sh_up", "sh_down", "sh_gate_vec")
+                  "s_gate", "s_up", "s_down", "sh_gate", "sh_up", "sh_down", "sh_gate_vec",
+                  "pre_expert_norm_w")
 
 
 class moe_weights_t(ctypes.Structure):
@@ -91,7 +93,8 @@ def make_config(shape: "_inputs.MoeShape", deterministic: bool = True,
     return moe_config_t(shape.num_tokens, shape.hidden, shape.num_experts, shape.router_width,
                         shape.top_k, shape.inter, shape.shared_inter, shape.scoring,
                         int(shape.norm_topk_prob), float(shape.routed_scaling_factor),
-                        shape.weight_dtype, int(deterministic), path)
+                        shape.weight_dtype, int(deterministic), path,
+                        int(shape.pre_expert_norm), float(shape.rms_norm_eps))
 
 
 def _ptr(t: Optional[torch.Tensor]):

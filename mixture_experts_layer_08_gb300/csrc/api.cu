@@ -10,6 +10,7 @@
 // bytes needed and available; the FP32 accumulator sits at a 256-byte aligned offset).
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <cstdio>
 #include <map>
 #include <mutex>
@@ -25,7 +26,7 @@ constexpr int kSmallRouterMaxTokens = 64;
 enum Region {
   // the decode chain's accumulators follow the header so one memset clears them all
   R_HDR, R_SYNC, R_HD, R_YD, R_ACC, R_SHY, R_LOGITS, R_IDX, R_W, R_ZSUM, R_BLK, R_LRANK, R_OFFS,
-  R_P2R, R_SPAIRS, R_ACTIVE, R_TILES, R_XQT, R_XST, R_XP, R_XS, R_HH, R_HS, R_Y, R_SHH, R_NUM
+  R_P2R, R_SPAIRS, R_ACTIVE, R_TILES, R_XQT, R_XST, R_XP, R_XS, R_HH, R_HS, R_Y, R_SHH, R_XN, R_NUM
 };
 
 struct Layout {
@@ -57,6 +58,8 @@ moe_status_t validate_config(const moe_config_t* c) {
   if (c->weight_dtype != MOE_W_BF16 && c->weight_dtype != MOE_W_FP8_E4M3_B128)
     return MOE_ERR_INVALID_ARG;
   if (c->path < MOE_PATH_AUTO || c->path > MOE_PATH_GROUPED) return MOE_ERR_INVALID_ARG;
+  if (c->pre_expert_norm && !(c->rms_norm_eps >= 0.0f && c->rms_norm_eps < INFINITY))
+    return MOE_ERR_INVALID_ARG;
   // identity experts are wired only on the softmax + correction-bias arm
   if (c->router_width != c->num_experts && c->scoring != MOE_SCORING_SOFTMAX_BIAS)
     return MOE_ERR_UNSUPPORTED;
@@ -98,6 +101,7 @@ Layout make_layout(const moe_config_t* c) {
   sz[R_P2R] = te * 4;
   sz[R_SPAIRS] = te * 4;
   sz[R_ACTIVE] = E * 4;
+  sz[R_XN] = c->pre_expert_norm ? N * H * 2 : 0;   // the routed experts' normed input
   if (L.path == MOE_PATH_GROUPED) {
     sz[R_BLK] = (size_t)L.nblk * E * 4;
     sz[R_LRANK] = te * 4;
@@ -223,8 +227,10 @@ moe_status_t validate_weights(const moe_config_t* c, const moe_weights_t* w) {
   if (c->weight_dtype == MOE_W_FP8_E4M3_B128 && (!w->s_gate || !w->s_up || !w->s_down))
     return MOE_ERR_INVALID_ARG;
   if (c->shared_inter > 0 && (!w->sh_gate || !w->sh_up || !w->sh_down)) return MOE_ERR_INVALID_ARG;
+  if (c->pre_expert_norm && !w->pre_expert_norm_w) return MOE_ERR_INVALID_ARG;
   const void* ps[] = {w->router_w, w->w_gate, w->w_up, w->w_down, w->sh_gate, w->sh_up,
-                      w->sh_down, w->sh_gate_vec};
+                      w->sh_down, w->sh_gate_vec, c->pre_expert_norm ? w->pre_expert_norm_w
+                                                                     : nullptr};
   for (const void* p : ps)
     if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
@@ -341,10 +347,18 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
   }
   CK(launch_topk(ra, st));
   const bool fp8 = c->weight_dtype == MOE_W_FP8_E4M3_B128;
+  // the routed experts' input: x, or its pre-expert RMSNorm (after the routing, which read x)
+  const __nv_bfloat16* xe = ra.x;
+  if (gather && c->pre_expert_norm) {
+    CK(launch_rms_norm_rows(ra.x, static_cast<const __nv_bfloat16*>(w->pre_expert_norm_w),
+                            c->rms_norm_eps, c->num_tokens, c->hidden,
+                            P.at<__nv_bfloat16>(R_XN), st));
+    xe = P.at<__nv_bfloat16>(R_XN);
+  }
   if (gather && fp8)
-    CK(launch_quant_rows(ra.x, c->num_tokens, c->hidden, P.at<uint8_t>(R_XQT),
+    CK(launch_quant_rows(xe, c->num_tokens, c->hidden, P.at<uint8_t>(R_XQT),
                          P.at<float>(R_XST), st));
-  CK(launch_sort(sa, ra.x, c->hidden, gather && !fp8 ? P.at<__nv_bfloat16>(R_XP) : nullptr,
+  CK(launch_sort(sa, xe, c->hidden, gather && !fp8 ? P.at<__nv_bfloat16>(R_XP) : nullptr,
                  gather && fp8 ? P.at<uint8_t>(R_XP) : nullptr,
                  gather && fp8 ? P.at<float>(R_XS) : nullptr, st));
   return MOE_OK;
@@ -523,6 +537,13 @@ moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const voi
   WsHeader* hdr = P.at<WsHeader>(R_HDR);
   MARK(MOE_STAGE_ROUTE, 0);
   CK(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));   // the kernel clears its accumulators
+  const void* xn = x;   // the routed experts' input
+  if (c->pre_expert_norm) {
+    CK(launch_rms_norm_rows(static_cast<const __nv_bfloat16*>(x),
+                            static_cast<const __nv_bfloat16*>(w->pre_expert_norm_w),
+                            c->rms_norm_eps, N, H, P.at<__nv_bfloat16>(R_XN), st));
+    xn = P.at<void>(R_XN);
+  }
   MARK(MOE_STAGE_ROUTE, 1);
   DecodeArgs d{};
   d.x = static_cast<const __nv_bfloat16*>(x);
@@ -564,7 +585,8 @@ moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const voi
   if (!make_map_bf16(&maps[kDmWg], w->w_gate, H, (uint64_t)E * I, bg) ||
       !make_map_bf16(&maps[kDmWu], w->w_up, H, (uint64_t)E * I, bg) ||
       !make_map_bf16(&maps[kDmWd], w->w_down, I, (uint64_t)E * H, bd) ||
-      !make_map_bf16(&maps[kDmX], x, H, N, kDecodeBoxRowsX))
+      !make_map_bf16(&maps[kDmX], x, H, N, kDecodeBoxRowsX) ||
+      !make_map_bf16(&maps[kDmXn], xn, H, N, kDecodeBoxRowsX))
     return MOE_ERR_CUDA;
   if (S > 0) {
     if (!make_map_bf16(&maps[kDmSg], w->sh_gate, H, S, bg) ||

@@ -804,7 +804,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const __grid_constant__ CUtensorMap tm_su,
                           const __grid_constant__ CUtensorMap tm_wd,
                           const __grid_constant__ CUtensorMap tm_sd,
-                          const __grid_constant__ CUtensorMap tm_x, const DecodeArgs a,
+                          const __grid_constant__ CUtensorMap tm_x,
+                          const __grid_constant__ CUtensorMap tm_xn, const DecodeArgs a,
                           const Plan pl) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ Routing meta;
@@ -847,6 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_wu);
     tma_prefetch_desc(&tm_wd);
     tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_xn);
     if (a.S) {
       tma_prefetch_desc(&tm_sg);
       tma_prefetch_desc(&tm_su);
@@ -874,8 +876,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       // the weight box of item k: its tensor map and coordinates
-      auto locate = [&](int k, bool& down, int& kc, const CUtensorMap*& m, int& row) {
-        int tile, slot, lt;
+      auto locate = [&](int k, bool& down, int& kc, int& slot, const CUtensorMap*& m, int& row) {
+        int tile, lt;
         sc.item(k, down, tile, kc, slot, lt);
         if (!down) {
           const int nt = slot >= 0 ? sc.nIt : sc.nSt;
@@ -899,13 +901,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < nitems; ++k) {
         if (!mbar_wait(&empty[s], ph ^ 1, hdr)) { ok = false; break; }
         bool down;
-        int kc, row;
+        int kc, slot, row;
         const CUtensorMap* m;
-        locate(k, down, kc, m, row);
+        locate(k, down, kc, slot, m, row);
         uint8_t* wst = ring + (size_t)s * kWBytes;
-        if (!down) {
+        if (!down) {   // (routed experts read their input xn, the shared expert x)
           mbar_arrive_expect_tx(&full[s], (uint32_t)(pl.bn_g * 128 + kTokBytes));
-          tma_load_2d(xtok + (size_t)s * kTokBytes, &tm_x, kc * kBox, 0, &full[s]);
+          tma_load_2d(xtok + (size_t)s * kTokBytes, slot >= 0 ? &tm_xn : &tm_x, kc * kBox, 0,
+                      &full[s]);
         } else {
           mbar_arrive_expect_tx(&full[s], (uint32_t)(pl.bn_d * 128));
         }
@@ -1212,7 +1215,8 @@ cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_forward_kernel, maps[kDmWg], maps[kDmWu], maps[kDmSg],
-                            maps[kDmSu], maps[kDmWd], maps[kDmSd], maps[kDmX], a, pl);
+                            maps[kDmSu], maps[kDmWd], maps[kDmSd], maps[kDmX], maps[kDmXn], a,
+                            pl);
 }
 
 }  // namespace moe

@@ -68,6 +68,9 @@ cudaError_t launch_router_small(const RouteArgs& a, const SortArgs& s, bool fuse
 // Scoring + top-K + weights, one warp per token.
 cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st);
 // Per 1x128 E4M3 quantisation of the token rows (FP8 experts): codes [N,H], scales [H/128,N].
+// xn[t,:] = bf16(x[t,:] * g / sqrt(mean(x[t,:]^2) + eps)), fp32 arithmetic; one warp per row.
+cudaError_t launch_rms_norm_rows(const __nv_bfloat16* x, const __nv_bfloat16* g, float eps, int N,
+                                 int H, __nv_bfloat16* xn, cudaStream_t st);
 cudaError_t launch_quant_rows(const __nv_bfloat16* x, int N, int H, uint8_t* q, float* sc,
                               cudaStream_t st);
 // Stable counting sort of the (token, slot) pairs by expert (count / scan / scatter) and the
@@ -118,8 +121,9 @@ struct DecodeArgs {
   __nv_bfloat16* out;              // [N,H]
 };
 // Tensor maps (bf16, box {64, rows}, 128-byte swizzle) the decode kernel streams from.
-enum DecodeMap { kDmWg = 0, kDmWu, kDmSg, kDmSu, kDmWd, kDmSd, kDmX, kDmNum };
-// Box rows: x 16; gate/up weights (Wg, Wu, Sg, Su) *bn_g; down weights (Wd, Sd) *bn_d.
+enum DecodeMap { kDmWg = 0, kDmWu, kDmSg, kDmSu, kDmWd, kDmSd, kDmX, kDmXn, kDmNum };
+// Box rows: x and the routed experts' input xn (x itself without a pre-expert norm) 16;
+// gate/up weights (Wg, Wu, Sg, Su) *bn_g; down weights (Wd, Sd) *bn_d.
 constexpr int kDecodeBoxRowsX = 16;
 void decode_tile_rows(int H, int I, int S, int* bn_g, int* bn_d);
 // The decode forward as one cooperative launch.

@@ -312,6 +312,50 @@ __global__ void __launch_bounds__(256) sort_scatter_kernel(SortArgs s, const __n
   }
 }
 
+// Pre-expert RMSNorm ("metrale_model_layers/layers/moe/forward_prefill.rs",
+// `pre_expert_norm`): one warp per token row; the sum of squares in fp32 (loads in flight four
+// at a time), then xn = bf16(x * g * (1 / sqrt(mean + eps))).
+__global__ void __launch_bounds__(256) rms_norm_rows_kernel(const __nv_bfloat16* x,
+                                                            const __nv_bfloat16* g, float eps,
+                                                            int N, int H, __nv_bfloat16* xn) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= N) return;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  const uint4* gs = reinterpret_cast<const uint4*>(g);
+  uint4* dst = reinterpret_cast<uint4*>(xn + (size_t)t * H);
+  const int C = H / 8;
+  float ss = 0.0f;
+  for (int c0 = 0; c0 < C; c0 += 4 * 32) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u * 32 + lane;
+      v[u] = c < C ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float f[8];
+      bf16x8_to_f32(v[u], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+    }
+  }
+  ss = warp_sum(ss);
+  const float inv = 1.0f / sqrtf(ss / (float)H + eps);
+  for (int c = lane; c < C; c += 32) {
+    float f[8], w[8];
+    bf16x8_to_f32(__ldg(src + c), f);
+    bf16x8_to_f32(__ldg(gs + c), w);
+    uint4 o;
+    o.x = pack_bf16x2(f[0] * w[0] * inv, f[1] * w[1] * inv);
+    o.y = pack_bf16x2(f[2] * w[2] * inv, f[3] * w[3] * inv);
+    o.z = pack_bf16x2(f[4] * w[4] * inv, f[5] * w[5] * inv);
+    o.w = pack_bf16x2(f[6] * w[6] * inv, f[7] * w[7] * inv);
+    dst[c] = o;
+  }
+}
+
 // One warp per token row: per 1x128 group, amax, scale = amax/448 (1 if 0) and the E4M3
 // code of value/scale (round to nearest even, saturating), all decided in fp32.
 // Codes [N, H]; scales [H/128, N].
@@ -360,6 +404,12 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* x,
 }
 
 }  // namespace
+
+cudaError_t launch_rms_norm_rows(const __nv_bfloat16* x, const __nv_bfloat16* g, float eps, int N,
+                                 int H, __nv_bfloat16* xn, cudaStream_t st) {
+  rms_norm_rows_kernel<<<(N + 7) / 8, 256, 0, st>>>(x, g, eps, N, H, xn);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quant_rows(const __nv_bfloat16* x, int N, int H, uint8_t* q, float* sc,
                               cudaStream_t st) {

@@ -67,6 +67,14 @@ SMALL = {
                                           inter=128, shared_inter=0, shared_gated=False,
                                           scoring=I.SCORING_SIGMOID_BIAS,
                                           correction_bias_std=0.05, norm_topk_prob=False),
+    # pre-expert RMSNorm of the routed experts' input (router and shared expert read raw x)
+    "prenorm_decode": I.DECODE.with_(name="prenorm_decode", hidden=512, num_experts=64,
+                                     router_width=64, inter=256, shared_inter=256,
+                                     pre_expert_norm=True),
+    "prenorm_grouped": I.PREFILL.with_(name="prenorm_grouped", num_tokens=300, hidden=512,
+                                       num_experts=16, router_width=16, top_k=4, inter=256,
+                                       shared_inter=256, shared_gated=True,
+                                       pre_expert_norm=True),
     "sigmoid_bias_small": I.PREFILL.with_(name="sigmoid_bias_small", num_tokens=200,
                                           hidden=512, num_experts=32, router_width=32,
                                           top_k=6, inter=256, shared_inter=0, zipf_s=0.0,
@@ -284,7 +292,9 @@ FP8_SMALL = I.FP8_PREFILL.with_(name="fp8_small", num_tokens=300, hidden=512, nu
 @pytest.mark.parametrize("shape", [FP8_SMALL,
                                    FP8_SMALL.with_(name="fp8_small_k4", num_tokens=77,
                                                    num_experts=16, router_width=16, top_k=4,
-                                                   inter=384, hidden=768)],
+                                                   inter=384, hidden=768),
+                                   FP8_SMALL.with_(name="fp8_small_prenorm",
+                                                   pre_expert_norm=True)],
                          ids=lambda s: s.name)
 def test_fp8_forward_matches_oracle(B, shape):
     inp = I.make_inputs(shape)
