@@ -537,13 +537,8 @@ moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const voi
   WsHeader* hdr = P.at<WsHeader>(R_HDR);
   MARK(MOE_STAGE_ROUTE, 0);
   CK(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));   // the kernel clears its accumulators
-  const void* xn = x;   // the routed experts' input
-  if (c->pre_expert_norm) {
-    CK(launch_rms_norm_rows(static_cast<const __nv_bfloat16*>(x),
-                            static_cast<const __nv_bfloat16*>(w->pre_expert_norm_w),
-                            c->rms_norm_eps, N, H, P.at<__nv_bfloat16>(R_XN), st));
-    xn = P.at<void>(R_XN);
-  }
+  // the routed experts' input: x, or its pre-expert RMSNorm (written by the kernel's phase 0)
+  const void* xn = c->pre_expert_norm ? P.at<void>(R_XN) : x;
   MARK(MOE_STAGE_ROUTE, 1);
   DecodeArgs d{};
   d.x = static_cast<const __nv_bfloat16*>(x);
@@ -552,6 +547,9 @@ moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const voi
   d.corr_bias = c->scoring != MOE_SCORING_SOFTMAX ? w->correction_bias : nullptr;
   d.forced = forced;
   d.sh_gate_vec = S > 0 ? static_cast<const __nv_bfloat16*>(w->sh_gate_vec) : nullptr;
+  d.norm_w = c->pre_expert_norm ? static_cast<const __nv_bfloat16*>(w->pre_expert_norm_w) : nullptr;
+  d.eps = c->rms_norm_eps;
+  d.xn = c->pre_expert_norm ? P.at<__nv_bfloat16>(R_XN) : nullptr;
   d.N = N;
   d.H = H;
   d.E = E;

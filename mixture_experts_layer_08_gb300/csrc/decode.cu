@@ -221,6 +221,51 @@ __device__ void router_rows(const DecodeArgs& a, uint8_t* scratch, size_t scratc
   }
 }
 
+// Phase 0, with a pre-expert norm: xn[t] = bf16(x[t] * g / sqrt(mean(x[t]^2) + eps)), token t
+// by block G-1-t (the blocks past the router rows are otherwise idle in this phase), from the
+// staged x rows `xs`. The routed experts' gate/up items stream xn by TMA after the grid
+// barrier, so the writes are fenced for the async proxy first.
+__device__ void pre_expert_norm_rows(const DecodeArgs& a, const __nv_bfloat16* xs, float* red) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = a.H / 8;
+  bool wrote = false;
+  for (int t = (int)gridDim.x - 1 - (int)blockIdx.x; t >= 0 && t < a.N; t += gridDim.x) {
+    const uint4* xr = reinterpret_cast<const uint4*>(xs + (size_t)t * a.H);
+    float ss = 0.0f;
+#pragma unroll 1
+    for (int c = tid; c < C; c += kThreads) {
+      float f[8];
+      bf16x8_to_f32(xr[c], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) tot += red[w];
+    const float inv = 1.0f / sqrtf(tot / (float)a.H + a.eps);
+    const uint4* gs = reinterpret_cast<const uint4*>(a.norm_w);
+    uint4* dst = reinterpret_cast<uint4*>(a.xn + (size_t)t * a.H);
+#pragma unroll 1
+    for (int c = tid; c < C; c += kThreads) {
+      float f[8], w[8];
+      bf16x8_to_f32(xr[c], f);
+      bf16x8_to_f32(__ldg(gs + c), w);
+      uint4 o;
+      o.x = pack_bf16x2(f[0] * w[0] * inv, f[1] * w[1] * inv);
+      o.y = pack_bf16x2(f[2] * w[2] * inv, f[3] * w[3] * inv);
+      o.z = pack_bf16x2(f[4] * w[4] * inv, f[5] * w[5] * inv);
+      o.w = pack_bf16x2(f[6] * w[6] * inv, f[7] * w[7] * inv);
+      dst[c] = o;
+    }
+    wrote = true;
+    __syncthreads();   // (red is reused)
+  }
+  if (wrote) asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Wide routers (R > 256): K rounds of a warp arg-max (route_token_warp_reg), then the same
 // weights and blend gate.
 __device__ void topk_rounds_warp(const DecodeArgs& a, int t, uint32_t* idx_s, Routing& rt) {
@@ -859,6 +904,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- phases 0 and 1: router logits (spread over the grid) and zeroed accumulators, then
   // each block's routing
   router_rows(a, smem, (size_t)stages * (kTokBytes + kWBytes), red_s);
+  if (a.norm_w) {   // (x is still staged at the start of the dynamic region when it fit)
+    const bool staged = (size_t)a.N * a.H * 2 <= (size_t)stages * (kTokBytes + kWBytes);
+    pre_expert_norm_rows(a, staged ? reinterpret_cast<const __nv_bfloat16*>(smem) : a.x, red_s);
+  }
   zero_accumulators(a);
   grid_barrier(hdr, gridDim.x);
   const bool split_routing = a.te <= 32 && a.R <= 256;

@@ -97,6 +97,9 @@ struct DecodeArgs {
   const float* corr_bias;          // [R] or null (selection only)
   const uint32_t* forced;          // [N,K] or null
   const __nv_bfloat16* sh_gate_vec;    // [H] or null
+  const __nv_bfloat16* norm_w;     // [H] pre-expert RMSNorm weight, or null (no norm)
+  float eps;                       // its epsilon
+  __nv_bfloat16* xn;               // [N,H] the routed experts' input, written in phase 0 (norm)
   int N, H, E, R, K, I, S, te, scoring, norm;
   float scale;
   float* logits;                   // [N,R]
