@@ -15,10 +15,14 @@
 //
 // Phases, separated by two grid barriers (all blocks are resident: a bounded spin on a
 // counter in the workspace header):
-//   0  router logits: one warp per router row, rows spread over the blocks;
-//   1  every block routes the whole batch into its own shared memory (softmax, top-K,
-//      renormalisation, identity-expert sums, shared-expert gate, stable sort by expert);
-//      block 0 also writes the routing to the workspace;
+//   0  router logits: one router row per block (the contraction over all its threads), rows
+//      spread over the blocks; with a pre-expert norm, blocks past the router rows write the
+//      routed experts' input xn = RMSNorm(x);
+//   1  every block routes the whole batch into its own shared memory (softmax or sigmoid
+//      scores, top-K, renormalisation, identity-expert sums, shared-expert gate, stable sort
+//      by expert); block 0 also writes the routing to the workspace. With at most 32 routed
+//      pairs (and a router up to 256 wide) this phase stops once the experts in use are
+//      known, and the epilogue warps finish the sort and the weights during phase 2;
 //   2  gate/up then down projections (below);
 //   3  out[t] = bf16(sum_k w * y[row(t,k)] (or the atomic accumulator) + zsum * x + gamma * Sh),
 //      output chunks spread over the blocks.
@@ -26,7 +30,8 @@
 // Shape of the work. The weights are the wide B operand: a tile is BN (256, or 128 when a
 // dimension is not a multiple of 256) rows of one projection of one slot, so every MMA reads
 // its weights at the full-rate N. The batch is the A operand (M = 128): rows 0..15 hold the
-// tokens (x for gate/up, SiLU(gate)*up of the slot's tokens for down), rows 16..127 read
+// tokens (x -- or xn for routed experts under a pre-expert norm -- for gate/up,
+// SiLU(gate)*up of the slot's tokens for down), rows 16..127 read
 // whatever shared memory follows and only produce accumulator rows that are never read. A
 // work item is one tile times one 64-column swizzle box of its contraction (BN x 128 bytes).
 // Items are numbered slot-major; every block takes a contiguous, balanced range of the gate/up
