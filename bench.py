@@ -173,10 +173,11 @@ def kernels_per_step(B, cfg):
     """Kernels of this library one forward launches (memsets are not kernels)."""
     decode = cfg.path == B.PATH_DECODE or (cfg.path == B.PATH_AUTO and cfg.num_tokens <= 16
                                             and cfg.weight_dtype == 0)
-    if decode:              # router, top-K, sort, projections and combine in one kernel (and
-        return 1 + (1 if cfg.pre_expert_norm else 0)   # the pre-expert norm's row kernel)
+    if decode:   # router, top-K, sort, projections, combine (and any pre-expert norm): one kernel
+        return 1
     # router, top-K, 3 sort, gate/up GEMM, down GEMM, combine; FP8 experts add the token-row
-    # quantiser and run the bf16 shared expert in two launches of its own
+    # quantiser and run the bf16 shared expert in two launches of its own; a pre-expert norm
+    # adds its row kernel
     norm = 1 if cfg.pre_expert_norm else 0
     if cfg.weight_dtype == 1:
         return 9 + (2 if cfg.shared_inter else 0) + norm

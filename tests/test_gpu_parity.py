@@ -267,7 +267,8 @@ def _sample_tokens(n, k=12, seed=0):
     return np.unique(np.concatenate([[0, n - 1], rng.choice(n, min(k, n), replace=False)]))
 
 
-@pytest.mark.parametrize("shape", [I.DECODE, I.PREFILL, I.ZERO_EXPERT], ids=lambda s: s.name)
+@pytest.mark.parametrize("shape", [I.DECODE, I.PREFILL, I.ZERO_EXPERT, I.DECODE_PRENORM],
+                         ids=lambda s: s.name)
 def test_full_size_sampled_tokens(B, shape):
     """The bench's launch configuration at full size; the oracle recomputes sampled tokens
     one by one, and the routing of every token is checked."""
