@@ -507,7 +507,7 @@ def main():
         line["gpu_launches"] += p["launches_per_step"] * max(3, args.steps // 2)
     if not args.no_extra:
         extra = {}
-        for shp in (I.ZERO_EXPERT, I.FP8_PREFILL, I.TINY, I.DECODE_PRENORM):
+        for shp in (I.ZERO_EXPERT, I.FP8_PREFILL, I.TINY, I.DECODE_PRENORM, I.DECODE_FP8):
             x = time_ours(B, shp, max(3, args.steps // 2), warmup, dev, peaks, with_e2e=False)
             xa = x["alg"]
             fp8 = shp.weight_dtype == I.WDTYPE_FP8_E4M3_B128

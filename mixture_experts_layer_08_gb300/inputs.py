@@ -80,10 +80,13 @@ ZERO_EXPERT = MoeShape("zero_expert_bf16_n1024", 1024, 2048, 256, 384, 8, 1024,
 FP8_PREFILL = MoeShape("fp8_prefill_n8192", 8192, 4096, 128, 128, 8, 1536,
                        weight_dtype=WDTYPE_FP8_E4M3_B128)
 
-# The decode workload with a pre-expert RMSNorm of the routed experts' input.
+# The decode workload with a pre-expert RMSNorm of the routed experts' input, and with E4M3
+# routed experts (128x128 block scales; the shared expert stays bf16).
 DECODE_PRENORM = DECODE.with_(name="decode_prenorm_bf16_n4", pre_expert_norm=True)
+DECODE_FP8 = DECODE.with_(name="decode_fp8_n4", weight_dtype=WDTYPE_FP8_E4M3_B128)
 
-WORKLOADS = {s.name: s for s in (TINY, DECODE, PREFILL, ZERO_EXPERT, FP8_PREFILL, DECODE_PRENORM)}
+WORKLOADS = {s.name: s for s in (TINY, DECODE, PREFILL, ZERO_EXPERT, FP8_PREFILL, DECODE_PRENORM,
+                                 DECODE_FP8)}
 
 
 def _gen(shape: MoeShape, key: str, device) -> torch.Generator:

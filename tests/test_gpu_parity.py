@@ -295,7 +295,12 @@ FP8_SMALL = I.FP8_PREFILL.with_(name="fp8_small", num_tokens=300, hidden=512, nu
                                                    num_experts=16, router_width=16, top_k=4,
                                                    inter=384, hidden=768),
                                    FP8_SMALL.with_(name="fp8_small_prenorm",
-                                                   pre_expert_norm=True)],
+                                                   pre_expert_norm=True),
+                                   # decode-sized: 4 tokens, top-8 of 32, a gated bf16 shared
+                                   # expert beside the E4M3 routed experts
+                                   FP8_SMALL.with_(name="fp8_decode_n4", num_tokens=4,
+                                                   num_experts=32, router_width=32, top_k=8,
+                                                   shared_inter=256, shared_gated=True)],
                          ids=lambda s: s.name)
 def test_fp8_forward_matches_oracle(B, shape):
     inp = I.make_inputs(shape)
@@ -305,8 +310,8 @@ def test_fp8_forward_matches_oracle(B, shape):
     check_out(got, ref["out"], FP8_ATOL, FP8_RTOL, FP8_REL_L2)
 
 
-def test_fp8_full_size_sampled_tokens(B):
-    shape = I.FP8_PREFILL
+@pytest.mark.parametrize("shape", [I.FP8_PREFILL, I.DECODE_FP8], ids=lambda s: s.name)
+def test_fp8_full_size_sampled_tokens(B, shape):
     inp = I.make_inputs(shape, device="cuda")
     got, gidx, gw = run_gpu(B, inp, 0)
     check_routing(gidx, O.moe_forward(inp, routing_only=True))
