@@ -110,6 +110,25 @@ def test_forward_refuses_before_touching_the_gpu(B):
     st = B.lib.moe_forward(ctypes.byref(cfg2), ctypes.byref(w), fake, fake, fake, 1 << 30, None,
                            None, None, None)
     assert st == B.MOE_ERR_INVALID_ARG
+    # a pre-expert norm without its weight vector
+    w.pre_expert_norm_w = None
+    cfg3 = _cfg(B, pre_expert_norm=True)
+    st = B.lib.moe_forward(ctypes.byref(cfg3), ctypes.byref(w), fake, fake, fake, 1 << 30, None,
+                           None, None, None)
+    assert st == B.MOE_ERR_INVALID_ARG
+
+
+def test_pre_expert_norm_config(B):
+    n = ctypes.c_size_t(0)
+    plain = B.moe_workspace_size(_cfg(B))
+    normed = B.moe_workspace_size(_cfg(B, pre_expert_norm=True))
+    assert normed >= plain + 16 * 256 * 2          # room for the [N, H] normed copy
+    for eps in (-1.0, float("inf"), float("nan")):
+        cfg = _cfg(B, pre_expert_norm=True, rms_norm_eps=eps)
+        assert B.lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == \
+            B.MOE_ERR_INVALID_ARG
+    cfg = _cfg(B, pre_expert_norm=False, rms_norm_eps=-1.0)   # ignored without the norm
+    assert B.lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == B.MOE_OK
 
 
 def test_zero_tokens_is_a_no_op(B):
