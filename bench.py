@@ -48,6 +48,13 @@ class L2Flush:
             torch.sum(self.r, dim=0, out=self.acc)
 
 
+def workload_config(shape):
+    """The workload keys of the JSON line's config, the same on both arms."""
+    return {"workload": shape.name, "N": shape.num_tokens, "H": shape.hidden,
+            "E": shape.num_experts, "R": shape.router_width, "K": shape.top_k,
+            "I": shape.inter, "S": shape.shared_inter, "parallelism": "replicas"}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -406,9 +413,7 @@ def main():
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": warmup, "ms_per_step": ms,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic",
-                "config": {"workload": shape.name, "N": shape.num_tokens, "H": shape.hidden,
-                           "E": shape.num_experts, "K": shape.top_k, "I": shape.inter,
-                           "S": shape.shared_inter},
+                "config": workload_config(shape),
                 "cpu_baseline": {"value": v, "unit": "tokens/s",
                                  "cores": min(threads, shape.num_tokens), "kind": "oracle",
                                  "sample": f"each step: the whole {shape.num_tokens}-token batch"},
@@ -453,12 +458,10 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": shape.name, "N": shape.num_tokens, "H": shape.hidden,
-                   "E": shape.num_experts, "R": shape.router_width, "K": shape.top_k,
-                   "I": shape.inter, "S": shape.shared_inter, "parallelism": "replicas",
-                   "l2": "flushed before every timed step (512 MiB write, then 512 MiB read; "
-                         "untimed)",
-                   "distinct_experts": r["rs"]["distinct"]},
+        "config": dict(workload_config(shape),
+                       l2="flushed before every timed step (512 MiB write, then 512 MiB read; "
+                          "untimed)",
+                       distinct_experts=r["rs"]["distinct"]),
         "roofline": {"bound": "hbm", "kernel": "decode_forward_kernel",
                      "achieved": gu_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gu_ach / peaks["hbm_gbs"], "traffic": traffic,
