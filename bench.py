@@ -29,6 +29,10 @@ sys.path.insert(0, ROOT)
 from mixture_experts_layer_08_gb300 import inputs as I  # noqa: E402
 
 METRIC = "MoE-layer tokens/s (prefill N=4096, decode N=4) and % tensor/HBM roofline"
+# The FP8 prefill workload cut to 2048 tokens and 32 experts (same H, I, K, block scales): the
+# grouped FP8 GEMMs see the same tiles, and a profiler capture holds under 2 GB of device memory.
+FP8_PREFILL_SMALL = I.FP8_PREFILL.with_(name="fp8_prefill_n2048_e32", num_tokens=2048,
+                                        num_experts=32, router_width=32)
 FLUSH_BYTES = 512 << 20
 
 
@@ -349,27 +353,88 @@ def time_graph(B, blk, inp, out, flush, steps, warmup):
         return {"error": f"{type(exc).__name__}: {exc}"[:300]}
 
 
-def cpu_oracle_tokens_per_s(inp, budget_s=12.0, max_tokens=None):
-    """Times the oracle (as it stands) on the host cores on a bounded sample of tokens."""
+def host_cpu():
+    """Host cores this process may run on and the CPU model (lscpu, else /proc/cpuinfo)."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for l in out.splitlines():
+            if l.strip().startswith("Model name:"):
+                model = l.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            for l in open("/proc/cpuinfo"):
+                if l.lower().startswith("model name"):
+                    model = l.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return {"host_cores": cores, "cpu_model": model or "unknown"}
+
+
+def _omp_threads(n):
+    """Sets the OpenMP thread count of this (the calling) thread's next parallel regions; the
+    oracle's library shares the process's libgomp."""
+    try:
+        import ctypes
+        ctypes.CDLL("libgomp.so.1").omp_set_num_threads(int(n))
+        return True
+    except OSError:
+        return False
+
+
+def _time_oracle(host, tokens, budget_s, max_reps=50):
     from oracle import oracle as O
-    n = inp.shape.num_tokens
-    tokens = np.arange(n if max_tokens is None else min(n, max_tokens))
-    host = inp.to("cpu")
     O.moe_forward(host, tokens=tokens[:1])   # build + warm-up, untimed
-    done, t0 = 0, time.time()
-    reps = 0
+    done, reps, t0 = 0, 0, time.time()
     while True:
         O.moe_forward(host, tokens=tokens)
         done += len(tokens)
         reps += 1
-        if time.time() - t0 > budget_s or reps >= 50:
+        if time.time() - t0 > budget_s or reps >= max_reps:
             break
     dt = time.time() - t0
-    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    return {"value": done / dt, "unit": "tokens/s", "cores": min(threads, len(tokens)),
-            "kind": "oracle",
-            "sample": f"{reps} x {len(tokens)} tokens of the {inp.shape.name} workload "
-                      f"(fp64 C oracle, OpenMP over tokens), {dt:.1f} s"}
+    return done / dt, reps, dt
+
+
+def cpu_oracle_tokens_per_s(inp, budget_s=12.0, max_tokens=None, extra=True):
+    """Times the oracle (as it stands) on the host cores on a bounded sample of tokens: the
+    given workload with every host core (OpenMP over tokens: a batch of n tokens keeps at
+    most n threads busy), and, when `extra`, the tiny and decode workloads on one thread and
+    a 64-token sample of the prefill workload on every core."""
+    hc = host_cpu()
+    n = inp.shape.num_tokens
+    tokens = np.arange(n if max_tokens is None else min(n, max_tokens))
+    host = inp.to("cpu")
+    _omp_threads(hc["host_cores"])
+    v, reps, dt = _time_oracle(host, tokens, budget_s)
+    res = {"value": v, "unit": "tokens/s", "cores": min(hc["host_cores"], len(tokens)),
+           "kind": "oracle", **hc,
+           "sample": f"{reps} x {len(tokens)} tokens of the {inp.shape.name} workload "
+                     f"(fp64 C oracle, OpenMP over tokens), {dt:.1f} s"}
+    if extra:
+        per = {}
+        if _omp_threads(1):
+            for shp, src in ((I.TINY, None), (I.DECODE, host if inp.shape == I.DECODE else None)):
+                h = src if src is not None else I.make_inputs(shp)
+                t = np.arange(shp.num_tokens)
+                tv, treps, tdt = _time_oracle(h, t, 3.0)
+                per[shp.name + "_1thread"] = {"value": tv, "unit": "tokens/s", "cores": 1,
+                                              "sample": f"{treps} x {len(t)} tokens, {tdt:.1f} s"}
+            _omp_threads(hc["host_cores"])
+        pre = I.make_inputs(I.PREFILL)
+        t = np.linspace(0, I.PREFILL.num_tokens - 1, 64).astype(np.int64)
+        pv, preps, pdt = _time_oracle(pre, t, 3.0)
+        per[I.PREFILL.name + "_sampled"] = {
+            "value": pv, "unit": "tokens/s", "cores": min(hc["host_cores"], len(t)),
+            "sample": f"{preps} x 64 evenly spaced tokens of {I.PREFILL.num_tokens}, {pdt:.1f} s"}
+        del pre
+        res["per_workload"] = per
+    return res
 
 
 def main():
@@ -382,7 +447,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the zero-expert, FP8 and tiny workloads")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--profile-only", choices=["decode", "prefill", "fp8", "zero_expert"],
+    ap.add_argument("--profile-only", choices=["decode", "prefill", "fp8", "zero_expert",
+                                               "fp8_small", "tiny", "decode_fp8"],
                     help="run one workload's timing loop only (for ncu captures); prints a "
                          "reduced line")
     args = ap.parse_args()
@@ -408,7 +474,8 @@ def main():
             times.append(time.time() - t0)
         ms = 1000 * statistics.mean(times)
         v = shape.num_tokens / (ms / 1000)
-        threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+        hc = host_cpu()
+        threads = int(os.environ.get("OMP_NUM_THREADS", hc["host_cores"]))
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": warmup, "ms_per_step": ms,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -416,6 +483,7 @@ def main():
                 "config": workload_config(shape),
                 "cpu_baseline": {"value": v, "unit": "tokens/s",
                                  "cores": min(threads, shape.num_tokens), "kind": "oracle",
+                                 **hc,
                                  "sample": f"each step: the whole {shape.num_tokens}-token batch"},
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
@@ -436,7 +504,8 @@ def main():
 
     if args.profile_only:
         shp = {"decode": I.DECODE, "prefill": I.PREFILL, "fp8": I.FP8_PREFILL,
-               "zero_expert": I.ZERO_EXPERT}[args.profile_only]
+               "zero_expert": I.ZERO_EXPERT, "fp8_small": FP8_PREFILL_SMALL, "tiny": I.TINY,
+               "decode_fp8": I.DECODE_FP8}[args.profile_only]
         r = time_ours(B, shp, args.steps, warmup, dev, peaks, with_e2e=False)
         print(json.dumps({"profile_only": shp.name, "ms_per_step": r["ms"],
                           "tokens_per_s": shp.num_tokens / (r["ms"] / 1000.0),
@@ -458,10 +527,10 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(workload_config(shape),
-                       l2="flushed before every timed step (512 MiB write, then 512 MiB read; "
-                          "untimed)",
-                       distinct_experts=r["rs"]["distinct"]),
+        "config": workload_config(shape),
+        "notes": {"l2": "flushed before every timed step (512 MiB write, then 512 MiB read; "
+                        "untimed)",
+                  "distinct_experts": r["rs"]["distinct"]},
         "roofline": {"bound": "hbm", "kernel": "decode_forward_kernel",
                      "achieved": gu_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gu_ach / peaks["hbm_gbs"], "traffic": traffic,

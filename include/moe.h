@@ -195,7 +195,9 @@ MOE_API moe_status_t moe_forward_profiled(const moe_config_t *cfg, const moe_wei
  *    (moe_workspace_size() with path = MOE_PATH_DECODE gives the bytes needed); grouped-only
  *    configurations return MOE_ERR_UNSUPPORTED.
  *  - The first call on each device looks up the array's device address (with that device
- *    current); make that first call before any stream capture.
+ *    current); make that first call before any stream capture. The address is kept for the
+ *    life of the process: do not use this entry point on a device after cudaDeviceReset()
+ *    (the library's device code is then loaded anew and the kept address is stale).
  *  - Every call shares the array and clears what must start at zero itself; calls that
  *    overlap on the GPU (unordered streams or host threads) race on it.
  *  - There is no caller workspace, so moe_read_device_status() cannot read this call's

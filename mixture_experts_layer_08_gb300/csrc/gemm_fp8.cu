@@ -15,28 +15,55 @@
 // "spark_model/layers/moe/forward.rs" (FP8 experts carry per-expert weight and scale tables;
 // FP8 experts reach a per-layer cosine of about 0.989 against BF16).
 //
-// Threads: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-9 promotion and
-// epilogue (two warps per TMEM lane quadrant, each owning half of the 256 columns).
+// Threads: three warpgroups (384 threads, one CTA per SM).
+//   warpgroup 0  warp 0 TMA producer; warp 1 TMEM owner + MMA issuer; warps 2-3 stage the
+//                next tile's scales (A row scales and B block scales) into one of two
+//                shared-memory buffers while the current tile is promoted.
+//   warpgroups 1-2  promotion + epilogue: two warps per TMEM lane quadrant, each owning one
+//                half of the 256 columns of its 32 rows (128 fp32 accumulators per thread).
+// Registers: the launch gives every thread 168; warpgroup 0 hands most of its share to the
+// promotion warpgroups (setmaxnreg: 40 vs 232 per thread, 128*40 + 256*232 = 384*168), so the
+// 128 accumulators and a 64-column TMEM read stay in registers. The host checks the launch
+// register count before the first launch (a split that asked for more than the launch holds
+// would never complete).
 #include "kernels.h"
 
 namespace moe {
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;            // 65536 / 384, rounded down to a multiple of 8
+constexpr int kRegsWg0 = 40;
+constexpr int kRegsPromo = 232;
+static_assert(128 * kRegsWg0 + 256 * kRegsPromo <= kThreads * kLaunchRegs, "register split");
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 128;                    // fp8 elements = bytes per swizzle row
 constexpr int kStages = 3;
 constexpr int kMaxKb = 32;                  // K blocks of 128 per tile (K <= 4096)
-constexpr int kEpi = 256;                   // promotion / epilogue threads
+constexpr int kPromo = 256;                 // promotion / epilogue threads
+constexpr int kStagers = 64;                // scale staging threads
 constexpr int kATile = kBM * kBK;           // 16 KB
 constexpr int kBTile = kBN * kBK;           // 32 KB
 constexpr int kStageBytes = kATile + kBTile;
 constexpr int kTmemCols = 2 * kBN;          // two partial buffers
-constexpr size_t kScaleBytes = (size_t)kMaxKb * kEpi * 4 + (size_t)8 * kMaxKb * 2 * 4;
-constexpr size_t kSmemBytes =
-    (size_t)kStages * kStageBytes + 1024 + 256 + 2 * 2 * 128 * 4 + kScaleBytes;
+// per scale buffer: A row scales [kb][128] and B block scales [half][kb][2]
+constexpr int kSaFloats = kMaxKb * kBM;
+constexpr int kSbFloats = 2 * kMaxKb * 2;
+constexpr int kScaleBufFloats = kSaFloats + kSbFloats;
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * 2 * 128 * 4 +
+                              (size_t)2 * kScaleBufFloats * 4;
+
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsPromo));
+}
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWg0));
+}
+
+// SiLU with the fast reciprocal divide (the result is rounded to bf16 or quantised to E4M3).
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // Hands this thread's row amax to the warp that owns the other column half of the same row
 // and returns the partner's; `seq` tags the tile so values of different tiles never mix.
@@ -59,6 +86,17 @@ __device__ __forceinline__ float exchange_amax(volatile float* am_s, volatile ui
   return am_s[o];
 }
 
+// acc[0..63] += s * v[0..63], two lanes of fp32 per instruction.
+__device__ __forceinline__ void fma_block64(float* acc, const float* v, float s) {
+  const float2 s2 = make_float2(s, s);
+#pragma unroll
+  for (int j = 0; j < 64; j += 2) {
+    const float2 r = __ffma2_rn(s2, make_float2(v[j], v[j + 1]), make_float2(acc[j], acc[j + 1]));
+    acc[j] = r.x;
+    acc[j + 1] = r.y;
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tm_a,
@@ -71,16 +109,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sB = smem + kStages * kATile;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   uint64_t* empty = full + kStages;
-  uint64_t* pfull = empty + kStages;
-  uint64_t* pempty = pfull + 2;
-  uint64_t* drain = pempty + 2;
+  uint64_t* pfull = empty + kStages;      // [2] K block partial in TMEM
+  uint64_t* pempty = pfull + 2;           // [2] partial read back by every promotion thread
+  uint64_t* sfull = pempty + 2;           // [2] a tile's scales staged
+  uint64_t* sempty = sfull + 2;           // [2] those scales no longer needed
+  uint64_t* drain = sempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   float* amax_s = reinterpret_cast<float*>(smem + kStages * kStageBytes + 256);  // [2][128]
-  uint32_t* seq_s = reinterpret_cast<uint32_t*>(amax_s + 2 * 128);                  // [2][128]
-  // per tile: each promotion thread's row scale for every K block ([kb][thread]), and each
-  // epilogue warp's weight-block scales ([warp][kb][gate/up])
-  float* sa_s = reinterpret_cast<float*>(seq_s + 2 * 128);
-  float* sb_s = sa_s + kMaxKb * kEpi;
+  uint32_t* seq_s = reinterpret_cast<uint32_t*>(amax_s + 2 * 128);                // [2][128]
+  float* scale_s = reinterpret_cast<float*>(seq_s + 2 * 128);                     // [2][buf]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WsHeader* hdr = g.status;
@@ -92,7 +129,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&pfull[i], 1);
-      mbar_init(&pempty[i], 256);
+      mbar_init(&pempty[i], kPromo);
+      mbar_init(&sfull[i], kStagers);
+      mbar_init(&sempty[i], kPromo);
     }
     mbar_init(drain, 1);
     fence_mbarrier_init();
@@ -110,126 +149,170 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_m = (int)g.hdr->num_mtiles;
   const int total = num_m * g.n_tiles;
 
-  if (warp == 0 && lane == 0) {
-    // ------------------------------------------------ TMA producer
-    int s = 0;
-    uint32_t ph = 0;
-    long long issued = 0;
-    bool ok = true;
-    constexpr int b_rows = MODE == 0 ? kBN / 2 : kBN;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const int m = tile / g.n_tiles, n = tile % g.n_tiles;
-      const int4 t = g.tiles[m];
-      const int brow = t.x * g.b_rows_per_expert + n * b_rows;
-      for (int kb = 0; kb < g.num_kb; ++kb) {
-        if (!mbar_wait(&empty[s], ph ^ 1, hdr)) { ok = false; break; }
-        mbar_arrive_expect_tx(&full[s], kStageBytes);
-        tma_load_2d(sA + s * kATile, &tm_a, kb * kBK, t.y, &full[s]);
-        tma_load_2d(sB + s * kBTile, &tm_b0, kb * kBK, brow, &full[s]);
-        if (MODE == 0) tma_load_2d(sB + s * kBTile + (kBN / 2) * kBK, &tm_b1, kb * kBK, brow, &full[s]);
-        ++issued;
-        if (++s == kStages) { s = 0; ph ^= 1; }
+  if (warp < 4) {
+    setmaxnreg_dec();
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------ TMA producer
+      int s = 0;
+      uint32_t ph = 0;
+      long long issued = 0;
+      bool ok = true;
+      constexpr int b_rows = MODE == 0 ? kBN / 2 : kBN;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const int m = tile / g.n_tiles, n = tile % g.n_tiles;
+        const int4 t = g.tiles[m];
+        const int brow = t.x * g.b_rows_per_expert + n * b_rows;
+        for (int kb = 0; kb < g.num_kb; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1, hdr)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[s], kStageBytes);
+          tma_load_2d(sA + s * kATile, &tm_a, kb * kBK, t.y, &full[s]);
+          tma_load_2d(sB + s * kBTile, &tm_b0, kb * kBK, brow, &full[s]);
+          if (MODE == 0)
+            tma_load_2d(sB + s * kBTile + (kBN / 2) * kBK, &tm_b1, kb * kBK, brow, &full[s]);
+          ++issued;
+          if (++s == kStages) { s = 0; ph ^= 1; }
+        }
       }
-    }
-    if (!ok) {
-      for (long long i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-        mbar_wait(&full[i % kStages], (uint32_t)((i / kStages) & 1), nullptr);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------ MMA issuer: one partial per K block
-    constexpr uint32_t idesc = idesc_make(kBM, kBN, 0, 0);   // E4M3 x E4M3 -> fp32
-    int s = 0;
-    uint32_t ph = 0;
-    uint32_t pc = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      for (int kb = 0; kb < g.num_kb; ++kb, ++pc) {
-        const uint32_t slot = pc & 1;
-        if (!mbar_wait(&pempty[slot], ((pc >> 1) & 1) ^ 1, hdr)) { ok = false; break; }
-        if (!mbar_wait(&full[s], ph, hdr)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t a0 = smem_u32(sA + s * kATile);
-        const uint32_t b0 = smem_u32(sB + s * kBTile);
-        const uint32_t d = tmem_base + slot * kBN;
+      if (!ok) {
+        for (long long i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+          mbar_wait(&full[i % kStages], (uint32_t)((i / kStages) & 1), nullptr);
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ------------------------------------------------ MMA issuer: one partial per K block
+      constexpr uint32_t idesc = idesc_make(kBM, kBN, 0, 0);   // E4M3 x E4M3 -> fp32
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t pc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        for (int kb = 0; kb < g.num_kb; ++kb, ++pc) {
+          const uint32_t slot = pc & 1;
+          if (!mbar_wait(&pempty[slot], ((pc >> 1) & 1) ^ 1, hdr)) { ok = false; break; }
+          if (!mbar_wait(&full[s], ph, hdr)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + s * kATile);
+          const uint32_t b0 = smem_u32(sB + s * kBTile);
+          const uint32_t d = tmem_base + slot * kBN;
 #pragma unroll
-        for (int k = 0; k < kBK / 32; ++k)
-          tc_mma_fp8(d, sdesc_k_sw128(a0 + k * 32), sdesc_k_sw128(b0 + k * 32), idesc,
-                     k != 0 ? 1u : 0u);
-        tc_commit(&empty[s]);
-        tc_commit(&pfull[slot]);
-        if (++s == kStages) { s = 0; ph ^= 1; }
+          for (int k = 0; k < kBK / 32; ++k)
+            tc_mma_fp8(d, sdesc_k_sw128(a0 + k * 32), sdesc_k_sw128(b0 + k * 32), idesc,
+                       k != 0 ? 1u : 0u);
+          tc_commit(&empty[s]);
+          tc_commit(&pfull[slot]);
+          if (++s == kStages) { s = 0; ph ^= 1; }
+        }
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, hdr);
+    } else if (warp >= 2) {
+      // ------------------------------------------------ scale stager (64 threads)
+      const int st = threadIdx.x - 64;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+        const int b = it & 1;
+        if (!mbar_wait(&sempty[b], (((uint32_t)it >> 1) & 1) ^ 1, hdr)) break;
+        const int m = tile / g.n_tiles, n = tile % g.n_tiles;
+        const int4 t = g.tiles[m];
+        float* sa_s = scale_s + b * kScaleBufFloats;
+        float* sb_s = sa_s + kSaFloats;
+        // A row scales: rows st and st + 64 of the tile for every K block, 16 loads in flight
+        const int r0 = t.y + st, r1 = t.y + st + 64;
+        const bool v0 = r0 < t.z, v1 = r1 < t.z;
+        for (int kb0 = 0; kb0 < g.num_kb; kb0 += 8) {
+          float a[8], c[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int kb = kb0 + u;
+            const float* col = g.sa + (size_t)kb * g.sa_stride;
+            a[u] = (kb < g.num_kb && v0) ? __ldg(col + r0) : 0.0f;
+            c[u] = (kb < g.num_kb && v1) ? __ldg(col + r1) : 0.0f;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int kb = kb0 + u;
+            if (kb < g.num_kb) {
+              sa_s[kb * kBM + st] = a[u];
+              sa_s[kb * kBM + st + 64] = c[u];
+            }
+          }
+        }
+        // B block scales of each column half: [half][kb][gate, up] (down: one per half)
+        {
+          const int half = st >> 5, kb = lane;
+          if (kb < g.num_kb) {
+            float b0, b1;
+            if (MODE == 0) {
+              const size_t bi = ((size_t)t.x * g.b_blocks_per_expert + n) * g.num_kb + kb;
+              b0 = __ldg(g.sb0 + bi);
+              b1 = __ldg(g.sb1 + bi);
+            } else {
+              const size_t bi =
+                  ((size_t)t.x * g.b_blocks_per_expert + 2 * n + half) * g.num_kb + kb;
+              b0 = b1 = __ldg(g.sb0 + bi);
+            }
+            sb_s[(half * kMaxKb + kb) * 2] = b0;
+            sb_s[(half * kMaxKb + kb) * 2 + 1] = b1;
+          }
+        }
+        mbar_arrive(&sfull[b]);   // (release: the stores above are seen by the waiters)
       }
     }
-    tc_commit(drain);
-    mbar_wait(drain, 0, hdr);
-  } else if (warp >= 2) {
+  } else {
+    setmaxnreg_inc();
     // ------------------------------------------------ promotion + epilogue
     const int q = warp & 3;                   // TMEM lane quadrant
-    const int half = (warp - 2) >> 2;         // column half of this warp
+    const int half = (warp - 4) >> 2;        // column half of this warp
     const int r_local = q * 32 + lane;
     uint32_t pc = 0;
     uint32_t tseq = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
       ++tseq;
       const int m = tile / g.n_tiles, n = tile % g.n_tiles;
       const int4 t = g.tiles[m];
-      const int e = t.x;
       const int row = t.y + r_local;
       const bool valid = row < t.z;
-      // this tile's scales into shared memory, loads in flight together: every promotion
-      // step below then reads them without a global round trip
-      const int et = threadIdx.x - 64, ew = et >> 5;
-      for (int kb = 0; kb < g.num_kb; ++kb)
-        sa_s[kb * kEpi + et] = valid ? __ldg(g.sa + (size_t)kb * g.sa_stride + row) : 0.0f;
-      if (lane < g.num_kb) {
-        float b0, b1;
-        if (MODE == 0) {
-          const size_t bi = ((size_t)e * g.b_blocks_per_expert + n) * g.num_kb + lane;
-          b0 = __ldg(g.sb0 + bi);
-          b1 = __ldg(g.sb1 + bi);
-        } else {
-          const size_t bi =
-              ((size_t)e * g.b_blocks_per_expert + 2 * n + half) * g.num_kb + lane;
-          b0 = b1 = __ldg(g.sb0 + bi);
-        }
-        sb_s[(ew * kMaxKb + lane) * 2] = b0;
-        sb_s[(ew * kMaxKb + lane) * 2 + 1] = b1;
-      }
-      __syncwarp();
+      const int b = it & 1;
+      const float* sa_s = scale_s + b * kScaleBufFloats;
+      const float* sb_s = sa_s + kSaFloats + half * kMaxKb * 2;
+      if (!mbar_wait(&sfull[b], ((uint32_t)it >> 1) & 1, hdr)) break;
       float acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
       for (int kb = 0; kb < g.num_kb; ++kb, ++pc) {
         const uint32_t slot = pc & 1;
-        const float sa = sa_s[kb * kEpi + et];
-        const float s0 = sa * sb_s[(ew * kMaxKb + kb) * 2];
-        const float s1 = sa * sb_s[(ew * kMaxKb + kb) * 2 + 1];
+        const float sa = sa_s[kb * kBM + r_local];
+        const float s0 = sa * sb_s[kb * 2];
+        const float s1 = MODE == 0 ? sa * sb_s[kb * 2 + 1] : s0;
         if (!mbar_wait(&pfull[slot], (pc >> 1) & 1, hdr)) { ok = false; break; }
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + slot * kBN;
-        // columns: SwiGLU -> gate [half*64, +64) and up [128 + half*64, +64); down -> [half*128, +128)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int col = MODE == 0 ? (c < 2 ? half * 64 + c * 32 : 128 + half * 64 + (c - 2) * 32)
-                                    : half * 128 + c * 32;
-          float v[32];
-          tmem_ld32(taddr + col, v);
-          const float sc = (MODE == 0 && c >= 2) ? s1 : s0;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(sc, v[j], acc[c * 32 + j]);
-        }
+        // columns: SwiGLU -> gate [half*64, +64) and up [128 + half*64, +64);
+        // down -> [half*128, +128)
+        const uint32_t c0 = MODE == 0 ? half * 64 : half * 128;
+        const uint32_t c1 = MODE == 0 ? 128 + half * 64 : half * 128 + 64;
+        float v[64];
+        tmem_ld32_nowait(taddr + c0, v);
+        tmem_ld32_nowait(taddr + c0 + 32, v + 32);
+        tmem_wait_ld();
+        fma_block64(acc, v, s0);
+        tmem_ld32_nowait(taddr + c1, v);
+        tmem_ld32_nowait(taddr + c1 + 32, v + 32);
+        tmem_wait_ld();
+        // the partial is in registers: the MMA may overwrite it
         tc_fence_before();
         mbar_arrive(&pempty[slot]);
+        fma_block64(acc + 64, v, s1);
       }
-      __syncwarp();     // the next tile rewrites this warp's scales
+      mbar_arrive(&sempty[b]);
       if (!ok) break;
       if (MODE == 0) {
         // h = SiLU(gate) * up for 64 columns; quantise each row's 128-wide group (two warps)
         float am = 0.0f;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          acc[j] = silu(acc[j]) * acc[64 + j];
+          acc[j] = silu_fast(acc[j]) * acc[64 + j];
           am = fmaxf(am, fabsf(acc[j]));
         }
         const float other = exchange_amax(amax_s, seq_s, half, r_local, am, tseq, hdr);
@@ -239,11 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (valid) {
           uint8_t* orow = static_cast<uint8_t*>(g.out) + (size_t)row * g.ldo + n * 128 + half * 64;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
+          for (int v4 = 0; v4 < 4; ++v4) {
             uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const int j = v * 16 + i * 4;
+              const int j = v4 * 16 + i * 4;
               const uint32_t lo = __nv_cvt_float2_to_fp8x2(
                   make_float2(__fdiv_rn(acc[j], scale), __fdiv_rn(acc[j + 1], scale)),
                   __NV_SATFINITE, __NV_E4M3);
@@ -252,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   __NV_SATFINITE, __NV_E4M3);
               w[i] = lo | (hi << 16);
             }
-            reinterpret_cast<uint4*>(orow)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            reinterpret_cast<uint4*>(orow)[v4] = make_uint4(w[0], w[1], w[2], w[3]);
           }
           if (half == 0) g.out_scales[(size_t)n * g.out_scale_stride + row] = scale;
         }
@@ -260,13 +343,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo +
                               n * kBN + half * 128;
 #pragma unroll
-        for (int v = 0; v < 16; ++v) {
+        for (int v8 = 0; v8 < 16; ++v8) {
           uint4 o;
-          o.x = pack_bf16x2(acc[8 * v + 0], acc[8 * v + 1]);
-          o.y = pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]);
-          o.z = pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]);
-          o.w = pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]);
-          reinterpret_cast<uint4*>(orow)[v] = o;
+          o.x = pack_bf16x2(acc[8 * v8 + 0], acc[8 * v8 + 1]);
+          o.y = pack_bf16x2(acc[8 * v8 + 2], acc[8 * v8 + 3]);
+          o.z = pack_bf16x2(acc[8 * v8 + 4], acc[8 * v8 + 5]);
+          o.w = pack_bf16x2(acc[8 * v8 + 6], acc[8 * v8 + 7]);
+          reinterpret_cast<uint4*>(orow)[v8] = o;
         }
       }
     }
@@ -280,11 +363,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The register split above assumes the launch gives every thread exactly kLaunchRegs.
+template <int MODE>
+cudaError_t check_launch_regs() {
+  static int ok[64];   // per device: 0 unknown, 1 checked
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && ok[dev]) return cudaSuccess;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, gemm_fp8_kernel<MODE>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidDeviceFunction;
+  if (dev >= 0 && dev < 64) ok[dev] = 1;
+  return cudaSuccess;
+}
+
 template <int MODE>
 cudaError_t launch_t(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                      const Fp8GemmArgs& g, int num_sms, cudaStream_t st) {
   auto kern = gemm_fp8_kernel<MODE>;
-  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(kern), kSmemBytes);
+  cudaError_t e = check_launch_regs<MODE>();
+  if (e != cudaSuccess) return e;
+  e = ensure_dyn_smem(reinterpret_cast<const void*>(kern), kSmemBytes);
   if (e != cudaSuccess) return e;
   const int max_tiles = g.max_mtiles * g.n_tiles;
   int grid = max_tiles < num_sms ? max_tiles : num_sms;
@@ -298,6 +399,7 @@ cudaError_t launch_t(const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
 cudaError_t launch_gemm_fp8(int mode, const CUtensorMap& a, const CUtensorMap& b0,
                             const CUtensorMap& b1, const Fp8GemmArgs& g, int num_sms,
                             cudaStream_t st) {
+  if (g.num_kb > kMaxKb) return cudaErrorInvalidValue;
   if (mode == 0) return launch_t<0>(a, b0, b1, g, num_sms, st);
   return launch_t<1>(a, b0, b1, g, num_sms, st);
 }

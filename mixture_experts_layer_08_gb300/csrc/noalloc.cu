@@ -9,7 +9,9 @@
 //
 // The array costs kStaticScratchBytes on every GPU that loads this library, until the
 // process exits. All calls share it, so two calls that overlap on the GPU (different
-// streams, or different host threads, without ordering between them) race on it.
+// streams, or different host threads, without ordering between them) race on it. Its device
+// address is looked up once per device and kept, so a cudaDeviceReset() (which reloads the
+// device code) makes the kept address stale: the entry point is not for use after one.
 #include <mutex>
 
 #include "kernels.h"

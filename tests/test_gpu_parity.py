@@ -180,19 +180,46 @@ def test_forward_matches_oracle(B, name, path):
     check_out(got, ref["out"])
 
 
-def test_forced_identity_experts_are_exact(B):
-    """Every slot on an identity expert, no shared expert: out == bf16(zsum * x) bitwise."""
-    shape = SMALL["zero_expert_small"]
+def _assert_identity_exact(got, x, w):
+    """Token by token: out[t] == bf16(z * x[t]) bit for bit, for one fp32 z -- the kernel's own
+    sum of the token's K identity-expert weights, which may add them in another order than
+    numpy: z is searched within 8 fp32 ulps of numpy's sum."""
+    xf = x.float()
+    for t in range(got.shape[0]):
+        z0 = np.float32(w[t].astype(np.float32).sum())
+        cands = [z0]
+        up = dn = z0
+        for _ in range(8):
+            up, dn = np.nextafter(up, np.float32(np.inf)), np.nextafter(dn, np.float32(-np.inf))
+            cands += [up, dn]
+        ok = False
+        for z in cands:
+            want = (torch.tensor(z, dtype=torch.float32) * xf[t]).to(torch.bfloat16).float().numpy()
+            if np.array_equal(got[t], want):
+                ok = True
+                break
+        assert ok, f"token {t}: out != bf16(zsum * x) for every zsum near {z0}"
+
+
+@pytest.mark.parametrize("path", [1, 2], ids=["decode", "grouped"])
+@pytest.mark.parametrize("name", ["zero_expert_small", "zero_expert_decode", "zero_split_decode"])
+def test_forced_identity_experts_are_exact(B, name, path):
+    """Every slot on an identity expert, no shared expert: out == bf16(zsum * x) bitwise, on
+    both chains (the decode kernel adds the identity experts in its combine phase, the grouped
+    chain in the combine kernel). zero_split_decode has at most 32 pairs and a router of at most
+    256 columns (the decode kernel's split routing); zero_expert_decode a 384-wide router."""
+    shape = (SMALL[name] if name in SMALL else
+             SMALL["zero_expert_small"].with_(name=name, num_tokens=4, num_experts=64,
+                                              router_width=96))
+    if path == 1 and shape.num_tokens > 16:
+        pytest.skip("decode chain is for <= 16 tokens")
     inp = I.make_inputs(shape)
     N, K, E, R = shape.num_tokens, shape.top_k, shape.num_experts, shape.router_width
     rng = np.random.default_rng(3)
     forced = np.stack([rng.choice(np.arange(E, R), K, replace=False) for _ in range(N)])
-    for path in (2,):
-        got, gidx, gw = run_gpu(B, inp, path, forced=forced)
-        assert (gidx == forced).all()
-        z = torch.tensor(gw.sum(axis=1), dtype=torch.float32)
-        want = (z[:, None] * inp.x.float()).to(torch.bfloat16).float().numpy()
-        assert np.array_equal(got, want)
+    got, gidx, gw = run_gpu(B, inp, path, forced=forced)
+    assert (gidx == forced).all()
+    _assert_identity_exact(got, inp.x, gw)
 
 
 def test_decode_and_grouped_chains_agree(B):
@@ -267,7 +294,16 @@ def _sample_tokens(n, k=12, seed=0):
     return np.unique(np.concatenate([[0, n - 1], rng.choice(n, min(k, n), replace=False)]))
 
 
-@pytest.mark.parametrize("shape", [I.DECODE, I.PREFILL, I.ZERO_EXPERT, I.DECODE_PRENORM],
+# the prefill workload's grouped chain with the sigmoid + correction-bias scoring (scaled,
+# not renormalised), and with the pre-expert RMSNorm of the routed experts' input
+PREFILL_SIGMOID = I.PREFILL.with_(name="prefill_sigmoid_bias", scoring=I.SCORING_SIGMOID_BIAS,
+                                  correction_bias_std=0.05, norm_topk_prob=False,
+                                  routed_scaling_factor=2.5)
+PREFILL_PRENORM = I.PREFILL.with_(name="prefill_prenorm", pre_expert_norm=True)
+
+
+@pytest.mark.parametrize("shape", [I.DECODE, I.PREFILL, I.ZERO_EXPERT, I.DECODE_PRENORM,
+                                   PREFILL_SIGMOID, PREFILL_PRENORM],
                          ids=lambda s: s.name)
 def test_full_size_sampled_tokens(B, shape):
     """The bench's launch configuration at full size; the oracle recomputes sampled tokens

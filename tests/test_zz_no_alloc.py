@@ -37,21 +37,29 @@ def _noalloc(B, cfg, w, x, out):
 @pytest.mark.parametrize("shape", [I.DECODE, I.TINY, I.DECODE.with_(num_tokens=16)],
                          ids=["decode_n4", "tiny_n16", "decode_n16"])
 def test_noalloc_matches_workspace_entry_point(B, shape):
+    """Deterministic mode: both entry points run the same kernel on the same inputs, so the
+    outputs must agree bit for bit on both calls (a scratch region the second call reused
+    without clearing would show here); the tolerance check is the one the parity tests use.
+    Then one call in the atomic-accumulation mode, whose FP32 accumulator the kernel clears in
+    the shared array itself, against moe_forward in the same mode within that tolerance."""
     inp = I.make_inputs(shape, device="cuda")
-    cfg = B.make_config(shape, True, B.PATH_DECODE)
     w = B.make_weights(inp)
-    ref = torch.empty_like(inp.x)
-    B.moe_forward(cfg, w, inp.x, ref, B.alloc_workspace(cfg))
-    torch.cuda.synchronize()
-    r = ref.float().cpu().numpy()
-    for _ in range(2):
-        out = torch.full_like(inp.x, float("nan"))
-        assert _noalloc(B, cfg, w, inp.x, out) == B.MOE_OK
+    for det in (True, False):
+        cfg = B.make_config(shape, det, B.PATH_DECODE)
+        ref = torch.empty_like(inp.x)
+        B.moe_forward(cfg, w, inp.x, ref, B.alloc_workspace(cfg))
         torch.cuda.synchronize()
-        got = out.float().cpu().numpy()
-        err = np.abs(got - r)
-        assert (err <= 2e-2 + 2e-2 * np.abs(r)).all(), f"max err {err.max()}"
-        assert np.linalg.norm(got - r) <= 1e-2 * np.linalg.norm(r)
+        r = ref.float().cpu().numpy()
+        for _ in range(2 if det else 1):
+            out = torch.full_like(inp.x, float("nan"))
+            assert _noalloc(B, cfg, w, inp.x, out) == B.MOE_OK
+            torch.cuda.synchronize()
+            got = out.float().cpu().numpy()
+            err = np.abs(got - r)
+            assert (err <= 2e-2 + 2e-2 * np.abs(r)).all(), f"max err {err.max()}"
+            assert np.linalg.norm(got - r) <= 1e-2 * np.linalg.norm(r)
+            if det:
+                assert torch.equal(out, ref)
 
 
 def test_noalloc_rejects_what_it_cannot_hold(B):
