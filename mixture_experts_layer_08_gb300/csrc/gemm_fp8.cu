@@ -17,12 +17,12 @@
 //
 // Threads: three warpgroups (384 threads, one CTA per SM).
 //   warpgroup 0  warp 0 TMA producer; warp 1 TMEM owner + MMA issuer; warps 2-3 stage the
-//                next tile's scales (A row scales and B block scales) into one of two
-//                shared-memory buffers while the current tile is promoted.
+//                scales (A row scales and B block scales), eight K blocks at a time, into one
+//                of two shared-memory buffers ahead of the promotion.
 //   warpgroups 1-2  promotion + epilogue: two warps per TMEM lane quadrant, each owning one
 //                half of the 256 columns of its 32 rows (128 fp32 accumulators per thread).
 // Registers: the launch gives every thread 168; warpgroup 0 hands most of its share to the
-// promotion warpgroups (setmaxnreg: 40 vs 232 per thread, 128*40 + 256*232 = 384*168), so the
+// promotion warpgroups (setmaxnreg: 56 vs 224 per thread, 128*56 + 256*224 = 384*168), so the
 // 128 accumulators and a 64-column TMEM read stay in registers. The host checks the launch
 // register count before the first launch (a split that asked for more than the launch holds
 // would never complete).
@@ -34,26 +34,29 @@ namespace {
 
 constexpr int kThreads = 384;
 constexpr int kLaunchRegs = 168;            // 65536 / 384, rounded down to a multiple of 8
-constexpr int kRegsWg0 = 40;
-constexpr int kRegsPromo = 232;
+constexpr int kRegsWg0 = 56;
+constexpr int kRegsPromo = 224;
 static_assert(128 * kRegsWg0 + 256 * kRegsPromo <= kThreads * kLaunchRegs, "register split");
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 128;                    // fp8 elements = bytes per swizzle row
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kMaxKb = 32;                  // K blocks of 128 per tile (K <= 4096)
-constexpr int kPromo = 256;                 // promotion / epilogue threads
-constexpr int kStagers = 64;                // scale staging threads
+constexpr int kPromoWarps = 8;              // promotion / epilogue warps
+constexpr int kStagerWarps = 2;             // scale staging warps
 constexpr int kATile = kBM * kBK;           // 16 KB
 constexpr int kBTile = kBN * kBK;           // 32 KB
 constexpr int kStageBytes = kATile + kBTile;
 constexpr int kTmemCols = 2 * kBN;          // two partial buffers
-// per scale buffer: A row scales [kb][128] and B block scales [half][kb][2]
-constexpr int kSaFloats = kMaxKb * kBM;
-constexpr int kSbFloats = 2 * kMaxKb * 2;
+// Scales are staged in chunks of kScKb K blocks through two buffers: A row scales [kb][128]
+// and B block scales [half][kb][2] (gate, up) of the chunk.
+constexpr int kScKb = 8;
+constexpr int kSaFloats = kScKb * kBM;
+constexpr int kSbFloats = 2 * kScKb * 2;
 constexpr int kScaleBufFloats = kSaFloats + kSbFloats;
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * 2 * 128 * 4 +
                               (size_t)2 * kScaleBufFloats * 4;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ void setmaxnreg_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsPromo));
@@ -62,8 +65,28 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWg0));
 }
 
-// SiLU with the fast reciprocal divide (the result is rounded to bf16 or quantised to E4M3).
-__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+// SiLU(z) = z * sigmoid(z) with sigmoid(z) = (1 + tanh(z/2)) / 2 from the hardware tanh
+// approximation (relative error about 2^-11): one special-function op per element instead of
+// an exponential and a reciprocal. The result is quantised to E4M3 (3 mantissa bits) next.
+__device__ __forceinline__ float silu_tanh(float z) {
+  const float hz = 0.5f * z;
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(hz));
+  return fmaf(hz, t, hz);
+}
+
+// q = v / s for a run of values sharing one divisor, by Markstein's method (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): r = 1/s correctly rounded once, then per value the product q0 = v * r,
+// its exact residual e = v - q0 * s (one fused multiply-add) and the corrected quotient
+// q0 + e * r -- the correctly rounded quotient for normal operands. Two values per
+// instruction (fp32x2).
+__device__ __forceinline__ float2 div_by(float2 v, float s, float r) {
+  const float2 r2 = make_float2(r, r);
+  const float2 q0 = __fmul2_rn(v, r2);
+  const float2 e = __ffma2_rn(make_float2(-q0.x, -q0.y), make_float2(s, s), v);
+  return __ffma2_rn(e, r2, q0);
+}
 
 // Hands this thread's row amax to the warp that owns the other column half of the same row
 // and returns the partner's; `seq` tags the tile so values of different tiles never mix.
@@ -86,11 +109,11 @@ __device__ __forceinline__ float exchange_amax(volatile float* am_s, volatile ui
   return am_s[o];
 }
 
-// acc[0..63] += s * v[0..63], two lanes of fp32 per instruction.
-__device__ __forceinline__ void fma_block64(float* acc, const float* v, float s) {
+// acc[0..31] += s * v[0..31], two lanes of fp32 per instruction.
+__device__ __forceinline__ void fma_block32(float* acc, const float* v, float s) {
   const float2 s2 = make_float2(s, s);
 #pragma unroll
-  for (int j = 0; j < 64; j += 2) {
+  for (int j = 0; j < 32; j += 2) {
     const float2 r = __ffma2_rn(s2, make_float2(v[j], v[j + 1]), make_float2(acc[j], acc[j + 1]));
     acc[j] = r.x;
     acc[j + 1] = r.y;
@@ -111,8 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kStages;
   uint64_t* pfull = empty + kStages;      // [2] K block partial in TMEM
   uint64_t* pempty = pfull + 2;           // [2] partial read back by every promotion thread
-  uint64_t* sfull = pempty + 2;           // [2] a tile's scales staged
-  uint64_t* sempty = sfull + 2;           // [2] those scales no longer needed
+  uint64_t* sfull = pempty + 2;           // [2] a chunk of scales staged
+  uint64_t* sempty = sfull + 2;           // [2] that chunk no longer needed
   uint64_t* drain = sempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   float* amax_s = reinterpret_cast<float*>(smem + kStages * kStageBytes + 256);  // [2][128]
@@ -129,9 +152,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&pfull[i], 1);
-      mbar_init(&pempty[i], kPromo);
-      mbar_init(&sfull[i], kStagers);
-      mbar_init(&sempty[i], kPromo);
+      // one arrival per warp (lane 0, after the warp's lanes are done)
+      mbar_init(&pempty[i], kPromoWarps);
+      mbar_init(&sfull[i], kStagerWarps);
+      mbar_init(&sempty[i], kPromoWarps);
     }
     mbar_init(drain, 1);
     fence_mbarrier_init();
@@ -207,39 +231,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 2) {
       // ------------------------------------------------ scale stager (64 threads)
       const int st = threadIdx.x - 64;
-      int it = 0;
-      for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-        const int b = it & 1;
-        if (!mbar_wait(&sempty[b], (((uint32_t)it >> 1) & 1) ^ 1, hdr)) break;
+      const int half = st >> 5;
+      uint32_t cc = 0;   // chunks staged so far (all tiles)
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const int m = tile / g.n_tiles, n = tile % g.n_tiles;
         const int4 t = g.tiles[m];
-        float* sa_s = scale_s + b * kScaleBufFloats;
-        float* sb_s = sa_s + kSaFloats;
-        // A row scales: rows st and st + 64 of the tile for every K block, 16 loads in flight
         const int r0 = t.y + st, r1 = t.y + st + 64;
         const bool v0 = r0 < t.z, v1 = r1 < t.z;
-        for (int kb0 = 0; kb0 < g.num_kb; kb0 += 8) {
-          float a[8], c[8];
+        for (int kc = 0; kc < g.num_kb; kc += kScKb, ++cc) {
+          const int b = cc & 1;
+          if (!mbar_wait(&sempty[b], ((cc >> 1) & 1) ^ 1, hdr)) { ok = false; break; }
+          float* sa_s = scale_s + b * kScaleBufFloats;
+          float* sb_s = sa_s + kSaFloats;
+          // A row scales: rows st and st + 64 of the tile, four K blocks in flight at a time
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int kb = kb0 + u;
-            const float* col = g.sa + (size_t)kb * g.sa_stride;
-            a[u] = (kb < g.num_kb && v0) ? __ldg(col + r0) : 0.0f;
-            c[u] = (kb < g.num_kb && v1) ? __ldg(col + r1) : 0.0f;
-          }
+          for (int u0 = 0; u0 < kScKb; u0 += 4) {
+            float a[4], c[4];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int kb = kb0 + u;
-            if (kb < g.num_kb) {
-              sa_s[kb * kBM + st] = a[u];
-              sa_s[kb * kBM + st + 64] = c[u];
+            for (int u = 0; u < 4; ++u) {
+              const int kb = kc + u0 + u;
+              const float* col = g.sa + (size_t)kb * g.sa_stride;
+              a[u] = (kb < g.num_kb && v0) ? __ldg(col + r0) : 0.0f;
+              c[u] = (kb < g.num_kb && v1) ? __ldg(col + r1) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              sa_s[(u0 + u) * kBM + st] = a[u];
+              sa_s[(u0 + u) * kBM + st + 64] = c[u];
             }
           }
-        }
-        // B block scales of each column half: [half][kb][gate, up] (down: one per half)
-        {
-          const int half = st >> 5, kb = lane;
-          if (kb < g.num_kb) {
+          // B block scales of this warp's column half: [half][kb][gate, up] (down: one)
+          if (lane < kScKb && kc + lane < g.num_kb) {
+            const int kb = kc + lane;
             float b0, b1;
             if (MODE == 0) {
               const size_t bi = ((size_t)t.x * g.b_blocks_per_expert + n) * g.num_kb + kb;
@@ -250,11 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                   ((size_t)t.x * g.b_blocks_per_expert + 2 * n + half) * g.num_kb + kb;
               b0 = b1 = __ldg(g.sb0 + bi);
             }
-            sb_s[(half * kMaxKb + kb) * 2] = b0;
-            sb_s[(half * kMaxKb + kb) * 2 + 1] = b1;
+            sb_s[(half * kScKb + lane) * 2] = b0;
+            sb_s[(half * kScKb + lane) * 2 + 1] = b1;
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sfull[b]);   // (release: the warp's stores are seen)
         }
-        mbar_arrive(&sfull[b]);   // (release: the stores above are seen by the waiters)
       }
     }
   } else {
@@ -264,27 +289,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 4) >> 2;        // column half of this warp
     const int r_local = q * 32 + lane;
     uint32_t pc = 0;
+    uint32_t cc = 0;   // scale chunks consumed so far
     uint32_t tseq = 0;
     bool ok = true;
-    int it = 0;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       ++tseq;
       const int m = tile / g.n_tiles, n = tile % g.n_tiles;
       const int4 t = g.tiles[m];
       const int row = t.y + r_local;
       const bool valid = row < t.z;
-      const int b = it & 1;
-      const float* sa_s = scale_s + b * kScaleBufFloats;
-      const float* sb_s = sa_s + kSaFloats + half * kMaxKb * 2;
-      if (!mbar_wait(&sfull[b], ((uint32_t)it >> 1) & 1, hdr)) break;
       float acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
       for (int kb = 0; kb < g.num_kb; ++kb, ++pc) {
         const uint32_t slot = pc & 1;
-        const float sa = sa_s[kb * kBM + r_local];
-        const float s0 = sa * sb_s[kb * 2];
-        const float s1 = MODE == 0 ? sa * sb_s[kb * 2 + 1] : s0;
+        // this K block's scales, from the chunk buffer of the stager
+        const int u = kb % kScKb;
+        const int b = cc & 1;
+        if (u == 0 && !mbar_wait(&sfull[b], (cc >> 1) & 1, hdr)) { ok = false; break; }
+        const float* sa_s = scale_s + b * kScaleBufFloats;
+        const float* sb_s = sa_s + kSaFloats + half * kScKb * 2;
+        const float sa = sa_s[u * kBM + r_local];
+        const float s0 = sa * sb_s[u * 2];
+        const float s1 = MODE == 0 ? sa * sb_s[u * 2 + 1] : s0;
+        if (u == kScKb - 1 || kb == g.num_kb - 1) {   // the chunk's last K block: release it
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sempty[b]);
+          ++cc;
+        }
         if (!mbar_wait(&pfull[slot], (pc >> 1) & 1, hdr)) { ok = false; break; }
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + slot * kBN;
@@ -292,33 +324,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         // down -> [half*128, +128)
         const uint32_t c0 = MODE == 0 ? half * 64 : half * 128;
         const uint32_t c1 = MODE == 0 ? 128 + half * 64 : half * 128 + 64;
-        float v[64];
-        tmem_ld32_nowait(taddr + c0, v);
-        tmem_ld32_nowait(taddr + c0 + 32, v + 32);
-        tmem_wait_ld();
-        fma_block64(acc, v, s0);
-        tmem_ld32_nowait(taddr + c1, v);
-        tmem_ld32_nowait(taddr + c1 + 32, v + 32);
-        tmem_wait_ld();
+        // two 32-column register buffers: each is promoted, then refilled with the next
+        // 32 columns while the other one is promoted, so the slot is released after the
+        // fourth read, with half of the promotion still to do
+        float v0[32], v1[32];
+        tmem_ld32_nowait(taddr + c0, v0);
+        tmem_ld32_nowait(taddr + c0 + 32, v1);
+        tmem_wait_ld_tied(v0);
+        tmem_tie(v1);
+        fma_block32(acc, v0, s0);
+        tmem_ld32_nowait(taddr + c1, v0);
+        fma_block32(acc + 32, v1, s0);
+        tmem_ld32_nowait(taddr + c1 + 32, v1);
+        tmem_wait_ld_tied(v0);
+        tmem_tie(v1);
         // the partial is in registers: the MMA may overwrite it
         tc_fence_before();
-        mbar_arrive(&pempty[slot]);
-        fma_block64(acc + 64, v, s1);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pempty[slot]);
+        fma_block32(acc + 64, v0, s1);
+        fma_block32(acc + 96, v1, s1);
       }
-      mbar_arrive(&sempty[b]);
       if (!ok) break;
       if (MODE == 0) {
         // h = SiLU(gate) * up for 64 columns; quantise each row's 128-wide group (two warps)
         float am = 0.0f;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          acc[j] = silu_fast(acc[j]) * acc[64 + j];
+          acc[j] = silu_tanh(acc[j]) * acc[64 + j];
           am = fmaxf(am, fabsf(acc[j]));
         }
         const float other = exchange_amax(amax_s, seq_s, half, r_local, am, tseq, hdr);
         if (other < 0.0f) break;
         am = fmaxf(am, other);
         const float scale = am > 0.0f ? __fdiv_rn(am, 448.0f) : 1.0f;
+        const float rcp = __frcp_rn(scale);
         if (valid) {
           uint8_t* orow = static_cast<uint8_t*>(g.out) + (size_t)row * g.ldo + n * 128 + half * 64;
 #pragma unroll
@@ -328,11 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 4; ++i) {
               const int j = v4 * 16 + i * 4;
               const uint32_t lo = __nv_cvt_float2_to_fp8x2(
-                  make_float2(__fdiv_rn(acc[j], scale), __fdiv_rn(acc[j + 1], scale)),
-                  __NV_SATFINITE, __NV_E4M3);
+                  div_by(make_float2(acc[j], acc[j + 1]), scale, rcp), __NV_SATFINITE, __NV_E4M3);
               const uint32_t hi = __nv_cvt_float2_to_fp8x2(
-                  make_float2(__fdiv_rn(acc[j + 2], scale), __fdiv_rn(acc[j + 3], scale)),
-                  __NV_SATFINITE, __NV_E4M3);
+                  div_by(make_float2(acc[j + 2], acc[j + 3]), scale, rcp), __NV_SATFINITE,
+                  __NV_E4M3);
               w[i] = lo | (hi << 16);
             }
             reinterpret_cast<uint4*>(orow)[v4] = make_uint4(w[0], w[1], w[2], w[3]);
