@@ -507,7 +507,7 @@ def main():
                "zero_expert": I.ZERO_EXPERT, "fp8_small": FP8_PREFILL_SMALL, "tiny": I.TINY,
                "decode_fp8": I.DECODE_FP8}[args.profile_only]
         r = time_ours(B, shp, args.steps, warmup, dev, peaks, with_e2e=False)
-        print(json.dumps({"profile_only": shp.name, "ms_per_step": r["ms"],
+        print(json.dumps({"profile_only": shp.name, "ms_per_step": r["ms"], "clocks": r["clocks"],
                           "tokens_per_s": shp.num_tokens / (r["ms"] / 1000.0),
                           "stage_us": {k: 1000 * v for k, v in r["stage_ms"].items()},
                           "Z": r["rs"]["Z"], "distinct_experts": r["rs"]["distinct"]}))
