@@ -141,11 +141,13 @@ def algorithmic(inp, rs):
     flops = flops_routed + 6.0 * s.num_tokens * H * S + 2.0 * s.num_tokens * H * R
     # the gate/up launch also runs the shared expert's gate/up projection (bf16 experts)
     gate_up_flops = 4.0 * rs["Z"] * H * I_ + 4.0 * s.num_tokens * H * S
+    down_flops = 2.0 * rs["Z"] * I_ * H + (2.0 * s.num_tokens * S * H
+                                            if s.weight_dtype != I.WDTYPE_FP8_E4M3_B128 else 0.0)
     gate_up_bytes = rs["distinct"] * 2 * I_ * H * wb + (2 * S * H * 2)
     # the decode chain's one kernel reads every touched expert, the shared expert, the router
     # and x, and writes out: all of the step's algorithmic bytes
     ffn_bytes = bytes_
-    return {"bytes": bytes_, "flops": flops, "gate_up_flops": gate_up_flops,
+    return {"bytes": bytes_, "flops": flops, "gate_up_flops": gate_up_flops, "down_flops": down_flops,
             "gate_up_bytes": gate_up_bytes, "ffn_bytes": ffn_bytes, "expert_bytes": expert_bytes}
 
 
@@ -571,6 +573,12 @@ def main():
                          # (ncu, one launch) over its CUDA-event time
                          "hbm_frac": (p_traffic / (gu / 1000.0) / 1e9 / peaks["hbm_gbs"]
                                       if p_traffic else None),
+                         "down_kernel": "gemm_bf16_kernel<256,bf16>",
+                         "down_tflops": pa["down_flops"] / (p["stage_ms"]["down"] / 1000.0) / 1e12,
+                         "down_frac": pa["down_flops"] / (p["stage_ms"]["down"] / 1000.0) / 1e12
+                         / peaks["bf16_tflops"],
+                         "down_traffic": measured_traffic("gemm_bf16_kernel<256,bf16>",
+                                                          I.PREFILL.name),
                          "step_tflops": pa["flops"] / (p["ms"] / 1000.0) / 1e12,
                          "step_frac": pa["flops"] / (p["ms"] / 1000.0) / 1e12 / peaks["bf16_tflops"]},
             "Z": p["rs"]["Z"], "max_expert_rows": int(p["rs"]["counts"].max()),
@@ -594,6 +602,14 @@ def main():
                 "gate_up_hbm_frac": xa["gate_up_bytes"] / (gu / 1000.0) / 1e9 / peaks["hbm_gbs"],
                 "tensor_peak_tflops": tpeak,
                 "tensor_peak_src": "2 x measured bf16 (nominal fp8:bf16 ratio)" if fp8 else "measured bf16",
+                "down_tflops": xa["down_flops"] / (x["stage_ms"]["down"] / 1000.0) / 1e12
+                if x["stage_ms"]["down"] > 0.01 else None,
+                "down_tensor_frac": xa["down_flops"] / (x["stage_ms"]["down"] / 1000.0) / 1e12 / tpeak
+                if x["stage_ms"]["down"] > 0.01 else None,
+                "gate_up_traffic": measured_traffic("gemm_fp8_kernel<0>" if fp8 else
+                                                    "gemm_bf16_kernel<256,SwiGLU>", shp.name),
+                "down_traffic": measured_traffic("gemm_fp8_kernel<1>" if fp8 else
+                                                 "gemm_bf16_kernel<256,bf16>", shp.name),
                 "step_hbm_frac": xa["bytes"] / (x["ms"] / 1000.0) / 1e9 / peaks["hbm_gbs"],
                 "step_tensor_frac": xa["flops"] / (x["ms"] / 1000.0) / 1e12 / tpeak,
                 "Z": x["rs"]["Z"], "distinct_experts": x["rs"]["distinct"]}
