@@ -185,7 +185,7 @@ def measured_traffic(kernel, workload):
 def kernels_per_step(B, cfg):
     """Kernels of this library one forward launches (memsets are not kernels)."""
     decode = cfg.path == B.PATH_DECODE or (cfg.path == B.PATH_AUTO and cfg.num_tokens <= 16
-                                            and cfg.weight_dtype == 0)
+                                            and cfg.inter <= 1024 and cfg.shared_inter <= 1024)
     if decode:   # router, top-K, sort, projections, combine (and any pre-expert norm): one kernel
         return 1
     # router, top-K, 3 sort, gate/up GEMM, down GEMM, combine; FP8 experts add the token-row

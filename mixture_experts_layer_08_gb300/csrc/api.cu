@@ -41,8 +41,9 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 int resolve_path(const moe_config_t* c) {
   if (c->path != MOE_PATH_AUTO) return c->path;
-  const bool decode_ok = c->weight_dtype == MOE_W_BF16 && c->num_tokens <= kDecodeMaxTokens &&
-                         c->inter <= 1024 && c->shared_inter <= 1024;
+  const bool decode_ok = c->num_tokens <= kDecodeMaxTokens && c->inter <= 1024 &&
+                         c->shared_inter <= 1024 &&
+                         (c->weight_dtype == MOE_W_BF16 || c->hidden % 256 == 0);
   return decode_ok ? MOE_PATH_DECODE : MOE_PATH_GROUPED;
 }
 
@@ -73,8 +74,8 @@ moe_status_t validate_config(const moe_config_t* c) {
     return MOE_ERR_UNSUPPORTED;
   const int path = resolve_path(c);
   if (path == MOE_PATH_DECODE &&
-      (c->weight_dtype != MOE_W_BF16 || c->num_tokens > kDecodeMaxTokens || c->inter > 1024 ||
-       c->shared_inter > 1024 || c->hidden > 8192))
+      (c->num_tokens > kDecodeMaxTokens || c->inter > 1024 || c->shared_inter > 1024 ||
+       c->hidden > 8192))
     return MOE_ERR_UNSUPPORTED;
   const long long te = (long long)c->num_tokens * c->top_k;
   if (te > (1ll << 30) || (long long)c->num_tokens * c->hidden > (1ll << 40))
@@ -123,10 +124,16 @@ Layout make_layout(const moe_config_t* c) {
   } else {
     sz[R_SYNC] = (kDecodeMaxPairs + 1) * 4;   // per-slot gate/up item counts
     const size_t L2 = I > S ? I : S;
-    sz[R_HD] = (te + N) * 2 * L2 * 4;   // gate and up products of every row
+    // gate and up products of every row (E4M3 experts: the shared expert's rows twice, one
+    // block per contraction part)
+    sz[R_HD] = (te + (c->weight_dtype == MOE_W_FP8_E4M3_B128 ? 2 : 1) * N) * 2 * L2 * 4;
     if (c->deterministic) sz[R_YD] = te * H * 4;
     else sz[R_ACC] = N * H * 4;
     sz[R_SHY] = S ? N * H * 4 : 0;
+    if (c->weight_dtype == MOE_W_FP8_E4M3_B128) {
+      sz[R_XQT] = N * H;                 // E4M3 codes of the routed experts' input
+      sz[R_XST] = (H / 128) * N * 4;     // and their 1x128 scales
+    }
   }
   size_t off = 0;
   for (int r = 0; r < R_NUM; ++r) {
@@ -577,15 +584,30 @@ moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const voi
   d.h_cnt = P.at<uint32_t>(R_SYNC);
   d.hdr = hdr;
   d.out = static_cast<__nv_bfloat16*>(out);
+  const bool fp8 = c->weight_dtype == MOE_W_FP8_E4M3_B128;
+  d.fp8 = fp8 ? 1 : 0;
+  d.s_gate = fp8 ? w->s_gate : nullptr;
+  d.s_up = fp8 ? w->s_up : nullptr;
+  d.s_down = fp8 ? w->s_down : nullptr;
+  d.xq = fp8 ? P.at<uint8_t>(R_XQT) : nullptr;
+  d.xs = fp8 ? P.at<float>(R_XST) : nullptr;
   CUtensorMap maps[kDmNum];
   int bg = 0, bd = 0;
   decode_tile_rows(H, I, S, &bg, &bd);
-  if (!make_map_bf16(&maps[kDmWg], w->w_gate, H, (uint64_t)E * I, bg) ||
-      !make_map_bf16(&maps[kDmWu], w->w_up, H, (uint64_t)E * I, bg) ||
-      !make_map_bf16(&maps[kDmWd], w->w_down, I, (uint64_t)E * H, bd) ||
-      !make_map_bf16(&maps[kDmX], x, H, N, kDecodeBoxRowsX) ||
-      !make_map_bf16(&maps[kDmXn], xn, H, N, kDecodeBoxRowsX))
+  if (fp8) {   // E4M3 routed weights and expert input: 128 codes per 128-byte box row
+    if (!make_map_u8(&maps[kDmWg], w->w_gate, H, (uint64_t)E * I, bg) ||
+        !make_map_u8(&maps[kDmWu], w->w_up, H, (uint64_t)E * I, bg) ||
+        !make_map_u8(&maps[kDmWd], w->w_down, I, (uint64_t)E * H, bd) ||
+        !make_map_bf16(&maps[kDmX], x, H, N, kDecodeBoxRowsX) ||
+        !make_map_u8(&maps[kDmXn], d.xq, H, N, kDecodeBoxRowsX))
+      return MOE_ERR_CUDA;
+  } else if (!make_map_bf16(&maps[kDmWg], w->w_gate, H, (uint64_t)E * I, bg) ||
+             !make_map_bf16(&maps[kDmWu], w->w_up, H, (uint64_t)E * I, bg) ||
+             !make_map_bf16(&maps[kDmWd], w->w_down, I, (uint64_t)E * H, bd) ||
+             !make_map_bf16(&maps[kDmX], x, H, N, kDecodeBoxRowsX) ||
+             !make_map_bf16(&maps[kDmXn], xn, H, N, kDecodeBoxRowsX)) {
     return MOE_ERR_CUDA;
+  }
   if (S > 0) {
     if (!make_map_bf16(&maps[kDmSg], w->sh_gate, H, S, bg) ||
         !make_map_bf16(&maps[kDmSu], w->sh_up, H, S, bg) ||

@@ -72,12 +72,16 @@ constexpr int kTmemCols = 512;            // two accumulators of up to 256 colum
 constexpr int kEpiThreads = 128;
 constexpr int kDrainWarp = 4;             // warp % 4 == 0: TMEM lanes 0..31
 constexpr int kStageLd = 68;              // drain staging row stride (floats; 16-byte rows)
+constexpr int kRaccLd = 260;              // E4M3 runs: fp32 run accumulator row stride (floats)
+constexpr int kRaccBytes = 16 * kRaccLd * 4;
+constexpr int kMaxHGroups = 8;            // 1x128 groups of a routed intermediate row (I <= 1024)
 constexpr int kSmemLimit = 227 * 1024;
 
 struct Plan {
   int stages;
   int bn_g, bn_d;   // weight rows per tile: gate/up, down
-  int hbytes;       // down-projection A operand: max(I, S) / 64 boxes of 16 rows x 128 bytes
+  int hbytes;       // down-projection A operand: boxes of 16 rows x 128 bytes (max(I, S) / 64;
+                    // E4M3 routed experts: max(I / 128, S / 64))
 };
 
 constexpr uint16_t kNoRow16 = 0xFFFF;
@@ -269,6 +273,35 @@ __device__ void pre_expert_norm_rows(const DecodeArgs& a, const __nv_bfloat16* x
     __syncthreads();   // (red is reused)
   }
   if (wrote) asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Phase 0 with E4M3 routed experts: their input rows (x, or xn under a pre-expert norm) as
+// E4M3 codes xq [N, H] with one scale per 1x128 group, xs [H/128, N]: scale = amax / 448 (1 if
+// the group is zero), code = value / scale rounded to nearest even, saturating, all decided in
+// fp32 (the rule of the grouped chain's quantiser). Token t by block G-1-t, one warp per group.
+// The routed gate/up items stream xq by TMA after the grid barrier: fenced for the async proxy.
+__device__ void quant_token_rows(const DecodeArgs& a, const __nv_bfloat16* src) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = (int)gridDim.x - 1 - (int)blockIdx.x;
+  if (t < 0 || t >= a.N) return;
+  const int G = a.H / 128;
+  for (int g = warp; g < G; g += kWarps) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(src + (size_t)t * a.H + g * 128 + lane * 4);
+    float f[4];
+    f[0] = __uint_as_float(raw.x << 16);
+    f[1] = __uint_as_float(raw.x & 0xffff0000u);
+    f[2] = __uint_as_float(raw.y << 16);
+    f[3] = __uint_as_float(raw.y & 0xffff0000u);
+    const float am = warp_max(fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3]))));
+    const float sc = am > 0.0f ? __fdiv_rn(am, 448.0f) : 1.0f;
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+        make_float2(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc)), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+        make_float2(__fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc)), __NV_SATFINITE, __NV_E4M3);
+    *reinterpret_cast<uint32_t*>(a.xq + (size_t)t * a.H + g * 128 + lane * 4) = lo | (hi << 16);
+    if (lane == 0) a.xs[(size_t)g * a.N + t] = sc;
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // Wide routers (R > 256): K rounds of a warp arg-max (route_token_warp_reg), then the same
@@ -751,9 +784,13 @@ __device__ void combine_chunks(const DecodeArgs& a, const Routing& rt) {
 // order (deterministic).
 struct Sched {
   int nIt, nSt;     // weight tiles of one gate (or up) projection: routed, shared
-  int Pg;           // items per gate/up tile (H / 64)
+  int Pg;           // items per shared gate/up tile (H / 64)
+  int Pgr;          // items per routed gate/up tile (H / 64; E4M3: H / 128)
+  int ks;           // parts a shared gate/up tile's contraction is split into (E4M3: 2, so
+                    // that every gate/up part has Pgr items); part kh accumulates into its
+                    // own rows of the gate/up buffer
   int nHt;          // weight tiles of a down projection
-  int Pdr, Pds;     // items per down tile: routed (I / 64), shared (S / 64)
+  int Pdr, Pds;     // items per down tile: routed (I / 64; E4M3: I / 128), shared (S / 64)
   int na;           // active routed slots
   int g_rt, g_items, d_ritems, d_items;
   int g0, ng, d0, total;   // this block's ranges
@@ -770,38 +807,49 @@ struct Sched {
     i0 = (int)((long long)n * b / G);
     cnt = (int)((long long)n * (b + 1) / G) - i0;
   }
-  __device__ void init(const DecodeArgs& a, const Plan& pl, int n_active) {
+  __device__ void init(const DecodeArgs& a, const Plan& pl, int n_active, bool fp8) {
+    const int rbox = fp8 ? 2 * kBox : kBox;   // contraction columns of a routed item
     nIt = a.I / pl.bn_g;
     nSt = a.S / pl.bn_g;
     Pg = a.H / kBox;
+    Pgr = a.H / rbox;
+    ks = Pg / Pgr;
     nHt = a.H / pl.bn_d;
-    Pdr = a.I / kBox;
+    Pdr = a.I / rbox;
     Pds = a.S / kBox;
     na = n_active;
     g_rt = na * 2 * nIt;
-    g_items = (g_rt + (a.S ? 2 * nSt : 0)) * Pg;
+    g_items = g_rt * Pgr + (a.S ? 2 * nSt : 0) * Pg;
     d_ritems = na * nHt * Pdr;
     d_items = d_ritems + (a.S ? nHt * Pds : 0);
     int nd;
-    range(g_items, Pg, g0, ng);
+    range(g_items, Pgr, g0, ng);
     range(d_items, Pdr > Pds ? Pdr : Pds, d0, nd);
     total = ng + nd;
   }
-  // this block's k-th item: phase, tile (unique within gate/up or within down), contraction
-  // box kc, slot (-1: shared expert), tile within the slot's projection(s) (gate/up: gate tiles
-  // first, then up tiles)
-  __device__ void item(int k, bool& down, int& tile, int& kc, int& slot, int& lt) const {
+  // this block's k-th item: phase, tile (unique within gate/up or within down; a shared
+  // gate/up tile's contraction parts count as tiles of their own), contraction box kc, slot
+  // (-1: shared expert), tile within the slot's projection(s) (gate/up: gate tiles first,
+  // then up tiles), contraction part kh of a shared gate/up tile
+  __device__ void item(int k, bool& down, int& tile, int& kc, int& slot, int& lt,
+                       int& kh) const {
     down = k >= ng;
+    kh = 0;
     if (!down) {
       const int it = g0 + k;
-      tile = it / Pg;
-      kc = it - tile * Pg;
-      if (tile < g_rt) {
+      if (it < g_rt * Pgr) {
+        tile = it / Pgr;
+        kc = it - tile * Pgr;
         slot = tile / (2 * nIt);
         lt = tile - slot * 2 * nIt;
       } else {
+        const int j = it - g_rt * Pgr;
+        const int part = j / Pgr;   // (Pg / ks == Pgr)
+        lt = part / ks;
+        kh = part - lt * ks;
+        kc = kh * Pgr + (j - part * Pgr);
+        tile = g_rt + part;
         slot = -1;
-        lt = tile - g_rt;
       }
     } else {
       const int it = d0 + (k - ng);
@@ -829,7 +877,7 @@ __device__ void zero_accumulators(const DecodeArgs& a) {
     uint4* q = reinterpret_cast<uint4*>(p);
     for (size_t i = tid; i < bytes / 16; i += nth) q[i] = make_uint4(0u, 0u, 0u, 0u);
   };
-  zero16(a.hd, (size_t)(a.te + a.N) * 2 * a.ldh * 4);
+  zero16(a.hd, (size_t)(a.te + (a.fp8 ? 2 : 1) * a.N) * 2 * a.ldh * 4);
   if (a.yd) zero16(a.yd, (size_t)a.te * a.H * 4);
   if (a.acc) zero16(a.acc, (size_t)a.N * a.H * 4);
   if (a.S > 0) zero16(a.shy, (size_t)a.N * a.H * 4);
@@ -847,6 +895,12 @@ __device__ __forceinline__ int slot_rows(const DecodeArgs& a, const Routing& m, 
   return m.slot_n[slot];
 }
 
+// FP8: the routed experts' weights are E4M3 with 128 x 128 block scales (the maps of Wg, Wu, Wd
+// and of the routed input are uint8 boxes of 128 codes); their items are 128 contraction
+// columns, multiplied on the tensor cores as E4M3 x E4M3 (kind::f8f6f4) one item at a time, and
+// each item's partial is scaled by its activation and weight block scales into an fp32 run
+// accumulator in shared memory before the run is added out. The shared expert stays bf16.
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_forward_kernel(const __grid_constant__ CUtensorMap tm_wg,
                           const __grid_constant__ CUtensorMap tm_wu,
@@ -863,6 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(16) float stage_rows[16 * kStageLd];   // drain staging, 16 rows x 64
   __shared__ float red_s[kDecodeMaxTokens * kWarps];           // router block reductions
+  __shared__ float hsc_s[FP8 ? 2 : 1][16 * kMaxHGroups];       // E4M3: the intermediate's scales
   // 1024-byte alignment for the 128-byte swizzle atoms. Layout: token boxes of the stages, two
   // buffers of the down-projection A operand, the weight ring (the A descriptors' rows 16..127
   // read on into what follows, always inside this allocation). An offset from the __shared__
@@ -873,6 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* xtok = smem;                                   // [stages][16 x 128 B]
   uint8_t* hb = xtok + (size_t)stages * kTokBytes;        // [2][max(I,S)/64][16 x 128 B]
   uint8_t* ring = hb + 2 * (size_t)pl.hbytes;             // [stages][BN x 128 B]
+  float* racc = reinterpret_cast<float*>(ring + (size_t)stages * kWBytes);   // E4M3: [16][kRaccLd]
   uint64_t* full = bars;
   uint64_t* empty = bars + kMaxStages;
   uint64_t* afull = bars + 2 * kMaxStages;                // [2] run accumulated
@@ -909,9 +965,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- phases 0 and 1: router logits (spread over the grid) and zeroed accumulators, then
   // each block's routing
   router_rows(a, smem, (size_t)stages * (kTokBytes + kWBytes), red_s);
-  if (a.norm_w) {   // (x is still staged at the start of the dynamic region when it fit)
+  {
+    // (x is still staged at the start of the dynamic region when it fit)
     const bool staged = (size_t)a.N * a.H * 2 <= (size_t)stages * (kTokBytes + kWBytes);
-    pre_expert_norm_rows(a, staged ? reinterpret_cast<const __nv_bfloat16*>(smem) : a.x, red_s);
+    const __nv_bfloat16* xs_src = staged ? reinterpret_cast<const __nv_bfloat16*>(smem) : a.x;
+    if (a.norm_w) pre_expert_norm_rows(a, xs_src, red_s);
+    if (FP8) {
+      __syncthreads();   // (this block's xn row, written just above, is read back below)
+      quant_token_rows(a, a.norm_w ? a.xn : xs_src);
+    }
   }
   zero_accumulators(a);
   grid_barrier(hdr, gridDim.x);
@@ -923,7 +985,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- phase 2: the projections
   Sched sc;
-  sc.init(a, pl, meta.n_active);
+  sc.init(a, pl, meta.n_active, FP8);
   const int nitems = sc.total;
 
   if (warp == 0) {
@@ -931,8 +993,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // the weight box of item k: its tensor map and coordinates
       auto locate = [&](int k, bool& down, int& kc, int& slot, const CUtensorMap*& m, int& row) {
-        int tile, lt;
-        sc.item(k, down, tile, kc, slot, lt);
+        int tile, lt, kh;
+        sc.item(k, down, tile, kc, slot, lt, kh);
         if (!down) {
           const int nt = slot >= 0 ? sc.nIt : sc.nSt;
           const bool up = lt >= nt;
@@ -959,14 +1021,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* m;
         locate(k, down, kc, slot, m, row);
         uint8_t* wst = ring + (size_t)s * kWBytes;
-        if (!down) {   // (routed experts read their input xn, the shared expert x)
+        // contraction coordinate of the box: 64 bf16 or (E4M3 routed experts) 128 codes
+        const int xc = kc * ((FP8 && slot >= 0) ? 2 * kBox : kBox);
+        if (!down) {   // (routed experts read their input xn / its codes, the shared expert x)
           mbar_arrive_expect_tx(&full[s], (uint32_t)(pl.bn_g * 128 + kTokBytes));
-          tma_load_2d(xtok + (size_t)s * kTokBytes, slot >= 0 ? &tm_xn : &tm_x, kc * kBox, 0,
-                      &full[s]);
+          tma_load_2d(xtok + (size_t)s * kTokBytes, slot >= 0 ? &tm_xn : &tm_x, xc, 0, &full[s]);
         } else {
           mbar_arrive_expect_tx(&full[s], (uint32_t)(pl.bn_d * 128));
         }
-        tma_load_2d(wst, m, kc * kBox, row, &full[s]);
+        tma_load_2d(wst, m, xc, row, &full[s]);
         ++issued;
         if (++s == stages) { s = 0; ph ^= 1; }
       }
@@ -979,20 +1042,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_g = idesc_make(128, pl.bn_g, 1, 1);
       const uint32_t idesc_d = idesc_make(128, pl.bn_d, 1, 1);
+      const uint32_t idesc_g8 = idesc_make(128, pl.bn_g, 0, 0);   // E4M3 x E4M3
+      const uint32_t idesc_d8 = idesc_make(128, pl.bn_d, 0, 0);
       int s = 0, run = -1, prev_tile = -1, bslot = -2, nb = 0;
       uint32_t ph = 0, hb_cur = 0;
       bool prev_down = false, ok = true, first = false;
       for (int k = 0; k < nitems && ok; ++k) {
         bool down;
-        int tile, kc, slot, lt;
-        sc.item(k, down, tile, kc, slot, lt);
-        if (run < 0 || down != prev_down || tile != prev_tile) {
+        int tile, kc, slot, lt, kh;
+        sc.item(k, down, tile, kc, slot, lt, kh);
+        // a new accumulation group: a new tile, or every item of an E4M3 routed expert (each
+        // K block carries its own scales, so its partial is drained on its own)
+        const bool f8 = FP8 && slot >= 0;
+        const bool new_tile = run < 0 || down != prev_down || tile != prev_tile;
+        if (new_tile || f8) {
           if (run >= 0) tc_commit(&afull[run & 1]);
           ++run;
           prev_down = down;
           prev_tile = tile;
           if (!mbar_wait(&aempty[run & 1], (((uint32_t)run >> 1) & 1) ^ 1, hdr)) { ok = false; break; }
-          if (down && slot != bslot) {   // the epilogue's nb-th build, in buffer nb % 2
+          if (new_tile && down && slot != bslot) {   // the epilogue's nb-th build, buffer nb % 2
             if (!mbar_wait(&bfull[nb & 1], (uint32_t)(nb >> 1) & 1, hdr)) { ok = false; break; }
             hb_cur = smem_u32(hb) + (uint32_t)(nb & 1) * (uint32_t)pl.hbytes;
             ++nb;
@@ -1007,11 +1076,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a0 = down ? hb_cur + (uint32_t)kc * kTokBytes
                                  : smem_u32(xtok) + (uint32_t)s * kTokBytes;
         const uint32_t b0 = smem_u32(ring) + (uint32_t)s * kWBytes;
-        const uint32_t idesc = down ? idesc_d : idesc_g;
+        if (f8) {   // 128 codes per row: 4 MMAs of K = 32
+          const uint32_t idesc = down ? idesc_d8 : idesc_g8;
 #pragma unroll
-        for (int kk = 0; kk < kBox / 16; ++kk)
-          tc_mma_bf16(d, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
-                      (first && kk == 0) ? 0u : 1u);
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_fp8(d, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
+                       (first && kk == 0) ? 0u : 1u);
+        } else {
+          const uint32_t idesc = down ? idesc_d : idesc_g;
+#pragma unroll
+          for (int kk = 0; kk < kBox / 16; ++kk)
+            tc_mma_bf16(d, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
+                        (first && kk == 0) ? 0u : 1u);
+        }
         first = false;
         tc_commit(&empty[s]);
         if (++s == stages) { s = 0; ph ^= 1; }
@@ -1028,30 +1105,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool drainer = warp == kDrainWarp;
     int run = -1, prev_tile = -1, bslot = -2, nb = 0;
     bool prev_down = false;
-    // the run being accumulated (phase, slot, tile within the slot, items) and whether the
-    // previous one was drained already
-    bool r_down = false, drained = true;
-    int r_slot = 0, r_lt = 0, r_len = 0, r_idx = -1;
+    // the accumulation group being drained next (phase, slot, tile within the slot, contraction
+    // box, whether it is an E4M3 item, whether it opens its tile's run) and the items of its
+    // tile's run so far; whether the previous group was drained already
+    bool r_down = false, r_f8 = false, r_first = true, drained = true;
+    int r_slot = 0, r_lt = 0, r_kc = 0, r_kh = 0, r_len = 0, r_idx = -1, r_buf = 0;
     bool ok = true;
-    // Warp 4 drains a finished run: TMEM lane j < 16 holds accumulator row j (token j of x on
-    // gate/up, the slot's j-th token on down) across the tile's BN columns. 64 columns at a
-    // time go through shared memory so that every row's partial sums leave as coalesced
-    // 32-lane atomic adds.
-    auto drain_run = [&](int rr, bool rdown, int rslot, int rlt, int rlen) {
-      if (!ok) return;
-      if (!mbar_wait(&afull[rr & 1], ((uint32_t)rr >> 1) & 1, hdr)) { ok = false; return; }
-      tc_fence_after();
+    // Output row of accumulator row `lane` (lanes < 16; nullptr: not drained) of a group, the
+    // factor its partial sums are scaled by (the routing weight in the atomic mode) and the
+    // tile's columns.
+    auto resolve_dst = [&](bool rdown, int rslot, int rlt, int rkh, float*& dst, float& scale,
+                           int& bn) {
       int r0;
       const int ntok = slot_rows(a, meta, rslot, r0);
-      const uint32_t tacc = tmem_base + (uint32_t)((rr & 1) * kMaxBN);
-      float* dst = nullptr;      // output row of accumulator row `lane` (lanes < 16)
-      float scale = 1.0f;
-      int bn;
+      dst = nullptr;
+      scale = 1.0f;
       if (!rdown) {
         bn = pl.bn_g;
         int row = -1;            // sorted row of (slot, token lane)
         if (rslot < 0) {
-          if (lane < a.N) row = a.te + lane;
+          if (lane < a.N) row = a.te + rkh * a.N + lane;   // (part rkh's rows)
         } else {
           for (int j = 0; j < ntok; ++j)
             if ((int)meta.row_tok[r0 + j] == lane) row = r0 + j;
@@ -1074,6 +1147,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+    };
+    // publish a finished gate/up run: the slot's count moves only after every partial sum of
+    // the run landed
+    auto publish = [&](bool rdown, int rslot, int rlen) {
+      if (!rdown) {
+        __syncwarp();
+        if (lane == 0)
+          red_release_add(a.h_cnt + (rslot < 0 ? kDecodeMaxPairs : rslot), (uint32_t)rlen);
+      }
+    };
+    // Warp 4 drains a finished run: TMEM lane j < 16 holds accumulator row j (token j of x on
+    // gate/up, the slot's j-th token on down) across the tile's BN columns. 64 columns at a
+    // time go through shared memory so that every row's partial sums leave as coalesced
+    // 32-lane atomic adds.
+    auto drain_run = [&](int rr, bool rdown, int rslot, int rlt, int rkh, int rlen) {
+      if (!ok) return;
+      if (!mbar_wait(&afull[rr & 1], ((uint32_t)rr >> 1) & 1, hdr)) { ok = false; return; }
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + (uint32_t)((rr & 1) * kMaxBN);
+      float* dst;
+      float scale;
+      int bn;
+      resolve_dst(rdown, rslot, rlt, rkh, dst, scale, bn);
       const uint32_t rows = __ballot_sync(0xffffffffu, dst != nullptr);
 #pragma unroll 1
       for (int c = 0; c < bn; c += 64) {
@@ -1101,21 +1197,89 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&aempty[rr & 1]);
-      if (!rdown) {
-        // publish: the slot's count moves only after every partial sum of the run landed
-        __syncwarp();
-        if (lane == 0) red_release_add(a.h_cnt + (rslot < 0 ? kDecodeMaxPairs : rslot), (uint32_t)rlen);
-      }
+      publish(rdown, rslot, rlen);
     };
-    auto drain_current = [&]() {
-      if (drainer && !drained && r_idx >= 0) drain_run(r_idx, r_down, r_slot, r_lt, r_len);
+    // E4M3: warp 4 drains one item (one 128-wide contraction block of a routed tile): every
+    // token row's partial sums times its activation scale (the token's, or on down the
+    // intermediate's) and the weight block scale of each 128-column half, into the fp32 run
+    // accumulator in shared memory (set by the run's first item); the run's last item adds the
+    // accumulator out like drain_run.
+    auto drain_item_f8 = [&](int rr, bool rdown, int rslot, int rlt, int rkc, int rbuf,
+                             bool rfirst, bool rlast, int rlen) {
+      if (!ok) return;
+      float* dst;
+      float scale;
+      int bn;
+      resolve_dst(rdown, rslot, rlt, 0, dst, scale, bn);
+      // the scales (loaded before the wait)
+      const int e = meta.slot_e[rslot];
+      float sa = 0.0f, sb0, sb1;
+      if (!rdown) {
+        if (lane < a.N) sa = a.xs[(size_t)rkc * a.N + lane];
+        const bool up = rlt >= sc.nIt;
+        const int rb = (up ? rlt - sc.nIt : rlt) * bn / 128;
+        const float* sp = (up ? a.s_up : a.s_gate) + ((size_t)e * (a.I / 128) + rb) * (a.H / 128) + rkc;
+        sb0 = __ldg(sp);
+        sb1 = bn > 128 ? __ldg(sp + a.H / 128) : 0.0f;
+      } else {
+        if (lane < 16) sa = hsc_s[FP8 ? rbuf : 0][lane * kMaxHGroups + rkc];
+        const int rb = rlt * bn / 128;
+        const float* sp = a.s_down + ((size_t)e * (a.H / 128) + rb) * (a.I / 128) + rkc;
+        sb0 = __ldg(sp);
+        sb1 = bn > 128 ? __ldg(sp + a.I / 128) : 0.0f;
+      }
+      if (!mbar_wait(&afull[rr & 1], ((uint32_t)rr >> 1) & 1, hdr)) { ok = false; return; }
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + (uint32_t)((rr & 1) * kMaxBN);
+      float* ra = racc + lane * kRaccLd;
+#pragma unroll 1
+      for (int c = 0; c < bn; c += 64) {
+        float v[64];
+        tmem_ld32_nowait(tacc + (uint32_t)c, v);
+        tmem_ld32_nowait(tacc + (uint32_t)c + 32, v + 32);
+        tmem_wait_ld();
+        if (lane < 16 && dst) {
+          const float f = sa * (c < 128 ? sb0 : sb1);
+          float4* r4 = reinterpret_cast<float4*>(ra + c);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float4 o = rfirst ? make_float4(0.0f, 0.0f, 0.0f, 0.0f) : r4[i];
+            r4[i] = make_float4(fmaf(f, v[4 * i], o.x), fmaf(f, v[4 * i + 1], o.y),
+                                fmaf(f, v[4 * i + 2], o.z), fmaf(f, v[4 * i + 3], o.w));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&aempty[rr & 1]);
+      if (!rlast) return;
+      const uint32_t rows = __ballot_sync(0xffffffffu, dst != nullptr);
+      for (uint32_t m = rows; m; m &= m - 1) {
+        const int j = __ffs(m) - 1;
+        float* dj = reinterpret_cast<float*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(dst), j));
+        const float sj = __shfl_sync(0xffffffffu, scale, j);
+#pragma unroll 1
+        for (int c = 0; c < bn; c += 32) atomicAdd(dj + c + lane, sj * racc[j * kRaccLd + c + lane]);
+      }
+      __syncwarp();
+      publish(rdown, rslot, rlen);
+    };
+    // drains the pending group; `run_ends`: the next group belongs to another tile (or there
+    // is none), so an E4M3 run's accumulator is added out
+    auto drain_current = [&](bool run_ends) {
+      if (drainer && !drained && r_idx >= 0) {
+        if (FP8 && r_f8)
+          drain_item_f8(r_idx, r_down, r_slot, r_lt, r_kc, r_buf, r_first, run_ends, r_len);
+        else
+          drain_run(r_idx, r_down, r_slot, r_lt, r_kh, r_len);
+      }
       drained = true;
     };
-    // SiLU(gate) * up of the slot's tokens as the bf16 A operand (buffer nb % 2), 16 rows per
-    // 64-column box with the 128-byte swizzle: row j's 16-byte chunk c of box kb at
-    // kb * 2048 + j * 128 + ((c ^ (j & 7)) * 16).
-    auto build_a = [&](int slot, uint8_t* buf) {
-      const uint32_t target = (uint32_t)((slot >= 0 ? 2 * sc.nIt : 2 * sc.nSt) * sc.Pg);
+    // waits until every gate/up item of `slot` has been added out (other blocks; bounded)
+    auto wait_slot = [&](int slot) {
+      const uint32_t target =
+          (uint32_t)(slot >= 0 ? 2 * sc.nIt * sc.Pgr : 2 * sc.nSt * sc.Pg);
       if (drainer && lane == 0) {
         const uint32_t* cnt = a.h_cnt + (slot < 0 ? kDecodeMaxPairs : slot);
         if (ld_acquire(cnt) < target) {
@@ -1129,6 +1293,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       named_sync(1, kEpiThreads);
+    };
+    // SiLU(gate) * up of the slot's tokens as the bf16 A operand (buffer nb % 2), 16 rows per
+    // 64-column box with the 128-byte swizzle: row j's 16-byte chunk c of box kb at
+    // kb * 2048 + j * 128 + ((c ^ (j & 7)) * 16).
+    auto build_a = [&](int slot, uint8_t* buf) {
+      wait_slot(slot);
       int r0;
       const int ntok = slot_rows(a, meta, slot, r0);
       const int L = slot >= 0 ? a.I : a.S;
@@ -1139,10 +1309,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = id / cpr, c = id - j * cpr;
         uint4 o;
         const float* hr = a.hd + (size_t)(r0 + j) * (2 * a.ldh) + c * 8;
-        const float4 g0v = __ldcg(reinterpret_cast<const float4*>(hr));
-        const float4 g1v = __ldcg(reinterpret_cast<const float4*>(hr + 4));
-        const float4 u0 = __ldcg(reinterpret_cast<const float4*>(hr + a.ldh));
-        const float4 u1 = __ldcg(reinterpret_cast<const float4*>(hr + a.ldh + 4));
+        float4 g0v = __ldcg(reinterpret_cast<const float4*>(hr));
+        float4 g1v = __ldcg(reinterpret_cast<const float4*>(hr + 4));
+        float4 u0 = __ldcg(reinterpret_cast<const float4*>(hr + a.ldh));
+        float4 u1 = __ldcg(reinterpret_cast<const float4*>(hr + a.ldh + 4));
+        if (FP8 && slot < 0) {   // the shared tiles' second contraction part, added in order
+          const float* h2 = hr + (size_t)a.N * (2 * a.ldh);
+          auto add4 = [](float4& x, const float4 y) { x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w; };
+          add4(g0v, __ldcg(reinterpret_cast<const float4*>(h2)));
+          add4(g1v, __ldcg(reinterpret_cast<const float4*>(h2 + 4)));
+          add4(u0, __ldcg(reinterpret_cast<const float4*>(h2 + a.ldh)));
+          add4(u1, __ldcg(reinterpret_cast<const float4*>(h2 + a.ldh + 4)));
+        }
         o.x = pack_bf16x2(silu(g0v.x) * u0.x, silu(g0v.y) * u0.y);
         o.y = pack_bf16x2(silu(g0v.z) * u0.z, silu(g0v.w) * u0.w);
         o.z = pack_bf16x2(silu(g1v.x) * u1.x, silu(g1v.y) * u1.y);
@@ -1154,34 +1332,73 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_sync(1, kEpiThreads);
       if (et == 0) mbar_arrive(&bfull[nb & 1]);
     };
+    // E4M3 routed slot: the intermediate h = SiLU(gate) * up quantised per 1x128 group (the
+    // rule of quant_token_rows) as the E4M3 A operand of the down items, 16 rows per 128-code
+    // box with the 128-byte swizzle, one warp per (token row, group); scales into hsc_s[nb % 2].
+    auto build_a_f8 = [&](int slot, uint8_t* buf) {
+      wait_slot(slot);
+      int r0;
+      const int ntok = slot_rows(a, meta, slot, r0);
+      const int G = a.I / 128;
+      const int wq = et >> 5;
+      for (int gi = wq; gi < ntok * G; gi += kEpiThreads / 32) {
+        const int j = gi / G, g = gi - j * G;
+        const float* hr = a.hd + (size_t)(r0 + j) * (2 * a.ldh) + g * 128 + lane * 4;
+        const float4 gv = __ldcg(reinterpret_cast<const float4*>(hr));
+        const float4 uv = __ldcg(reinterpret_cast<const float4*>(hr + a.ldh));
+        const float h0 = silu(gv.x) * uv.x, h1 = silu(gv.y) * uv.y;
+        const float h2 = silu(gv.z) * uv.z, h3 = silu(gv.w) * uv.w;
+        const float am = warp_max(fmaxf(fmaxf(fabsf(h0), fabsf(h1)), fmaxf(fabsf(h2), fabsf(h3))));
+        const float sc8 = am > 0.0f ? __fdiv_rn(am, 448.0f) : 1.0f;
+        const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(h0, sc8), __fdiv_rn(h1, sc8)), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(h2, sc8), __fdiv_rn(h3, sc8)), __NV_SATFINITE, __NV_E4M3);
+        *reinterpret_cast<uint32_t*>(buf + (size_t)g * 2048 + j * 128 +
+                                     ((((lane >> 2) ^ (j & 7)) << 4) | ((lane & 3) << 2))) =
+            lo | (hi << 16);
+        if (lane == 0) hsc_s[FP8 ? (nb & 1) : 0][j * kMaxHGroups + g] = sc8;
+      }
+      fence_proxy_async_smem();
+      named_sync(1, kEpiThreads);
+      if (et == 0) mbar_arrive(&bfull[nb & 1]);
+    };
     for (int k = 0; k < nitems; ++k) {
       bool down;
-      int tile, kc, slot, lt;
-      sc.item(k, down, tile, kc, slot, lt);
-      if (run < 0 || down != prev_down || tile != prev_tile) {
+      int tile, kc, slot, lt, kh;
+      sc.item(k, down, tile, kc, slot, lt, kh);
+      const bool f8 = FP8 && slot >= 0;
+      const bool new_tile = run < 0 || down != prev_down || tile != prev_tile;
+      if (new_tile || f8) {
         ++run;
         prev_down = down;
         prev_tile = tile;
-        if (down && slot != bslot) {
+        if (new_tile && down && slot != bslot) {
           // The previous gate/up run is published first (the count may wait on it). Otherwise
           // the next buffer is free -- the runs that read it, two slot changes back, are
           // drained -- and the build overlaps the MMAs of the previous run.
-          if (!r_down) drain_current();
-          build_a(slot, hb + (size_t)(nb & 1) * pl.hbytes);
+          if (!r_down) drain_current(true);
+          if (f8) build_a_f8(slot, hb + (size_t)(nb & 1) * pl.hbytes);
+          else build_a(slot, hb + (size_t)(nb & 1) * pl.hbytes);
           ++nb;
           bslot = slot;
         }
-        drain_current();
+        drain_current(new_tile);
         r_idx = run;
         r_down = down;
         r_slot = slot;
         r_lt = lt;
-        r_len = 0;
+        r_kc = kc;
+        r_kh = kh;
+        r_f8 = f8;
+        r_buf = (nb - 1) & 1;   // (down: the buffer of this slot's build)
+        r_first = new_tile;
+        if (new_tile) r_len = 0;
         drained = false;
       }
       ++r_len;
     }
-    drain_current();
+    drain_current(true);
   }
   tc_fence_before();
   __syncthreads();
@@ -1220,12 +1437,17 @@ cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, 
   if (a.te > kDecodeMaxPairs || a.N > kDecodeMaxTokens || a.N < 1 || !a.h_cnt ||
       a.H % 128 || a.I % 128 || a.S % 128 || a.R > 1024 || a.E > 1024 || a.K > 32)
     return cudaErrorInvalidValue;
-  const int L = a.I > a.S ? a.I : a.S;
+  if (a.fp8 && (!a.s_gate || !a.s_up || !a.s_down || !a.xq || !a.xs || a.I > 128 * kMaxHGroups))
+    return cudaErrorInvalidValue;
   Plan pl{};
   decode_tile_rows(a.H, a.I, a.S, &pl.bn_g, &pl.bn_d);
-  pl.hbytes = (L / kBox) * kTokBytes;
+  // boxes of the down A operand: routed I / 64 (bf16) or I / 128 (E4M3), shared S / 64
+  const int hb_boxes = a.fp8 ? (a.I / 128 > a.S / kBox ? a.I / 128 : a.S / kBox)
+                             : (a.I > a.S ? a.I : a.S) / kBox;
+  pl.hbytes = hb_boxes * kTokBytes;
   const int per_stage = kTokBytes + kWBytes;
-  const int fixed = 1024 + 2 * pl.hbytes;   // alignment slack + two down A operands
+  // alignment slack + two down A operands (+ the E4M3 run accumulator)
+  const int fixed = 1024 + 2 * pl.hbytes + (a.fp8 ? kRaccBytes : 0);
   // (the static shared memory -- routing, barriers, drain staging -- stays within 16 KB)
   pl.stages = (kSmemLimit - 16384 - fixed) / per_stage;
   if (pl.stages > kMaxStages) pl.stages = kMaxStages;
@@ -1238,7 +1460,8 @@ cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, 
                                    (a.R <= 256 ? 8 + (size_t)a.N * a.R * 16 : 0);
   if (scratch > (size_t)pl.stages * (kTokBytes + kWBytes)) return cudaErrorInvalidValue;
   const size_t sm = (size_t)fixed + (size_t)pl.stages * per_stage;
-  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(decode_forward_kernel), sm);
+  auto kern = a.fp8 ? decode_forward_kernel<true> : decode_forward_kernel<false>;
+  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(kern), sm);
   if (e != cudaSuccess) return e;
   // the down phase waits on other blocks' gate/up work: all blocks must be resident (checked
   // once per device and shared-memory size)
@@ -1249,13 +1472,13 @@ cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, 
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(mu);
-    if (!ok.count({dev, sm})) {
+    const size_t key = sm * 2 + (a.fp8 ? 1 : 0);
+    if (!ok.count({dev, key})) {
       int per_sm = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_forward_kernel, kThreads,
-                                                        sm);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, sm);
       if (e != cudaSuccess) return e;
       if (per_sm < 1) return cudaErrorInvalidConfiguration;
-      ok.insert({dev, sm});
+      ok.insert({dev, key});
     }
   }
   cudaLaunchConfig_t cfg = {};
@@ -1268,7 +1491,7 @@ cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, 
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_forward_kernel, maps[kDmWg], maps[kDmWu], maps[kDmSg],
+  return cudaLaunchKernelEx(&cfg, kern, maps[kDmWg], maps[kDmWu], maps[kDmSg],
                             maps[kDmSu], maps[kDmWd], maps[kDmSd], maps[kDmX], maps[kDmXn], a,
                             pl);
 }

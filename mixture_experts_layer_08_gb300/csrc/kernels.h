@@ -122,8 +122,17 @@ struct DecodeArgs {
                                    // (the last entry: shared expert)
   WsHeader* hdr;                   // done_blocks (grid barriers) zero on entry
   __nv_bfloat16* out;              // [N,H]
+  // E4M3 routed experts (the shared expert stays bf16)
+  int fp8;
+  const float* s_gate;             // [E, I/128, H/128] block scales of Wg
+  const float* s_up;               // [E, I/128, H/128] of Wu
+  const float* s_down;             // [E, H/128, I/128] of Wd
+  uint8_t* xq;                     // [N, H] E4M3 codes of the routed experts' input (phase 0)
+  float* xs;                       // [H/128, N] their 1x128 scales
 };
-// Tensor maps (bf16, box {64, rows}, 128-byte swizzle) the decode kernel streams from.
+// Tensor maps (box 128 bytes wide, 128-byte swizzle) the decode kernel streams from: bf16
+// {64, rows}, or with E4M3 routed experts uint8 {128, rows} for Wg, Wu, Wd and the routed
+// experts' input (kDmXn then maps the E4M3 codes xq).
 enum DecodeMap { kDmWg = 0, kDmWu, kDmSg, kDmSu, kDmWd, kDmSd, kDmX, kDmXn, kDmNum };
 // Box rows: x and the routed experts' input xn (x itself without a pre-expert norm) 16;
 // gate/up weights (Wg, Wu, Sg, Su) *bn_g; down weights (Wd, Sd) *bn_d.

@@ -65,3 +65,5 @@ def test_launches_per_forward(B):
     assert n(I.DECODE, B.PATH_GROUPED) == 8
     assert n(I.FP8_PREFILL) == 9                 # + the token-row quantiser, no shared expert
     assert n(I.FP8_PREFILL.with_(shared_inter=512)) == 11
+    assert n(I.DECODE_FP8) == 1                  # E4M3 experts through the decode kernel too
+    assert n(I.DECODE_FP8, B.PATH_GROUPED) == 11

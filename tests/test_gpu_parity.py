@@ -346,6 +346,38 @@ def test_fp8_forward_matches_oracle(B, shape):
     check_out(got, ref["out"], FP8_ATOL, FP8_RTOL, FP8_REL_L2)
 
 
+# decode-sized FP8 batches, on the decode kernel (E4M3 items, per-item scale promotion) and on
+# the grouped chain: 32 routed pairs with a gated shared expert; 64 pairs over 128-row gate/up
+# tiles (I = 384); a pre-expert norm (the kernel quantises xn)
+FP8_DECODE = [FP8_SMALL.with_(name="fp8_decode_n4", num_tokens=4, num_experts=32, router_width=32,
+                              top_k=8, shared_inter=256, shared_gated=True),
+              FP8_SMALL.with_(name="fp8_decode_n16_k4", num_tokens=16, num_experts=16,
+                              router_width=16, top_k=4, inter=384, hidden=768, shared_inter=128),
+              FP8_SMALL.with_(name="fp8_decode_prenorm", num_tokens=3, num_experts=16,
+                              router_width=16, top_k=2, pre_expert_norm=True)]
+
+
+@pytest.mark.parametrize("path", [1, 2], ids=["decode", "grouped"])
+@pytest.mark.parametrize("shape", FP8_DECODE, ids=lambda s: s.name)
+def test_fp8_decode_matches_oracle(B, shape, path):
+    inp = I.make_inputs(shape)
+    got, gidx, gw = run_gpu(B, inp, path)
+    check_routing(gidx, O.moe_forward(inp, routing_only=True))
+    ref = O.moe_forward(inp, forced_idx=gidx)
+    check_out(got, ref["out"], FP8_ATOL, FP8_RTOL, FP8_REL_L2)
+
+
+def test_fp8_decode_kernel_modes(B):
+    """E4M3 experts on the decode kernel: the deterministic mode repeats bit for bit, the
+    FP32-atomic accumulation matches the oracle."""
+    inp = I.make_inputs(FP8_DECODE[0])
+    first = run_gpu(B, inp, 1)[0]
+    for _ in range(3):
+        assert np.array_equal(run_gpu(B, inp, 1)[0], first)
+    got, gidx, _ = run_gpu(B, inp, 1, deterministic=False)
+    check_out(got, O.moe_forward(inp, forced_idx=gidx)["out"], FP8_ATOL, FP8_RTOL, FP8_REL_L2)
+
+
 @pytest.mark.parametrize("shape", [I.FP8_PREFILL, I.DECODE_FP8], ids=lambda s: s.name)
 def test_fp8_full_size_sampled_tokens(B, shape):
     inp = I.make_inputs(shape, device="cuda")
