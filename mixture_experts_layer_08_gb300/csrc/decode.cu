@@ -1241,12 +1241,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < 16 && dst) {
           const float f = sa * (c < 128 ? sb0 : sb1);
           float4* r4 = reinterpret_cast<float4*>(ra + c);
+          // all 16 loads in flight before the first update
+          float4 o[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float4 o = rfirst ? make_float4(0.0f, 0.0f, 0.0f, 0.0f) : r4[i];
-            r4[i] = make_float4(fmaf(f, v[4 * i], o.x), fmaf(f, v[4 * i + 1], o.y),
-                                fmaf(f, v[4 * i + 2], o.z), fmaf(f, v[4 * i + 3], o.w));
-          }
+          for (int i = 0; i < 16; ++i) o[i] = rfirst ? make_float4(0.0f, 0.0f, 0.0f, 0.0f) : r4[i];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            r4[i] = make_float4(fmaf(f, v[4 * i], o[i].x), fmaf(f, v[4 * i + 1], o[i].y),
+                                fmaf(f, v[4 * i + 2], o[i].z), fmaf(f, v[4 * i + 3], o[i].w));
         }
       }
       tc_fence_before();
