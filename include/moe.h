@@ -142,8 +142,9 @@ MOE_API moe_status_t moe_workspace_size(const moe_config_t *cfg, size_t *bytes);
  *  workspace  device scratch of >= moe_workspace_size() bytes, 256-byte aligned; its contents
  *             on entry do not matter; it must not be used by another call still in flight.
  *  topk_idx_out / topk_w_out  nullable uint32 / fp32 [N,K]: the routing actually used.
- *  forced_idx nullable uint32 [N,K] expert ids that replace the top-K selection (test hook;
- *             the weights are then the probabilities of those ids, renormalised as configured).
+ *  forced_idx nullable uint32 [N,K] expert ids (< router_width) that replace the top-K
+ *             selection (test hook; the weights are then the probabilities of those ids,
+ *             renormalised as configured).
  * Pages: forward_prefill.rs `forward_prefill` (prefill chain), forward.rs `forward`
  * (decode), forward_atomic_c4.rs (atomic decode accumulation), forward.rs `apply_zero_expert`. */
 MOE_API moe_status_t moe_forward(const moe_config_t *cfg, const moe_weights_t *weights, const void *x,

@@ -333,6 +333,15 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
   }
   if (c->num_tokens <= kSmallRouterMaxTokens) {
     CK(launch_router_small(ra, sa, false, st));
+    CK(launch_topk(ra, st));
+  } else if (router_topk_tc_supported(c->num_tokens, c->hidden, c->router_width, num_sms())) {
+    // router GEMM + scoring + top-K in one launch
+    CUtensorMap mx, mw;
+    const int R = c->router_width;
+    if (!make_map_bf16(&mx, x, c->hidden, c->num_tokens, 128) ||
+        !make_map_bf16(&mw, w->router_w, c->hidden, R, R <= 256 ? R : 128))
+      return MOE_ERR_CUDA;
+    CK(launch_router_topk_tc(ra, mx, mw, num_sms(), st));
   } else {
     // router logits on the tensor cores: [N,H] x [R,H]^T -> fp32 [N,R]
     CUtensorMap maps[2][3];
@@ -351,8 +360,8 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
     g.p[0].n_valid = c->router_width;
     g.status = hdr;
     CK(launch_gemm_bf16(kGemmStoreF32, 128, maps, g, num_sms(), st));
+    CK(launch_topk(ra, st));
   }
-  CK(launch_topk(ra, st));
   const bool fp8 = c->weight_dtype == MOE_W_FP8_E4M3_B128;
   // the routed experts' input: x, or its pre-expert RMSNorm (after the routing, which read x)
   const __nv_bfloat16* xe = ra.x;

@@ -67,6 +67,13 @@ cudaError_t launch_router_small(const RouteArgs& a, const SortArgs& s, bool fuse
                                 cudaStream_t st);
 // Scoring + top-K + weights, one warp per token.
 cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st);
+// Router GEMM on the tensor cores with the scoring + top-K fused (logits, idx, w, zsum): the
+// contraction of each 128-token tile split over a cluster of CTAs whose partial sums are
+// combined in a fixed order. tm_x: x [N,H], box {64, 128}; tm_w: router [R,H], box {64, R}
+// for R <= 256, else {64, 128}. Supported when router_topk_tc_supported().
+bool router_topk_tc_supported(int N, int H, int R, int num_sms);
+cudaError_t launch_router_topk_tc(const RouteArgs& a, const CUtensorMap& tm_x,
+                                  const CUtensorMap& tm_w, int num_sms, cudaStream_t st);
 // Per 1x128 E4M3 quantisation of the token rows (FP8 experts): codes [N,H], scales [H/128,N].
 // xn[t,:] = bf16(x[t,:] * g / sqrt(mean(x[t,:]^2) + eps)), fp32 arithmetic; one warp per row.
 cudaError_t launch_rms_norm_rows(const __nv_bfloat16* x, const __nv_bfloat16* g, float eps, int N,

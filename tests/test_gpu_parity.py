@@ -75,6 +75,19 @@ SMALL = {
                                        num_experts=16, router_width=16, top_k=4, inter=256,
                                        shared_inter=256, shared_gated=True,
                                        pre_expert_norm=True),
+    # the fused tensor-core router (N > 64, R a multiple of 32): a ragged last token tile,
+    # R > 256 (two MMAs per K step) with identity experts and the correction bias
+    "fused_router_wide": I.ZERO_EXPERT.with_(name="fused_router_wide", num_tokens=300,
+                                             hidden=1024, num_experts=256, router_width=384,
+                                             top_k=8, inter=128),
+    "fused_router_narrow": I.PREFILL.with_(name="fused_router_narrow", num_tokens=333,
+                                           hidden=768, num_experts=64, router_width=64,
+                                           top_k=6, inter=256, shared_inter=128,
+                                           shared_gated=True),
+    # K > 8: the fused router's K rounds of arg-max instead of its sorting networks
+    "fused_router_k12": I.PREFILL.with_(name="fused_router_k12", num_tokens=130, hidden=512,
+                                        num_experts=64, router_width=64, top_k=12, inter=128,
+                                        shared_inter=0, zipf_s=0.0),
     "sigmoid_bias_small": I.PREFILL.with_(name="sigmoid_bias_small", num_tokens=200,
                                           hidden=512, num_experts=32, router_width=32,
                                           top_k=6, inter=256, shared_inter=0, zipf_s=0.0,
@@ -163,6 +176,42 @@ def test_route_matches_oracle(B, name, path):
     np.testing.assert_array_equal(p2r.cpu().numpy().view(np.uint32), o_p2r)
 
 
+@pytest.mark.parametrize("name", ["fused_router_wide", "fused_router_narrow",
+                                  "fused_router_k12", "sigmoid_bias_small"])
+def test_fused_router_is_repeatable(B, name):
+    """The tensor-core router with the top-K fused (N > 64, R a multiple of 32) splits each
+    token tile's contraction over a cluster of CTAs and combines the partial sums through
+    distributed shared memory in a fixed order: 12 launches give bit-identical ids, weights
+    and zsum, each a valid routing against the oracle."""
+    shape = SMALL[name]
+    inp = I.make_inputs(shape)
+    dev = inp.to("cuda")
+    cfg = B.make_config(shape, True, 2)
+    ws = B.alloc_workspace(cfg)
+    w = B.make_weights(dev)
+    N, K, E = shape.num_tokens, shape.top_k, shape.num_experts
+    ref = O.moe_forward(inp, routing_only=True)
+    far = ref["gap"] > TIE_GAP
+    first = None
+    for _ in range(12):
+        idx = torch.empty(N, K, dtype=torch.int32, device="cuda")
+        wt = torch.empty(N, K, dtype=torch.float32, device="cuda")
+        zs = torch.empty(N, dtype=torch.float32, device="cuda")
+        offs = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+        spairs = torch.empty(N * K, dtype=torch.int32, device="cuda")
+        p2r = torch.empty(N * K, dtype=torch.int32, device="cuda")
+        B.moe_route(cfg, w, dev.x, ws, None, idx, wt, zs, offs, spairs, p2r)
+        torch.cuda.synchronize()
+        got = (idx.cpu().numpy(), wt.cpu().numpy(), zs.cpu().numpy())
+        check_routing(got[0], ref)
+        np.testing.assert_allclose(got[1][far], ref["w"][far], rtol=1e-5, atol=1e-7)
+        if first is None:
+            first = got
+        else:
+            for a, b in zip(first, got):
+                np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
 # ------------------------------------------------------------------ whole forward
 
 @pytest.mark.parametrize("name", list(SMALL))
@@ -202,12 +251,14 @@ def _assert_identity_exact(got, x, w):
 
 
 @pytest.mark.parametrize("path", [1, 2], ids=["decode", "grouped"])
-@pytest.mark.parametrize("name", ["zero_expert_small", "zero_expert_decode", "zero_split_decode"])
+@pytest.mark.parametrize("name", ["zero_expert_small", "zero_expert_decode", "zero_split_decode",
+                                  "fused_router_wide"])
 def test_forced_identity_experts_are_exact(B, name, path):
     """Every slot on an identity expert, no shared expert: out == bf16(zsum * x) bitwise, on
     both chains (the decode kernel adds the identity experts in its combine phase, the grouped
     chain in the combine kernel). zero_split_decode has at most 32 pairs and a router of at most
-    256 columns (the decode kernel's split routing); zero_expert_decode a 384-wide router."""
+    256 columns (the decode kernel's split routing); zero_expert_decode a 384-wide router;
+    fused_router_wide the tensor-core router with the top-K fused (forced ids)."""
     shape = (SMALL[name] if name in SMALL else
              SMALL["zero_expert_small"].with_(name=name, num_tokens=4, num_experts=64,
                                               router_width=96))
