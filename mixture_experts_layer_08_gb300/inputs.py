@@ -15,6 +15,13 @@ in the fixed order x, Wr, Wg, Wu, Wd, Sg, Su, Sd, g, bias):
   scale per 128x128 block (``scale = amax / 448``, 1 where the block is all zero); the
   rounding to E4M3 is done by ``torch``'s own cast, so neither the kernels nor the oracle
   supply it.
+* NVFP4 experts: the packed representation is drawn directly (no quantiser): each 4-bit
+  E2M1 code has a uniform sign bit and a magnitude index 0..7 from the fixed categorical
+  distribution ``NVFP4_MAG_PROBS``; every 16 consecutive elements along the contraction
+  share one E4M3 scale code drawn uniformly from 0x30..0x3F (the E4M3 values in [0.5, 2));
+  each expert matrix has one fp32 ``scale2 = 0.007 * (1 + 0.1 * N(0, 1))``, which puts the
+  weights near the ``N(0, 0.02)`` magnitude of the bf16 experts. Codes are packed two per
+  byte, element ``2j`` in the low nibble and ``2j + 1`` in the high nibble.
 
 Weight layout is ``[out_features, in_features]`` (K-contiguous): gate/up ``[E, I, H]``,
 down ``[E, H, I]``, shared gate/up ``[S, H]``, shared down ``[H, S]``.
@@ -33,10 +40,14 @@ SCORING_SIGMOID_BIAS = 2
 
 WDTYPE_BF16 = 0
 WDTYPE_FP8_E4M3_B128 = 1
+WDTYPE_NVFP4 = 2
+
+# probabilities of the E2M1 magnitude indices 0..7 of the drawn NVFP4 codes
+NVFP4_MAG_PROBS = (0.10, 0.16, 0.18, 0.16, 0.14, 0.14, 0.08, 0.04)
 
 _TENSOR_IDS = {"x": 0, "router_w": 1, "w_gate": 2, "w_up": 3, "w_down": 4,
                "sh_gate": 5, "sh_up": 6, "sh_down": 7, "sh_gate_vec": 8, "bias": 9,
-               "norm_w": 10}
+               "norm_w": 10, "sf_gate": 11, "sf_up": 12, "sf_down": 13, "scale2": 14}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -84,9 +95,13 @@ FP8_PREFILL = MoeShape("fp8_prefill_n8192", 8192, 4096, 128, 128, 8, 1536,
 # routed experts (128x128 block scales; the shared expert stays bf16).
 DECODE_PRENORM = DECODE.with_(name="decode_prenorm_bf16_n4", pre_expert_norm=True)
 DECODE_FP8 = DECODE.with_(name="decode_fp8_n4", weight_dtype=WDTYPE_FP8_E4M3_B128)
+# NVFP4 routed experts (E2M1 + E4M3 scale per 16 + fp32 scale per expert matrix) on the
+# decode and prefill shapes
+DECODE_NVFP4 = DECODE.with_(name="decode_nvfp4_n4", weight_dtype=WDTYPE_NVFP4)
+PREFILL_NVFP4 = PREFILL.with_(name="prefill_nvfp4_n4096", weight_dtype=WDTYPE_NVFP4)
 
 WORKLOADS = {s.name: s for s in (TINY, DECODE, PREFILL, ZERO_EXPERT, FP8_PREFILL, DECODE_PRENORM,
-                                 DECODE_FP8)}
+                                 DECODE_FP8, DECODE_NVFP4, PREFILL_NVFP4)}
 
 
 def _gen(shape: MoeShape, key: str, device) -> torch.Generator:
@@ -117,6 +132,26 @@ def quantize_weight_e4m3_b128(w: torch.Tensor):
     return q8.view(torch.uint8), scale.to(torch.float32).contiguous()
 
 
+def draw_nvfp4(shape: "MoeShape", key: str, size, device):
+    """Draw a packed NVFP4 matrix ``[E, rows, cols]`` (see the module docstring): returns
+    (codes uint8 ``[E, rows, cols/2]``, E4M3 scale codes uint8 ``[E, rows, cols/16]``)."""
+    E, rows, cols = size
+    assert cols % 16 == 0
+    g = _gen(shape, key, device)
+    cum = torch.tensor(NVFP4_MAG_PROBS, dtype=torch.float64).cumsum(0)[:-1]
+    cum = cum.to(device=device, dtype=torch.float32)
+    packed = torch.empty(E, rows, cols // 2, dtype=torch.uint8, device=device)
+    for e in range(E):   # one expert at a time keeps the temporaries small
+        u = torch.rand(rows, cols, generator=g, device=device)
+        neg = u >= 0.5
+        mag = torch.bucketize((u - 0.5 * neg.float()) * 2.0, cum, right=True)
+        code = (mag | (neg.to(torch.int64) << 3)).to(torch.uint8)
+        packed[e] = code[:, 0::2] | (code[:, 1::2] << 4)
+    sf = torch.randint(0x30, 0x40, (E, rows, cols // 16), generator=_gen(shape, "sf_" + key[2:],
+                       device), device=device, dtype=torch.int64).to(torch.uint8)
+    return packed, sf
+
+
 @dataclasses.dataclass
 class MoeInputs:
     """All tensors of one forward. bf16 tensors are torch.bfloat16; FP8 weights are uint8
@@ -130,6 +165,12 @@ class MoeInputs:
     s_gate: Optional[torch.Tensor] = None
     s_up: Optional[torch.Tensor] = None
     s_down: Optional[torch.Tensor] = None
+    sf_gate: Optional[torch.Tensor] = None     # NVFP4: E4M3 scale codes per 16 elements
+    sf_up: Optional[torch.Tensor] = None
+    sf_down: Optional[torch.Tensor] = None
+    scale2_gate: Optional[torch.Tensor] = None  # NVFP4: fp32 [E] per expert matrix
+    scale2_up: Optional[torch.Tensor] = None
+    scale2_down: Optional[torch.Tensor] = None
     sh_gate: Optional[torch.Tensor] = None
     sh_up: Optional[torch.Tensor] = None
     sh_down: Optional[torch.Tensor] = None
@@ -158,6 +199,9 @@ def make_inputs(shape: MoeShape, device="cpu", x_only_tokens: Optional[int] = No
     router_w = _randn(shape, "router_w", (R, H), 0.02, device).to(bf)
     out = {}
     for key, size in (("w_gate", (E, I, H)), ("w_up", (E, I, H)), ("w_down", (E, H, I))):
+        if shape.weight_dtype == WDTYPE_NVFP4:
+            out[key], out["sf_" + key[2:]] = draw_nvfp4(shape, key, size, device)
+            continue
         w = _randn(shape, key, size, 0.02, device)
         if shape.weight_dtype == WDTYPE_FP8_E4M3_B128:
             q, s = quantize_weight_e4m3_b128(w)
@@ -166,6 +210,11 @@ def make_inputs(shape: MoeShape, device="cpu", x_only_tokens: Optional[int] = No
         else:
             out[key] = w.to(bf)
         del w
+    if shape.weight_dtype == WDTYPE_NVFP4:
+        s2 = 0.007 * (1.0 + 0.1 * _randn(shape, "scale2", (3, E), 1.0, device))
+        out["scale2_gate"], out["scale2_up"], out["scale2_down"] = (s2[0].contiguous(),
+                                                                    s2[1].contiguous(),
+                                                                    s2[2].contiguous())
     sh = {}
     if S > 0:
         sh["sh_gate"] = _randn(shape, "sh_gate", (S, H), 0.02, device).to(bf)

@@ -30,6 +30,11 @@
  *    the contraction dim to E4M3 with scale = amax/448 (1 if amax == 0), the quantisation
  *    decided in fp32 (the kernel's precision); weights arrive as E4M3 codes with one fp32
  *    scale per 128x128 block. Everything after the quantisation is fp64.
+ *  - NVFP4 experts (the decode page's packed weights + `scale_ptrs` + `scale2_vals` tables,
+ *    "spark_model/layers/moe/forward.rs", NVFP4 decode arm): weight = E2M1 code x E4M3 scale
+ *    of its group of 16 consecutive elements along the contraction x the matrix's fp32
+ *    scale2; codes packed two per byte, element 2j in the low nibble. Activations stay bf16
+ *    (the pages' w4a16 GEMV): nothing is quantised, everything is fp64.
  *
  * Parity pins: see the oracle tests (brute-force top-K, closed forms, dense SwiGLU through a
  * library matmul, exact identity-expert results, E4M3 against torch's float8 type, and a
@@ -47,6 +52,14 @@ double orc_bf16_to_f64(uint16_t b) {
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* E2M1 (OCP MX FP4): bit 3 sign, bits 2-1 exponent (bias 1), bit 0 mantissa; exponent 0
+ * encodes the subnormals 0 and 0.5; no infinities or NaN. */
+double orc_e2m1_decode(uint8_t nib) {
+    int s = (nib >> 3) & 1, e = (nib >> 1) & 3, m = nib & 1;
+    double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -mag : mag;
 }
 
 /* E4M3 (OCP FP8, "fn" variant): 1 sign, 4 exponent bits (bias 7), 3 mantissa bits; no
@@ -115,7 +128,7 @@ typedef struct {
                                  2 sigmoid + selection-only correction bias */
     int32_t norm_topk_prob;
     double routed_scaling_factor;
-    int32_t weight_dtype;     /* 0 bf16, 1 E4M3 + fp32 128x128 block scales */
+    int32_t weight_dtype;     /* 0 bf16, 1 E4M3 + fp32 128x128 block scales, 2 NVFP4 */
     double rms_norm_eps;      /* with pre_expert_norm_w: epsilon of the pre-expert RMSNorm */
 } orc_config_t;
 
@@ -128,6 +141,8 @@ typedef struct {
     const uint16_t *sh_gate, *sh_up, *sh_down; /* bf16 [S,H], [S,H], [H,S] */
     const uint16_t *sh_gate_vec;      /* bf16 [H] or NULL */
     const uint16_t *pre_expert_norm_w; /* bf16 [H] or NULL: RMSNorm of the routed experts' input */
+    const uint8_t *sf_gate, *sf_up, *sf_down; /* NVFP4: E4M3 scale codes [E,rows,cols/16] */
+    const float *scale2_gate, *scale2_up, *scale2_down; /* NVFP4: fp32 [E] */
 } orc_weights_t;
 
 /* Router logits of one token, fp64: L[r] = sum_h x[h] * Wr[r,h] (+ logit bias[r]). */
@@ -201,13 +216,27 @@ static void route_token(const orc_config_t *c, const orc_weights_t *w, const dou
 
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
+/* One expert weight matrix [E, rows, cols] and its scales (by weight dtype). */
+typedef struct {
+    const void *w;
+    const float *s;        /* FP8: fp32 [E, rows/128, cols/128] */
+    const uint8_t *sf;     /* NVFP4: E4M3 codes [E, rows, cols/16] */
+    const float *scale2;   /* NVFP4: fp32 [E] */
+} orc_mat_t;
+
 /* Weight element (row, col) of expert e of a [E, rows, cols] matrix, decoded to fp64. */
-static double wget(const orc_config_t *c, const void *base, const float *scales, int e,
-                   int rows, int cols, int row, int col) {
+static double wget(const orc_config_t *c, orc_mat_t m, int e, int rows, int cols, int row,
+                   int col) {
+    if (c->weight_dtype == 2) {
+        uint8_t byte = ((const uint8_t *)m.w)[((size_t)e * rows + row) * (cols / 2) + col / 2];
+        uint8_t nib = (col & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+        uint8_t sc = m.sf[((size_t)e * rows + row) * (cols / 16) + col / 16];
+        return orc_e2m1_decode(nib) * orc_e4m3_decode(sc) * (double)m.scale2[e];
+    }
     size_t off = ((size_t)e * rows + row) * cols + col;
-    if (c->weight_dtype == 0) return orc_bf16_to_f64(((const uint16_t *)base)[off]);
-    double s = (double)scales[((size_t)e * (rows / 128) + row / 128) * (cols / 128) + col / 128];
-    return orc_e4m3_decode(((const uint8_t *)base)[off]) * s;
+    if (c->weight_dtype == 0) return orc_bf16_to_f64(((const uint16_t *)m.w)[off]);
+    double s = (double)m.s[((size_t)e * (rows / 128) + row / 128) * (cols / 128) + col / 128];
+    return orc_e4m3_decode(((const uint8_t *)m.w)[off]) * s;
 }
 
 /* y[H] = (SiLU(xe . Wg_e^T) * (xe . Wu_e^T)) . Wd_e^T for routed expert e. `xe` is the
@@ -215,11 +244,14 @@ static double wget(const orc_config_t *c, const void *base, const float *scales,
 static void expert_ffn(const orc_config_t *c, const orc_weights_t *w, int e, const double *xe,
                        double *hbuf, float *hbuf32, double *y) {
     int H = c->hidden, I = c->inter;
+    orc_mat_t mg = {w->w_gate, w->s_gate, w->sf_gate, w->scale2_gate};
+    orc_mat_t mu = {w->w_up, w->s_up, w->sf_up, w->scale2_up};
+    orc_mat_t md = {w->w_down, w->s_down, w->sf_down, w->scale2_down};
     for (int i = 0; i < I; ++i) {
         double g = 0.0, u = 0.0;
         for (int h = 0; h < H; ++h) {
-            g += xe[h] * wget(c, w->w_gate, w->s_gate, e, I, H, i, h);
-            u += xe[h] * wget(c, w->w_up, w->s_up, e, I, H, i, h);
+            g += xe[h] * wget(c, mg, e, I, H, i, h);
+            u += xe[h] * wget(c, mu, e, I, H, i, h);
         }
         hbuf[i] = silu(g) * u;
     }
@@ -230,7 +262,7 @@ static void expert_ffn(const orc_config_t *c, const orc_weights_t *w, int e, con
     }
     for (int h = 0; h < H; ++h) {
         double acc = 0.0;
-        for (int i = 0; i < I; ++i) acc += hbuf[i] * wget(c, w->w_down, w->s_down, e, H, I, h, i);
+        for (int i = 0; i < I; ++i) acc += hbuf[i] * wget(c, md, e, H, I, h, i);
         y[h] = acc;
     }
 }
@@ -298,6 +330,10 @@ int orc_moe_forward(const orc_config_t *c, const orc_weights_t *w, const uint16_
     if (N < 0 || H <= 0 || E <= 0 || R < E || K <= 0 || K > R || K > 64 || I <= 0 || S < 0)
         return -1;
     if (c->weight_dtype == 1 && (H % 128 || I % 128)) return -1;
+    if (c->weight_dtype == 2 && (H % 16 || I % 16 || !w->sf_gate || !w->sf_up || !w->sf_down ||
+                                 !w->scale2_gate || !w->scale2_up || !w->scale2_down))
+        return -1;
+    if (c->weight_dtype < 0 || c->weight_dtype > 2) return -1;
     if (tokens == NULL) n_sel = N;
     int bad = 0;
 #pragma omp parallel for schedule(dynamic, 1)

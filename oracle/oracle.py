@@ -13,7 +13,8 @@ Two independent fp64 formulations of the same block:
   permutes or gathers, so it also cross-checks the sort/unpermute reading.
 
 Plus the stable expert sort (``sort_by_expert``) that defines the permutation outputs, and
-the E4M3 helpers. Citations are to the pages of MoE dispatch code the block is taken from
+the E4M3 / E2M1 helpers. NVFP4 experts: the C file decodes each E2M1 nibble from its bit
+fields, the dense form from a table of the format's eight magnitudes. Citations are to the pages of MoE dispatch code the block is taken from
 (see ``moe_oracle.c``'s header).
 
 Parity pins live in ``tests/test_oracle_pins.py``. Parity unpinned: full-size outputs
@@ -61,7 +62,8 @@ class _Config(ctypes.Structure):
 
 _WEIGHTS = ("router_w", "router_logit_bias", "correction_bias", "w_gate", "w_up", "w_down",
             "s_gate", "s_up", "s_down", "sh_gate", "sh_up", "sh_down", "sh_gate_vec",
-            "pre_expert_norm_w")
+            "pre_expert_norm_w", "sf_gate", "sf_up", "sf_down", "scale2_gate", "scale2_up",
+            "scale2_down")
 
 
 class _Weights(ctypes.Structure):
@@ -76,6 +78,8 @@ def _load():
             lib.orc_moe_forward.restype = ctypes.c_int
             lib.orc_moe_forward.argtypes = [ctypes.POINTER(_Config), ctypes.POINTER(_Weights)] \
                 + [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 9 + [ctypes.c_int]
+            lib.orc_e2m1_decode.restype = ctypes.c_double
+            lib.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
             lib.orc_e4m3_decode.restype = ctypes.c_double
             lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
             lib.orc_e4m3_encode.restype = ctypes.c_uint8
@@ -146,6 +150,11 @@ def moe_forward(inp, tokens=None, forced_idx=None, routing_only: bool = False):
         raise ValueError("oracle rejected the configuration or token list")
     return {"out": out, "idx": idx, "w": w, "zsum": zsum, "gap": gap, "gamma": gamma,
             "sel": sel}
+
+
+def e2m1_decode(nibble: int) -> float:
+    """The C oracle's decode of one 4-bit E2M1 code."""
+    return _load().orc_e2m1_decode(nibble)
 
 
 def e4m3_decode(code: int) -> float:
@@ -259,6 +268,22 @@ def _quant_rows_np(a: np.ndarray) -> np.ndarray:
     return deq.reshape(n, m)
 
 
+# E2M1 magnitudes of codes 0..7 as the OCP MX format lists them; bit 3 is the sign.
+_E2M1_MAGNITUDES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def _dequant_nvfp4(packed: torch.Tensor, sf: torch.Tensor, scale2: torch.Tensor) -> np.ndarray:
+    """[E, rows, cols/2] packed E2M1 codes (element 2j in the low nibble), [E, rows, cols/16]
+    E4M3 scale codes, fp32 [E] -> fp64 [E, rows, cols]."""
+    p = packed.detach().cpu().numpy()
+    codes = np.stack([p & 15, p >> 4], axis=-1).reshape(*p.shape[:-1], p.shape[-1] * 2)
+    mag = np.asarray(_E2M1_MAGNITUDES)[codes & 7]
+    val = np.where(codes >= 8, -mag, mag)
+    scal = _e4m3_table()[sf.detach().cpu().numpy().astype(np.int64)]       # [E, rows, cols/16]
+    val = val * np.repeat(scal, 16, axis=-1)
+    return val * scale2.detach().cpu().double().numpy()[:, None, None]
+
+
 def moe_forward_dense(inp, forced_idx=None):
     """O-dense: every expert on every token (fp64 matmuls), masked by the routing.
     Returns dict with ``out`` [N,H], ``idx`` [N,K], ``w`` [N,K]."""
@@ -298,6 +323,11 @@ def moe_forward_dense(inp, forced_idx=None):
         Wu = _dequant_blocks(inp.w_up, inp.s_up)
         Wd = _dequant_blocks(inp.w_down, inp.s_down)
         xe = _quant_rows_np(xr)
+    elif s.weight_dtype == 2:
+        Wg = _dequant_nvfp4(inp.w_gate, inp.sf_gate, inp.scale2_gate)
+        Wu = _dequant_nvfp4(inp.w_up, inp.sf_up, inp.scale2_up)
+        Wd = _dequant_nvfp4(inp.w_down, inp.sf_down, inp.scale2_down)
+        xe = xr
     else:
         Wg, Wu, Wd = _f64(inp.w_gate), _f64(inp.w_up), _f64(inp.w_down)
         xe = xr

@@ -440,3 +440,78 @@ def test_fp8_formulations_agree_and_stay_near_unquantised():
     c = O.moe_forward_dense(ref_inp, forced_idx=a["idx"])
     rel_q = np.linalg.norm(a["out"] - c["out"]) / np.linalg.norm(c["out"])
     assert 1e-4 < rel_q < 0.08
+
+
+# ------------------------------------------------------------------ NVFP4 experts
+
+E2M1_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "e2m1_ocp_mx.txt")
+
+
+def test_e2m1_decode_all_codes_match_the_ocp_table():
+    rows = [l.split() for l in open(E2M1_GOLDEN) if l.strip() and not l.startswith("#")]
+    assert len(rows) == 16
+    for code, val in rows:
+        got = O.e2m1_decode(int(code))
+        assert got == float(val) and math.copysign(1.0, got) == math.copysign(1.0, float(val))
+
+
+def _nvfp4_inputs(shape, placements, sf_codes, scale2):
+    """NVFP4 weights that are zero except for hand-placed codes. `placements` maps a matrix
+    name to [(row, col, code)]; `sf_codes` to {(row, group): E4M3 code} (others 0x38 = 1.0);
+    `scale2` to its fp32 value. Returns the inputs and the dense fp64 matrices they encode,
+    built from the placements by hand (value table, scale table, product)."""
+    base = I.make_inputs(shape.with_(weight_dtype=I.WDTYPE_BF16))
+    E, H, Ii = shape.num_experts, shape.hidden, shape.inter
+    e2m1 = {2: 1.0, 5: 3.0, 7: 6.0, 9: -0.5, 12: -2.0}
+    e4m3 = {0x38: 1.0, 0x40: 2.0, 0x30: 0.5, 0x3C: 1.5}
+    kw, dense = {}, {}
+    for name, (rows, cols) in (("gate", (Ii, H)), ("up", (Ii, H)), ("down", (H, Ii))):
+        packed = torch.zeros(E, rows, cols // 2, dtype=torch.uint8)
+        sf = torch.full((E, rows, cols // 16), 0x38, dtype=torch.uint8)
+        d = torch.zeros(E, rows, cols, dtype=torch.float64)
+        for (r, g), code in sf_codes.get(name, {}).items():
+            sf[0, r, g] = code
+        for r, c, code in placements.get(name, []):
+            byte = int(packed[0, r, c // 2])
+            byte |= code << 4 if c % 2 else code
+            packed[0, r, c // 2] = byte
+            d[0, r, c] = e2m1[code] * e4m3[int(sf[0, r, c // 16])] * scale2[name]
+        kw["w_" + name], kw["sf_" + name] = packed, sf
+        kw["scale2_" + name] = torch.full((E,), scale2[name], dtype=torch.float32)
+        dense[name] = d
+    inp = I.MoeInputs(shape=shape, x=base.x, router_w=base.router_w, **kw)
+    return inp, dense
+
+
+def test_nvfp4_packing_scales_and_scale2_against_dense_swiglu():
+    """E = R = K = 1: the block is one dense SwiGLU FFN whose weights are the hand-placed
+    values: the nibble order (odd columns in the high nibble), the 16-wide scale groups and
+    the per-matrix scale2 are checked against torch's matmul + silu."""
+    shape = I.TINY.with_(num_experts=1, router_width=1, top_k=1, shared_inter=0, hidden=64,
+                         inter=32, weight_dtype=I.WDTYPE_NVFP4)
+    placements = {
+        "gate": [(0, 5, 2), (0, 21, 7), (3, 0, 9), (3, 63, 12), (31, 16, 5)],
+        "up": [(0, 4, 5), (0, 21, 2), (3, 1, 7), (3, 62, 9), (31, 17, 12)],
+        "down": [(0, 0, 2), (7, 3, 5), (7, 31, 9), (63, 16, 7), (40, 15, 12)],
+    }
+    sf_codes = {"gate": {(0, 1): 0x40, (3, 3): 0x30}, "up": {(0, 1): 0x3C},
+                "down": {(7, 1): 0x40, (63, 1): 0x30}}
+    scale2 = {"gate": 0.25, "up": 0.5, "down": 0.125}
+    inp, d = _nvfp4_inputs(shape, placements, sf_codes, scale2)
+    x = inp.x.double()
+    g = x @ d["gate"][0].T
+    u = x @ d["up"][0].T
+    want = (torch.nn.functional.silu(g) * u) @ d["down"][0].T
+    assert (want != 0).sum() > 3
+    for impl in (O.moe_forward, O.moe_forward_dense):
+        np.testing.assert_allclose(impl(inp)["out"], want.numpy(), rtol=1e-12, atol=1e-15)
+
+
+def test_nvfp4_formulations_agree():
+    shape = I.PREFILL.with_(name="nvfp4_pin", num_tokens=24, hidden=256, num_experts=6,
+                            router_width=6, top_k=2, inter=128, shared_inter=64,
+                            weight_dtype=I.WDTYPE_NVFP4)
+    inp = I.make_inputs(shape)
+    a, b = O.moe_forward(inp), O.moe_forward_dense(inp)
+    np.testing.assert_array_equal(a["idx"], b["idx"])
+    np.testing.assert_allclose(a["out"], b["out"], rtol=1e-10, atol=1e-15)
