@@ -64,9 +64,17 @@ typedef enum {
 
 typedef enum {
   MOE_W_BF16 = 0,               /* routed expert weights bf16 */
-  MOE_W_FP8_E4M3_B128 = 1       /* routed expert weights E4M3 + one fp32 scale per 128x128 block;
+  MOE_W_FP8_E4M3_B128 = 1,      /* routed expert weights E4M3 + one fp32 scale per 128x128 block;
                                    expert inputs and the SwiGLU intermediate are quantised per
                                    1x128 (along the contraction) to E4M3, scale = amax/448 */
+  MOE_W_NVFP4 = 2               /* routed expert weights NVFP4: E2M1 codes packed two per byte
+                                   (element 2j in the low nibble), one E4M3 scale per 16
+                                   consecutive elements along the contraction (sf_*), one fp32
+                                   scale2 per expert matrix; weight = e2m1 * sf * scale2.
+                                   Activations stay bf16 (no quantisation). Needs hidden and
+                                   inter multiples of 256; runs on the grouped chain
+                                   ("spark_model/layers/moe/forward.rs", NVFP4 decode arm:
+                                   packed, scale and scale2 tables) */
 } moe_wdtype_t;
 
 typedef enum {
@@ -118,9 +126,9 @@ typedef struct {
   const float *router_logit_bias;  /* nullable fp32 [R], added to the logits before softmax */
   const float *correction_bias;    /* fp32 [R], required by the *_BIAS scorings (selection only),
                                       ignored with MOE_SCORING_SOFTMAX */
-  const void *w_gate;              /* [E,I,H] bf16 or E4M3 */
-  const void *w_up;                /* [E,I,H] bf16 or E4M3 */
-  const void *w_down;              /* [E,H,I] bf16 or E4M3 */
+  const void *w_gate;              /* [E,I,H] bf16 or E4M3; NVFP4: packed [E,I,H/2] */
+  const void *w_up;                /* [E,I,H] bf16 or E4M3; NVFP4: packed [E,I,H/2] */
+  const void *w_down;              /* [E,H,I] bf16 or E4M3; NVFP4: packed [E,H,I/2] */
   const float *s_gate;             /* FP8 only: fp32 [E,I/128,H/128] */
   const float *s_up;               /* FP8 only: fp32 [E,I/128,H/128] */
   const float *s_down;             /* FP8 only: fp32 [E,H/128,I/128] */
@@ -130,6 +138,12 @@ typedef struct {
   const void *sh_gate_vec;         /* nullable bf16 [H]: shared blend weight sigmoid(x . g);
                                       NULL = weight 1 */
   const void *pre_expert_norm_w;   /* bf16 [H], required iff pre_expert_norm */
+  const void *sf_gate;             /* NVFP4 only: E4M3 codes [E,I,H/16] */
+  const void *sf_up;               /* NVFP4 only: E4M3 codes [E,I,H/16] */
+  const void *sf_down;             /* NVFP4 only: E4M3 codes [E,H,I/16] */
+  const float *scale2_gate;        /* NVFP4 only: fp32 [E] */
+  const float *scale2_up;          /* NVFP4 only: fp32 [E] */
+  const float *scale2_down;        /* NVFP4 only: fp32 [E] */
 } moe_weights_t;
 
 /* Bytes of device workspace moe_forward / moe_route need for `cfg` (path resolved as in

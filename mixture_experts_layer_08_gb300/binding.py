@@ -47,7 +47,8 @@ class moe_config_t(ctypes.Structure):
 
 _WEIGHT_FIELDS = ("router_w", "router_logit_bias", "correction_bias", "w_gate", "w_up", "w_down",
                   "s_gate", "s_up", "s_down", "sh_gate", "sh_up", "sh_down", "sh_gate_vec",
-                  "pre_expert_norm_w")
+                  "pre_expert_norm_w", "sf_gate", "sf_up", "sf_down", "scale2_gate",
+                  "scale2_up", "scale2_down")
 
 
 class moe_weights_t(ctypes.Structure):

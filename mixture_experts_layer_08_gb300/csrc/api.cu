@@ -42,7 +42,7 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 int resolve_path(const moe_config_t* c) {
   if (c->path != MOE_PATH_AUTO) return c->path;
   const bool decode_ok = c->num_tokens <= kDecodeMaxTokens && c->inter <= 1024 &&
-                         c->shared_inter <= 1024 &&
+                         c->shared_inter <= 1024 && c->weight_dtype != MOE_W_NVFP4 &&
                          (c->weight_dtype == MOE_W_BF16 || c->hidden % 256 == 0);
   return decode_ok ? MOE_PATH_DECODE : MOE_PATH_GROUPED;
 }
@@ -56,7 +56,8 @@ moe_status_t validate_config(const moe_config_t* c) {
   if (c->scoring != MOE_SCORING_SOFTMAX && c->scoring != MOE_SCORING_SOFTMAX_BIAS &&
       c->scoring != MOE_SCORING_SIGMOID_BIAS)
     return MOE_ERR_INVALID_ARG;
-  if (c->weight_dtype != MOE_W_BF16 && c->weight_dtype != MOE_W_FP8_E4M3_B128)
+  if (c->weight_dtype != MOE_W_BF16 && c->weight_dtype != MOE_W_FP8_E4M3_B128 &&
+      c->weight_dtype != MOE_W_NVFP4)
     return MOE_ERR_INVALID_ARG;
   if (c->path < MOE_PATH_AUTO || c->path > MOE_PATH_GROUPED) return MOE_ERR_INVALID_ARG;
   if (c->pre_expert_norm && !(c->rms_norm_eps >= 0.0f && c->rms_norm_eps < INFINITY))
@@ -72,7 +73,11 @@ moe_status_t validate_config(const moe_config_t* c) {
   if (c->weight_dtype == MOE_W_FP8_E4M3_B128 &&
       (c->hidden % 256 || c->hidden > 4096 || c->inter > 4096))
     return MOE_ERR_UNSUPPORTED;
+  // NVFP4 experts: the scale codes of 16 groups (256 elements) are one 16-byte TMA box
+  if (c->weight_dtype == MOE_W_NVFP4 && (c->hidden % 256 || c->inter % 256))
+    return MOE_ERR_UNSUPPORTED;
   const int path = resolve_path(c);
+  if (path == MOE_PATH_DECODE && c->weight_dtype == MOE_W_NVFP4) return MOE_ERR_UNSUPPORTED;
   if (path == MOE_PATH_DECODE &&
       (c->num_tokens > kDecodeMaxTokens || c->inter > 1024 || c->shared_inter > 1024 ||
        c->hidden > 8192))
@@ -212,6 +217,21 @@ bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t row
   return r == CUDA_SUCCESS;
 }
 
+// 2D byte map over a [rows, inner] row-major matrix, box {box_inner, box_rows}, no swizzle
+// (NVFP4 codes and scale codes).
+bool make_map_u8_plain(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows,
+                       uint32_t box_inner, uint32_t box_rows) {
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2D E4M3 (byte) map over a [rows, inner] row-major matrix; box {128, box_rows}.
 bool make_map_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows,
                  uint32_t box_rows) {
@@ -232,6 +252,11 @@ moe_status_t validate_weights(const moe_config_t* c, const moe_weights_t* w) {
   if (!w || !w->router_w || !w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
   if (c->scoring != MOE_SCORING_SOFTMAX && !w->correction_bias) return MOE_ERR_INVALID_ARG;
   if (c->weight_dtype == MOE_W_FP8_E4M3_B128 && (!w->s_gate || !w->s_up || !w->s_down))
+    return MOE_ERR_INVALID_ARG;
+  if (c->weight_dtype == MOE_W_NVFP4 &&
+      (!w->sf_gate || !w->sf_up || !w->sf_down || !w->scale2_gate || !w->scale2_up ||
+       !w->scale2_down || !aligned16(w->sf_gate) || !aligned16(w->sf_up) ||
+       !aligned16(w->sf_down)))
     return MOE_ERR_INVALID_ARG;
   if (c->shared_inter > 0 && (!w->sh_gate || !w->sh_up || !w->sh_down)) return MOE_ERR_INVALID_ARG;
   if (c->pre_expert_norm && !w->pre_expert_norm_w) return MOE_ERR_INVALID_ARG;
@@ -389,8 +414,9 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
   const int sms = num_sms();
   const int bn_h = (H % 256 == 0) ? 256 : 128;   // N-tile of the projections back to H
   const bool fp8 = c->weight_dtype == MOE_W_FP8_E4M3_B128;
+  const bool nv = c->weight_dtype == MOE_W_NVFP4;
   // Shared expert: a dense SwiGLU FFN on all N rows. With bf16 experts it is problem 0 of the
-  // routed launches below; with FP8 experts it runs as its own bf16 launches here.
+  // routed launches below; with FP8 or NVFP4 experts it runs as its own bf16 launches here.
   CUtensorMap sh_gu[3], sh_dn[3];
   GemmProblem sh_gu_p{}, sh_dn_p{};
   if (S > 0) {
@@ -414,7 +440,7 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
     sh_dn_p.ldo = H;
   }
   MARK(MOE_STAGE_SHARED, 0);
-  if (S > 0 && fp8) {
+  if (S > 0 && (fp8 || nv)) {
     CUtensorMap maps[2][3] = {{sh_gu[0], sh_gu[1], sh_gu[2]}, {sh_gu[0], sh_gu[1], sh_gu[2]}};
     GemmArgs g{};
     g.nprob = 1;
@@ -468,6 +494,46 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
     g.out_scales = nullptr;
     MARK(MOE_STAGE_DOWN, 0);
     CK(launch_gemm_fp8(1, mh, md, md, g, sms, st));
+    MARK(MOE_STAGE_DOWN, 1);
+  } else if (nv) {
+    // NVFP4 experts: codes and scale codes streamed, dequantised in shared memory
+    CUtensorMap gu[5], dn[5];
+    const uint64_t rows = (uint64_t)L.te;
+    if (!make_map_bf16(&gu[0], P.at<void>(R_XP), H, rows, 128) ||
+        !make_map_u8_plain(&gu[1], w->w_gate, H / 2, (uint64_t)E * I, 32, 128) ||
+        !make_map_u8_plain(&gu[2], w->w_up, H / 2, (uint64_t)E * I, 32, 128) ||
+        !make_map_u8_plain(&gu[3], w->sf_gate, H / 16, (uint64_t)E * I, 16, 128) ||
+        !make_map_u8_plain(&gu[4], w->sf_up, H / 16, (uint64_t)E * I, 16, 128) ||
+        !make_map_bf16(&dn[0], P.at<void>(R_HH), I, rows, 128) ||
+        !make_map_u8_plain(&dn[1], w->w_down, I / 2, (uint64_t)E * H, 32, bn_h) ||
+        !make_map_u8_plain(&dn[3], w->sf_down, I / 16, (uint64_t)E * H, 16, bn_h))
+      return MOE_ERR_CUDA;
+    dn[2] = dn[1];
+    dn[4] = dn[3];
+    NvGemmArgs g{};
+    g.tiles = P.at<int4>(R_TILES);
+    g.hdr = hdr;
+    g.max_mtiles = L.max_mtiles;
+    g.n_tiles = I / 128;
+    g.num_kb = H / 64;
+    g.b_rows_per_expert = I;
+    g.s2_0 = w->scale2_gate;
+    g.s2_1 = w->scale2_up;
+    g.out = P.at<void>(R_HH);
+    g.ldo = I;
+    g.status = hdr;
+    MARK(MOE_STAGE_GATE_UP, 0);
+    CK(launch_gemm_nvfp4(kGemmSwiGLU, 256, gu, g, sms, st));
+    MARK(MOE_STAGE_GATE_UP, 1);
+    g.n_tiles = H / bn_h;
+    g.num_kb = I / 64;
+    g.b_rows_per_expert = H;
+    g.s2_0 = w->scale2_down;
+    g.s2_1 = w->scale2_down;
+    g.out = P.at<void>(R_Y);
+    g.ldo = H;
+    MARK(MOE_STAGE_DOWN, 0);
+    CK(launch_gemm_nvfp4(kGemmStoreBF16, bn_h, dn, g, sms, st));
     MARK(MOE_STAGE_DOWN, 1);
   } else {
     // routed problem (plus the shared expert as problem 0 when present)

@@ -1,0 +1,358 @@
+// Grouped GEMM with NVFP4 expert weights on the 5th-generation tensor cores (sm_103a).
+//
+// D[rows of expert e, n-tile] = A[rows, K] . dequant(B_e)[n-tile rows, K]^T over the
+// expert-sorted bf16 rows, where B is packed E2M1 codes (two per byte, element 2j in the low
+// nibble) with one E4M3 scale per 16 elements along K and one fp32 scale2 per expert
+// matrix. The epilogue is the bf16 kernel's (SwiGLU to bf16, or a bf16 store) with scale2
+// applied to the fp32 accumulators first.
+//
+// Pages: "spark_model/layers/moe/forward.rs" (NVFP4 arm of the decode forward: packed expert
+// weights with a per-group scale table and one scale2 value per expert matrix,
+// `moe_expert_gate_up_shared` / `moe_expert_silu_down_shared`) and
+// "metrale_model_layers/layers/moe/forward_prefill.rs" (`run_routed_grouped_gemm` over the
+// expert-sorted rows).
+//
+// The block-scaled tcgen05 MMA kinds take E4M3 scales only with both operands in FP4
+// (kind::mxf4nvf4), and an FP8 x FP4 product (kind::mxf8f6f4) only with power-of-two scales.
+// The activations stay bf16 here (the pages' w4a16), so the weights are dequantised in shared
+// memory instead -- exactly: an E2M1 value times an E4M3 scale has at most 5 significant bits
+// and fits bf16 -- and fed to the bf16 MMA. HBM carries 0.5 + 1/16 bytes per weight.
+//
+// Design (one persistent CTA per SM, 448 threads, 3 pipeline stages):
+//   warp 0      TMA producer, per stage: the A tile 128 x 64 (bf16, 128-byte swizzle), the
+//               packed codes of the BN weight rows (BN x 32 bytes) and their scale codes
+//               (BN x 16 bytes: the 4 groups of this stage and of the 3 stages after it,
+//               reloaded with each stage so the box stays 16 bytes wide).
+//   warp 1      TMEM allocation and the MMA issuer (M=128, N=BN, K=16 x 4 per stage).
+//   warps 2-5   epilogue (TMEM lane quadrant warp % 4): scale2, then SwiGLU or bf16 store.
+//   warps 6-13  converters: one weight row per thread, 8 chunks of 8 elements each: 4 code
+//               bytes -> 4 bf16 pairs through a 256-entry table, times the group's scale
+//               (exact), one 16-byte store into the 128-byte-swizzled B tile; then a proxy
+//               fence and one arrival per warp on the stage's full barrier (which the MMA
+//               waits on; the converters saw the A tile land on the same barrier as the codes).
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kNvThreads = 448;
+constexpr int kNvConvWarps = 8;
+constexpr int kNvConvBase = 192;          // first converter thread
+constexpr int kNvBM = 128;
+constexpr int kNvATile = kNvBM * 128;     // 16 KB
+
+template <int BN>
+struct NvCfg {
+  static constexpr int kStages = 3;
+  static constexpr int kBTile = BN * 128;   // bf16, 64 elements per row
+  static constexpr int kCTile = BN * 32;    // packed codes, 64 elements per row
+  static constexpr int kSTile = BN * 16;    // scale codes, 16 groups per row
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr size_t kTables = 256 * 4 + 256 * 2;
+  static constexpr size_t kSmemBytes =
+      (size_t)kStages * (kNvATile + kBTile + kCTile + kSTile) + kTables + 1024 + 256;
+};
+
+// E2M1 (OCP MX FP4) value of a 4-bit code: bit 3 sign, bits 2-1 exponent (bias 1), bit 0
+// mantissa; exponent 0 holds 0 and 0.5.
+__device__ __forceinline__ float e2m1_value(uint32_t nib) {
+  const uint32_t e = (nib >> 1) & 3u, m = nib & 1u;
+  const float mag = e == 0 ? 0.5f * (float)m : ldexpf(1.0f + 0.5f * (float)m, (int)e - 1);
+  return (nib & 8u) ? -mag : mag;
+}
+
+// E4M3 (OCP FP8) value of a code: bit 7 sign, bits 6-3 exponent (bias 7), bits 2-0 mantissa;
+// exponent 0 holds the subnormals m * 2^-9.
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  const float mag = e == 0 ? ldexpf((float)m, -9) : ldexpf(1.0f + 0.125f * (float)m, (int)e - 7);
+  return (c & 0x80u) ? -mag : mag;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
+  __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
+  __nv_bfloat162 z = __hmul2(x, y);
+  return *reinterpret_cast<uint32_t*>(&z);
+}
+
+struct NvTile {
+  int e, row0, row1, n;
+};
+
+__device__ __forceinline__ void nv_tile_of(const NvGemmArgs& g, int tile, NvTile& t) {
+  const int m = tile / g.n_tiles;
+  t.n = tile % g.n_tiles;
+  const int4 v = g.tiles[m];
+  t.e = v.x;
+  t.row0 = v.y;
+  t.row1 = v.z;
+}
+
+template <int BN, int MODE>
+__global__ void __launch_bounds__(kNvThreads, 1)
+    gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_a,
+                      const __grid_constant__ CUtensorMap tm_c0,
+                      const __grid_constant__ CUtensorMap tm_c1,
+                      const __grid_constant__ CUtensorMap tm_s0,
+                      const __grid_constant__ CUtensorMap tm_s1, const NvGemmArgs g) {
+  using C = NvCfg<BN>;
+  constexpr int S = C::kStages;
+  constexpr bool kGlu = MODE == kGemmSwiGLU;
+  constexpr int b_rows = kGlu ? BN / 2 : BN;   // rows per weight matrix in one tile
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * kNvATile;
+  uint8_t* sC = sB + S * C::kBTile;
+  uint8_t* sS = sC + S * C::kCTile;
+  uint32_t* lut_pair = reinterpret_cast<uint32_t*>(sS + S * C::kSTile);   // byte -> bf16x2
+  uint16_t* lut_scale = reinterpret_cast<uint16_t*>(lut_pair + 256);     // E4M3 -> bf16
+  uint64_t* full = reinterpret_cast<uint64_t*>(lut_scale + 256);
+  uint64_t* empty = full + S;
+  uint64_t* cfull = empty + S;
+  uint64_t* tfull = cfull + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  WsHeader* hdr = g.status;
+
+  // dequantisation tables, from the two formats' definitions (bf16 holds both exactly)
+  for (int i = threadIdx.x; i < 256; i += kNvThreads) {
+    lut_pair[i] = pack_bf16x2(e2m1_value(i & 15), e2m1_value(i >> 4));
+    lut_scale[i] = __bfloat16_as_ushort(__float2bfloat16_rn(e4m3_value(i)));
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], kNvConvWarps);   // B converted (after cfull: A landed too)
+      mbar_init(&empty[s], 1);
+      mbar_init(&cfull[s], 1);             // A tile, codes and scale codes landed
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
+    }
+    mbar_init(drain, 1);
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_c0);
+    tma_prefetch_desc(&tm_s0);
+    if (kGlu) {
+      tma_prefetch_desc(&tm_c1);
+      tma_prefetch_desc(&tm_s1);
+    }
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = (int)g.hdr->num_mtiles * g.n_tiles;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------ TMA producer
+    int s = 0;
+    uint32_t ph = 0;
+    long long issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      NvTile t;
+      nv_tile_of(g, tile, t);
+      const int brow = t.e * g.b_rows_per_expert + t.n * b_rows;
+      for (int kb = 0; kb < g.num_kb; ++kb) {
+        if (!mbar_wait(&empty[s], ph ^ 1, hdr)) { ok = false; break; }
+        mbar_arrive_expect_tx(&cfull[s], kNvATile + C::kCTile + C::kSTile);
+        tma_load_2d(sA + s * kNvATile, &tm_a, kb * 64, t.row0, &cfull[s]);
+        uint8_t* cs = sC + s * C::kCTile;
+        uint8_t* ss = sS + s * C::kSTile;
+        tma_load_2d(cs, &tm_c0, kb * 32, brow, &cfull[s]);
+        tma_load_2d(ss, &tm_s0, (kb >> 2) * 16, brow, &cfull[s]);
+        if (kGlu) {
+          tma_load_2d(cs + b_rows * 32, &tm_c1, kb * 32, brow, &cfull[s]);
+          tma_load_2d(ss + b_rows * 16, &tm_s1, (kb >> 2) * 16, brow, &cfull[s]);
+        }
+        ++issued;
+        if (++s == S) { s = 0; ph ^= 1; }
+      }
+    }
+    if (!ok) {
+      // let the copies already issued land before the CTA can exit
+      for (long long i = issued > S ? issued - S : 0; i < issued; ++i) {
+        mbar_wait(&cfull[i % S], (uint32_t)((i / S) & 1), nullptr);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_make(kNvBM, BN, 1, 1);
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      if (!mbar_wait(&tempty[acc], ((it >> 1) & 1) ^ 1, hdr)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d = tmem_base + acc * BN;
+      for (int kb = 0; kb < g.num_kb; ++kb) {
+        if (!mbar_wait(&full[s], ph, hdr)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sA + s * kNvATile);
+        const uint32_t b0 = smem_u32(sB + s * C::kBTile);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc_mma_bf16(d, sdesc_k_sw128(a0 + k * 32), sdesc_k_sw128(b0 + k * 32), idesc,
+                      (kb | k) != 0 ? 1u : 0u);
+        tc_commit(&empty[s]);
+        if (++s == S) { s = 0; ph ^= 1; }
+      }
+      if (ok) tc_commit(&tfull[acc]);
+    }
+    tc_commit(drain);
+    mbar_wait(drain, 0, hdr);
+  } else if (warp >= 2 && warp < 6) {
+    // ------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int r_local = q * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+      NvTile t;
+      nv_tile_of(g, tile, t);
+      const int acc = it & 1;
+      if (!mbar_wait(&tfull[acc], (it >> 1) & 1, hdr)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      const int row = t.row0 + r_local;
+      const bool valid = row < t.row1;
+      const float s2a = g.s2_0[t.e];
+      if (kGlu) {
+        const float s2u = g.s2_1[t.e];
+        __nv_bfloat16* orow =
+            static_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + t.n * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          float gv[32], uv[32];
+          tmem_ld32(taddr + c, gv);
+          tmem_ld32(taddr + BN / 2 + c, uv);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float h[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                h[j] = silu(gv[8 * v + j] * s2a) * (uv[8 * v + j] * s2u);
+              uint4 o;
+              o.x = pack_bf16x2(h[0], h[1]);
+              o.y = pack_bf16x2(h[2], h[3]);
+              o.z = pack_bf16x2(h[4], h[5]);
+              o.w = pack_bf16x2(h[6], h[7]);
+              dst[v] = o;
+            }
+          }
+        }
+      } else {
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + t.n * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(taddr + c, v);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint4 o;
+              o.x = pack_bf16x2(v[8 * j + 0] * s2a, v[8 * j + 1] * s2a);
+              o.y = pack_bf16x2(v[8 * j + 2] * s2a, v[8 * j + 3] * s2a);
+              o.z = pack_bf16x2(v[8 * j + 4] * s2a, v[8 * j + 5] * s2a);
+              o.w = pack_bf16x2(v[8 * j + 6] * s2a, v[8 * j + 7] * s2a);
+              dst[j] = o;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+  } else if (warp >= kNvConvBase / 32) {
+    // ------------------------------------------------ converters
+    const int r = threadIdx.x - kNvConvBase;   // B-tile row of this thread
+    int s = 0;
+    uint32_t ph = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      bool ok = true;
+      for (int kb = 0; kb < g.num_kb; ++kb) {
+        if (!mbar_wait(&cfull[s], ph, hdr)) { ok = false; break; }
+        if (r < BN) {
+          const uint8_t* crow = sC + s * C::kCTile + r * 32;
+          const uint4 c0 = *reinterpret_cast<const uint4*>(crow);
+          const uint4 c1 = *reinterpret_cast<const uint4*>(crow + 16);
+          const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(sS + s * C::kSTile + r * 16 +
+                                                                  (kb & 3) * 4);
+          uint32_t scl[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t b = lut_scale[(sc4 >> (8 * q)) & 255u];
+            scl[q] = b | (b << 16);
+          }
+          const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          uint8_t* brow = sB + s * C::kBTile + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t w = words[c];
+            const uint32_t sc = scl[c >> 1];
+            uint4 o;
+            o.x = bf16x2_mul(lut_pair[w & 255u], sc);
+            o.y = bf16x2_mul(lut_pair[(w >> 8) & 255u], sc);
+            o.z = bf16x2_mul(lut_pair[(w >> 16) & 255u], sc);
+            o.w = bf16x2_mul(lut_pair[w >> 24], sc);
+            *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) = o;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+        if (++s == S) { s = 0; ph ^= 1; }
+      }
+      if (!ok) break;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+template <int BN, int MODE>
+cudaError_t launch_nv(const CUtensorMap maps[5], const NvGemmArgs& g, int num_sms,
+                      cudaStream_t st) {
+  using C = NvCfg<BN>;
+  auto kern = gemm_nvfp4_kernel<BN, MODE>;
+  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(kern), C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int max_tiles = g.max_mtiles * g.n_tiles;
+  int grid = max_tiles < num_sms ? max_tiles : num_sms;
+  if (grid < 1) grid = 1;
+  kern<<<grid, kNvThreads, C::kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], g);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_nvfp4(int mode, int bn, const CUtensorMap maps[5], const NvGemmArgs& g,
+                              int num_sms, cudaStream_t st) {
+  if (mode == kGemmSwiGLU && bn == 256) return launch_nv<256, kGemmSwiGLU>(maps, g, num_sms, st);
+  if (mode == kGemmStoreBF16 && bn == 256)
+    return launch_nv<256, kGemmStoreBF16>(maps, g, num_sms, st);
+  if (mode == kGemmStoreBF16 && bn == 128)
+    return launch_nv<128, kGemmStoreBF16>(maps, g, num_sms, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -439,6 +439,61 @@ def test_fp8_full_size_sampled_tokens(B, shape):
     check_out(got[toks], ref["out"], FP8_ATOL, FP8_RTOL, FP8_REL_L2)
 
 
+# ------------------------------------------------------------------ NVFP4 experts
+
+# The weights are dequantised exactly to bf16 and the activations stay bf16 (w4a16): the same
+# arithmetic as the bf16 experts, so the same bars.
+NV_SMALL = I.PREFILL.with_(name="nvfp4_small", num_tokens=300, hidden=512, num_experts=16,
+                           router_width=16, top_k=4, inter=256, shared_inter=256,
+                           shared_gated=True, weight_dtype=I.WDTYPE_NVFP4)
+NV_SHAPES = [
+    NV_SMALL,
+    # decode-sized: 4 tokens, top-8 of 32
+    NV_SMALL.with_(name="nvfp4_decode_n4", num_tokens=4, num_experts=32, router_width=32,
+                   top_k=8),
+    # 6 gate/up n-tiles, 12 down contraction stages (3 scale boxes), no shared expert
+    NV_SMALL.with_(name="nvfp4_wide", num_tokens=130, hidden=1024, inter=768, num_experts=8,
+                   router_width=8, top_k=2, shared_inter=0, zipf_s=0.0),
+    # sigmoid + correction bias, pre-expert RMSNorm of the routed experts' input
+    NV_SMALL.with_(name="nvfp4_sigmoid_prenorm", num_tokens=200, hidden=768, inter=512,
+                   num_experts=32, router_width=32, top_k=6, shared_inter=0, zipf_s=0.0,
+                   scoring=I.SCORING_SIGMOID_BIAS, correction_bias_std=0.05,
+                   pre_expert_norm=True, norm_topk_prob=False, routed_scaling_factor=1.5),
+]
+
+
+@pytest.mark.parametrize("shape", NV_SHAPES, ids=lambda s: s.name)
+def test_nvfp4_forward_matches_oracle(B, shape):
+    inp = I.make_inputs(shape)
+    got, gidx, gw = run_gpu(B, inp, 0)
+    check_routing(gidx, O.moe_forward(inp, routing_only=True))
+    ref = O.moe_forward(inp, forced_idx=gidx)
+    check_out(got, ref["out"])
+    # the grouped chain in deterministic mode repeats bit for bit
+    assert np.array_equal(run_gpu(B, inp, 0)[0], got)
+
+
+def test_nvfp4_rejected_where_unsupported(B):
+    """NVFP4 needs hidden and inter multiples of 256, and runs on the grouped chain only."""
+    ok = NV_SMALL.with_(num_tokens=4)
+    assert B.moe_workspace_size(B.make_config(ok, True, 2)) > 0
+    for bad, path in ((NV_SMALL.with_(inter=384), 0), (ok, 1)):
+        with pytest.raises(B.MoeError):
+            B.moe_workspace_size(B.make_config(bad, True, path))
+
+
+@pytest.mark.parametrize("shape", [I.DECODE_NVFP4, I.PREFILL_NVFP4], ids=lambda s: s.name)
+def test_nvfp4_full_size(B, shape):
+    inp = I.make_inputs(shape, device="cuda")
+    got, gidx, gw = run_gpu(B, inp, 0)
+    check_routing(gidx, O.moe_forward(inp, routing_only=True))
+    toks = _sample_tokens(shape.num_tokens, k=10) if shape.num_tokens > 16 else \
+        list(range(shape.num_tokens))
+    ref = O.moe_forward(inp, tokens=toks, forced_idx=gidx)
+    np.testing.assert_allclose(gw[toks], ref["w"], rtol=1e-5, atol=1e-7)
+    check_out(got[toks], ref["out"])
+
+
 # ------------------------------------------------------------------ failure detection
 
 def test_bounded_wait_reports_timeout_and_context_survives(B):
