@@ -133,17 +133,19 @@ def algorithmic(inp, rs):
     """Work the method must do (routed rows Z, not tile-padded; touched experts read once)."""
     s = inp.shape
     H, I_, S, R = s.hidden, s.inter, s.shared_inter, s.router_width
-    wb = 1 if s.weight_dtype == I.WDTYPE_FP8_E4M3_B128 else 2
+    # bytes per expert weight: bf16 2, E4M3 1 (block scales negligible), NVFP4 half a byte
+    # of code plus one E4M3 scale per 16
+    wb = {I.WDTYPE_FP8_E4M3_B128: 1.0, I.WDTYPE_NVFP4: 0.5 + 1.0 / 16}.get(s.weight_dtype, 2.0)
+    own_shared = s.weight_dtype != I.WDTYPE_BF16   # shared expert in launches of its own
     expert_bytes = 3 * I_ * H * wb
     bytes_ = (rs["distinct"] * expert_bytes + 3 * S * H * 2 + R * H * 2
               + 2 * s.num_tokens * H * 2 + (H * 2 if s.shared_gated else 0))
     flops_routed = 6.0 * rs["Z"] * H * I_
     flops = flops_routed + 6.0 * s.num_tokens * H * S + 2.0 * s.num_tokens * H * R
-    # the gate/up launch also runs the shared expert's gate/up projection (bf16 experts)
-    gate_up_flops = 4.0 * rs["Z"] * H * I_ + 4.0 * s.num_tokens * H * S
-    down_flops = 2.0 * rs["Z"] * I_ * H + (2.0 * s.num_tokens * S * H
-                                            if s.weight_dtype != I.WDTYPE_FP8_E4M3_B128 else 0.0)
-    gate_up_bytes = rs["distinct"] * 2 * I_ * H * wb + (2 * S * H * 2)
+    # with bf16 experts the gate/up and down launches also run the shared expert's projections
+    gate_up_flops = 4.0 * rs["Z"] * H * I_ + (0.0 if own_shared else 4.0 * s.num_tokens * H * S)
+    down_flops = 2.0 * rs["Z"] * I_ * H + (0.0 if own_shared else 2.0 * s.num_tokens * S * H)
+    gate_up_bytes = rs["distinct"] * 2 * I_ * H * wb + (0 if own_shared else 2 * S * H * 2)
     # the decode chain's one kernel reads every touched expert, the shared expert, the router
     # and x, and writes out: all of the step's algorithmic bytes
     ffn_bytes = bytes_
@@ -182,19 +184,42 @@ def measured_traffic(kernel, workload):
     return None
 
 
-def kernels_per_step(B, cfg):
+def fused_router(cfg, num_sms):
+    """Whether the grouped chain routes with the fused tensor-core router (one launch: router
+    GEMM, scoring and top-K) -- the library's own rule: more than 64 tokens, a router width
+    that is a multiple of 32 up to 384 (of 128 above 256), the contraction split over a
+    cluster of at least 2 CTAs, and the shared memory it needs."""
+    N, H, R = cfg.num_tokens, cfg.hidden, cfg.router_width
+    if N <= 64 or R < 32 or R > 384 or R % 32 or H % 64 or (R > 256 and R % 128):
+        return False
+    mt, nkb, ks = (N + 127) // 128, H // 64, 1
+    while ks < 8 and mt * ks * 2 <= num_sms and nkb % (ks * 2) == 0:
+        ks *= 2
+    stage = 16384 + R * 128
+    nst = min(8, (192 * 1024) // stage, nkb // ks)
+    ld = R + 4
+    if nst < 1 or (128 - 128 // ks) * ld < 32 * 2 * R:
+        return False
+    region = (max(nst * stage, 128 * ld * 4) + 7) & ~7
+    return region + 1024 + 18 * 8 <= 227 * 1024
+
+
+def kernels_per_step(B, cfg, num_sms=152):
     """Kernels of this library one forward launches (memsets are not kernels)."""
     decode = cfg.path == B.PATH_DECODE or (cfg.path == B.PATH_AUTO and cfg.num_tokens <= 16
-                                            and cfg.inter <= 1024 and cfg.shared_inter <= 1024)
+                                            and cfg.inter <= 1024 and cfg.shared_inter <= 1024
+                                            and cfg.weight_dtype != 2)
     if decode:   # router, top-K, sort, projections, combine (and any pre-expert norm): one kernel
         return 1
-    # router, top-K, 3 sort, gate/up GEMM, down GEMM, combine; FP8 experts add the token-row
-    # quantiser and run the bf16 shared expert in two launches of its own; a pre-expert norm
-    # adds its row kernel
-    norm = 1 if cfg.pre_expert_norm else 0
+    # routing: the fused router (1) or router + top-K (2); then 3 sort, gate/up GEMM, down GEMM,
+    # combine; FP8 experts add the token-row quantiser; FP8 and NVFP4 experts run the bf16
+    # shared expert in two launches of their own; a pre-expert norm adds its row kernel
+    n = (1 if fused_router(cfg, num_sms) else 2) + 6 + (1 if cfg.pre_expert_norm else 0)
     if cfg.weight_dtype == 1:
-        return 9 + (2 if cfg.shared_inter else 0) + norm
-    return 8 + norm
+        n += 1
+    if cfg.weight_dtype in (1, 2) and cfg.shared_inter:
+        n += 2
+    return n
 
 
 def replicas_value(ms_local, tokens_per_replica, device="cpu"):
@@ -302,7 +327,8 @@ def time_ours(B, shape, steps, warmup, dev, peaks, with_e2e=True):
     res = {"inp": inp, "rs": rs, "alg": alg, "ms": ms, "ms_dirty": ms_dirty, "ms_atomic": ms_atomic, "stage_ms": {k: statistics.mean(v)
                                                                      for k, v in stage_ms.items()},
            "clocks": clk.summary(), "wall_s": t_wall,
-           "launches_per_step": kernels_per_step(B, blk.cfg)}
+           "launches_per_step": kernels_per_step(
+               B, blk.cfg, torch.cuda.get_device_properties(0).multi_processor_count)}
     if with_e2e:
         res["graph"] = time_graph(B, blk, inp, out, flush, steps, warmup)
         hx = torch.empty(inp.x.shape, dtype=inp.x.dtype, pin_memory=True)
@@ -450,7 +476,8 @@ def main():
                     help="skip the zero-expert, FP8 and tiny workloads")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--profile-only", choices=["decode", "prefill", "fp8", "zero_expert",
-                                               "fp8_small", "tiny", "decode_fp8"],
+                                               "fp8_small", "tiny", "decode_fp8",
+                                               "decode_nvfp4", "prefill_nvfp4"],
                     help="run one workload's timing loop only (for ncu captures); prints a "
                          "reduced line")
     args = ap.parse_args()
@@ -507,7 +534,8 @@ def main():
     if args.profile_only:
         shp = {"decode": I.DECODE, "prefill": I.PREFILL, "fp8": I.FP8_PREFILL,
                "zero_expert": I.ZERO_EXPERT, "fp8_small": FP8_PREFILL_SMALL, "tiny": I.TINY,
-               "decode_fp8": I.DECODE_FP8}[args.profile_only]
+               "decode_fp8": I.DECODE_FP8, "decode_nvfp4": I.DECODE_NVFP4,
+               "prefill_nvfp4": I.PREFILL_NVFP4}[args.profile_only]
         r = time_ours(B, shp, args.steps, warmup, dev, peaks, with_e2e=False)
         print(json.dumps({"profile_only": shp.name, "ms_per_step": r["ms"], "clocks": r["clocks"],
                           "tokens_per_s": shp.num_tokens / (r["ms"] / 1000.0),
@@ -587,10 +615,12 @@ def main():
         line["gpu_launches"] += p["launches_per_step"] * max(3, args.steps // 2)
     if not args.no_extra:
         extra = {}
-        for shp in (I.ZERO_EXPERT, I.FP8_PREFILL, I.TINY, I.DECODE_PRENORM, I.DECODE_FP8):
+        for shp in (I.ZERO_EXPERT, I.FP8_PREFILL, I.TINY, I.DECODE_PRENORM, I.DECODE_FP8,
+                    I.DECODE_NVFP4, I.PREFILL_NVFP4):
             x = time_ours(B, shp, max(3, args.steps // 2), warmup, dev, peaks, with_e2e=False)
             xa = x["alg"]
             fp8 = shp.weight_dtype == I.WDTYPE_FP8_E4M3_B128
+            nv = shp.weight_dtype == I.WDTYPE_NVFP4   # dequantised to bf16: the bf16 MMA
             tpeak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
             gu = x["stage_ms"]["gate_up"]
             extra[shp.name] = {
@@ -606,10 +636,12 @@ def main():
                 if x["stage_ms"]["down"] > 0.01 else None,
                 "down_tensor_frac": xa["down_flops"] / (x["stage_ms"]["down"] / 1000.0) / 1e12 / tpeak
                 if x["stage_ms"]["down"] > 0.01 else None,
-                "gate_up_traffic": measured_traffic("gemm_fp8_kernel<0>" if fp8 else
-                                                    "gemm_bf16_kernel<256,SwiGLU>", shp.name),
-                "down_traffic": measured_traffic("gemm_fp8_kernel<1>" if fp8 else
-                                                 "gemm_bf16_kernel<256,bf16>", shp.name),
+                "gate_up_traffic": measured_traffic(
+                    "gemm_fp8_kernel<0>" if fp8 else "gemm_nvfp4_kernel<256,SwiGLU>" if nv
+                    else "gemm_bf16_kernel<256,SwiGLU>", shp.name),
+                "down_traffic": measured_traffic(
+                    "gemm_fp8_kernel<1>" if fp8 else "gemm_nvfp4_kernel<256,bf16>" if nv
+                    else "gemm_bf16_kernel<256,bf16>", shp.name),
                 "step_hbm_frac": xa["bytes"] / (x["ms"] / 1000.0) / 1e9 / peaks["hbm_gbs"],
                 "step_tensor_frac": xa["flops"] / (x["ms"] / 1000.0) / 1e12 / tpeak,
                 "Z": x["rs"]["Z"], "distinct_experts": x["rs"]["distinct"]}

@@ -71,8 +71,10 @@ typedef enum {
                                    (element 2j in the low nibble), one E4M3 scale per 16
                                    consecutive elements along the contraction (sf_*), one fp32
                                    scale2 per expert matrix; weight = e2m1 * sf * scale2.
-                                   Activations stay bf16 (no quantisation). Needs hidden and
-                                   inter multiples of 256; runs on the grouped chain
+                                   Activations are not quantised: the experts read x (or xn)
+                                   and the SwiGLU intermediate as f16, exact for bf16 values
+                                   of magnitude in [2^-14, 65504] (larger overflow). Needs
+                                   hidden and inter multiples of 256; runs on the grouped chain
                                    ("spark_model/layers/moe/forward.rs", NVFP4 decode arm:
                                    packed, scale and scale2 tables) */
 } moe_wdtype_t;

@@ -347,6 +347,7 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
   sa.tiles = P.at<int4>(R_TILES);
   sa.xq_tok = P.at<uint8_t>(R_XQT);
   sa.xs_tok = P.at<float>(R_XST);
+  sa.xp_f16 = c->weight_dtype == MOE_W_NVFP4;
   sa.N = c->num_tokens;
   sa.hdr = hdr;
 
@@ -496,7 +497,8 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
     CK(launch_gemm_fp8(1, mh, md, md, g, sms, st));
     MARK(MOE_STAGE_DOWN, 1);
   } else if (nv) {
-    // NVFP4 experts: codes and scale codes streamed, dequantised in shared memory
+    // NVFP4 experts: codes and scale codes streamed, dequantised to f16 in shared memory;
+    // the gathered rows and the SwiGLU intermediate are f16 (2-byte maps)
     CUtensorMap gu[5], dn[5];
     const uint64_t rows = (uint64_t)L.te;
     if (!make_map_bf16(&gu[0], P.at<void>(R_XP), H, rows, 128) ||

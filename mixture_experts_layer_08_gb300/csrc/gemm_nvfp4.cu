@@ -1,10 +1,10 @@
 // Grouped GEMM with NVFP4 expert weights on the 5th-generation tensor cores (sm_103a).
 //
 // D[rows of expert e, n-tile] = A[rows, K] . dequant(B_e)[n-tile rows, K]^T over the
-// expert-sorted bf16 rows, where B is packed E2M1 codes (two per byte, element 2j in the low
+// expert-sorted rows, where B is packed E2M1 codes (two per byte, element 2j in the low
 // nibble) with one E4M3 scale per 16 elements along K and one fp32 scale2 per expert
-// matrix. The epilogue is the bf16 kernel's (SwiGLU to bf16, or a bf16 store) with scale2
-// applied to the fp32 accumulators first.
+// matrix. Epilogue: scale2 on the fp32 accumulators, then SiLU(gate) * up to f16 (gate/up),
+// or a bf16 store (down).
 //
 // Pages: "spark_model/layers/moe/forward.rs" (NVFP4 arm of the decode forward: packed expert
 // weights with a per-group scale table and one scale2 value per expert matrix,
@@ -14,22 +14,27 @@
 //
 // The block-scaled tcgen05 MMA kinds take E4M3 scales only with both operands in FP4
 // (kind::mxf4nvf4), and an FP8 x FP4 product (kind::mxf8f6f4) only with power-of-two scales.
-// The activations stay bf16 here (the pages' w4a16), so the weights are dequantised in shared
-// memory instead -- exactly: an E2M1 value times an E4M3 scale has at most 5 significant bits
-// and fits bf16 -- and fed to the bf16 MMA. HBM carries 0.5 + 1/16 bytes per weight.
+// The activations keep 16 bits here (the pages' w4a16), so the weights are dequantised in
+// shared memory instead, exactly: an E2M1 value times an E4M3 scale has at most 5 significant
+// bits and lies in [2^-10, 2688], so it is an f16 (and the hardware converts both formats to
+// f16 in one instruction per pair). The MMA is kind::f16 with f16 operands: the activations
+// are the gathered token rows (or the SwiGLU intermediate) in f16, exact for the bf16 inputs
+// in f16's normal range. HBM carries 0.5 + 1/16 bytes per weight.
 //
 // Design (one persistent CTA per SM, 448 threads, 3 pipeline stages):
-//   warp 0      TMA producer, per stage: the A tile 128 x 64 (bf16, 128-byte swizzle), the
+//   warp 0      TMA producer, per stage: the A tile 128 x 64 (f16, 128-byte swizzle), the
 //               packed codes of the BN weight rows (BN x 32 bytes) and their scale codes
 //               (BN x 16 bytes: the 4 groups of this stage and of the 3 stages after it,
-//               reloaded with each stage so the box stays 16 bytes wide).
+//               reloaded with each stage so the box stays 16 bytes wide), all completing on
+//               the stage's cfull barrier.
 //   warp 1      TMEM allocation and the MMA issuer (M=128, N=BN, K=16 x 4 per stage).
 //   warps 2-5   epilogue (TMEM lane quadrant warp % 4): scale2, then SwiGLU or bf16 store.
 //   warps 6-13  converters: one weight row per thread, 8 chunks of 8 elements each: 4 code
-//               bytes -> 4 bf16 pairs through a 256-entry table, times the group's scale
-//               (exact), one 16-byte store into the 128-byte-swizzled B tile; then a proxy
-//               fence and one arrival per warp on the stage's full barrier (which the MMA
-//               waits on; the converters saw the A tile land on the same barrier as the codes).
+//               bytes -> 4 f16 pairs (cvt e2m1x2), times the group's scale (exact), one
+//               16-byte store into the 128-byte-swizzled B tile; then a proxy fence and one
+//               arrival per warp on the stage's full barrier, which the MMA waits on.
+#include <cuda_fp16.h>
+
 #include "kernels.h"
 
 namespace moe {
@@ -49,32 +54,39 @@ struct NvCfg {
   static constexpr int kCTile = BN * 32;    // packed codes, 64 elements per row
   static constexpr int kSTile = BN * 16;    // scale codes, 16 groups per row
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr size_t kTables = 256 * 4 + 256 * 2;
   static constexpr size_t kSmemBytes =
-      (size_t)kStages * (kNvATile + kBTile + kCTile + kSTile) + kTables + 1024 + 256;
+      (size_t)kStages * (kNvATile + kBTile + kCTile + kSTile) + 1024 + 256;
 };
 
-// E2M1 (OCP MX FP4) value of a 4-bit code: bit 3 sign, bits 2-1 exponent (bias 1), bit 0
-// mantissa; exponent 0 holds 0 and 0.5.
-__device__ __forceinline__ float e2m1_value(uint32_t nib) {
-  const uint32_t e = (nib >> 1) & 3u, m = nib & 1u;
-  const float mag = e == 0 ? 0.5f * (float)m : ldexpf(1.0f + 0.5f * (float)m, (int)e - 1);
-  return (nib & 8u) ? -mag : mag;
+// Two E2M1 codes (one byte, element 2j in the low nibble) -> f16x2 (element 2j in the low
+// half), by the hardware conversion.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t d;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(d)
+      : "r"(byte));
+  return d;
 }
 
-// E4M3 (OCP FP8) value of a code: bit 7 sign, bits 6-3 exponent (bias 7), bits 2-0 mantissa;
-// exponent 0 holds the subnormals m * 2^-9.
-__device__ __forceinline__ float e4m3_value(uint32_t c) {
-  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
-  const float mag = e == 0 ? ldexpf((float)m, -9) : ldexpf(1.0f + 0.125f * (float)m, (int)e - 7);
-  return (c & 0x80u) ? -mag : mag;
+// Two E4M3 codes (low 16 bits, the first in the low byte) -> f16x2.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+      : "=r"(d)
+      : "r"(two));
+  return d;
 }
 
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
-  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
-  __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
-  __nv_bfloat162 z = __hmul2(x, y);
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  __half2 x = *reinterpret_cast<__half2*>(&a);
+  __half2 y = *reinterpret_cast<__half2*>(&b);
+  __half2 z = __hmul2(x, y);
   return *reinterpret_cast<uint32_t*>(&z);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
 }
 
 struct NvTile {
@@ -108,9 +120,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
   uint8_t* sB = sA + S * kNvATile;
   uint8_t* sC = sB + S * C::kBTile;
   uint8_t* sS = sC + S * C::kCTile;
-  uint32_t* lut_pair = reinterpret_cast<uint32_t*>(sS + S * C::kSTile);   // byte -> bf16x2
-  uint16_t* lut_scale = reinterpret_cast<uint16_t*>(lut_pair + 256);     // E4M3 -> bf16
-  uint64_t* full = reinterpret_cast<uint64_t*>(lut_scale + 256);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sS + S * C::kSTile);
   uint64_t* empty = full + S;
   uint64_t* cfull = empty + S;
   uint64_t* tfull = cfull + S;
@@ -121,11 +131,6 @@ __global__ void __launch_bounds__(kNvThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WsHeader* hdr = g.status;
 
-  // dequantisation tables, from the two formats' definitions (bf16 holds both exactly)
-  for (int i = threadIdx.x; i < 256; i += kNvThreads) {
-    lut_pair[i] = pack_bf16x2(e2m1_value(i & 15), e2m1_value(i >> 4));
-    lut_scale[i] = __bfloat16_as_ushort(__float2bfloat16_rn(e4m3_value(i)));
-  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], kNvConvWarps);   // B converted (after cfull: A landed too)
@@ -187,7 +192,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = idesc_make(kNvBM, BN, 1, 1);
+    constexpr uint32_t idesc = idesc_make(kNvBM, BN, 0, 0);   // f16 x f16
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -230,8 +235,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
       const float s2a = g.s2_0[t.e];
       if (kGlu) {
         const float s2u = g.s2_1[t.e];
-        __nv_bfloat16* orow =
-            static_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + t.n * (BN / 2);
+        __half* orow = static_cast<__half*>(g.out) + (size_t)row * g.ldo + t.n * (BN / 2);
 #pragma unroll 1
         for (int c = 0; c < BN / 2; c += 32) {
           float gv[32], uv[32];
@@ -246,10 +250,10 @@ __global__ void __launch_bounds__(kNvThreads, 1)
               for (int j = 0; j < 8; ++j)
                 h[j] = silu(gv[8 * v + j] * s2a) * (uv[8 * v + j] * s2u);
               uint4 o;
-              o.x = pack_bf16x2(h[0], h[1]);
-              o.y = pack_bf16x2(h[2], h[3]);
-              o.z = pack_bf16x2(h[4], h[5]);
-              o.w = pack_bf16x2(h[6], h[7]);
+              o.x = pack_f16x2(h[0], h[1]);
+              o.y = pack_f16x2(h[2], h[3]);
+              o.z = pack_f16x2(h[4], h[5]);
+              o.w = pack_f16x2(h[6], h[7]);
               dst[v] = o;
             }
           }
@@ -292,12 +296,10 @@ __global__ void __launch_bounds__(kNvThreads, 1)
           const uint4 c1 = *reinterpret_cast<const uint4*>(crow + 16);
           const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(sS + s * C::kSTile + r * 16 +
                                                                   (kb & 3) * 4);
-          uint32_t scl[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t b = lut_scale[(sc4 >> (8 * q)) & 255u];
-            scl[q] = b | (b << 16);
-          }
+          // the 4 group scales as f16 pairs (s, s)
+          const uint32_t s01 = e4m3x2_to_f16x2(sc4), s23 = e4m3x2_to_f16x2(sc4 >> 16);
+          const uint32_t scl[4] = {__byte_perm(s01, 0, 0x1010), __byte_perm(s01, 0, 0x3232),
+                                   __byte_perm(s23, 0, 0x1010), __byte_perm(s23, 0, 0x3232)};
           const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
           uint8_t* brow = sB + s * C::kBTile + r * 128;
 #pragma unroll
@@ -305,10 +307,10 @@ __global__ void __launch_bounds__(kNvThreads, 1)
             const uint32_t w = words[c];
             const uint32_t sc = scl[c >> 1];
             uint4 o;
-            o.x = bf16x2_mul(lut_pair[w & 255u], sc);
-            o.y = bf16x2_mul(lut_pair[(w >> 8) & 255u], sc);
-            o.z = bf16x2_mul(lut_pair[(w >> 16) & 255u], sc);
-            o.w = bf16x2_mul(lut_pair[w >> 24], sc);
+            o.x = f16x2_mul(e2m1x2_to_f16x2(w), sc);
+            o.y = f16x2_mul(e2m1x2_to_f16x2(w >> 8), sc);
+            o.z = f16x2_mul(e2m1x2_to_f16x2(w >> 16), sc);
+            o.w = f16x2_mul(e2m1x2_to_f16x2(w >> 24), sc);
             *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) = o;
           }
         }

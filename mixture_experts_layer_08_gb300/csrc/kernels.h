@@ -56,6 +56,7 @@ struct SortArgs {
   int4* tiles;                     // [max m-tiles] (expert, row0, row1, 0)
   const uint8_t* xq_tok;           // FP8 experts: E4M3 codes of each token row [N, H]
   const float* xs_tok;             // and their 1x128 scales [H/128, N]
+  int xp_f16;                      // gather x rows as f16 (NVFP4 experts) instead of bf16
   int N;
   WsHeader* hdr;
 };
@@ -226,8 +227,8 @@ cudaError_t launch_gemm_fp8(int mode, const CUtensorMap& a, const CUtensorMap& b
                             const CUtensorMap& b1, const Fp8GemmArgs& g, int num_sms,
                             cudaStream_t st);
 
-// NVFP4 grouped GEMM over the expert-sorted bf16 rows (weights dequantised to bf16 in shared
-// memory, bf16 MMA, scale2 in the epilogue). mode kGemmSwiGLU (bn 256: 128 gate + 128 up
+// NVFP4 grouped GEMM over the expert-sorted f16 rows (weights dequantised exactly to f16 in
+// shared memory, f16 MMA, scale2 in the epilogue). mode kGemmSwiGLU (bn 256: 128 gate + 128 up
 // rows) or kGemmStoreBF16 (bn 256 or 128).
 struct NvGemmArgs {
   const int4* tiles;               // m-tile list (expert, row0, row1, 0)
@@ -238,11 +239,11 @@ struct NvGemmArgs {
   int b_rows_per_expert;           // rows of one expert matrix (I for gate/up, H for down)
   const float* s2_0;               // [E] scale2 of B0 (gate, or down)
   const float* s2_1;               // [E] scale2 of B1 (up)
-  void* out;                       // bf16 [rows, ldo]
+  void* out;                       // f16 [rows, ldo] (SwiGLU) or bf16 (store)
   int ldo;
   WsHeader* status;
 };
-// maps: A bf16 [rows, K] box {64, 128} (128-byte swizzle); codes of B0 and B1: uint8
+// maps: A f16 [rows, K] box {64, 128} (128-byte swizzle); codes of B0 and B1: uint8
 // [E*rows, K/2] box {32, b_rows}; scale codes of B0 and B1: uint8 [E*rows, K/16] box
 // {16, b_rows} (no swizzle); b_rows = bn/2 for SwiGLU, else bn. Needs K % 256 == 0.
 cudaError_t launch_gemm_nvfp4(int mode, int bn, const CUtensorMap maps[5], const NvGemmArgs& g,

@@ -9,6 +9,8 @@
 // selection, unbiased softmax x scaling for the weights, selected identity experts folded
 // into zero_accum; the single-CTA fused gate+top-K was too slow for 256 experts, so here
 // routing is one warp per token and the router spreads its columns over many blocks).
+#include <cuda_fp16.h>
+
 #include "kernels.h"
 #include "route_dev.cuh"
 
@@ -282,6 +284,19 @@ __global__ void __launch_bounds__(256) sort_scatter_kernel(SortArgs s, const __n
       for (int u = 0; u < 8; ++u) {
         const int c = c0 + u * 32 + lane;
         if (c < H / 8) v[u] = __ldg(src + c);
+      }
+      if (s.xp_f16) {
+        // the NVFP4 experts' f16 MMA operand: bf16 -> f16 (exact in f16's normal range)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint32_t* w = reinterpret_cast<uint32_t*>(&v[u]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[q]);
+            const __half2 h = __floats2half2_rn(__low2float(b), __high2float(b));
+            w[q] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+        }
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {

@@ -60,10 +60,14 @@ def test_launches_per_forward(B):
     n = lambda shape, path=B.PATH_AUTO: b.kernels_per_step(B, B.make_config(shape, True, path))
     assert n(I.DECODE) == 1                      # one cooperative kernel
     assert n(I.DECODE_PRENORM) == 1              # the norm runs in its phase 0
-    assert n(I.PREFILL) == 8                     # router, top-K, 3 sort, 2 GEMMs, combine
-    assert n(I.PREFILL.with_(pre_expert_norm=True)) == 9
-    assert n(I.DECODE, B.PATH_GROUPED) == 8
-    assert n(I.FP8_PREFILL) == 9                 # + the token-row quantiser, no shared expert
-    assert n(I.FP8_PREFILL.with_(shared_inter=512)) == 11
+    assert n(I.PREFILL) == 7                     # fused router, 3 sort, 2 GEMMs, combine
+    assert n(I.PREFILL.with_(pre_expert_norm=True)) == 8
+    assert n(I.PREFILL.with_(num_experts=144, router_width=144)) == 8   # 144 % 32: not fused
+    assert n(I.ZERO_EXPERT) == 7                 # a 384-wide router, fused
+    assert n(I.DECODE, B.PATH_GROUPED) == 8      # 4 tokens: router + top-K
+    assert n(I.FP8_PREFILL) == 8                 # + the token-row quantiser, no shared expert
+    assert n(I.FP8_PREFILL.with_(shared_inter=512)) == 10
     assert n(I.DECODE_FP8) == 1                  # E4M3 experts through the decode kernel too
     assert n(I.DECODE_FP8, B.PATH_GROUPED) == 11
+    assert n(I.DECODE_NVFP4) == 10               # NVFP4: grouped chain, shared expert apart
+    assert n(I.PREFILL_NVFP4) == 9
