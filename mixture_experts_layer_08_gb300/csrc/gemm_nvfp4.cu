@@ -21,18 +21,21 @@
 // are the gathered token rows (or the SwiGLU intermediate) in f16, exact for the bf16 inputs
 // in f16's normal range. HBM carries 0.5 + 1/16 bytes per weight.
 //
-// Design (one persistent CTA per SM, 448 threads, 3 pipeline stages):
-//   warp 0      TMA producer, per stage: the A tile 128 x 64 (f16, 128-byte swizzle), the
+// Design (one persistent CTA per SM, 448 threads; a ring of 4 loads and a ring of 3
+// converted B tiles):
+//   warp 0      TMA producer, per step: the A tile 128 x 64 (f16, 128-byte swizzle), the
 //               packed codes of the BN weight rows (BN x 32 bytes) and their scale codes
-//               (BN x 16 bytes: the 4 groups of this stage and of the 3 stages after it,
-//               reloaded with each stage so the box stays 16 bytes wide), all completing on
-//               the stage's cfull barrier.
-//   warp 1      TMEM allocation and the MMA issuer (M=128, N=BN, K=16 x 4 per stage).
+//               (BN x 16 bytes: the 4 groups of this step and of the 3 steps after it,
+//               reloaded with each step so the box stays 16 bytes wide), all completing on
+//               the load slot's barrier.
+//   warp 1      TMEM allocation and the MMA issuer (M=128, N=BN, K=16 x 4 per step); each
+//               step's commit frees its load slot and its B slot.
 //   warps 2-5   epilogue (TMEM lane quadrant warp % 4): scale2, then SwiGLU or bf16 store.
 //   warps 6-13  converters: one weight row per thread, 8 chunks of 8 elements each: 4 code
 //               bytes -> 4 f16 pairs (cvt e2m1x2), times the group's scale (exact), one
 //               16-byte store into the 128-byte-swizzled B tile; then a proxy fence and one
-//               arrival per warp on the stage's full barrier, which the MMA waits on.
+//               arrival per warp on the B slot's barrier, which the MMA waits on (the
+//               converters saw the load -- the A tile too -- land first).
 #include <cuda_fp16.h>
 
 #include "kernels.h"
@@ -49,13 +52,14 @@ constexpr int kNvATile = kNvBM * 128;     // 16 KB
 
 template <int BN>
 struct NvCfg {
-  static constexpr int kStages = 3;
+  static constexpr int kStages = 4;     // load ring: A tile + codes + scale codes
+  static constexpr int kBStages = 3;    // converted B tiles
   static constexpr int kBTile = BN * 128;   // bf16, 64 elements per row
   static constexpr int kCTile = BN * 32;    // packed codes, 64 elements per row
   static constexpr int kSTile = BN * 16;    // scale codes, 16 groups per row
   static constexpr int kTmemCols = 2 * BN;
   static constexpr size_t kSmemBytes =
-      (size_t)kStages * (kNvATile + kBTile + kCTile + kSTile) + 1024 + 256;
+      (size_t)kStages * (kNvATile + kCTile + kSTile) + (size_t)kBStages * kBTile + 1024 + 256;
 };
 
 // Two E2M1 codes (one byte, element 2j in the low nibble) -> f16x2 (element 2j in the low
@@ -111,6 +115,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
                       const __grid_constant__ CUtensorMap tm_s1, const NvGemmArgs g) {
   using C = NvCfg<BN>;
   constexpr int S = C::kStages;
+  constexpr int SB = C::kBStages;
   constexpr bool kGlu = MODE == kGemmSwiGLU;
   constexpr int b_rows = kGlu ? BN / 2 : BN;   // rows per weight matrix in one tile
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -118,12 +123,13 @@ __global__ void __launch_bounds__(kNvThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + S * kNvATile;
-  uint8_t* sC = sB + S * C::kBTile;
+  uint8_t* sC = sB + SB * C::kBTile;
   uint8_t* sS = sC + S * C::kCTile;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sS + S * C::kSTile);
-  uint64_t* empty = full + S;
-  uint64_t* cfull = empty + S;
-  uint64_t* tfull = cfull + S;
+  uint64_t* lfull = reinterpret_cast<uint64_t*>(sS + S * C::kSTile);   // load landed
+  uint64_t* lempty = lfull + S;      // load slot free (its MMA done)
+  uint64_t* bfull = lempty + S;      // B tile converted
+  uint64_t* bempty = bfull + SB;     // B slot free (its MMA done)
+  uint64_t* tfull = bempty + SB;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -133,9 +139,12 @@ __global__ void __launch_bounds__(kNvThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], kNvConvWarps);   // B converted (after cfull: A landed too)
-      mbar_init(&empty[s], 1);
-      mbar_init(&cfull[s], 1);             // A tile, codes and scale codes landed
+      mbar_init(&lfull[s], 1);    // A tile, codes and scale codes landed
+      mbar_init(&lempty[s], 1);
+    }
+    for (int s = 0; s < SB; ++s) {
+      mbar_init(&bfull[s], kNvConvWarps);
+      mbar_init(&bempty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
@@ -169,16 +178,16 @@ __global__ void __launch_bounds__(kNvThreads, 1)
       nv_tile_of(g, tile, t);
       const int brow = t.e * g.b_rows_per_expert + t.n * b_rows;
       for (int kb = 0; kb < g.num_kb; ++kb) {
-        if (!mbar_wait(&empty[s], ph ^ 1, hdr)) { ok = false; break; }
-        mbar_arrive_expect_tx(&cfull[s], kNvATile + C::kCTile + C::kSTile);
-        tma_load_2d(sA + s * kNvATile, &tm_a, kb * 64, t.row0, &cfull[s]);
+        if (!mbar_wait(&lempty[s], ph ^ 1, hdr)) { ok = false; break; }
+        mbar_arrive_expect_tx(&lfull[s], kNvATile + C::kCTile + C::kSTile);
+        tma_load_2d(sA + s * kNvATile, &tm_a, kb * 64, t.row0, &lfull[s]);
         uint8_t* cs = sC + s * C::kCTile;
         uint8_t* ss = sS + s * C::kSTile;
-        tma_load_2d(cs, &tm_c0, kb * 32, brow, &cfull[s]);
-        tma_load_2d(ss, &tm_s0, (kb >> 2) * 16, brow, &cfull[s]);
+        tma_load_2d(cs, &tm_c0, kb * 32, brow, &lfull[s]);
+        tma_load_2d(ss, &tm_s0, (kb >> 2) * 16, brow, &lfull[s]);
         if (kGlu) {
-          tma_load_2d(cs + b_rows * 32, &tm_c1, kb * 32, brow, &cfull[s]);
-          tma_load_2d(ss + b_rows * 16, &tm_s1, (kb >> 2) * 16, brow, &cfull[s]);
+          tma_load_2d(cs + b_rows * 32, &tm_c1, kb * 32, brow, &lfull[s]);
+          tma_load_2d(ss + b_rows * 16, &tm_s1, (kb >> 2) * 16, brow, &lfull[s]);
         }
         ++issued;
         if (++s == S) { s = 0; ph ^= 1; }
@@ -187,14 +196,14 @@ __global__ void __launch_bounds__(kNvThreads, 1)
     if (!ok) {
       // let the copies already issued land before the CTA can exit
       for (long long i = issued > S ? issued - S : 0; i < issued; ++i) {
-        mbar_wait(&cfull[i % S], (uint32_t)((i / S) & 1), nullptr);
+        mbar_wait(&lfull[i % S], (uint32_t)((i / S) & 1), nullptr);
       }
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------ MMA issuer
     constexpr uint32_t idesc = idesc_make(kNvBM, BN, 0, 0);   // f16 x f16
-    int s = 0;
-    uint32_t ph = 0;
+    int s = 0, sb = 0;
+    uint32_t ph = 0, phb = 0;
     bool ok = true;
     int it = 0;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
@@ -203,16 +212,19 @@ __global__ void __launch_bounds__(kNvThreads, 1)
       tc_fence_after();
       const uint32_t d = tmem_base + acc * BN;
       for (int kb = 0; kb < g.num_kb; ++kb) {
-        if (!mbar_wait(&full[s], ph, hdr)) { ok = false; break; }
+        // the converters saw this step's load land before they finished its B tile
+        if (!mbar_wait(&bfull[sb], phb, hdr)) { ok = false; break; }
         tc_fence_after();
         const uint32_t a0 = smem_u32(sA + s * kNvATile);
-        const uint32_t b0 = smem_u32(sB + s * C::kBTile);
+        const uint32_t b0 = smem_u32(sB + sb * C::kBTile);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           tc_mma_bf16(d, sdesc_k_sw128(a0 + k * 32), sdesc_k_sw128(b0 + k * 32), idesc,
                       (kb | k) != 0 ? 1u : 0u);
-        tc_commit(&empty[s]);
+        tc_commit(&lempty[s]);
+        tc_commit(&bempty[sb]);
         if (++s == S) { s = 0; ph ^= 1; }
+        if (++sb == SB) { sb = 0; phb ^= 1; }
       }
       if (ok) tc_commit(&tfull[acc]);
     }
@@ -284,12 +296,15 @@ __global__ void __launch_bounds__(kNvThreads, 1)
   } else if (warp >= kNvConvBase / 32) {
     // ------------------------------------------------ converters
     const int r = threadIdx.x - kNvConvBase;   // B-tile row of this thread
-    int s = 0;
-    uint32_t ph = 0;
+    int s = 0, sb = 0;
+    uint32_t ph = 0, phb = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       bool ok = true;
       for (int kb = 0; kb < g.num_kb; ++kb) {
-        if (!mbar_wait(&cfull[s], ph, hdr)) { ok = false; break; }
+        if (!mbar_wait(&lfull[s], ph, hdr) || !mbar_wait(&bempty[sb], phb ^ 1, hdr)) {
+          ok = false;
+          break;
+        }
         if (r < BN) {
           const uint8_t* crow = sC + s * C::kCTile + r * 32;
           const uint4 c0 = *reinterpret_cast<const uint4*>(crow);
@@ -301,7 +316,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
           const uint32_t scl[4] = {__byte_perm(s01, 0, 0x1010), __byte_perm(s01, 0, 0x3232),
                                    __byte_perm(s23, 0, 0x1010), __byte_perm(s23, 0, 0x3232)};
           const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-          uint8_t* brow = sB + s * C::kBTile + r * 128;
+          uint8_t* brow = sB + sb * C::kBTile + r * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint32_t w = words[c];
@@ -316,8 +331,9 @@ __global__ void __launch_bounds__(kNvThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full[s]);
+        if (lane == 0) mbar_arrive(&bfull[sb]);
         if (++s == S) { s = 0; ph ^= 1; }
+        if (++sb == SB) { sb = 0; phb ^= 1; }
       }
       if (!ok) break;
     }
