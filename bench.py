@@ -207,8 +207,7 @@ def fused_router(cfg, num_sms):
 def kernels_per_step(B, cfg, num_sms=152):
     """Kernels of this library one forward launches (memsets are not kernels)."""
     decode = cfg.path == B.PATH_DECODE or (cfg.path == B.PATH_AUTO and cfg.num_tokens <= 16
-                                            and cfg.inter <= 1024 and cfg.shared_inter <= 1024
-                                            and cfg.weight_dtype != 2)
+                                            and cfg.inter <= 1024 and cfg.shared_inter <= 1024)
     if decode:   # router, top-K, sort, projections, combine (and any pre-expert norm): one kernel
         return 1
     # routing: the fused router (1) or router + top-K (2); then 3 sort, gate/up GEMM, down GEMM,

@@ -74,16 +74,19 @@ typedef enum {
                                    Activations are not quantised: the experts read x (or xn)
                                    and the SwiGLU intermediate as f16, exact for bf16 values
                                    of magnitude in [2^-14, 65504] (larger overflow). Needs
-                                   hidden and inter multiples of 256; runs on the grouped chain
+                                   hidden and inter multiples of 256; both chains
                                    ("spark_model/layers/moe/forward.rs", NVFP4 decode arm:
                                    packed, scale and scale2 tables) */
 } moe_wdtype_t;
 
 typedef enum {
-  MOE_PATH_AUTO = 0,            /* decode chain for bf16 experts and num_tokens <= 16, else grouped */
+  MOE_PATH_AUTO = 0,            /* decode chain for num_tokens <= 16 (inter and shared_inter
+                                   <= 1024; E4M3 and NVFP4 experts: hidden % 256 == 0), else
+                                   grouped */
   MOE_PATH_DECODE = 1,          /* one cooperative kernel: routing, tcgen05 projections streaming
-                                   each touched expert's weights once, combine (bf16 experts,
-                                   num_tokens <= 16, inter and shared_inter <= 1024) */
+                                   each touched expert's weights once, combine (bf16, E4M3 or
+                                   NVFP4 experts, num_tokens <= 16, inter and shared_inter <=
+                                   1024) */
   MOE_PATH_GROUPED = 2          /* sort + tcgen05 grouped GEMM chain (any num_tokens) */
 } moe_path_t;
 

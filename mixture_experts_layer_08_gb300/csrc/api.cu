@@ -42,7 +42,7 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 int resolve_path(const moe_config_t* c) {
   if (c->path != MOE_PATH_AUTO) return c->path;
   const bool decode_ok = c->num_tokens <= kDecodeMaxTokens && c->inter <= 1024 &&
-                         c->shared_inter <= 1024 && c->weight_dtype != MOE_W_NVFP4 &&
+                         c->shared_inter <= 1024 &&
                          (c->weight_dtype == MOE_W_BF16 || c->hidden % 256 == 0);
   return decode_ok ? MOE_PATH_DECODE : MOE_PATH_GROUPED;
 }
@@ -77,7 +77,6 @@ moe_status_t validate_config(const moe_config_t* c) {
   if (c->weight_dtype == MOE_W_NVFP4 && (c->hidden % 256 || c->inter % 256))
     return MOE_ERR_UNSUPPORTED;
   const int path = resolve_path(c);
-  if (path == MOE_PATH_DECODE && c->weight_dtype == MOE_W_NVFP4) return MOE_ERR_UNSUPPORTED;
   if (path == MOE_PATH_DECODE &&
       (c->num_tokens > kDecodeMaxTokens || c->inter > 1024 || c->shared_inter > 1024 ||
        c->hidden > 8192))
@@ -139,6 +138,7 @@ Layout make_layout(const moe_config_t* c) {
       sz[R_XQT] = N * H;                 // E4M3 codes of the routed experts' input
       sz[R_XST] = (H / 128) * N * 4;     // and their 1x128 scales
     }
+    if (c->weight_dtype == MOE_W_NVFP4) sz[R_XQT] = N * H * 2;   // its f16 copy
   }
   size_t off = 0;
   for (int r = 0; r < R_NUM; ++r) {
@@ -668,6 +668,12 @@ moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const voi
   d.s_down = fp8 ? w->s_down : nullptr;
   d.xq = fp8 ? P.at<uint8_t>(R_XQT) : nullptr;
   d.xs = fp8 ? P.at<float>(R_XST) : nullptr;
+  const bool nv = c->weight_dtype == MOE_W_NVFP4;
+  d.nv = nv ? 1 : 0;
+  d.s2_gate = nv ? w->scale2_gate : nullptr;
+  d.s2_up = nv ? w->scale2_up : nullptr;
+  d.s2_down = nv ? w->scale2_down : nullptr;
+  d.xh = nv ? P.at<__half>(R_XQT) : nullptr;
   CUtensorMap maps[kDmNum];
   int bg = 0, bd = 0;
   decode_tile_rows(H, I, S, &bg, &bd);
@@ -677,6 +683,16 @@ moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const voi
         !make_map_u8(&maps[kDmWd], w->w_down, I, (uint64_t)E * H, bd) ||
         !make_map_bf16(&maps[kDmX], x, H, N, kDecodeBoxRowsX) ||
         !make_map_u8(&maps[kDmXn], d.xq, H, N, kDecodeBoxRowsX))
+      return MOE_ERR_CUDA;
+  } else if (nv) {   // NVFP4: codes {32, rows}, scale codes {16, rows}, f16 input copy
+    if (!make_map_u8_plain(&maps[kDmWg], w->w_gate, H / 2, (uint64_t)E * I, 32, bg) ||
+        !make_map_u8_plain(&maps[kDmWu], w->w_up, H / 2, (uint64_t)E * I, 32, bg) ||
+        !make_map_u8_plain(&maps[kDmWd], w->w_down, I / 2, (uint64_t)E * H, 32, bd) ||
+        !make_map_u8_plain(&maps[kDmFg], w->sf_gate, H / 16, (uint64_t)E * I, 16, bg) ||
+        !make_map_u8_plain(&maps[kDmFu], w->sf_up, H / 16, (uint64_t)E * I, 16, bg) ||
+        !make_map_u8_plain(&maps[kDmFd], w->sf_down, I / 16, (uint64_t)E * H, 16, bd) ||
+        !make_map_bf16(&maps[kDmX], x, H, N, kDecodeBoxRowsX) ||
+        !make_map_bf16(&maps[kDmXn], d.xh, H, N, kDecodeBoxRowsX))
       return MOE_ERR_CUDA;
   } else if (!make_map_bf16(&maps[kDmWg], w->w_gate, H, (uint64_t)E * I, bg) ||
              !make_map_bf16(&maps[kDmWu], w->w_up, H, (uint64_t)E * I, bg) ||
@@ -694,6 +710,11 @@ moe_status_t run_decode(const moe_config_t* c, const moe_weights_t* w, const voi
     maps[kDmSg] = maps[kDmWg];
     maps[kDmSu] = maps[kDmWu];
     maps[kDmSd] = maps[kDmWd];
+  }
+  if (!nv) {   // never read without NVFP4 experts
+    maps[kDmFg] = maps[kDmWg];
+    maps[kDmFu] = maps[kDmWu];
+    maps[kDmFd] = maps[kDmWd];
   }
   MARK(MOE_STAGE_SHARED, 0);
   MARK(MOE_STAGE_SHARED, 1);

@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -62,6 +63,64 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
+
+// ------------------------------------------------------------------ NVFP4 -> f16
+
+// Two E2M1 codes (one byte, element 2j in the low nibble) -> f16x2 (element 2j in the low
+// half), by the hardware conversion.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t d;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(d)
+      : "r"(byte));
+  return d;
+}
+
+// Two E4M3 codes (low 16 bits, the first in the low byte) -> f16x2.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+      : "=r"(d)
+      : "r"(two));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  __half2 x = *reinterpret_cast<__half2*>(&a);
+  __half2 y = *reinterpret_cast<__half2*>(&b);
+  __half2 z = __hmul2(x, y);
+  return *reinterpret_cast<uint32_t*>(&z);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// One weight row of a 64-element NVFP4 box -> f16, written as row `r` of a 128-byte-swizzled
+// tile at `brow` (16-byte chunk c at ((c ^ (r % 8)) * 16)): 32 code bytes `crow` (element 2j
+// in the low nibble), the 4 group scale codes `sc4` (first group in the low byte). Exact: an
+// E2M1 value times an E4M3 scale has at most 5 significant bits and fits f16.
+__device__ __forceinline__ void nvfp4_row_to_f16(const uint8_t* crow, uint32_t sc4, uint8_t* brow,
+                                                 int r) {
+  const uint4 c0 = *reinterpret_cast<const uint4*>(crow);
+  const uint4 c1 = *reinterpret_cast<const uint4*>(crow + 16);
+  const uint32_t s01 = e4m3x2_to_f16x2(sc4), s23 = e4m3x2_to_f16x2(sc4 >> 16);
+  const uint32_t scl[4] = {__byte_perm(s01, 0, 0x1010), __byte_perm(s01, 0, 0x3232),
+                           __byte_perm(s23, 0, 0x1010), __byte_perm(s23, 0, 0x3232)};
+  const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t w = words[c];
+    const uint32_t sc = scl[c >> 1];
+    uint4 o;
+    o.x = f16x2_mul(e2m1x2_to_f16x2(w), sc);
+    o.y = f16x2_mul(e2m1x2_to_f16x2(w >> 8), sc);
+    o.z = f16x2_mul(e2m1x2_to_f16x2(w >> 16), sc);
+    o.w = f16x2_mul(e2m1x2_to_f16x2(w >> 24), sc);
+    *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) = o;
+  }
+}
 
 // ------------------------------------------------------------------ programmatic dependent launch
 

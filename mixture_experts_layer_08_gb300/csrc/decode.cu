@@ -61,11 +61,14 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kWarps = kThreads / 32;
+constexpr int kConvBase = 192;            // warps 6-9: NVFP4 converters (idle otherwise)
+constexpr int kConvWarps = 4;
 constexpr int kBox = 64;                  // contraction columns per item (one 128-byte row)
 constexpr int kMaxBN = 256;
 constexpr int kWBytes = kMaxBN * 128;     // weight box of a stage, 32 KB
+constexpr int kCodeBytes = kMaxBN * 48;   // NVFP4: codes (32 B) + scale codes (16 B) per row
 constexpr int kTokBytes = 16 * 128;       // token rows of one contraction box, 2 KB
 constexpr int kMaxStages = 8;
 constexpr int kTmemCols = 512;            // two accumulators of up to 256 columns
@@ -300,6 +303,28 @@ __device__ void quant_token_rows(const DecodeArgs& a, const __nv_bfloat16* src) 
         make_float2(__fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc)), __NV_SATFINITE, __NV_E4M3);
     *reinterpret_cast<uint32_t*>(a.xq + (size_t)t * a.H + g * 128 + lane * 4) = lo | (hi << 16);
     if (lane == 0) a.xs[(size_t)g * a.N + t] = sc;
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Phase 0 with NVFP4 routed experts: their input rows (x, or xn under a pre-expert norm) as
+// f16 (exact for bf16 values in f16's normal range), the A operand of the routed f16 MMAs.
+// Token t by block G-1-t; fenced for the TMA reads of phase 2.
+__device__ void half_token_rows(const DecodeArgs& a, const __nv_bfloat16* src) {
+  const int t = (int)gridDim.x - 1 - (int)blockIdx.x;
+  if (t < 0 || t >= a.N) return;
+  const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)t * a.H);
+  uint4* d4 = reinterpret_cast<uint4*>(a.xh + (size_t)t * a.H);
+  for (int c = threadIdx.x; c < a.H / 8; c += kThreads) {
+    uint4 v = s4[c];
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[q]);
+      const __half2 h = __floats2half2_rn(__low2float(b), __high2float(b));
+      w[q] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    d4[c] = v;
   }
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -900,7 +925,14 @@ __device__ __forceinline__ int slot_rows(const DecodeArgs& a, const Routing& m, 
 // columns, multiplied on the tensor cores as E4M3 x E4M3 (kind::f8f6f4) one item at a time, and
 // each item's partial is scaled by its activation and weight block scales into an fp32 run
 // accumulator in shared memory before the run is added out. The shared expert stays bf16.
-template <bool FP8>
+//
+// NVFP4: the routed experts' weights are packed E2M1 codes with one E4M3 scale per 16 elements
+// and one fp32 scale2 per expert matrix. Their items keep the bf16 items' shape (64 contraction
+// columns): the producer streams the codes and scale codes of the box into a codes ring, four
+// converter warps (6-9) dequantise them exactly to f16 in the item's weight slot (128-byte
+// swizzle), and the MMA multiplies f16 x f16 with the routed input (and the SwiGLU intermediate)
+// in f16; scale2 multiplies each run's partial sums when it is drained.
+template <bool FP8, bool NV>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_forward_kernel(const __grid_constant__ CUtensorMap tm_wg,
                           const __grid_constant__ CUtensorMap tm_wu,
@@ -909,11 +941,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const __grid_constant__ CUtensorMap tm_wd,
                           const __grid_constant__ CUtensorMap tm_sd,
                           const __grid_constant__ CUtensorMap tm_x,
-                          const __grid_constant__ CUtensorMap tm_xn, const DecodeArgs a,
+                          const __grid_constant__ CUtensorMap tm_xn,
+                          const __grid_constant__ CUtensorMap tm_fg,
+                          const __grid_constant__ CUtensorMap tm_fu,
+                          const __grid_constant__ CUtensorMap tm_fd, const DecodeArgs a,
                           const Plan pl) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ Routing meta;
-  __shared__ uint64_t bars[2 * kMaxStages + 8];
+  __shared__ uint64_t bars[3 * kMaxStages + 8];
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(16) float stage_rows[16 * kStageLd];   // drain staging, 16 rows x 64
   __shared__ float red_s[kDecodeMaxTokens * kWarps];           // router block reductions
@@ -929,19 +964,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* hb = xtok + (size_t)stages * kTokBytes;        // [2][max(I,S)/64][16 x 128 B]
   uint8_t* ring = hb + 2 * (size_t)pl.hbytes;             // [stages][BN x 128 B]
   float* racc = reinterpret_cast<float*>(ring + (size_t)stages * kWBytes);   // E4M3: [16][kRaccLd]
+  uint8_t* codes = ring + (size_t)stages * kWBytes;       // NVFP4: [stages][BN x 48 B]
   uint64_t* full = bars;
   uint64_t* empty = bars + kMaxStages;
   uint64_t* afull = bars + 2 * kMaxStages;                // [2] run accumulated
   uint64_t* aempty = afull + 2;                           // [2] run drained
   uint64_t* bfull = aempty + 2;                           // [2] down A operand built
   uint64_t* drain = bfull + 2;                            // every MMA complete
+  uint64_t* cfull = bars + 2 * kMaxStages + 8;            // NVFP4: a box's codes landed
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WsHeader* hdr = a.hdr;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], NV ? 1 + kConvWarps : 1);   // (NVFP4: + the converter warps)
       mbar_init(&empty[s], 1);
+      if (NV) mbar_init(&cfull[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&afull[i], 1);
@@ -960,6 +998,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_su);
       tma_prefetch_desc(&tm_sd);
     }
+    if (NV) {
+      tma_prefetch_desc(&tm_fg);
+      tma_prefetch_desc(&tm_fu);
+      tma_prefetch_desc(&tm_fd);
+    }
   }
   if (warp == 1) tmem_alloc(&tmem_slot, kTmemCols);
   // ---- phases 0 and 1: router logits (spread over the grid) and zeroed accumulators, then
@@ -973,6 +1016,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (FP8) {
       __syncthreads();   // (this block's xn row, written just above, is read back below)
       quant_token_rows(a, a.norm_w ? a.xn : xs_src);
+    }
+    if (NV) {
+      __syncthreads();
+      half_token_rows(a, a.norm_w ? a.xn : xs_src);
     }
   }
   zero_accumulators(a);
@@ -1023,27 +1070,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* wst = ring + (size_t)s * kWBytes;
         // contraction coordinate of the box: 64 bf16 or (E4M3 routed experts) 128 codes
         const int xc = kc * ((FP8 && slot >= 0) ? 2 * kBox : kBox);
+        // NVFP4 routed item: its weights reach the slot through the converters
+        const bool nvi = NV && slot >= 0;
+        const int bn = down ? pl.bn_d : pl.bn_g;
+        const uint32_t wbytes = nvi ? 0u : (uint32_t)(bn * 128);
         if (!down) {   // (routed experts read their input xn / its codes, the shared expert x)
-          mbar_arrive_expect_tx(&full[s], (uint32_t)(pl.bn_g * 128 + kTokBytes));
+          mbar_arrive_expect_tx(&full[s], wbytes + kTokBytes);
           tma_load_2d(xtok + (size_t)s * kTokBytes, slot >= 0 ? &tm_xn : &tm_x, xc, 0, &full[s]);
+        } else if (wbytes) {
+          mbar_arrive_expect_tx(&full[s], wbytes);
         } else {
-          mbar_arrive_expect_tx(&full[s], (uint32_t)(pl.bn_d * 128));
+          mbar_arrive(&full[s]);
         }
-        tma_load_2d(wst, m, xc, row, &full[s]);
+        if (nvi) {
+          uint8_t* cst = codes + (size_t)s * kCodeBytes;
+          const CUtensorMap* f = m == &tm_wg ? &tm_fg : (m == &tm_wu ? &tm_fu : &tm_fd);
+          mbar_arrive_expect_tx(&cfull[s], (uint32_t)(bn * 48));
+          tma_load_2d(cst, m, kc * 32, row, &cfull[s]);
+          tma_load_2d(cst + bn * 32, f, (kc >> 2) * 16, row, &cfull[s]);
+        } else {
+          tma_load_2d(wst, m, xc, row, &full[s]);
+          if (NV) mbar_arrive(&cfull[s]);   // (the converters pass the item on)
+        }
         ++issued;
         if (++s == stages) { s = 0; ph ^= 1; }
       }
       if (!ok)   // let the copies already issued land before the block can exit
-        for (int i = issued > stages ? issued - stages : 0; i < issued; ++i)
+        for (int i = issued > stages ? issued - stages : 0; i < issued; ++i) {
+          if (NV) mbar_wait(&cfull[i % stages], (uint32_t)((i / stages) & 1), nullptr);
           mbar_wait(&full[i % stages], (uint32_t)((i / stages) & 1), nullptr);
+        }
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc_g = idesc_make(128, pl.bn_g, 1, 1);
       const uint32_t idesc_d = idesc_make(128, pl.bn_d, 1, 1);
-      const uint32_t idesc_g8 = idesc_make(128, pl.bn_g, 0, 0);   // E4M3 x E4M3
-      const uint32_t idesc_d8 = idesc_make(128, pl.bn_d, 0, 0);
+      const uint32_t idesc_g8 = idesc_make(128, pl.bn_g, 0, 0);   // E4M3 x E4M3 (f8f6f4)
+      const uint32_t idesc_d8 = idesc_make(128, pl.bn_d, 0, 0);   // (f16: f16 x f16, NVFP4)
       int s = 0, run = -1, prev_tile = -1, bslot = -2, nb = 0;
       uint32_t ph = 0, hb_cur = 0;
       bool prev_down = false, ok = true, first = false;
@@ -1083,7 +1147,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_mma_fp8(d, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
                        (first && kk == 0) ? 0u : 1u);
         } else {
-          const uint32_t idesc = down ? idesc_d : idesc_g;
+          const bool f16 = NV && slot >= 0;   // NVFP4 routed item: f16 operands
+          const uint32_t idesc = f16 ? (down ? idesc_d8 : idesc_g8) : (down ? idesc_d : idesc_g);
 #pragma unroll
           for (int kk = 0; kk < kBox / 16; ++kk)
             tc_mma_bf16(d, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
@@ -1097,6 +1162,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every MMA of this thread complete before TMEM is released
       tc_commit(drain);
       mbar_wait(drain, 0, hdr);
+    }
+  } else if (warp >= kConvBase / 32) {
+    // ------------------------------------------------ NVFP4 converters (warps 6-9)
+    if (NV) {
+      const int ct = threadIdx.x - kConvBase;   // 0..127
+      int s = 0;
+      uint32_t ph = 0;
+      for (int k = 0; k < nitems; ++k) {
+        bool down;
+        int tile, kc, slot, lt, kh;
+        sc.item(k, down, tile, kc, slot, lt, kh);
+        if (!mbar_wait(&cfull[s], ph, hdr)) break;
+        if (slot >= 0) {
+          const int bn = down ? pl.bn_d : pl.bn_g;
+          const uint8_t* cst = codes + (size_t)s * kCodeBytes;
+          uint8_t* wst = ring + (size_t)s * kWBytes;
+          for (int r = ct; r < bn; r += kConvWarps * 32) {
+            const uint32_t sc4 =
+                *reinterpret_cast<const uint32_t*>(cst + bn * 32 + r * 16 + (kc & 3) * 4);
+            nvfp4_row_to_f16(cst + r * 32, sc4, wst + r * 128, r);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+        if (++s == stages) { s = 0; ph ^= 1; }
+      }
     }
   } else {
     // ------------------------------------------------ epilogue
@@ -1132,6 +1224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nt = rslot >= 0 ? sc.nIt : sc.nSt;
         const int col = (rlt < nt ? 0 : a.ldh) + (rlt < nt ? rlt : rlt - nt) * bn;
         if (row >= 0) dst = a.hd + (size_t)row * (2 * a.ldh) + col;
+        if (NV && rslot >= 0) scale = (rlt < nt ? a.s2_gate : a.s2_up)[meta.slot_e[rslot]];
       } else {
         bn = pl.bn_d;
         const int c0 = rlt * bn;
@@ -1145,6 +1238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             dst = a.yd + (size_t)row * a.H + c0;
           }
+          if (NV && rslot >= 0) scale *= a.s2_down[meta.slot_e[rslot]];
         }
       }
     };
@@ -1323,10 +1417,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           add4(u0, __ldcg(reinterpret_cast<const float4*>(h2 + a.ldh)));
           add4(u1, __ldcg(reinterpret_cast<const float4*>(h2 + a.ldh + 4)));
         }
-        o.x = pack_bf16x2(silu(g0v.x) * u0.x, silu(g0v.y) * u0.y);
-        o.y = pack_bf16x2(silu(g0v.z) * u0.z, silu(g0v.w) * u0.w);
-        o.z = pack_bf16x2(silu(g1v.x) * u1.x, silu(g1v.y) * u1.y);
-        o.w = pack_bf16x2(silu(g1v.z) * u1.z, silu(g1v.w) * u1.w);
+        if (NV && slot >= 0) {   // the NVFP4 down items' f16 operand
+          o.x = pack_f16x2(silu(g0v.x) * u0.x, silu(g0v.y) * u0.y);
+          o.y = pack_f16x2(silu(g0v.z) * u0.z, silu(g0v.w) * u0.w);
+          o.z = pack_f16x2(silu(g1v.x) * u1.x, silu(g1v.y) * u1.y);
+          o.w = pack_f16x2(silu(g1v.z) * u1.z, silu(g1v.w) * u1.w);
+        } else {
+          o.x = pack_bf16x2(silu(g0v.x) * u0.x, silu(g0v.y) * u0.y);
+          o.y = pack_bf16x2(silu(g0v.z) * u0.z, silu(g0v.w) * u0.w);
+          o.z = pack_bf16x2(silu(g1v.x) * u1.x, silu(g1v.y) * u1.y);
+          o.w = pack_bf16x2(silu(g1v.z) * u1.z, silu(g1v.w) * u1.w);
+        }
         *reinterpret_cast<uint4*>(buf + (size_t)(c >> 3) * 2048 + j * 128 +
                                   (((c & 7) ^ (j & 7)) << 4)) = o;
       }
@@ -1441,13 +1542,15 @@ cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, 
     return cudaErrorInvalidValue;
   if (a.fp8 && (!a.s_gate || !a.s_up || !a.s_down || !a.xq || !a.xs || a.I > 128 * kMaxHGroups))
     return cudaErrorInvalidValue;
+  if (a.nv && (a.fp8 || !a.s2_gate || !a.s2_up || !a.s2_down || !a.xh || a.H % 256 || a.I % 256))
+    return cudaErrorInvalidValue;
   Plan pl{};
   decode_tile_rows(a.H, a.I, a.S, &pl.bn_g, &pl.bn_d);
   // boxes of the down A operand: routed I / 64 (bf16) or I / 128 (E4M3), shared S / 64
   const int hb_boxes = a.fp8 ? (a.I / 128 > a.S / kBox ? a.I / 128 : a.S / kBox)
                              : (a.I > a.S ? a.I : a.S) / kBox;
   pl.hbytes = hb_boxes * kTokBytes;
-  const int per_stage = kTokBytes + kWBytes;
+  const int per_stage = kTokBytes + kWBytes + (a.nv ? kCodeBytes : 0);
   // alignment slack + two down A operands (+ the E4M3 run accumulator)
   const int fixed = 1024 + 2 * pl.hbytes + (a.fp8 ? kRaccBytes : 0);
   // (the static shared memory -- routing, barriers, drain staging -- stays within 16 KB)
@@ -1462,7 +1565,8 @@ cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, 
                                    (a.R <= 256 ? 8 + (size_t)a.N * a.R * 16 : 0);
   if (scratch > (size_t)pl.stages * (kTokBytes + kWBytes)) return cudaErrorInvalidValue;
   const size_t sm = (size_t)fixed + (size_t)pl.stages * per_stage;
-  auto kern = a.fp8 ? decode_forward_kernel<true> : decode_forward_kernel<false>;
+  auto kern = a.fp8 ? decode_forward_kernel<true, false>
+                    : (a.nv ? decode_forward_kernel<false, true> : decode_forward_kernel<false, false>);
   cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(kern), sm);
   if (e != cudaSuccess) return e;
   // the down phase waits on other blocks' gate/up work: all blocks must be resident (checked
@@ -1474,7 +1578,7 @@ cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, 
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(mu);
-    const size_t key = sm * 2 + (a.fp8 ? 1 : 0);
+    const size_t key = sm * 4 + (a.fp8 ? 1 : 0) + (a.nv ? 2 : 0);
     if (!ok.count({dev, key})) {
       int per_sm = 0;
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, sm);
@@ -1494,8 +1598,8 @@ cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, maps[kDmWg], maps[kDmWu], maps[kDmSg],
-                            maps[kDmSu], maps[kDmWd], maps[kDmSd], maps[kDmX], maps[kDmXn], a,
-                            pl);
+                            maps[kDmSu], maps[kDmWd], maps[kDmSd], maps[kDmX], maps[kDmXn],
+                            maps[kDmFg], maps[kDmFu], maps[kDmFd], a, pl);
 }
 
 }  // namespace moe

@@ -36,8 +36,6 @@
 //               16-byte store into the 128-byte-swizzled B tile; then a proxy fence and one
 //               arrival per warp on the B slot's barrier, which the MMA waits on (the
 //               converters saw the load -- the A tile too -- land first).
-#include <cuda_fp16.h>
-
 #include "kernels.h"
 
 namespace moe {
@@ -61,37 +59,6 @@ struct NvCfg {
   static constexpr size_t kSmemBytes =
       (size_t)kStages * (kNvATile + kCTile + kSTile) + (size_t)kBStages * kBTile + 1024 + 256;
 };
-
-// Two E2M1 codes (one byte, element 2j in the low nibble) -> f16x2 (element 2j in the low
-// half), by the hardware conversion.
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t d;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(d)
-      : "r"(byte));
-  return d;
-}
-
-// Two E4M3 codes (low 16 bits, the first in the low byte) -> f16x2.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  uint32_t d;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
-      : "=r"(d)
-      : "r"(two));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
-  __half2 x = *reinterpret_cast<__half2*>(&a);
-  __half2 y = *reinterpret_cast<__half2*>(&b);
-  __half2 z = __hmul2(x, y);
-  return *reinterpret_cast<uint32_t*>(&z);
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
 
 struct NvTile {
   int e, row0, row1, n;
@@ -306,28 +273,9 @@ __global__ void __launch_bounds__(kNvThreads, 1)
           break;
         }
         if (r < BN) {
-          const uint8_t* crow = sC + s * C::kCTile + r * 32;
-          const uint4 c0 = *reinterpret_cast<const uint4*>(crow);
-          const uint4 c1 = *reinterpret_cast<const uint4*>(crow + 16);
           const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(sS + s * C::kSTile + r * 16 +
                                                                   (kb & 3) * 4);
-          // the 4 group scales as f16 pairs (s, s)
-          const uint32_t s01 = e4m3x2_to_f16x2(sc4), s23 = e4m3x2_to_f16x2(sc4 >> 16);
-          const uint32_t scl[4] = {__byte_perm(s01, 0, 0x1010), __byte_perm(s01, 0, 0x3232),
-                                   __byte_perm(s23, 0, 0x1010), __byte_perm(s23, 0, 0x3232)};
-          const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-          uint8_t* brow = sB + sb * C::kBTile + r * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint32_t w = words[c];
-            const uint32_t sc = scl[c >> 1];
-            uint4 o;
-            o.x = f16x2_mul(e2m1x2_to_f16x2(w), sc);
-            o.y = f16x2_mul(e2m1x2_to_f16x2(w >> 8), sc);
-            o.z = f16x2_mul(e2m1x2_to_f16x2(w >> 16), sc);
-            o.w = f16x2_mul(e2m1x2_to_f16x2(w >> 24), sc);
-            *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) = o;
-          }
+          nvfp4_row_to_f16(sC + s * C::kCTile + r * 32, sc4, sB + sb * C::kBTile + r * 128, r);
         }
         fence_proxy_async_smem();
         __syncwarp();

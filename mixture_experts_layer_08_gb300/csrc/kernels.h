@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -137,11 +138,20 @@ struct DecodeArgs {
   const float* s_down;             // [E, H/128, I/128] of Wd
   uint8_t* xq;                     // [N, H] E4M3 codes of the routed experts' input (phase 0)
   float* xs;                       // [H/128, N] their 1x128 scales
+  // NVFP4 routed experts (the shared expert stays bf16)
+  int nv;
+  const float* s2_gate;            // [E] scale2 of Wg
+  const float* s2_up;              // [E] of Wu
+  const float* s2_down;            // [E] of Wd
+  __half* xh;                      // [N, H] f16 copy of the routed experts' input (phase 0)
 };
 // Tensor maps (box 128 bytes wide, 128-byte swizzle) the decode kernel streams from: bf16
 // {64, rows}, or with E4M3 routed experts uint8 {128, rows} for Wg, Wu, Wd and the routed
-// experts' input (kDmXn then maps the E4M3 codes xq).
-enum DecodeMap { kDmWg = 0, kDmWu, kDmSg, kDmSu, kDmWd, kDmSd, kDmX, kDmXn, kDmNum };
+// experts' input (kDmXn then maps the E4M3 codes xq). With NVFP4 routed experts Wg, Wu, Wd map
+// the packed codes (uint8 {32, rows}, no swizzle), kDmFg, kDmFu, kDmFd their scale codes
+// (uint8 {16, rows}), and kDmXn the f16 input copy xh ({64, 16}, 128-byte swizzle).
+enum DecodeMap { kDmWg = 0, kDmWu, kDmSg, kDmSu, kDmWd, kDmSd, kDmX, kDmXn, kDmFg, kDmFu, kDmFd,
+                 kDmNum };
 // Box rows: x and the routed experts' input xn (x itself without a pre-expert norm) 16;
 // gate/up weights (Wg, Wu, Sg, Su) *bn_g; down weights (Wd, Sd) *bn_d.
 constexpr int kDecodeBoxRowsX = 16;

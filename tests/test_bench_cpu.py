@@ -69,5 +69,6 @@ def test_launches_per_forward(B):
     assert n(I.FP8_PREFILL.with_(shared_inter=512)) == 10
     assert n(I.DECODE_FP8) == 1                  # E4M3 experts through the decode kernel too
     assert n(I.DECODE_FP8, B.PATH_GROUPED) == 11
-    assert n(I.DECODE_NVFP4) == 10               # NVFP4: grouped chain, shared expert apart
+    assert n(I.DECODE_NVFP4) == 1                # NVFP4 experts through the decode kernel
+    assert n(I.DECODE_NVFP4, B.PATH_GROUPED) == 10   # grouped: shared expert apart
     assert n(I.PREFILL_NVFP4) == 9

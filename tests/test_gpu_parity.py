@@ -462,24 +462,37 @@ NV_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("shape", NV_SHAPES, ids=lambda s: s.name)
-def test_nvfp4_forward_matches_oracle(B, shape):
+@pytest.mark.parametrize("path", [0, 1, 2], ids=["auto", "decode", "grouped"])
+@pytest.mark.parametrize("shape", NV_SHAPES + [
+    # decode-sized on the decode kernel: 16 tokens, top-4, an ungated shared expert
+    NV_SMALL.with_(name="nvfp4_decode_n16", num_tokens=16, num_experts=16, router_width=16,
+                   top_k=4, shared_gated=False)], ids=lambda s: s.name)
+def test_nvfp4_forward_matches_oracle(B, shape, path):
+    if path == 1 and shape.num_tokens > 16:
+        pytest.skip("decode chain is for <= 16 tokens")
     inp = I.make_inputs(shape)
-    got, gidx, gw = run_gpu(B, inp, 0)
+    got, gidx, gw = run_gpu(B, inp, path)
     check_routing(gidx, O.moe_forward(inp, routing_only=True))
     ref = O.moe_forward(inp, forced_idx=gidx)
     check_out(got, ref["out"])
-    # the grouped chain in deterministic mode repeats bit for bit
-    assert np.array_equal(run_gpu(B, inp, 0)[0], got)
+    # deterministic mode repeats bit for bit
+    assert np.array_equal(run_gpu(B, inp, path)[0], got)
+
+
+def test_nvfp4_decode_kernel_atomic_mode(B):
+    """NVFP4 experts on the decode kernel with the FP32-atomic down accumulation."""
+    inp = I.make_inputs(NV_SHAPES[1])
+    got, gidx, _ = run_gpu(B, inp, 1, deterministic=False)
+    check_out(got, O.moe_forward(inp, forced_idx=gidx)["out"])
 
 
 def test_nvfp4_rejected_where_unsupported(B):
-    """NVFP4 needs hidden and inter multiples of 256, and runs on the grouped chain only."""
+    """NVFP4 needs hidden and inter multiples of 256."""
     ok = NV_SMALL.with_(num_tokens=4)
-    assert B.moe_workspace_size(B.make_config(ok, True, 2)) > 0
-    for bad, path in ((NV_SMALL.with_(inter=384), 0), (ok, 1)):
-        with pytest.raises(B.MoeError):
-            B.moe_workspace_size(B.make_config(bad, True, path))
+    for path in (1, 2):
+        assert B.moe_workspace_size(B.make_config(ok, True, path)) > 0
+    with pytest.raises(B.MoeError):
+        B.moe_workspace_size(B.make_config(NV_SMALL.with_(inter=384), True, 0))
 
 
 @pytest.mark.parametrize("shape", [I.DECODE_NVFP4, I.PREFILL_NVFP4], ids=lambda s: s.name)
