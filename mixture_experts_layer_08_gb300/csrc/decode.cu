@@ -61,10 +61,10 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kWarps = kThreads / 32;
-constexpr int kConvBase = 192;            // warps 6-9: NVFP4 converters (idle otherwise)
+constexpr int kThreads = 192;             // block size (NVFP4 experts: + kConvWarps warps)
+constexpr int kConvBase = 192;            // warps 6-9: NVFP4 converters
 constexpr int kConvWarps = 4;
+constexpr int kMaxWarps = (kThreads + 32 * kConvWarps) / 32;
 constexpr int kBox = 64;                  // contraction columns per item (one 128-byte row)
 constexpr int kMaxBN = 256;
 constexpr int kWBytes = kMaxBN * 128;     // weight box of a stage, 32 KB
@@ -88,6 +88,10 @@ struct Plan {
 };
 
 constexpr uint16_t kNoRow16 = 0xFFFF;
+
+// This launch's block size (kThreads, or kThreads + 32 * kConvWarps with NVFP4 experts).
+__device__ __forceinline__ int nthr() { return (int)blockDim.x; }
+__device__ __forceinline__ int nwarps() { return (int)(blockDim.x >> 5); }
 
 // Routing of the batch; every block computes its own copy in shared memory.
 struct Routing {
@@ -157,14 +161,14 @@ __device__ void router_rows(const DecodeArgs& a, uint8_t* scratch, size_t scratc
   auto row_ptr = [&](int r) {
     return reinterpret_cast<const uint4*>(r < a.R ? a.router_w + (size_t)r * a.H : a.sh_gate_vec);
   };
-  constexpr int kPer = 8;   // chunks per thread per pass (H <= 8 * 8 * kThreads)
+  constexpr int kPer = 8;   // chunks per thread per pass (H <= 8 * 8 * nthr())
   uint4 wv[kPer];
   const int r_first = blockIdx.x;
   if (r_first < rows) {
     const uint4* wr = row_ptr(r_first);
 #pragma unroll
     for (int q = 0; q < kPer; ++q) {
-      const int c = q * kThreads + tid;
+      const int c = q * nthr() + tid;
       if (c < chunks) wv[q] = __ldg(wr + c);
     }
   }
@@ -174,16 +178,16 @@ __device__ void router_rows(const DecodeArgs& a, uint8_t* scratch, size_t scratc
     uint4* d = reinterpret_cast<uint4*>(scratch);
     const uint4* sx = reinterpret_cast<const uint4*>(a.x);
     const int n = (int)(xbytes / 16);
-    for (int i0 = 0; i0 < n; i0 += 8 * kThreads) {
+    for (int i0 = 0; i0 < n; i0 += 8 * nthr()) {
       uint4 tmp[8];   // eight loads in flight per thread
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int i = i0 + u * kThreads + tid;
+        const int i = i0 + u * nthr() + tid;
         if (i < n) tmp[u] = __ldg(sx + i);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int i = i0 + u * kThreads + tid;
+        const int i = i0 + u * nthr() + tid;
         if (i < n) d[i] = tmp[u];
       }
     }
@@ -192,11 +196,11 @@ __device__ void router_rows(const DecodeArgs& a, uint8_t* scratch, size_t scratc
   }
   for (int r = r_first; r < rows; r += gridDim.x) {
     const uint4* wr = row_ptr(r);
-    for (int c0 = 0; c0 < chunks; c0 += kPer * kThreads) {
+    for (int c0 = 0; c0 < chunks; c0 += kPer * nthr()) {
       if (r != r_first || c0 != 0) {   // (the first pass was loaded above)
 #pragma unroll
         for (int q = 0; q < kPer; ++q) {
-          const int c = c0 + q * kThreads + tid;
+          const int c = c0 + q * nthr() + tid;
           if (c < chunks) wv[q] = __ldg(wr + c);
         }
       }
@@ -208,7 +212,7 @@ __device__ void router_rows(const DecodeArgs& a, uint8_t* scratch, size_t scratc
         float acc = 0.0f;
 #pragma unroll
         for (int q = 0; q < kPer; ++q) {
-          const int c = c0 + q * kThreads + tid;
+          const int c = c0 + q * nthr() + tid;
           if (c < chunks) {
             float wf[8], xf[8];
             bf16x8_to_f32(wv[q], wf);
@@ -218,14 +222,14 @@ __device__ void router_rows(const DecodeArgs& a, uint8_t* scratch, size_t scratc
           }
         }
         acc = warp_sum(acc);
-        if (lane == 0) red[t * kWarps + warp] = (c0 == 0 ? 0.0f : red[t * kWarps + warp]) + acc;
+        if (lane == 0) red[t * nwarps() + warp] = (c0 == 0 ? 0.0f : red[t * nwarps() + warp]) + acc;
       }
     }
     __syncthreads();
     if (tid < a.N) {
       float v = 0.0f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) v += red[tid * kWarps + w];
+      for (int w = 0; w < nwarps(); ++w) v += red[tid * nwarps() + w];
       if (r < a.R) a.logits[(size_t)tid * a.R + r] = v;
       else a.hdr->gate_dot[tid] = v;
     }
@@ -245,7 +249,7 @@ __device__ void pre_expert_norm_rows(const DecodeArgs& a, const __nv_bfloat16* x
     const uint4* xr = reinterpret_cast<const uint4*>(xs + (size_t)t * a.H);
     float ss = 0.0f;
 #pragma unroll 1
-    for (int c = tid; c < C; c += kThreads) {
+    for (int c = tid; c < C; c += nthr()) {
       float f[8];
       bf16x8_to_f32(xr[c], f);
 #pragma unroll
@@ -256,12 +260,12 @@ __device__ void pre_expert_norm_rows(const DecodeArgs& a, const __nv_bfloat16* x
     __syncthreads();
     float tot = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) tot += red[w];
+    for (int w = 0; w < nwarps(); ++w) tot += red[w];
     const float inv = 1.0f / sqrtf(tot / (float)a.H + a.eps);
     const uint4* gs = reinterpret_cast<const uint4*>(a.norm_w);
     uint4* dst = reinterpret_cast<uint4*>(a.xn + (size_t)t * a.H);
 #pragma unroll 1
-    for (int c = tid; c < C; c += kThreads) {
+    for (int c = tid; c < C; c += nthr()) {
       float f[8], w[8];
       bf16x8_to_f32(xr[c], f);
       bf16x8_to_f32(__ldg(gs + c), w);
@@ -288,7 +292,7 @@ __device__ void quant_token_rows(const DecodeArgs& a, const __nv_bfloat16* src) 
   const int t = (int)gridDim.x - 1 - (int)blockIdx.x;
   if (t < 0 || t >= a.N) return;
   const int G = a.H / 128;
-  for (int g = warp; g < G; g += kWarps) {
+  for (int g = warp; g < G; g += nwarps()) {
     const uint2 raw = *reinterpret_cast<const uint2*>(src + (size_t)t * a.H + g * 128 + lane * 4);
     float f[4];
     f[0] = __uint_as_float(raw.x << 16);
@@ -315,7 +319,7 @@ __device__ void half_token_rows(const DecodeArgs& a, const __nv_bfloat16* src) {
   if (t < 0 || t >= a.N) return;
   const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)t * a.H);
   uint4* d4 = reinterpret_cast<uint4*>(a.xh + (size_t)t * a.H);
-  for (int c = threadIdx.x; c < a.H / 8; c += kThreads) {
+  for (int c = threadIdx.x; c < a.H / 8; c += nthr()) {
     uint4 v = s4[c];
     uint32_t* w = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
@@ -471,8 +475,8 @@ __device__ void route_active_split(const DecodeArgs& a, Routing& rt, uint8_t* sc
   unsigned long long* k_s = reinterpret_cast<unsigned long long*>(scratch + 128);
   float* p_s = reinterpret_cast<float*>(k_s + (size_t)N * R);             // [N][R]
   float* cb_s = p_s + (size_t)N * R;                                        // [N][R]
-  if (warp == kWarps - 1) rt.bits[lane] = 0u;
-  for (int t = warp; t < N; t += kWarps) {
+  if (warp == nwarps() - 1) rt.bits[lane] = 0u;
+  for (int t = warp; t < N; t += nwarps()) {
     const size_t o = (size_t)t * R;
     if (R <= 128) token_topk<4>(a, t, p_s + o, cb_s + o, k_s + o, idx_s + t * K, rt);
     else token_topk<8>(a, t, p_s + o, cb_s + o, k_s + o, idx_s + t * K, rt);
@@ -595,7 +599,7 @@ __device__ void route_block(const DecodeArgs& a, Routing& rt, uint8_t* scratch) 
   float* cb_s = p_s + (size_t)N * R;                                        // [N][R]
   if (te > 32)
     for (int i = tid; i < nch * E; i += blockDim.x) chunk_s[i] = 0;
-  for (int t = warp; t < N; t += kWarps) {
+  for (int t = warp; t < N; t += nwarps()) {
     const size_t o = (size_t)t * R;
     if (R <= 128) token_topk<4>(a, t, p_s + o, cb_s + o, k_s + o, idx_s + t * K, rt);
     else if (R <= 256) token_topk<8>(a, t, p_s + o, cb_s + o, k_s + o, idx_s + t * K, rt);
@@ -607,7 +611,7 @@ __device__ void route_block(const DecodeArgs& a, Routing& rt, uint8_t* scratch) 
   // warp sorts, else ahead of it)
   if (R <= 256) {
     const int w0 = te <= 32 ? 1 : 0;
-    for (int t = warp - w0; t >= 0 && t < N; t += kWarps - w0)
+    for (int t = warp - w0; t >= 0 && t < N; t += nwarps() - w0)
       token_weights(a, t, p_s + (size_t)t * R, idx_s + t * K, rt);
   }
   if (te <= 32) {
@@ -657,7 +661,7 @@ __device__ void route_block(const DecodeArgs& a, Routing& rt, uint8_t* scratch) 
       }
   } else {
     // ranks inside each chunk, and the chunk's count of every expert (its group's last lane)
-    for (int j0 = 0; j0 < te; j0 += kThreads) {
+    for (int j0 = 0; j0 < te; j0 += nthr()) {
       const int j = j0 + tid;
       const uint32_t e = j < te ? idx_s[j] : 0xFFFFFFFFu;
       const bool real = j < te && (int)e < E;
@@ -669,7 +673,7 @@ __device__ void route_block(const DecodeArgs& a, Routing& rt, uint8_t* scratch) 
     // per expert: rows (sum over chunks), first row and slot (block scans), each chunk's first
     // row
     uint32_t carry_rows = 0, carry_slots = 0;
-    for (int e0 = 0; e0 < E; e0 += kThreads) {
+    for (int e0 = 0; e0 < E; e0 += nthr()) {
       const int e = e0 + tid;
       uint32_t tot = 0;
       if (e < E)
@@ -702,7 +706,7 @@ __device__ void route_block(const DecodeArgs& a, Routing& rt, uint8_t* scratch) 
       rt.rows = (int)carry_rows;
     }
     __syncthreads();
-    for (int j = tid; j < te; j += kThreads) {
+    for (int j = tid; j < te; j += nthr()) {
       const uint32_t e = idx_s[j];
       if ((int)e >= E) {
         rt.pair_row[j] = kNoRow16;
@@ -933,7 +937,7 @@ __device__ __forceinline__ int slot_rows(const DecodeArgs& a, const Routing& m, 
 // swizzle), and the MMA multiplies f16 x f16 with the routed input (and the SwiGLU intermediate)
 // in f16; scale2 multiplies each run's partial sums when it is drained.
 template <bool FP8, bool NV>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(NV ? kThreads + 32 * kConvWarps : kThreads, 1)
     decode_forward_kernel(const __grid_constant__ CUtensorMap tm_wg,
                           const __grid_constant__ CUtensorMap tm_wu,
                           const __grid_constant__ CUtensorMap tm_sg,
@@ -951,7 +955,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bars[3 * kMaxStages + 8];
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(16) float stage_rows[16 * kStageLd];   // drain staging, 16 rows x 64
-  __shared__ float red_s[kDecodeMaxTokens * kWarps];           // router block reductions
+  __shared__ float red_s[kDecodeMaxTokens * kMaxWarps];        // router block reductions
   __shared__ float hsc_s[FP8 ? 2 : 1][16 * kMaxHGroups];       // E4M3: the intermediate's scales
   // 1024-byte alignment for the 128-byte swizzle atoms. Layout: token boxes of the stages, two
   // buffers of the down-projection A operand, the weight ring (the A descriptors' rows 16..127
@@ -1565,6 +1569,7 @@ cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, 
                                    (a.R <= 256 ? 8 + (size_t)a.N * a.R * 16 : 0);
   if (scratch > (size_t)pl.stages * (kTokBytes + kWBytes)) return cudaErrorInvalidValue;
   const size_t sm = (size_t)fixed + (size_t)pl.stages * per_stage;
+  const int nthreads = a.nv ? kThreads + 32 * kConvWarps : kThreads;
   auto kern = a.fp8 ? decode_forward_kernel<true, false>
                     : (a.nv ? decode_forward_kernel<false, true> : decode_forward_kernel<false, false>);
   cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(kern), sm);
@@ -1581,7 +1586,7 @@ cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, 
     const size_t key = sm * 4 + (a.fp8 ? 1 : 0) + (a.nv ? 2 : 0);
     if (!ok.count({dev, key})) {
       int per_sm = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, sm);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, nthreads, sm);
       if (e != cudaSuccess) return e;
       if (per_sm < 1) return cudaErrorInvalidConfiguration;
       ok.insert({dev, key});
@@ -1589,7 +1594,7 @@ cudaError_t launch_decode_forward(const DecodeArgs& a, const CUtensorMap* maps, 
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sm_count());
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(nthreads);
   cfg.dynamicSmemBytes = sm;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
