@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();   // (launched as a programmatic dependent: the previous kernel's results)
 
   const int num_m = (int)g.hdr->num_mtiles;
   const int total = num_m * g.n_tiles;
@@ -429,8 +430,7 @@ cudaError_t launch_t(const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
   const int max_tiles = g.max_mtiles * g.n_tiles;
   int grid = max_tiles < num_sms ? max_tiles : num_sms;
   if (grid < 1) grid = 1;
-  kern<<<grid, kThreads, kSmemBytes, st>>>(a, b0, b1, g);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(grid), dim3(kThreads), kSmemBytes, st, a, b0, b1, g);
 }
 
 }  // namespace

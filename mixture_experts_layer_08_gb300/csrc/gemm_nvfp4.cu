@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();   // (launched as a programmatic dependent: the previous kernel's results)
   const int total = (int)g.hdr->num_mtiles * g.n_tiles;
 
   if (warp == 0 && lane == 0) {
@@ -305,8 +306,8 @@ cudaError_t launch_nv(const CUtensorMap maps[5], const NvGemmArgs& g, int num_sm
   const int max_tiles = g.max_mtiles * g.n_tiles;
   int grid = max_tiles < num_sms ? max_tiles : num_sms;
   if (grid < 1) grid = 1;
-  kern<<<grid, kNvThreads, C::kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], g);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(grid), dim3(kNvThreads), C::kSmemBytes, st, maps[0],
+                          maps[1], maps[2], maps[3], maps[4], g);
 }
 
 }  // namespace

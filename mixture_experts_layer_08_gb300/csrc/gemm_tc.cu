@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();   // (launched as a programmatic dependent: the previous kernel's results)
 
   const int tot0 = problem_mtiles(g.p[0]) * g.p[0].n_tiles;
   const int total = tot0 + (g.nprob > 1 ? problem_mtiles(g.p[1]) * g.p[1].n_tiles : 0);
@@ -292,9 +293,8 @@ cudaError_t launch_t(const CUtensorMap maps[2][3], const GemmArgs& g, int num_sm
   int grid = max_tiles < num_sms ? max_tiles : num_sms;
   if (grid < 1) grid = 1;
   const int j = g.nprob > 1 ? 1 : 0;   // unused maps of a one-problem launch repeat problem 0's
-  kern<<<grid, kThreads, C::kSmemBytes, st>>>(maps[0][0], maps[0][1], maps[0][2], maps[j][0],
-                                              maps[j][1], maps[j][2], g);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, st, maps[0][0],
+                          maps[0][1], maps[0][2], maps[j][0], maps[j][1], maps[j][2], g);
 }
 
 }  // namespace

@@ -180,6 +180,7 @@ constexpr int kSortBlock = 1024;
 // Per block of 1024 pairs: per-expert counts and each pair's rank among the block's earlier
 // pairs of the same expert.
 __global__ void __launch_bounds__(kSortBlock) sort_count_kernel(SortArgs s) {
+  pdl_wait();   // the routing (or count) results
   extern __shared__ uint32_t wcnt[];                 // [32 warps][E]
   const int E = s.E;
   const int j = blockIdx.x * kSortBlock + threadIdx.x;
@@ -209,6 +210,7 @@ __global__ void __launch_bounds__(kSortBlock) sort_count_kernel(SortArgs s) {
 
 // One block: expert totals, row offsets, per-block bases (in place), m-tile list, active list.
 __global__ void __launch_bounds__(1024) sort_scan_kernel(SortArgs s, int nblk) {
+  pdl_wait();   // the counts
   __shared__ uint32_t scan_s[40];
   const int E = s.E;
   uint32_t run_off = 0, run_act = 0, run_tiles = 0;
@@ -259,6 +261,7 @@ __global__ void __launch_bounds__(1024) sort_scan_kernel(SortArgs s, int nblk) {
 __global__ void __launch_bounds__(256) sort_scatter_kernel(SortArgs s, const __nv_bfloat16* x,
                                                            int H, __nv_bfloat16* xp,
                                                            uint8_t* xq, float* xsc) {
+  pdl_wait();   // the counts and offsets
   const int lane = threadIdx.x & 31;
   const int j = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (j >= s.te) return;
@@ -477,9 +480,15 @@ cudaError_t launch_sort(const SortArgs& s, const __nv_bfloat16* x, int H, __nv_b
     cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(sort_count_kernel), sm);
     if (e != cudaSuccess) return e;
   }
-  sort_count_kernel<<<nblk, kSortBlock, sm, st>>>(s);
-  sort_scan_kernel<<<1, 1024, 0, st>>>(s, nblk);
-  sort_scatter_kernel<<<(s.te + 7) / 8, 256, 0, st>>>(s, x, H, xp, xq, xs);
+  // programmatic dependents: each kernel launches as its predecessor drains and waits for
+  // its results (pdl_wait) before reading them
+  cudaError_t e = launch_dependent(sort_count_kernel, dim3(nblk), dim3(kSortBlock), sm, st, s);
+  if (e != cudaSuccess) return e;
+  e = launch_dependent(sort_scan_kernel, dim3(1), dim3(1024), 0, st, s, nblk);
+  if (e != cudaSuccess) return e;
+  e = launch_dependent(sort_scatter_kernel, dim3((s.te + 7) / 8), dim3(256), 0, st, s, x, H, xp,
+                       xq, xs);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
