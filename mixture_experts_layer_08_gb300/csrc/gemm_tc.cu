@@ -18,8 +18,10 @@
 //   warp 1      allocates TMEM (2 x BN fp32 columns: two accumulators), one lane issues
 //               tcgen05.mma (M=128, N=BN, K=16) x 4 per stage and commits stage releases.
 //   warps 2-5   epilogue: tcgen05.ld of the finished accumulator (warp w reads TMEM lanes
-//               32*(w%4)...), fused activation, masked stores; releases the accumulator so the
-//               MMA of the next tile overlaps this epilogue.
+//               32*(w%4)...), fused activation, masked stores (the down projection's bf16
+//               rows staged in shared memory so that every store instruction writes whole
+//               128-byte lines); releases the accumulator so the MMA of the next tile overlaps
+//               this epilogue.
 // Tiles are (m-tile, n-tile) pairs, m-tiles taken from the device-built list of 128-row
 // windows of each expert; n is the fastest index so the CTAs working at the same time share
 // A rows and the same expert's weights in L2.
@@ -33,6 +35,8 @@ constexpr int kThreads = 192;
 constexpr int kBM = 128;
 constexpr int kBK = 64;                 // bf16 elements per 128-byte swizzle row
 constexpr int kATileBytes = kBM * 128;  // 16 KB
+constexpr int kEpiWarps = 4;
+constexpr int kStageRowsBytes = 32 * 128;   // one epilogue warp: 32 rows x 64 bf16 outputs
 
 template <int BN>
 struct Cfg {
@@ -40,8 +44,15 @@ struct Cfg {
   static constexpr int kBTileBytes = BN * 128;
   static constexpr int kStageBytes = kATileBytes + kBTileBytes;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024 + 256;
 };
+
+// Ring, barrier block (256 B), the epilogue warps' staging rows (bf16 store only), alignment
+// slack.
+template <int BN, int MODE>
+constexpr size_t smem_bytes() {
+  return (size_t)Cfg<BN>::kStages * Cfg<BN>::kStageBytes + 256 +
+         (MODE == kGemmStoreBF16 ? kEpiWarps * kStageRowsBytes : 0) + 1024;
+}
 
 // Per-tile view of the problem it belongs to (selected without dynamic param indexing).
 struct Tile {
@@ -203,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ epilogue
     const int q = warp & 3;                  // TMEM lane quadrant of this warp
     const int r_local = q * 32 + lane;
+    uint8_t* stg = smem + S * C::kStageBytes + 256 + (warp - 2) * kStageRowsBytes;
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       Tile t;
@@ -235,23 +247,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if (MODE == kGemmStoreBF16) {
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(t.out) + (size_t)row * t.ldo + t.n * BN;
+        // 64 output columns at a time: this thread packs its row's 128 bytes into the warp's
+        // staging rows (16-byte chunks XOR-swizzled by row), then the warp writes 4 rows of
+        // 128 bytes per store instruction, rows past the m-tile's end skipped.
+        constexpr int out_cols = BN;
+        __nv_bfloat16* obase = static_cast<__nv_bfloat16*>(t.out) + t.n * out_cols;
+        uint8_t* my_row = stg + lane * 128;
+        const int jj = lane & 7;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
-          tmem_ld32(taddr + c, v);
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+        for (int c = 0; c < out_cols; c += 64) {
+          uint4 pk[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint4 o;
-              o.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
-              o.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
-              o.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
-              o.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
-              dst[j] = o;
+          for (int h = 0; h < 2; ++h) {
+            float gv[32];
+            tmem_ld32(taddr + c + 32 * h, gv);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              pk[4 * h + v].x = pack_bf16x2(gv[8 * v + 0], gv[8 * v + 1]);
+              pk[4 * h + v].y = pack_bf16x2(gv[8 * v + 2], gv[8 * v + 3]);
+              pk[4 * h + v].z = pack_bf16x2(gv[8 * v + 4], gv[8 * v + 5]);
+              pk[4 * h + v].w = pack_bf16x2(gv[8 * v + 6], gv[8 * v + 7]);
             }
           }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(my_row + ((j ^ (lane & 7)) << 4)) = pk[j];
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + (lane >> 3);
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((jj ^ (rr & 7)) << 4));
+            const int grow = t.row0 + q * 32 + rr;
+            if (grow < t.row1)
+              *reinterpret_cast<uint4*>(obase + (size_t)grow * t.ldo + c + 8 * jj) = val;
+          }
+          __syncwarp();
         }
       } else {
         float* orow = static_cast<float*>(t.out) + (size_t)row * t.ldo;
@@ -286,14 +316,14 @@ cudaError_t launch_t(const CUtensorMap maps[2][3], const GemmArgs& g, int num_sm
                      cudaStream_t st) {
   using C = Cfg<BN>;
   auto kern = gemm_bf16_kernel<BN, MODE>;
-  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(kern), C::kSmemBytes);
+  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(kern), smem_bytes<BN, MODE>());
   if (e != cudaSuccess) return e;
   int max_tiles = g.p[0].max_mtiles * g.p[0].n_tiles;
   if (g.nprob > 1) max_tiles += g.p[1].max_mtiles * g.p[1].n_tiles;
   int grid = max_tiles < num_sms ? max_tiles : num_sms;
   if (grid < 1) grid = 1;
   const int j = g.nprob > 1 ? 1 : 0;   // unused maps of a one-problem launch repeat problem 0's
-  return launch_dependent(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, st, maps[0][0],
+  return launch_dependent(kern, dim3(grid), dim3(kThreads), smem_bytes<BN, MODE>(), st, maps[0][0],
                           maps[0][1], maps[0][2], maps[j][0], maps[j][1], maps[j][2], g);
 }
 
