@@ -385,4 +385,37 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Stores CHUNKS 16-byte chunks (8: 128 bytes, 4: 64 bytes) of each of the warp's 32 rows,
+// lane l holding row l's chunks in pk, through the warp's staging area stg (32 * CHUNKS * 16
+// bytes of shared memory): the rows are written there with their chunks XOR-swizzled (no bank
+// conflicts either way), then every store instruction writes 32 / CHUNKS whole row segments.
+// Row r goes to gcol + r * ld_bytes; rows r >= nvalid are skipped.
+template <int CHUNKS>
+__device__ __forceinline__ int staged_swizzle(int r) {
+  return CHUNKS == 8 ? (r & 7) : ((r >> 1) & 3);
+}
+
+template <int CHUNKS>
+__device__ __forceinline__ void warp_store_rows(uint8_t* stg, const uint4 (&pk)[CHUNKS],
+                                                uint8_t* gcol, size_t ld_bytes, int nvalid) {
+  static_assert(CHUNKS == 8 || CHUNKS == 4, "row segment of 64 or 128 bytes");
+  constexpr int kRowBytes = CHUNKS * 16;
+  constexpr int kRowsPerStore = 32 / CHUNKS;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < CHUNKS; ++j)
+    *reinterpret_cast<uint4*>(stg + lane * kRowBytes + ((j ^ staged_swizzle<CHUNKS>(lane)) << 4)) =
+        pk[j];
+  __syncwarp();
+  const int jj = lane % CHUNKS;
+#pragma unroll
+  for (int i = 0; i < CHUNKS; ++i) {
+    const int r = i * kRowsPerStore + lane / CHUNKS;
+    const uint4 v = *reinterpret_cast<const uint4*>(
+        stg + r * kRowBytes + ((jj ^ staged_swizzle<CHUNKS>(r)) << 4));
+    if (r < nvalid) *reinterpret_cast<uint4*>(gcol + (size_t)r * ld_bytes + jj * 16) = v;
+  }
+  __syncwarp();
+}
+
 }  // namespace moe

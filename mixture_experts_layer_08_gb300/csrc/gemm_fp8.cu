@@ -54,9 +54,15 @@ constexpr int kScKb = 8;
 constexpr int kSaFloats = kScKb * kBM;
 constexpr int kSbFloats = 2 * kScKb * 2;
 constexpr int kScaleBufFloats = kSaFloats + kSbFloats;
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * 2 * 128 * 4 +
-                              (size_t)2 * kScaleBufFloats * 4;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+constexpr size_t kSmemBase = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * 2 * 128 * 4 +
+                             (size_t)2 * kScaleBufFloats * 4;
+constexpr int kStageRowBytes = 32 * 64;     // down: one promotion warp's staging rows
+// (the down projection adds the promotion warps' staging rows)
+template <int MODE>
+constexpr size_t smem_bytes() {
+  return kSmemBase + (MODE == 1 ? (size_t)kPromoWarps * kStageRowBytes : 0);
+}
+static_assert(smem_bytes<1>() <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ void setmaxnreg_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsPromo));
@@ -141,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* amax_s = reinterpret_cast<float*>(smem + kStages * kStageBytes + 256);  // [2][128]
   uint32_t* seq_s = reinterpret_cast<uint32_t*>(amax_s + 2 * 128);                // [2][128]
   float* scale_s = reinterpret_cast<float*>(seq_s + 2 * 128);                     // [2][buf]
+  uint8_t* stg_all = reinterpret_cast<uint8_t*>(scale_s + 2 * kScaleBufFloats);    // down only
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WsHeader* hdr = g.status;
@@ -379,17 +386,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (half == 0) g.out_scales[(size_t)n * g.out_scale_stride + row] = scale;
         }
-      } else if (valid) {
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo +
-                              n * kBN + half * 128;
+      } else {
+        // 32 columns at a time through the warp's staging rows: 64-byte row segments, 8 rows
+        // per store instruction
+        uint8_t* stg = stg_all + (warp - 4) * kStageRowBytes;
+        uint8_t* obase = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(g.out) +
+                                                    (size_t)(t.y + q * 32) * g.ldo + n * kBN +
+                                                    half * 128);
 #pragma unroll
-        for (int v8 = 0; v8 < 16; ++v8) {
-          uint4 o;
-          o.x = pack_bf16x2(acc[8 * v8 + 0], acc[8 * v8 + 1]);
-          o.y = pack_bf16x2(acc[8 * v8 + 2], acc[8 * v8 + 3]);
-          o.z = pack_bf16x2(acc[8 * v8 + 4], acc[8 * v8 + 5]);
-          o.w = pack_bf16x2(acc[8 * v8 + 6], acc[8 * v8 + 7]);
-          reinterpret_cast<uint4*>(orow)[v8] = o;
+        for (int c = 0; c < 128; c += 32) {
+          uint4 pk[4];
+#pragma unroll
+          for (int v8 = 0; v8 < 4; ++v8) {
+            pk[v8].x = pack_bf16x2(acc[c + 8 * v8 + 0], acc[c + 8 * v8 + 1]);
+            pk[v8].y = pack_bf16x2(acc[c + 8 * v8 + 2], acc[c + 8 * v8 + 3]);
+            pk[v8].z = pack_bf16x2(acc[c + 8 * v8 + 4], acc[c + 8 * v8 + 5]);
+            pk[v8].w = pack_bf16x2(acc[c + 8 * v8 + 6], acc[c + 8 * v8 + 7]);
+          }
+          warp_store_rows<4>(stg, pk, obase + c * 2, (size_t)g.ldo * 2, t.z - t.y - q * 32);
         }
       }
     }
@@ -425,12 +439,12 @@ cudaError_t launch_t(const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
   auto kern = gemm_fp8_kernel<MODE>;
   cudaError_t e = check_launch_regs<MODE>();
   if (e != cudaSuccess) return e;
-  e = ensure_dyn_smem(reinterpret_cast<const void*>(kern), kSmemBytes);
+  e = ensure_dyn_smem(reinterpret_cast<const void*>(kern), smem_bytes<MODE>());
   if (e != cudaSuccess) return e;
   const int max_tiles = g.max_mtiles * g.n_tiles;
   int grid = max_tiles < num_sms ? max_tiles : num_sms;
   if (grid < 1) grid = 1;
-  return launch_dependent(kern, dim3(grid), dim3(kThreads), kSmemBytes, st, a, b0, b1, g);
+  return launch_dependent(kern, dim3(grid), dim3(kThreads), smem_bytes<MODE>(), st, a, b0, b1, g);
 }
 
 }  // namespace

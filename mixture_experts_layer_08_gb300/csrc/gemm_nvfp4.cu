@@ -56,9 +56,17 @@ struct NvCfg {
   static constexpr int kCTile = BN * 32;    // packed codes, 64 elements per row
   static constexpr int kSTile = BN * 16;    // scale codes, 16 groups per row
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr size_t kSmemBytes =
-      (size_t)kStages * (kNvATile + kCTile + kSTile) + (size_t)kBStages * kBTile + 1024 + 256;
+  static constexpr size_t kRingBytes =
+      (size_t)kStages * (kNvATile + kCTile + kSTile) + (size_t)kBStages * kBTile;
 };
+
+constexpr int kNvStageRows = 32 * 128;   // bf16 store: one epilogue warp's staging rows
+
+// Rings, barrier block (256 B), the down projection's staging rows, alignment slack.
+template <int BN, int MODE>
+constexpr size_t nv_smem_bytes() {
+  return NvCfg<BN>::kRingBytes + 256 + (MODE == kGemmSwiGLU ? 0 : 4 * kNvStageRows) + 1024;
+}
 
 struct NvTile {
   int e, row0, row1, n;
@@ -100,6 +108,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint8_t* stg_all = smem + C::kRingBytes + 256;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WsHeader* hdr = g.status;
@@ -239,23 +248,27 @@ __global__ void __launch_bounds__(kNvThreads, 1)
           }
         }
       } else {
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + t.n * BN;
+        // 64 output columns at a time through the warp's staging rows: whole 128-byte row
+        // segments per store instruction
+        uint8_t* stg = stg_all + (warp - 2) * kNvStageRows;
+        uint8_t* obase = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(g.out) +
+                                                    (size_t)(t.row0 + q * 32) * g.ldo + t.n * BN);
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
-          tmem_ld32(taddr + c, v);
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+        for (int c = 0; c < BN; c += 64) {
+          uint4 pk[8];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float v[32];
+            tmem_ld32(taddr + c + 32 * h, v);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              uint4 o;
-              o.x = pack_bf16x2(v[8 * j + 0] * s2a, v[8 * j + 1] * s2a);
-              o.y = pack_bf16x2(v[8 * j + 2] * s2a, v[8 * j + 3] * s2a);
-              o.z = pack_bf16x2(v[8 * j + 4] * s2a, v[8 * j + 5] * s2a);
-              o.w = pack_bf16x2(v[8 * j + 6] * s2a, v[8 * j + 7] * s2a);
-              dst[j] = o;
+              pk[4 * h + j].x = pack_bf16x2(v[8 * j + 0] * s2a, v[8 * j + 1] * s2a);
+              pk[4 * h + j].y = pack_bf16x2(v[8 * j + 2] * s2a, v[8 * j + 3] * s2a);
+              pk[4 * h + j].z = pack_bf16x2(v[8 * j + 4] * s2a, v[8 * j + 5] * s2a);
+              pk[4 * h + j].w = pack_bf16x2(v[8 * j + 6] * s2a, v[8 * j + 7] * s2a);
             }
           }
+          warp_store_rows<8>(stg, pk, obase + c * 2, (size_t)g.ldo * 2, t.row1 - t.row0 - q * 32);
         }
       }
       tc_fence_before();
@@ -301,12 +314,12 @@ cudaError_t launch_nv(const CUtensorMap maps[5], const NvGemmArgs& g, int num_sm
                       cudaStream_t st) {
   using C = NvCfg<BN>;
   auto kern = gemm_nvfp4_kernel<BN, MODE>;
-  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(kern), C::kSmemBytes);
+  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(kern), nv_smem_bytes<BN, MODE>());
   if (e != cudaSuccess) return e;
   const int max_tiles = g.max_mtiles * g.n_tiles;
   int grid = max_tiles < num_sms ? max_tiles : num_sms;
   if (grid < 1) grid = 1;
-  return launch_dependent(kern, dim3(grid), dim3(kNvThreads), C::kSmemBytes, st, maps[0],
+  return launch_dependent(kern, dim3(grid), dim3(kNvThreads), nv_smem_bytes<BN, MODE>(), st, maps[0],
                           maps[1], maps[2], maps[3], maps[4], g);
 }
 

@@ -247,41 +247,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if (MODE == kGemmStoreBF16) {
-        // 64 output columns at a time: this thread packs its row's 128 bytes into the warp's
-        // staging rows (16-byte chunks XOR-swizzled by row), then the warp writes 4 rows of
-        // 128 bytes per store instruction, rows past the m-tile's end skipped.
-        constexpr int out_cols = BN;
-        __nv_bfloat16* obase = static_cast<__nv_bfloat16*>(t.out) + t.n * out_cols;
-        uint8_t* my_row = stg + lane * 128;
-        const int jj = lane & 7;
+        // 64 output columns at a time through the warp's staging rows: whole 128-byte row
+        // segments per store instruction
+        uint8_t* obase = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(t.out) +
+                                                    (size_t)(t.row0 + q * 32) * t.ldo + t.n * BN);
 #pragma unroll 1
-        for (int c = 0; c < out_cols; c += 64) {
+        for (int c = 0; c < BN; c += 64) {
           uint4 pk[8];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            float gv[32];
-            tmem_ld32(taddr + c + 32 * h, gv);
+            float v[32];
+            tmem_ld32(taddr + c + 32 * h, v);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              pk[4 * h + v].x = pack_bf16x2(gv[8 * v + 0], gv[8 * v + 1]);
-              pk[4 * h + v].y = pack_bf16x2(gv[8 * v + 2], gv[8 * v + 3]);
-              pk[4 * h + v].z = pack_bf16x2(gv[8 * v + 4], gv[8 * v + 5]);
-              pk[4 * h + v].w = pack_bf16x2(gv[8 * v + 6], gv[8 * v + 7]);
+            for (int j = 0; j < 4; ++j) {
+              pk[4 * h + j].x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+              pk[4 * h + j].y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+              pk[4 * h + j].z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+              pk[4 * h + j].w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
             }
           }
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(my_row + ((j ^ (lane & 7)) << 4)) = pk[j];
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rr = 4 * i + (lane >> 3);
-            const uint4 val = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((jj ^ (rr & 7)) << 4));
-            const int grow = t.row0 + q * 32 + rr;
-            if (grow < t.row1)
-              *reinterpret_cast<uint4*>(obase + (size_t)grow * t.ldo + c + 8 * jj) = val;
-          }
-          __syncwarp();
+          warp_store_rows<8>(stg, pk, obase + c * 2, (size_t)t.ldo * 2, t.row1 - t.row0 - q * 32);
         }
       } else {
         float* orow = static_cast<float*>(t.out) + (size_t)row * t.ldo;
