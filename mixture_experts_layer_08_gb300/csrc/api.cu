@@ -110,7 +110,7 @@ Layout make_layout(const moe_config_t* c) {
   if (L.path == MOE_PATH_GROUPED) {
     sz[R_BLK] = (size_t)L.nblk * E * 4;
     sz[R_LRANK] = te * 4;
-    sz[R_TILES] = (size_t)L.max_mtiles * 16;
+    sz[R_TILES] = (size_t)3 * L.max_mtiles * 16;   // the list + two scratch lists
     if (c->weight_dtype == MOE_W_FP8_E4M3_B128) {
       sz[R_XQT] = N * H;                 // E4M3 codes of each token row
       sz[R_XST] = (H / 128) * N * 4;     // and their scales
@@ -345,6 +345,8 @@ moe_status_t run_routing(const moe_config_t* c, const moe_weights_t* w, const vo
   sa.sorted_pairs = P.at<uint32_t>(R_SPAIRS);
   sa.active = P.at<uint32_t>(R_ACTIVE);
   sa.tiles = P.at<int4>(R_TILES);
+  sa.tiles_tmp = sa.tiles ? sa.tiles + L.max_mtiles : nullptr;
+  sa.max_mtiles = L.max_mtiles;
   sa.xq_tok = P.at<uint8_t>(R_XQT);
   sa.xs_tok = P.at<float>(R_XST);
   sa.xp_f16 = c->weight_dtype == MOE_W_NVFP4;

@@ -55,6 +55,8 @@ struct SortArgs {
   uint32_t* sorted_pairs;          // [te]
   uint32_t* active;                // [E] experts with rows, ascending
   int4* tiles;                     // [max m-tiles] (expert, row0, row1, 0)
+  int4* tiles_tmp;                 // [2 * max m-tiles] scratch for ordering the list
+  int max_mtiles;
   const uint8_t* xq_tok;           // FP8 experts: E4M3 codes of each token row [N, H]
   const float* xs_tok;             // and their 1x128 scales [H/128, N]
   int xp_f16;                      // gather x rows as f16 (NVFP4 experts) instead of bf16

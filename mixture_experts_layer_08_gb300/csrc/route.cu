@@ -208,12 +208,27 @@ __global__ void __launch_bounds__(kSortBlock) sort_count_kernel(SortArgs s) {
   if (j < s.te) s.local_rank[j] = real ? wcnt[wid * E + e] + rank_w : kNoRow;
 }
 
-// One block: expert totals, row offsets, per-block bases (in place), m-tile list, active list.
+// Number of the n one-tile slots that sit before position p of a list of T m-tiles, the j-th
+// one-tile slot being at floor((2j + 1) * T / (2n)) (n <= T, so the slots are distinct).
+__device__ __forceinline__ uint32_t slots_before(uint32_t p, uint32_t n, uint32_t T) {
+  const uint64_t a = 2ull * n * p;
+  if (a <= T) return 0;
+  const uint64_t l = (a + T - 1) / (2ull * T);
+  return l < n ? (uint32_t)l : n;
+}
+
+// Expert offsets, active experts, per-block row starts and the m-tile list. The list puts the
+// m-tiles of the experts with a single m-tile (whose weights are read from HBM for that one
+// tile) evenly among the m-tiles of the others (kept consecutive per expert, so their weight
+// tiles are reused from L2), so that every wave of the persistent GEMMs mixes HBM-bound and
+// tensor-bound tiles instead of meeting long runs of one kind.
 __global__ void __launch_bounds__(1024) sort_scan_kernel(SortArgs s, int nblk) {
   pdl_wait();   // the counts
   __shared__ uint32_t scan_s[40];
   const int E = s.E;
-  uint32_t run_off = 0, run_act = 0, run_tiles = 0;
+  int4* heavy = s.tiles_tmp;                   // m-tiles of experts with two or more
+  int4* single = s.tiles_tmp + s.max_mtiles;   // the one m-tile of each other expert
+  uint32_t run_off = 0, run_act = 0, run_heavy = 0, run_single = 0;
   for (int base = 0; base < E; base += blockDim.x) {
     int e = base + threadIdx.x;
     uint32_t c = 0;
@@ -225,9 +240,12 @@ __global__ void __launch_bounds__(1024) sort_scan_kernel(SortArgs s, int nblk) {
     uint32_t act = block_excl_scan(c > 0 ? 1u : 0u, scan_s, &scan_s[32]);
     uint32_t tot_a = scan_s[32];
     __syncthreads();
-    uint32_t nt = (c + 127) / 128;
-    uint32_t tstart = block_excl_scan(nt, scan_s, &scan_s[32]);
-    uint32_t tot_t = scan_s[32];
+    const uint32_t nt = (c + 127) / 128;
+    uint32_t hstart = block_excl_scan(nt > 1 ? nt : 0u, scan_s, &scan_s[32]);
+    uint32_t tot_h = scan_s[32];
+    __syncthreads();
+    uint32_t sidx = block_excl_scan(nt == 1 ? 1u : 0u, scan_s, &scan_s[32]);
+    uint32_t tot_s = scan_s[32];
     __syncthreads();
     if (e < E) {
       uint32_t o = run_off + off;
@@ -239,21 +257,34 @@ __global__ void __launch_bounds__(1024) sort_scan_kernel(SortArgs s, int nblk) {
         s.blk_counts[(size_t)b * E + e] = r;
         r += cb;
       }
-      for (uint32_t i = 0; i < nt; ++i) {
-        uint32_t r0 = o + 128 * i;
-        uint32_t r1 = min(o + c, r0 + 128);
-        s.tiles[run_tiles + tstart + i] = make_int4(e, (int)r0, (int)r1, 0);
+      if (nt == 1) {
+        single[run_single + sidx] = make_int4(e, (int)o, (int)(o + c), 0);
+      } else {
+        for (uint32_t i = 0; i < nt; ++i) {
+          uint32_t r0 = o + 128 * i;
+          uint32_t r1 = min(o + c, r0 + 128);
+          heavy[run_heavy + hstart + i] = make_int4(e, (int)r0, (int)r1, 0);
+        }
       }
     }
     run_off += tot_c;
     run_act += tot_a;
-    run_tiles += tot_t;
+    run_heavy += tot_h;
+    run_single += tot_s;
     __syncthreads();
+  }
+  // merge: position p holds one-tile slot j = slots_before(p) if the next position has one
+  // more slot before it, else the (p - slots_before(p))-th m-tile of the others
+  const uint32_t T = run_heavy + run_single;
+  for (uint32_t p = threadIdx.x; p < T; p += blockDim.x) {
+    const uint32_t lp = slots_before(p, run_single, T);
+    const uint32_t lq = slots_before(p + 1, run_single, T);
+    s.tiles[p] = lq > lp ? single[lp] : heavy[p - lp];
   }
   if (threadIdx.x == 0) {
     s.offsets[E] = run_off;
     s.hdr->num_active = run_act;
-    s.hdr->num_mtiles = run_tiles;
+    s.hdr->num_mtiles = T;
   }
 }
 
