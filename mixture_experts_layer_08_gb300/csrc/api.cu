@@ -597,7 +597,7 @@ moe_status_t run_grouped(const moe_config_t* c, const moe_weights_t* w, const vo
   ca.x = static_cast<const __nv_bfloat16*>(x);
   ca.pair_to_row = P.at<uint32_t>(R_P2R);
   ca.w = P.at<float>(R_W);
-  ca.zsum = P.at<float>(R_ZSUM);
+  ca.zsum = c->router_width > c->num_experts ? P.at<float>(R_ZSUM) : nullptr;
   ca.y = P.at<void>(R_Y);
   ca.y_is_f32 = 0;
   ca.shy = S > 0 ? P.at<void>(R_SHY) : nullptr;

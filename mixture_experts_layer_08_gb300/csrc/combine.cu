@@ -74,7 +74,9 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(CombineArgs a) {
   // Everything produced before the expert projections (routing, x) is read before waiting on
   // the previous kernel: it finished at least two launches back.
   float acc[8];
-  {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  if (a.zsum) {   // (null without identity experts: no x read)
     const float z = a.zsum[t];
     float xf[8];
 #pragma unroll

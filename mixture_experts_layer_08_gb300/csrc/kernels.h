@@ -166,7 +166,7 @@ struct CombineArgs {
   const __nv_bfloat16* x;
   const uint32_t* pair_to_row;
   const float* w;
-  const float* zsum;
+  const float* zsum;               // identity-expert weight per token; null without them
   const void* y;                   // [rows, H] bf16 (y_is_f32 = 0) or fp32; may be null
   int y_is_f32;
   const float* acc;                // [N,H] or null
