@@ -206,8 +206,13 @@ def fused_router(cfg, num_sms):
 
 def kernels_per_step(B, cfg, num_sms=152):
     """Kernels of this library one forward launches (memsets are not kernels)."""
-    decode = cfg.path == B.PATH_DECODE or (cfg.path == B.PATH_AUTO and cfg.num_tokens <= 16
-                                            and cfg.inter <= 1024 and cfg.shared_inter <= 1024)
+    per_weight = {0: 2.0, 1: 1.0}.get(cfg.weight_dtype, 0.5625)
+    touched = (min(cfg.num_experts, cfg.num_tokens * cfg.top_k) * 3.0 * cfg.inter * cfg.hidden
+               * per_weight + 3.0 * cfg.shared_inter * cfg.hidden * 2.0)
+    decode = cfg.path == B.PATH_DECODE or (
+        cfg.path == B.PATH_AUTO and cfg.num_tokens <= 16 and cfg.inter <= 1024
+        and cfg.shared_inter <= 1024 and (cfg.weight_dtype == 0 or cfg.hidden % 256 == 0)
+        and touched >= 8.0 * (1 << 20))
     if decode:   # router, top-K, sort, projections, combine (and any pre-expert norm): one kernel
         return 1
     # routing: the fused router (1) or router + top-K (2); then 3 sort, gate/up GEMM, down GEMM,

@@ -81,8 +81,10 @@ typedef enum {
 
 typedef enum {
   MOE_PATH_AUTO = 0,            /* decode chain for num_tokens <= 16 (inter and shared_inter
-                                   <= 1024; E4M3 and NVFP4 experts: hidden % 256 == 0), else
-                                   grouped */
+                                   <= 1024; E4M3 and NVFP4 experts: hidden % 256 == 0) when the
+                                   weights the batch may touch -- min(num_experts, num_tokens *
+                                   top_k) experts' three matrices plus the shared expert's --
+                                   come to at least 8 MiB; else grouped */
   MOE_PATH_DECODE = 1,          /* one cooperative kernel: routing, tcgen05 projections streaming
                                    each touched expert's weights once, combine (bf16, E4M3 or
                                    NVFP4 experts, num_tokens <= 16, inter and shared_inter <=

@@ -10,6 +10,7 @@
 // bytes needed and available; the FP32 accumulator sits at a 256-byte aligned offset).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <map>
@@ -39,11 +40,26 @@ struct Layout {
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
+// Weight bytes a forward may stream (every expert the batch can touch, and the shared
+// expert), below which the grouped chain's short launches beat the decode kernel's fixed cost
+// (its cross-block waits and run-once code: ~50 us for a few MB of weights, against ~36 us).
+constexpr double kDecodeMinWeightBytes = 8.0 * (1 << 20);
+
+double touched_weight_bytes(const moe_config_t* c) {
+  const double per_weight = c->weight_dtype == MOE_W_BF16            ? 2.0
+                            : c->weight_dtype == MOE_W_FP8_E4M3_B128 ? 1.0
+                                                                     : 0.5625;
+  const int experts = std::min(c->num_experts, c->num_tokens * c->top_k);
+  return (double)experts * 3.0 * c->inter * c->hidden * per_weight +
+         3.0 * c->shared_inter * c->hidden * 2.0;
+}
+
 int resolve_path(const moe_config_t* c) {
   if (c->path != MOE_PATH_AUTO) return c->path;
   const bool decode_ok = c->num_tokens <= kDecodeMaxTokens && c->inter <= 1024 &&
                          c->shared_inter <= 1024 &&
-                         (c->weight_dtype == MOE_W_BF16 || c->hidden % 256 == 0);
+                         (c->weight_dtype == MOE_W_BF16 || c->hidden % 256 == 0) &&
+                         touched_weight_bytes(c) >= kDecodeMinWeightBytes;
   return decode_ok ? MOE_PATH_DECODE : MOE_PATH_GROUPED;
 }
 

@@ -59,6 +59,8 @@ def test_launches_per_forward(B):
     b = _bench()
     n = lambda shape, path=B.PATH_AUTO: b.kernels_per_step(B, B.make_config(shape, True, path))
     assert n(I.DECODE) == 1                      # one cooperative kernel
+    assert n(I.TINY) == 8                        # 1.6 MB of weights: the grouped chain
+    assert n(I.TINY, B.PATH_DECODE) == 1
     assert n(I.DECODE_PRENORM) == 1              # the norm runs in its phase 0
     assert n(I.PREFILL) == 7                     # fused router, 3 sort, 2 GEMMs, combine
     assert n(I.PREFILL.with_(pre_expert_norm=True)) == 8
