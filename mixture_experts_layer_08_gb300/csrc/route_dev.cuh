@@ -31,44 +31,51 @@ __device__ void route_token_warp(const float* L, const float* logit_bias, const 
                                  const uint32_t* forced, float* p, float* sel, uint32_t* idx_out,
                                  float* w_out, float* zsum_out, uint32_t* idx_smem) {
   const int lane = threadIdx.x & 31;
+  const bool biased = selection_biased(scoring) && corr_bias;
   float mx = -INFINITY;
   for (int r0 = 0; r0 < R; r0 += 128) {
-    float v[4];   // four loads in flight before any is used
+    // four columns' logits and biases in flight before any is used
+    float v[4], lb[4], cb[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int r = r0 + u * 32 + lane;
       v[u] = r < R ? __ldcg(L + r) : 0.0f;
+      lb[u] = (r < R && logit_bias) ? logit_bias[r] : 0.0f;
+      cb[u] = (r < R && biased) ? corr_bias[r] : 0.0f;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int r = r0 + u * 32 + lane;
       if (r < R) {
-        const float x = v[u] + (logit_bias ? logit_bias[r] : 0.0f);
+        const float x = v[u] + lb[u];
         p[r] = x;
+        sel[r] = cb[u];   // the selection bias; the score is added below
         mx = fmaxf(mx, x);
       }
     }
   }
-  const bool biased = selection_biased(scoring) && corr_bias;
   if (scoring == MOE_SCORING_SIGMOID_BIAS) {
+#pragma unroll 4
     for (int r = lane; r < R; r += 32) {
       const float pr = sigmoid_score(p[r]);
       p[r] = pr;
-      sel[r] = pr + (biased ? corr_bias[r] : 0.0f);
+      sel[r] = pr + sel[r];
     }
   } else {
     mx = warp_max(mx);
     float den = 0.0f;
+#pragma unroll 4
     for (int r = lane; r < R; r += 32) {
       float e = expf(p[r] - mx);
       p[r] = e;
       den += e;
     }
     den = warp_sum(den);
+#pragma unroll 4
     for (int r = lane; r < R; r += 32) {
       float pr = p[r] / den;
       p[r] = pr;
-      sel[r] = pr + (biased ? corr_bias[r] : 0.0f);
+      sel[r] = pr + sel[r];
     }
   }
   __syncwarp();
@@ -80,6 +87,7 @@ __device__ void route_token_warp(const float* L, const float* logit_bias, const 
     } else {
       float bv = -INFINITY;
       best = 0x7fffffff;
+#pragma unroll 4
       for (int r = lane; r < R; r += 32) {
         float v = sel[r];
         if (ranks_before(v, r, bv, best)) { bv = v; best = r; }
