@@ -222,8 +222,8 @@ MOE_API moe_status_t moe_forward_profiled(const moe_config_t *cfg, const moe_wei
  *    (the library's device code is then loaded anew and the kept address is stale).
  *  - Every call shares the array and clears what must start at zero itself; calls that
  *    overlap on the GPU (unordered streams or host threads) race on it.
- *  - There is no caller workspace, so moe_read_device_status() cannot read this call's
- *    device status word; a device wait that times out still ends its kernel.
+ *  - There is no caller workspace: moe_noalloc_read_device_status() reads this call's device
+ *    status word (a device wait that times out still ends its kernel).
  * x, out, stream and the weights are as for moe_forward. */
 MOE_API moe_status_t moe_forward_decode_noalloc(const moe_config_t *cfg,
                                                 const moe_weights_t *weights, const void *x,
@@ -232,6 +232,11 @@ MOE_API moe_status_t moe_forward_decode_noalloc(const moe_config_t *cfg,
 /* Synchronises `stream` and reads the device status word of `workspace` into *status
  * (MOE_OK or MOE_ERR_DEVICE_TIMEOUT). For tests and debugging; it blocks the host. */
 MOE_API moe_status_t moe_read_device_status(const void *workspace, void *stream, int32_t *status);
+
+/* The same for moe_forward_decode_noalloc: synchronises `stream` and reads the status word of
+ * the library's 4 MiB array on the current device, i.e. of the last no-alloc call there
+ * (each call clears it first, so read it before the next call). */
+MOE_API moe_status_t moe_noalloc_read_device_status(void *stream, int32_t *status);
 
 /* Failure-detection self test: clears the workspace status word, then one device thread waits
  * (with the same bounded wait every kernel here uses) on a barrier that nothing completes,

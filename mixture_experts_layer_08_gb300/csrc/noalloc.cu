@@ -25,6 +25,18 @@ static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 std::mutex g_scratch_mu;
 void* g_scratch_addr[64];   // device address of g_static_scratch, per device ordinal
 
+// Host code sees g_static_scratch only as a host-side stand-in; the kernels need its device
+// address, looked up once per device with that device current (null on failure).
+void* scratch_address(int dev) {
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return nullptr;
+    g_scratch_addr[dev] = p;
+  }
+  return g_scratch_addr[dev];
+}
+
 }  // namespace
 
 extern "C" MOE_API moe_status_t moe_forward_decode_noalloc(const moe_config_t* cfg,
@@ -42,20 +54,19 @@ extern "C" MOE_API moe_status_t moe_forward_decode_noalloc(const moe_config_t* c
   if (c.num_tokens == 0) return MOE_OK;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-  void* scratch = nullptr;
-  {
-    // Host code sees g_static_scratch only as a host-side stand-in; the kernels need its
-    // device address, looked up once per device with that device current.
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-      void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-      g_scratch_addr[dev] = p;
-    }
-    scratch = g_scratch_addr[dev];
-  }
+  void* scratch = scratch_address(dev);
+  if (!scratch) return MOE_ERR_CUDA;
   // moe_forward clears every part of the scratch that must start at zero (the header with
   // its status word and counters, and the atomic accumulator) before using it.
   return moe_forward(&c, weights, x, out, scratch, kStaticScratchBytes, stream, nullptr, nullptr,
                      nullptr);
+}
+
+extern "C" MOE_API moe_status_t moe_noalloc_read_device_status(void* stream, int32_t* status) {
+  if (!status) return MOE_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  void* scratch = scratch_address(dev);
+  if (!scratch) return MOE_ERR_CUDA;
+  return moe_read_device_status(scratch, stream, status);
 }

@@ -74,3 +74,19 @@ def test_noalloc_rejects_what_it_cannot_hold(B):
     big = B.make_config(I.DECODE.with_(num_tokens=16, top_k=32, hidden=8192, inter=1024))
     assert B.moe_workspace_size(big) > (4 << 20)
     assert _noalloc(B, big, w, inp.x, out) == B.MOE_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_noalloc_status_word_reads_ok_after_a_call(B):
+    """moe_noalloc_read_device_status reads the status word of the no-alloc array: MOE_OK
+    after a forward whose device waits all completed."""
+    fn = B.lib.moe_noalloc_read_device_status
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
+    inp = I.make_inputs(I.TINY, device="cuda")
+    w = B.make_weights(inp)
+    cfg = B.make_config(I.TINY, True, B.PATH_DECODE)
+    out = torch.empty_like(inp.x)
+    assert _noalloc(B, cfg, w, inp.x, out) == B.MOE_OK
+    st = ctypes.c_int32(-1)
+    assert fn(torch.cuda.current_stream().cuda_stream, ctypes.byref(st)) == B.MOE_OK
+    assert st.value == B.MOE_OK
